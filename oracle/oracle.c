@@ -1,0 +1,401 @@
+/*
+ * CPU oracle for the routed-MoE expert FFN over Q4_1 / Q2_K weights.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library calls, links or
+ * loads this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline leg do.  It is deliberately plain and slow: one value at a time,
+ * fp64 arithmetic, no blocking, no fusion.  It shares no code, header, table
+ * or constant generator with the CUDA path.
+ *
+ * Sources (web pages this oracle is written from):
+ *  [DS4-1]  molayo1419.me, "ds4.c 해독하기 1/8" -- DeepSeek V4 Flash shape
+ *           (43 layers, 256 routed experts, n_expert_used = 6).
+ *  [DS4-2]  molayo1419.me, "【#2】ds4.c 해독하기" -- asymmetric 2-bit
+ *           quantisation: the quants.c type-trait table (Q2_K = 256 values in
+ *           84 bytes), the ds4q_write_q2_k_block_ref layout table
+ *           (scales @0, qs @16, d @80, dmin @82) and the qs_out packing
+ *           expression; w1 = gate, w2 = down, w3 = up.
+ *  [Q41]    thakicloud.com, "자체 저비트 포맷을 llama.cpp로 옮기기: 복원값이
+ *           비트까지 같은 GGUF Q4_1 재부호화" -- sections "Q4_1 블록이 어떻게
+ *           생겼나" (the 20-byte block and its nibble order), "무손실이 성립하는
+ *           조건 두 개" (the two lossless conditions), "실제로 돌린 코드" (the
+ *           block writer), "비트 폭과 그룹 크기는 메타데이터에서만 읽습니다"
+ *           (bits and group are explicit), "텐서 이름과 KV 메타데이터" (ne[0]
+ *           is the input dimension; row-major [out, in] equals block order).
+ *
+ * Readings where the pages are silent or truncated (each also listed in
+ * the design doc): the 4th term of the Q2_K packing expression is the 6-bit shift
+ * of value l+96; the low nibble of a Q2_K scale byte is the scale and the
+ * high nibble the min; the min is subtracted; router scoring is a plain
+ * dot product (+ optional bias) with a softmax over the k selected experts;
+ * top-k ties go to the lower expert id and NaN ranks below -inf; the FFN is
+ * SwiGLU, silu(gate) * up, with the hidden activation rounded to bf16;
+ * expert tensors are experts-major.
+ *
+ * Pins: every function here is checked by tests/test_oracle_*.py against
+ * facts the pages fix or mathematics fixes (hand-derived golden blocks,
+ * single-code bit positions, exact closed forms, brute force, invariants).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_OK = 0, ORC_EINVAL = 1, ORC_EBLOCKER = 2, ORC_EUNSUPPORTED = 3 };
+enum { ORC_Q4_1 = 1, ORC_Q2_K = 2 };
+
+/* ---------------------------------------------------------------- formats */
+
+/* [DS4-2] type-trait table: Q2_K holds 256 values in 84 bytes.
+ * [Q41] "Q4_1 블록이 어떻게 생겼나": Q4_1 holds 32 values in 20 bytes. */
+int orc_block_values(int qtype) { return qtype == ORC_Q4_1 ? 32 : qtype == ORC_Q2_K ? 256 : 0; }
+int orc_block_bytes(int qtype) { return qtype == ORC_Q4_1 ? 20 : qtype == ORC_Q2_K ? 84 : 0; }
+
+/* IEEE binary16 -> double, exact (normals, subnormals, inf, NaN). */
+double orc_f16(uint16_t h) {
+  int sign = h >> 15, e = (h >> 10) & 0x1F, f = h & 0x3FF;
+  double v;
+  if (e == 0) v = ldexp((double)f, -24);
+  else if (e == 31) v = f ? NAN : INFINITY;
+  else v = ldexp((double)(1024 + f), e - 25);
+  return sign ? -v : v;
+}
+
+/* bf16 -> double, exact. */
+double orc_bf16(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* double -> bf16 bit pattern, round to nearest, ties to even, done on the
+ * integer significand of the double so that there is exactly one rounding. */
+uint16_t orc_round_bf16(double v) {
+  uint64_t u;
+  memcpy(&u, &v, 8);
+  uint16_t s = (uint16_t)((u >> 48) & 0x8000);
+  int E = (int)((u >> 52) & 0x7FF);
+  uint64_t M = u & ((1ULL << 52) - 1);
+  if (E == 0x7FF) return M ? (uint16_t)(s | 0x7FC0) : (uint16_t)(s | 0x7F80);
+  if (E == 0) return s; /* double subnormals are far below bf16's range */
+  uint64_t sig = (1ULL << 52) | M;     /* value = sig * 2^(E - 1075) */
+  int e = E - 1023;                    /* value = 1.x * 2^e */
+  /* bf16 keeps 8 significand bits for e >= -126; below that the quantum is
+   * fixed at 2^-133. Number of low significand bits to drop: */
+  int drop = 52 - 7;
+  if (e < -126) drop += (-126 - e);
+  if (drop > 60) return s;            /* rounds to zero */
+  uint64_t rem = sig & ((1ULL << drop) - 1), half = 1ULL << (drop - 1);
+  uint64_t q = sig >> drop;
+  if (rem > half || (rem == half && (q & 1))) q++;
+  /* q is the significand in units of the quantum 2^(e - 7) (normal) or
+   * 2^-133 (subnormal). Re-assemble. */
+  if (e < -126) {
+    /* q < 2^7 subnormal, q == 2^7 becomes the smallest normal */
+    if (q >= 128) return (uint16_t)(s | (1 << 7) | (q - 128));
+    return (uint16_t)(s | q);
+  }
+  if (q == 256) { q = 128; e += 1; }  /* carry into the exponent */
+  if (e > 127) return (uint16_t)(s | 0x7F80);
+  return (uint16_t)(s | ((e + 127) << 7) | (q - 128));
+}
+
+void orc_round_bf16_array(const double *in, int64_t n, uint16_t *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_round_bf16(in[i]);
+}
+
+static void put16(uint8_t *p, uint16_t v) { p[0] = (uint8_t)(v & 0xFF); p[1] = (uint8_t)(v >> 8); }
+static uint16_t get16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+/* ------------------------------------------------------------------ Q4_1 */
+/* [Q41] "Q4_1 블록이 어떻게 생겼나": fp16 d, fp16 m, uint8 qs[16]; value j
+ * sits in the low 4 bits of qs[j], value j+16 in the high 4 bits of qs[j];
+ * the decoded value is d * q + m. */
+
+int orc_q41_pack(const uint8_t *codes, const uint16_t *d, const uint16_t *m,
+                 int64_t nb, uint8_t *out) {
+  for (int64_t b = 0; b < nb; ++b) {
+    uint8_t *blk = out + 20 * b;
+    const uint8_t *q = codes + 32 * b;
+    put16(blk + 0, d[b]);
+    put16(blk + 2, m[b]);
+    for (int j = 0; j < 16; ++j) {
+      if (q[j] > 15 || q[j + 16] > 15) return ORC_EBLOCKER;
+      blk[4 + j] = (uint8_t)(q[j] | (q[j + 16] << 4));
+    }
+  }
+  return ORC_OK;
+}
+
+void orc_q41_unpack(const uint8_t *blocks, int64_t nb, uint8_t *codes,
+                    uint16_t *d, uint16_t *m) {
+  for (int64_t b = 0; b < nb; ++b) {
+    const uint8_t *blk = blocks + 20 * b;
+    d[b] = get16(blk + 0);
+    m[b] = get16(blk + 2);
+    for (int j = 0; j < 16; ++j) {
+      codes[32 * b + j] = blk[4 + j] & 0x0F;
+      codes[32 * b + j + 16] = blk[4 + j] >> 4;
+    }
+  }
+}
+
+/* One decoded value: d*q + m. d*q is exact in double (11 x 4 bits) and so is
+ * the sum (fp16 exponents span < 53 bits), so the cast is the single
+ * rounding of the exact value to fp32. */
+static float q41_value(const uint8_t *blk, int j) {
+  double d = orc_f16(get16(blk + 0)), m = orc_f16(get16(blk + 2));
+  int q = j < 16 ? (blk[4 + j] & 0x0F) : (blk[4 + j - 16] >> 4);
+  return (float)(d * (double)q + m);
+}
+
+void orc_q41_dequant(const uint8_t *blocks, int64_t nb, float *out) {
+  for (int64_t b = 0; b < nb; ++b)
+    for (int j = 0; j < 32; ++j) out[32 * b + j] = q41_value(blocks + 20 * b, j);
+}
+
+/* [Q41] "무손실이 성립하는 조건 두 개" + "실제로 돌린 코드" + "비트 폭과 그룹
+ * 크기는 메타데이터에서만 읽습니다": re-encode asymmetric codes with an
+ * explicit bit width and group size into Q4_1.  Lossless iff the group is a
+ * multiple of 32 (a group never straddles a block; its (scale, min) pair is
+ * copied into group/32 blocks) and the bit width is at most 4 (codes fit a
+ * nibble).  Violations, or a code outside the declared bit range, are a
+ * BLOCKER: nothing is recomputed, clipped or regrouped. */
+int orc_q41_reencode(int bits, int group, const uint8_t *codes,
+                     const uint16_t *scale, const uint16_t *mins, int64_t n,
+                     uint8_t *out) {
+  if (bits < 1 || group < 1 || n < 0) return ORC_EINVAL;
+  if (group % 32 != 0 || bits > 4) return ORC_EBLOCKER;
+  if (n % group != 0) return ORC_EINVAL;
+  int maxc = (1 << bits) - 1;
+  for (int64_t i = 0; i < n; ++i)
+    if (codes[i] > maxc) return ORC_EBLOCKER;
+  int64_t nb = n / 32;
+  for (int64_t b = 0; b < nb; ++b) {
+    int64_t g = (32 * b) / group; /* the group this block lies in */
+    uint8_t *blk = out + 20 * b;
+    put16(blk + 0, scale[g]);
+    put16(blk + 2, mins[g]);
+    for (int j = 0; j < 16; ++j)
+      blk[4 + j] = (uint8_t)(codes[32 * b + j] | (codes[32 * b + j + 16] << 4));
+  }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ Q2_K */
+/* [DS4-2] layout table: scales[16] at byte 0 (one scale/min nibble pair per
+ * 16-value sub-block), qs[64] at byte 16 (256 2-bit codes), fp16 d at 80,
+ * fp16 dmin at 82.  Packing expression: for j in {0, 128} and l in 0..31,
+ * qs[j/4 + l] = L[j+l] | L[j+l+32] << 2 | L[j+l+64] << 4 | (reading: the
+ * truncated 4th term) L[j+l+96] << 6.  Reading: low nibble = scale, high
+ * nibble = min, value = d*sc*q - dmin*mn. */
+
+static int q2k_qs_index(int i) { return 32 * (i / 128) + (i % 32); }
+static int q2k_qs_shift(int i) { return 2 * ((i % 128) / 32); }
+
+int orc_q2k_pack(const uint8_t *codes, const uint8_t *sc, const uint8_t *mn,
+                 const uint16_t *d, const uint16_t *dmin, int64_t nb,
+                 uint8_t *out) {
+  for (int64_t b = 0; b < nb; ++b) {
+    uint8_t *blk = out + 84 * b;
+    memset(blk, 0, 84);
+    for (int n = 0; n < 16; ++n) {
+      uint8_t s = sc[16 * b + n], m = mn[16 * b + n];
+      if (s > 15 || m > 15) return ORC_EBLOCKER;
+      blk[n] = (uint8_t)(s | (m << 4));
+    }
+    for (int i = 0; i < 256; ++i) {
+      uint8_t q = codes[256 * b + i];
+      if (q > 3) return ORC_EBLOCKER;
+      blk[16 + q2k_qs_index(i)] |= (uint8_t)(q << q2k_qs_shift(i));
+    }
+    put16(blk + 80, d[b]);
+    put16(blk + 82, dmin[b]);
+  }
+  return ORC_OK;
+}
+
+void orc_q2k_unpack(const uint8_t *blocks, int64_t nb, uint8_t *codes,
+                    uint8_t *sc, uint8_t *mn, uint16_t *d, uint16_t *dmin) {
+  for (int64_t b = 0; b < nb; ++b) {
+    const uint8_t *blk = blocks + 84 * b;
+    for (int n = 0; n < 16; ++n) {
+      sc[16 * b + n] = blk[n] & 0x0F;
+      mn[16 * b + n] = blk[n] >> 4;
+    }
+    for (int i = 0; i < 256; ++i)
+      codes[256 * b + i] = (blk[16 + q2k_qs_index(i)] >> q2k_qs_shift(i)) & 3;
+    d[b] = get16(blk + 80);
+    dmin[b] = get16(blk + 82);
+  }
+}
+
+/* d*sc*q (<= 17 significand bits) and dmin*mn (<= 15) are exact in double and
+ * so is their difference; the cast is the one rounding to fp32. */
+static float q2k_value(const uint8_t *blk, int i) {
+  double d = orc_f16(get16(blk + 80)), dmin = orc_f16(get16(blk + 82));
+  int n = i / 16;
+  int sc = blk[n] & 0x0F, mn = blk[n] >> 4;
+  int q = (blk[16 + q2k_qs_index(i)] >> q2k_qs_shift(i)) & 3;
+  return (float)(d * (double)sc * (double)q - dmin * (double)mn);
+}
+
+void orc_q2k_dequant(const uint8_t *blocks, int64_t nb, float *out) {
+  for (int64_t b = 0; b < nb; ++b)
+    for (int i = 0; i < 256; ++i) out[256 * b + i] = q2k_value(blocks + 84 * b, i);
+}
+
+int orc_dequant(int qtype, const uint8_t *blocks, int64_t n_values, float *out) {
+  int bv = orc_block_values(qtype);
+  if (!bv) return ORC_EUNSUPPORTED;
+  if (n_values % bv) return ORC_EINVAL;
+  if (qtype == ORC_Q4_1) orc_q41_dequant(blocks, n_values / 32, out);
+  else orc_q2k_dequant(blocks, n_values / 256, out);
+  return ORC_OK;
+}
+
+/* --------------------------------------------------------------- routing */
+/* [DS4-1] model shape: 256 routed experts, 6 used per token.  The pages do
+ * not print the router; reading: logit[t,e] = sum_j x[t,j] * Wr[e,j]
+ * (+ bias[e]), every product exact in double (bf16 x fp32 = 32 bits), the sum
+ * accumulated in double in index order and rounded once to fp32. */
+void orc_router_logits(const uint16_t *x, const float *Wr, const float *bias,
+                       int T, int D, int E, float *logits) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int j = 0; j < D; ++j)
+        acc += orc_bf16(x[(int64_t)t * D + j]) * (double)Wr[(int64_t)e * D + j];
+      if (bias) acc += (double)bias[e];
+      logits[(int64_t)t * E + e] = (float)acc;
+    }
+}
+
+/* a ranks before b: larger logit first, NaN below everything, ties -> lower id */
+static int ranks_before(float va, int a, float vb, int b) {
+  int na = isnan(va), nb = isnan(vb);
+  if (na || nb) {
+    if (na && nb) return a < b;
+    return nb; /* a is a number, b is NaN */
+  }
+  if (va != vb) return va > vb;
+  return a < b;
+}
+
+/* Top-k by (logit desc, id asc), then w_i = exp(l_i - m) / sum_j exp(l_j - m)
+ * over the k selected, m = the largest selected logit, in double, rounded to
+ * fp32.  Selection is k passes of a plain linear scan. */
+void orc_topk_softmax(const float *logits, int T, int E, int k, int32_t *idx,
+                      float *w) {
+  char *taken = (char *)malloc((size_t)E);
+  double *ex = (double *)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+  for (int t = 0; t < T; ++t) {
+    const float *l = logits + (int64_t)t * E;
+    memset(taken, 0, (size_t)E);
+    for (int i = 0; i < k; ++i) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || ranks_before(l[e], e, l[best], best)) best = e;
+      }
+      taken[best] = 1;
+      idx[(int64_t)t * k + i] = best;
+    }
+    double m = (double)l[idx[(int64_t)t * k]];
+    double s = 0.0;
+    for (int i = 0; i < k; ++i) {
+      ex[i] = exp((double)l[idx[(int64_t)t * k + i]] - m);
+      s += ex[i];
+    }
+    for (int i = 0; i < k; ++i) w[(int64_t)t * k + i] = (float)(ex[i] / s);
+  }
+  free(taken);
+  free(ex);
+}
+
+/* ------------------------------------------------------------------- FFN */
+/* Expert matrices are experts-major: expert e of a [rows x cols] matrix
+ * starts at e * rows * row_bytes, row r at + r * row_bytes, and a row holds
+ * its cols values as cols / block_values consecutive blocks ([Q41] "텐서
+ * 이름과 KV 메타데이터": ne[0] is the input dimension and row-major [out, in]
+ * order is block order).  gate = w1 and up = w3 are [d_ff x d_model],
+ * down = w2 is [d_model x d_ff] ([DS4-2]). */
+
+static int64_t row_bytes(int qtype, int cols) {
+  return (int64_t)cols / orc_block_values(qtype) * orc_block_bytes(qtype);
+}
+
+/* out[r] = sum_j W[r, j] * in[j] in double over the exact fp32 weights. */
+static void matvec(int qtype, const uint8_t *mat, int rows, int cols,
+                   const double *in, double *out, float *rowbuf) {
+  int64_t rb = row_bytes(qtype, cols);
+  for (int r = 0; r < rows; ++r) {
+    orc_dequant(qtype, mat + (int64_t)r * rb, cols, rowbuf);
+    double acc = 0.0;
+    for (int j = 0; j < cols; ++j) acc += (double)rowbuf[j] * in[j];
+    out[r] = acc;
+  }
+}
+
+/* One (token, expert) pair: g = Wg x, u = Wu x, h = bf16(silu(g) * u) with
+ * silu(z) = z / (1 + exp(-z)), y = Wd h (y kept in double). */
+int orc_expert_ffn(int D, int F, int qg, const uint8_t *gate, int qu,
+                   const uint8_t *up, int qd, const uint8_t *down, int e,
+                   const uint16_t *x, double *y, uint16_t *h_out,
+                   double *g_out, double *u_out) {
+  if (!orc_block_values(qg) || !orc_block_values(qu) || !orc_block_values(qd))
+    return ORC_EUNSUPPORTED;
+  if (D <= 0 || F <= 0 || D % orc_block_values(qg) || D % orc_block_values(qu) ||
+      F % orc_block_values(qd))
+    return ORC_EINVAL;
+  double *xin = (double *)malloc(sizeof(double) * (size_t)D);
+  double *g = (double *)malloc(sizeof(double) * (size_t)F);
+  double *u = (double *)malloc(sizeof(double) * (size_t)F);
+  double *h = (double *)malloc(sizeof(double) * (size_t)F);
+  float *rowbuf = (float *)malloc(sizeof(float) * (size_t)(D > F ? D : F));
+  for (int j = 0; j < D; ++j) xin[j] = orc_bf16(x[j]);
+  matvec(qg, gate + (int64_t)e * F * row_bytes(qg, D), F, D, xin, g, rowbuf);
+  matvec(qu, up + (int64_t)e * F * row_bytes(qu, D), F, D, xin, u, rowbuf);
+  for (int r = 0; r < F; ++r) {
+    double silu = g[r] / (1.0 + exp(-g[r]));
+    uint16_t hb = orc_round_bf16(silu * u[r]);
+    if (h_out) h_out[r] = hb;
+    h[r] = orc_bf16(hb);
+  }
+  if (g_out) memcpy(g_out, g, sizeof(double) * (size_t)F);
+  if (u_out) memcpy(u_out, u, sizeof(double) * (size_t)F);
+  matvec(qd, down + (int64_t)e * D * row_bytes(qd, F), D, F, h, y, rowbuf);
+  free(xin); free(g); free(u); free(h); free(rowbuf);
+  return ORC_OK;
+}
+
+/* Whole layer: out[t, c] = sum_{i<k} w[t,i] * y_{t,i}[c] in double, summed in
+ * rank order i = 0..k-1, rounded once to fp32. */
+int orc_moe_ffn(int D, int F, int E, int qg, const uint8_t *gate, int qu,
+                const uint8_t *up, int qd, const uint8_t *down,
+                const uint16_t *x, const int32_t *idx, const float *w, int T,
+                int k, float *out) {
+  if (!orc_block_values(qg) || !orc_block_values(qu) || !orc_block_values(qd))
+    return ORC_EUNSUPPORTED;
+  if (D % orc_block_values(qg) || D % orc_block_values(qu) ||
+      F % orc_block_values(qd))
+    return ORC_EINVAL;
+  for (int64_t i = 0; i < (int64_t)T * k; ++i)
+    if (idx[i] < 0 || idx[i] >= E) return ORC_EINVAL;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int t = 0; t < T; ++t) {
+    double *acc = (double *)calloc((size_t)D, sizeof(double));
+    double *y = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int i = 0; i < k; ++i) {
+      orc_expert_ffn(D, F, qg, gate, qu, up, qd, down, idx[(int64_t)t * k + i],
+                     x + (int64_t)t * D, y, NULL, NULL, NULL);
+      double wi = (double)w[(int64_t)t * k + i];
+      for (int c = 0; c < D; ++c) acc[c] += wi * y[c];
+    }
+    for (int c = 0; c < D; ++c) out[(int64_t)t * D + c] = (float)acc[c];
+    free(acc); free(y);
+  }
+  return ORC_OK;
+}
