@@ -1,0 +1,171 @@
+"""Python binding of libds4moe (the C ABI declared in include/ds4moe.h).
+
+Argument marshalling only: every step of the routed-MoE path runs in the
+library's sm_103a kernels.  Tensors are PyTorch CUDA tensors (PyTorch is
+used for device memory and streams); host-side packing takes numpy arrays.
+There is no fallback: if the compiled library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libds4moe.so")
+
+DS4MOE_OK, DS4MOE_EINVAL, DS4MOE_EBLOCKER, DS4MOE_EUNSUPPORTED = 0, 1, 2, 3
+DS4MOE_ECUDA, DS4MOE_ETIMEOUT, DS4MOE_EDEVICE, DS4MOE_ESPACE = 4, 5, 6, 7
+DS4MOE_Q4_1, DS4MOE_Q2_K, DS4MOE_IQ2_XXS = 1, 2, 3
+QTYPES = {"q4_1": DS4MOE_Q4_1, "q2_k": DS4MOE_Q2_K, "iq2_xxs": DS4MOE_IQ2_XXS}
+
+# Every symbol include/ds4moe.h declares.
+EXPORTS = (
+    "ds4moe_block_values", "ds4moe_block_bytes", "ds4moe_status_string", "ds4moe_quantize_ref",
+    "ds4moe_dequant", "ds4moe_workspace_bytes", "ds4moe_workspace_init", "ds4moe_route_topk",
+    "ds4moe_ffn_decode", "ds4moe_ffn_prefill", "ds4moe_stream_status",
+)
+
+
+class Ds4moeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+class Layer(ctypes.Structure):
+    """Mirror of ds4moe_layer."""
+    _fields_ = [("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("n_expert", ctypes.c_int32),
+                ("q_gate", ctypes.c_int32), ("q_up", ctypes.c_int32), ("q_down", ctypes.c_int32),
+                ("gate", ctypes.c_void_p), ("up", ctypes.c_void_p), ("down", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library; raises if it has not been built (no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libds4moe.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        p, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        L.ds4moe_block_values.argtypes = [i32]
+        L.ds4moe_block_values.restype = i32
+        L.ds4moe_block_bytes.argtypes = [i32]
+        L.ds4moe_block_bytes.restype = i32
+        L.ds4moe_status_string.argtypes = [i32]
+        L.ds4moe_status_string.restype = ctypes.c_char_p
+        L.ds4moe_quantize_ref.argtypes = [i32, i32, i32, p, p, p, p, p, i64, p, sz]
+        L.ds4moe_dequant.argtypes = [i32, p, i64, p, p]
+        L.ds4moe_workspace_bytes.argtypes = [ctypes.POINTER(Layer), i32, i32, i32]
+        L.ds4moe_workspace_bytes.restype = sz
+        L.ds4moe_workspace_init.argtypes = [p, sz, p]
+        L.ds4moe_route_topk.argtypes = [p, p, p, i32, i32, i32, i32, p, p, p, p, sz, p]
+        L.ds4moe_ffn_decode.argtypes = [ctypes.POINTER(Layer), p, p, p, i32, i32, p, p, sz, p]
+        L.ds4moe_ffn_prefill.argtypes = [ctypes.POINTER(Layer), p, p, p, i32, i32, p, p, sz, p]
+        L.ds4moe_stream_status.argtypes = [p, p]
+        for name in EXPORTS:
+            if name not in ("ds4moe_block_values", "ds4moe_block_bytes", "ds4moe_status_string",
+                            "ds4moe_workspace_bytes"):
+                getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().ds4moe_status_string(status).decode()
+
+
+def _check(status: int, what: str):
+    if status != DS4MOE_OK:
+        raise Ds4moeError(status, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def block_values(qtype: int) -> int:
+    return lib().ds4moe_block_values(qtype)
+
+
+def block_bytes(qtype: int) -> int:
+    return lib().ds4moe_block_bytes(qtype)
+
+
+def make_layer(d_model, d_ff, n_expert, q_gate, q_up, q_down, gate, up, down) -> Layer:
+    """Layer descriptor over three device tensors of experts-major block bytes."""
+    return Layer(d_model, d_ff, n_expert, q_gate, q_up, q_down, _ptr(gate), _ptr(up), _ptr(down))
+
+
+# ------------------------------------------------------------- entry points
+def ds4moe_quantize_ref(out_type, bits, group, codes, scale_f16, min_f16, sub_sc=None, sub_mn=None):
+    """Host packing (numpy in, numpy uint8 block bytes out)."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scale_f16 = np.ascontiguousarray(scale_f16, dtype=np.uint16)
+    min_f16 = np.ascontiguousarray(min_f16, dtype=np.uint16)
+    sub_sc = None if sub_sc is None else np.ascontiguousarray(sub_sc, dtype=np.uint8)
+    sub_mn = None if sub_mn is None else np.ascontiguousarray(sub_mn, dtype=np.uint8)
+    n = codes.size
+    bv = max(block_values(out_type), 1)
+    out = np.zeros(n // bv * max(block_bytes(out_type), 0), dtype=np.uint8)
+    st = lib().ds4moe_quantize_ref(out_type, bits, group, codes.ctypes.data, scale_f16.ctypes.data,
+                                   min_f16.ctypes.data, None if sub_sc is None else sub_sc.ctypes.data,
+                                   None if sub_mn is None else sub_mn.ctypes.data, n,
+                                   out.ctypes.data if out.size else None, out.nbytes)
+    _check(st, "ds4moe_quantize_ref")
+    return out
+
+
+def ds4moe_dequant(qtype, blocks, n_values, out, stream=None):
+    _check(lib().ds4moe_dequant(qtype, _ptr(blocks), n_values, _ptr(out), _stream(stream)), "ds4moe_dequant")
+
+
+def ds4moe_workspace_bytes(layer: Layer, T: int, k: int, prefill: bool = False) -> int:
+    return int(lib().ds4moe_workspace_bytes(ctypes.byref(layer), T, k, int(bool(prefill))))
+
+
+def ds4moe_workspace_init(ws, stream=None):
+    _check(lib().ds4moe_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "ds4moe_workspace_init")
+
+
+def ds4moe_route_topk(x, Wr, bias, k, idx, w, logits, ws, stream=None):
+    T, D = x.shape
+    E = Wr.shape[0]
+    _check(lib().ds4moe_route_topk(_ptr(x), _ptr(Wr), _ptr(bias), T, D, E, k, _ptr(idx), _ptr(w),
+                                   _ptr(logits), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "ds4moe_route_topk")
+
+
+def ds4moe_ffn_decode(layer: Layer, x, idx, w, out, ws, stream=None):
+    T, k = idx.shape
+    _check(lib().ds4moe_ffn_decode(ctypes.byref(layer), _ptr(x), _ptr(idx), _ptr(w), T, k, _ptr(out),
+                                   _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "ds4moe_ffn_decode")
+
+
+def ds4moe_ffn_prefill(layer: Layer, x, idx, w, out, ws, stream=None):
+    T, k = idx.shape
+    _check(lib().ds4moe_ffn_prefill(ctypes.byref(layer), _ptr(x), _ptr(idx), _ptr(w), T, k, _ptr(out),
+                                    _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "ds4moe_ffn_prefill")
+
+
+def ds4moe_stream_status(ws, stream=None) -> int:
+    """Synchronizes and returns (and clears) the workspace's device status."""
+    return int(lib().ds4moe_stream_status(_ptr(ws), _stream(stream)))

@@ -1,0 +1,470 @@
+// C-ABI entry points of libds4moe plus the small kernels of the hot path:
+// block dequantisation, the router (compensated dot product), top-k with a
+// softmax over the selected experts, token->expert bucketing and the
+// weighted combine.  The expert GEMV/GEMM kernels live in ffn_decode.cu and
+// ffn_prefill.cu.
+#include <cstdio>
+#include <cstring>
+
+#include "internal.cuh"
+
+using namespace ds4;
+
+namespace ds4 {
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+}  // namespace ds4
+
+namespace {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+inline bool qtype_ok(int q) { return q == DS4MOE_Q4_1 || q == DS4MOE_Q2_K; }
+
+ds4moe_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return DS4MOE_OK;
+  fprintf(stderr, "ds4moe: CUDA error %s\n", cudaGetErrorString(e));
+  return DS4MOE_ECUDA;
+}
+
+// ------------------------------------------------------------------ dequant
+// Q4_1 ([Q41] "Q4_1 블록이 어떻게 생겼나"): one thread per (block, byte j);
+// writes values j (low nibble) and j+16 (high nibble) as fmaf(d, q, m): d*q is
+// exact in fp32, so this is the single rounding of d*q + m.
+__global__ void k_dequant_q41(const uint8_t *__restrict__ blk, int64_t nb, float *__restrict__ out) {
+  const int64_t n = nb * 16;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t b = i >> 4;
+    const int j = (int)(i & 15);
+    const uint8_t *p = blk + b * kQ41Bytes;
+    const float d = f16_bits_to_f32(p[0] | (p[1] << 8));
+    const float m = f16_bits_to_f32(p[2] | (p[3] << 8));
+    const uint32_t q = p[4 + j];
+    out[b * 32 + j] = fmaf(d, (float)(q & 15u), m);
+    out[b * 32 + j + 16] = fmaf(d, (float)(q >> 4), m);
+  }
+}
+
+// Q2_K ([DS4-2] layout table and qs packing): one thread per (block, qs byte);
+// qs byte 32h + l carries values 128h + l + 32s in bits 2s..2s+1.  d*sc and
+// dmin*mn are exact, so fmaf(d*sc, q, -dmin*mn) is the single rounding.
+__global__ void k_dequant_q2k(const uint8_t *__restrict__ blk, int64_t nb, float *__restrict__ out) {
+  const int64_t n = nb * 64;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t b = i >> 6;
+    const int byte = (int)(i & 63), h = byte >> 5, l = byte & 31;
+    const uint8_t *p = blk + b * kQ2KBytes;
+    const float d = f16_bits_to_f32(p[80] | (p[81] << 8));
+    const float dmin = f16_bits_to_f32(p[82] | (p[83] << 8));
+    const uint32_t q = p[16 + byte];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int v = 128 * h + l + 32 * s;
+      const uint32_t scb = p[v >> 4];
+      out[b * 256 + v] = fmaf(d * (float)(scb & 15u), (float)((q >> (2 * s)) & 3u), -(dmin * (float)(scb >> 4)));
+    }
+  }
+}
+
+// ------------------------------------------------------------------- router
+// Error-free transforms (Ogita, Rump, Oishi, "Accurate sum and dot product",
+// SIAM J. Sci. Comput. 26(6), 2005): TwoProduct via FMA and Knuth's TwoSum.
+__device__ __forceinline__ void two_prod(float a, float b, float &p, float &e) {
+  p = __fmul_rn(a, b);
+  e = fmaf(a, b, -p);
+}
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// One warp per (t, e): Dot2 over d_model, lanes own interleaved float4
+// slices, the (sum, error) pairs are merged across lanes with TwoSum, the
+// bias is added with TwoSum, and the result is rounded once.
+__global__ void k_router_logits(const uint16_t *__restrict__ x, const float *__restrict__ Wr,
+                                const float *__restrict__ bias, int T, int D, int E,
+                                float *__restrict__ logits) {
+  const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= (int64_t)T * E) return;
+  const int t = (int)(gw / E), e = (int)(gw % E);
+  const uint16_t *xr = x + (int64_t)t * D;
+  const float *wr = Wr + (int64_t)e * D;
+  float s = 0.f, c = 0.f;
+  for (int j = 4 * lane; j < D; j += 128) {
+    const float4 wv = *reinterpret_cast<const float4 *>(wr + j);
+    const uint2 xv = *reinterpret_cast<const uint2 *>(xr + j);
+    const float xs[4] = {bf16_bits_to_f32(xv.x & 0xFFFFu), bf16_bits_to_f32(xv.x >> 16),
+                         bf16_bits_to_f32(xv.y & 0xFFFFu), bf16_bits_to_f32(xv.y >> 16)};
+    const float ws[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float p, pe, se;
+      two_prod(xs[q], ws[q], p, pe);
+      two_sum(s, p, s, se);
+      c = __fadd_rn(c, __fadd_rn(pe, se));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    const float so = __shfl_xor_sync(0xffffffffu, s, off);
+    const float co = __shfl_xor_sync(0xffffffffu, c, off);
+    float se;
+    two_sum(s, so, s, se);
+    c = __fadd_rn(c, __fadd_rn(co, se));
+  }
+  if (lane == 0) {
+    if (bias) {
+      float se;
+      two_sum(s, bias[e], s, se);
+      c = __fadd_rn(c, se);
+    }
+    logits[(int64_t)t * E + e] = __fadd_rn(s, c);
+  }
+}
+
+// a ranks before b: larger first, NaN below everything, ties to lower id.
+__device__ __forceinline__ bool ranks_before(float va, int a, float vb, int b) {
+  if (b < 0) return a >= 0;
+  if (a < 0) return false;
+  const bool na = isnan(va), nb = isnan(vb);
+  if (na || nb) return (na && nb) ? a < b : nb;
+  if (va != vb) return va > vb;
+  return a < b;
+}
+
+// One warp per token: k rounds of a warp arg-max, then a softmax over the k
+// selected logits in double, summed in rank order.
+__global__ void k_topk_softmax(const float *__restrict__ logits, int T, int E, int k,
+                               int32_t *__restrict__ idx, float *__restrict__ w) {
+  const int t = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float *l = logits + (int64_t)t * E;
+  uint32_t taken = 0;  // bit j: entry lane + 32 j already selected
+  float my_v = 0.f;
+  int my_e = -1;
+  for (int i = 0; i < k; ++i) {
+    float bv = 0.f;
+    int be = -1;
+    for (int j = 0, e = lane; e < E; ++j, e += 32) {
+      if (taken & (1u << j)) continue;
+      const float v = l[e];
+      if (ranks_before(v, e, bv, be)) { bv = v; be = e; }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (ranks_before(ov, oe, bv, be)) { bv = ov; be = oe; }
+    }
+    if (be >= 0 && (be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == i) { my_v = bv; my_e = be; }
+  }
+  const double m = (double)__shfl_sync(0xffffffffu, my_v, 0);
+  const double ex = lane < k ? exp((double)my_v - m) : 0.0;
+  double sum = 0.0;
+  for (int i = 0; i < k; ++i) sum += __shfl_sync(0xffffffffu, ex, i);
+  if (lane < k) {
+    idx[(int64_t)t * k + lane] = my_e;
+    w[(int64_t)t * k + lane] = (float)(ex / sum);
+  }
+}
+
+// ---------------------------------------------------------------- bucketing
+// One CTA of 1024 threads.  Pairs p = t*k + i are grouped by expert, stable
+// in p (hence in token order).  Phase A: warp w walks its contiguous slice of
+// pairs 32 at a time and ranks each pair among same-expert pairs of the slice
+// (__match_any_sync); Phase B: per-expert totals, exclusive offsets and
+// per-warp bases; Phase C: scatter.  Also builds the list of active experts.
+__global__ void __launch_bounds__(1024) k_bucket(const int32_t *__restrict__ idx, int P, int E,
+                                                 WsHeader *__restrict__ hdr, int32_t *__restrict__ counts,
+                                                 int32_t *__restrict__ offs, int32_t *__restrict__ active,
+                                                 int32_t *__restrict__ perm, int32_t *__restrict__ inv,
+                                                 int32_t *__restrict__ lrank) {
+  extern __shared__ int32_t sm[];
+  int32_t *wcnt = sm;              // [32][E]
+  int32_t *soff = sm + 32 * E;     // [E + 1]
+  __shared__ int32_t warp_tot[32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  for (int i = tid; i < 32 * E; i += 1024) wcnt[i] = 0;
+  __syncthreads();
+  const int R = (P + 31) / 32;
+  const int p0 = wid * R, p1 = min(P, p0 + R);
+  for (int b = p0; b < p1; b += 32) {
+    const int p = b + lane;
+    int e = -1;
+    if (p < p1) {
+      e = idx[p];
+      if (e < 0 || e >= E) { record_status(hdr, DS4MOE_EDEVICE); e = -1; }
+    }
+    const unsigned mask = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(mask & ((1u << lane) - 1u));
+    int base = 0;
+    if (e >= 0) base = wcnt[wid * E + e];
+    __syncwarp();
+    if (e >= 0 && rank == 0) wcnt[wid * E + e] = base + __popc(mask);
+    __syncwarp();
+    if (p < p1) lrank[p] = e >= 0 ? base + rank : -1;
+  }
+  __syncthreads();
+  // Phase B: totals and per-warp exclusive bases (one thread per expert)
+  for (int e = tid; e < E; e += 1024) {
+    int run = 0;
+    for (int w2 = 0; w2 < 32; ++w2) {
+      const int c = wcnt[w2 * E + e];
+      wcnt[w2 * E + e] = run;
+      run += c;
+    }
+    soff[e] = run;  // count, scanned below
+    counts[e] = run;
+  }
+  __syncthreads();
+  // exclusive scan of soff[0..E) (E <= 1024: one element per thread)
+  {
+    const int v = tid < E ? soff[tid] : 0;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      int wt = warp_tot[lane], wi = wt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, wi, off);
+        if (lane >= off) wi += o;
+      }
+      warp_tot[lane] = wi - wt;  // exclusive
+    }
+    __syncthreads();
+    const int excl = warp_tot[wid] + incl - v;
+    __syncthreads();
+    if (tid < E) { soff[tid] = excl; offs[tid] = excl; }
+    if (tid == E - 1) offs[E] = excl + v;
+    // active list: flags (count > 0) scanned the same way
+    const int f = (tid < E && v > 0) ? 1 : 0;
+    int fi = f;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, fi, off);
+      if (lane >= off) fi += o;
+    }
+    if (lane == 31) warp_tot[wid] = fi;
+    __syncthreads();
+    if (wid == 0) {
+      int wt = warp_tot[lane], wi = wt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, wi, off);
+        if (lane >= off) wi += o;
+      }
+      warp_tot[lane] = wi - wt;
+      if (lane == 31) hdr->n_active = wi;
+    }
+    __syncthreads();
+    if (f) active[warp_tot[wid] + fi - 1] = tid;
+  }
+  __syncthreads();
+  // Phase C: scatter
+  for (int p = tid; p < P; p += 1024) {
+    const int r = lrank[p];
+    if (r < 0) { inv[p] = -1; continue; }
+    const int e = idx[p];
+    const int wslice = p / R;
+    const int pos = soff[e] + wcnt[wslice * E + e] + r;
+    perm[pos] = p;
+    inv[p] = pos;
+  }
+}
+
+__global__ void k_clear_header(WsHeader *hdr) {
+  if (threadIdx.x == 0) {
+    hdr->status = 0;
+    hdr->n_active = 0;
+    hdr->route_done = 0;
+  }
+}
+
+// ------------------------------------------------------------- validation
+ds4moe_status check_layer(const ds4moe_layer *L) {
+  if (!L) return DS4MOE_EINVAL;
+  if (L->q_gate == DS4MOE_IQ2_XXS || L->q_up == DS4MOE_IQ2_XXS || L->q_down == DS4MOE_IQ2_XXS)
+    return DS4MOE_EUNSUPPORTED;
+  if (!qtype_ok(L->q_gate) || !qtype_ok(L->q_up) || !qtype_ok(L->q_down)) return DS4MOE_EUNSUPPORTED;
+  if (L->d_model <= 0 || L->d_ff <= 0 || L->n_expert < 1 || L->n_expert > 1024) return DS4MOE_EINVAL;
+  if (L->d_model % block_vals(L->q_gate) || L->d_model % block_vals(L->q_up) ||
+      L->d_ff % block_vals(L->q_down) || L->d_ff % 16 || L->d_model % 16)
+    return DS4MOE_EINVAL;
+  if (!L->gate || !L->up || !L->down) return DS4MOE_EINVAL;
+  if (!aligned16(L->gate) || !aligned16(L->up) || !aligned16(L->down)) return DS4MOE_EINVAL;
+  return DS4MOE_OK;
+}
+
+ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, const int32_t *idx,
+                      const float *w, int32_t T, int32_t k, float *out, void *ws, size_t ws_bytes,
+                      void *stream) {
+  ds4moe_status st = check_layer(L);
+  if (st != DS4MOE_OK) return st;
+  if (T < 0 || k < 1 || k > 32 || k > L->n_expert) return DS4MOE_EINVAL;
+  if (T == 0) return DS4MOE_OK;
+  if ((int64_t)T * k > (1 << 24)) return DS4MOE_EINVAL;
+  if (!x || !idx || !w || !out || !ws) return DS4MOE_EINVAL;
+  if (!aligned16(x) || !aligned16(idx) || !aligned16(w) || !aligned16(out) || !aligned16(ws))
+    return DS4MOE_EINVAL;
+  const WsLayout lay = ws_layout(*L, T, k, prefill);
+  if (ws_bytes < lay.total) return DS4MOE_ESPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  FfnArgs a{};
+  a.L = *L;
+  a.x = x;
+  a.w = w;
+  a.T = T;
+  a.k = k;
+  a.out = out;
+  a.hdr = ws_ptr<WsHeader>(ws, lay.hdr);
+  a.offs = ws_ptr<int32_t>(ws, lay.offs);
+  a.active = ws_ptr<int32_t>(ws, lay.active);
+  a.perm = ws_ptr<int32_t>(ws, lay.perm);
+  a.inv = ws_ptr<int32_t>(ws, lay.inv);
+  a.h = ws_ptr<uint16_t>(ws, lay.h);
+  a.y = ws_ptr<float>(ws, lay.y);
+  const int E = L->n_expert, P = T * k;
+  const size_t smem = sizeof(int32_t) * (32 * (size_t)E + E + 1);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(k_bucket, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    attr_set = true;
+  }
+  k_bucket<<<1, 1024, smem, s>>>(idx, P, E, a.hdr, ws_ptr<int32_t>(ws, lay.counts), ws_ptr<int32_t>(ws, lay.offs),
+                                 ws_ptr<int32_t>(ws, lay.active), ws_ptr<int32_t>(ws, lay.perm),
+                                 ws_ptr<int32_t>(ws, lay.inv), ws_ptr<int32_t>(ws, lay.lrank));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_status(e);
+  e = prefill ? launch_ffn_prefill(a, s) : launch_ffn_decode(a, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = launch_combine(a, s);
+  return cuda_status(e);
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+extern "C" {
+
+int32_t ds4moe_block_values(int32_t qtype) { return block_vals(qtype); }
+int32_t ds4moe_block_bytes(int32_t qtype) { return block_bytes(qtype); }
+
+const char *ds4moe_status_string(int32_t s) {
+  switch (s) {
+    case DS4MOE_OK: return "ok";
+    case DS4MOE_EINVAL: return "invalid argument";
+    case DS4MOE_EBLOCKER: return "lossless re-encode condition violated (BLOCKER)";
+    case DS4MOE_EUNSUPPORTED: return "unsupported block format";
+    case DS4MOE_ECUDA: return "CUDA error";
+    case DS4MOE_ETIMEOUT: return "device wait timed out";
+    case DS4MOE_EDEVICE: return "device-detected data error";
+    case DS4MOE_ESPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+ds4moe_status ds4moe_dequant(int32_t qtype, const void *blocks, int64_t n_values, float *out,
+                             void *stream) {
+  if (qtype == DS4MOE_IQ2_XXS) return DS4MOE_EUNSUPPORTED;
+  if (!qtype_ok(qtype)) return DS4MOE_EUNSUPPORTED;
+  if (n_values < 0 || n_values % block_vals(qtype)) return DS4MOE_EINVAL;
+  if (n_values == 0) return DS4MOE_OK;
+  if (!blocks || !out || !aligned16(blocks) || !aligned16(out)) return DS4MOE_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t nb = n_values / block_vals(qtype);
+  const int64_t work = qtype == DS4MOE_Q4_1 ? nb * 16 : nb * 64;
+  const int threads = 256;
+  const int64_t want = (work + threads - 1) / threads;
+  const int grid = (int)(want < (int64_t)num_sms() * 32 ? want : (int64_t)num_sms() * 32);
+  if (qtype == DS4MOE_Q4_1)
+    k_dequant_q41<<<grid, threads, 0, s>>>(static_cast<const uint8_t *>(blocks), nb, out);
+  else
+    k_dequant_q2k<<<grid, threads, 0, s>>>(static_cast<const uint8_t *>(blocks), nb, out);
+  return cuda_status(cudaGetLastError());
+}
+
+size_t ds4moe_workspace_bytes(const ds4moe_layer *L, int32_t T, int32_t k, int32_t prefill) {
+  if (!L || T < 0 || k < 1 || L->n_expert < 1 || L->d_model <= 0 || L->d_ff <= 0) return 0;
+  return ws_layout(*L, T, k, prefill).total;
+}
+
+ds4moe_status ds4moe_workspace_init(void *ws, size_t ws_bytes, void *stream) {
+  if (!ws || !aligned16(ws) || ws_bytes < sizeof(WsHeader)) return DS4MOE_EINVAL;
+  k_clear_header<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<WsHeader *>(ws));
+  return cuda_status(cudaGetLastError());
+}
+
+ds4moe_status ds4moe_route_topk(const uint16_t *x, const float *Wr, const float *bias, int32_t T,
+                                int32_t d_model, int32_t n_expert, int32_t k, int32_t *idx, float *w,
+                                float *logits, void *ws, size_t ws_bytes, void *stream) {
+  if (T < 0 || d_model <= 0 || d_model % 4 || n_expert < 1 || n_expert > 1024 || k < 1 || k > 32 ||
+      k > n_expert)
+    return DS4MOE_EINVAL;
+  if (T == 0) return DS4MOE_OK;
+  if (!x || !Wr || !idx || !w || !ws) return DS4MOE_EINVAL;
+  if (!aligned16(x) || !aligned16(Wr) || !aligned16(idx) || !aligned16(w) || !aligned16(ws) ||
+      (bias && !aligned16(bias)) || (logits && !aligned16(logits)))
+    return DS4MOE_EINVAL;
+  if ((int64_t)d_model * 2 % 16) return DS4MOE_EINVAL;  // bf16 rows start 16-byte aligned
+  ds4moe_layer shape{};
+  shape.d_model = d_model;
+  shape.d_ff = 16;
+  shape.n_expert = n_expert;
+  const WsLayout lay = ws_layout(shape, T, k, 0);
+  const size_t need = logits ? sizeof(WsHeader) : lay.logits + align256(sizeof(float) * (size_t)T * n_expert);
+  if (ws_bytes < need) return DS4MOE_ESPACE;
+  float *lg = logits ? logits : ws_ptr<float>(ws, lay.logits);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t warps = (int64_t)T * n_expert;
+  k_router_logits<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(x, Wr, bias, T, d_model, n_expert, lg);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_status(e);
+  k_topk_softmax<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(lg, T, n_expert, k, idx, w);
+  return cuda_status(cudaGetLastError());
+}
+
+ds4moe_status ds4moe_ffn_decode(const ds4moe_layer *L, const uint16_t *x, const int32_t *idx,
+                                const float *w, int32_t T, int32_t k, float *out, void *ws,
+                                size_t ws_bytes, void *stream) {
+  return run_ffn(false, L, x, idx, w, T, k, out, ws, ws_bytes, stream);
+}
+
+ds4moe_status ds4moe_ffn_prefill(const ds4moe_layer *L, const uint16_t *x, const int32_t *idx,
+                                 const float *w, int32_t T, int32_t k, float *out, void *ws,
+                                 size_t ws_bytes, void *stream) {
+  return run_ffn(true, L, x, idx, w, T, k, out, ws, ws_bytes, stream);
+}
+
+ds4moe_status ds4moe_stream_status(void *ws, void *stream) {
+  if (!ws || !aligned16(ws)) return DS4MOE_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t st = 0;
+  cudaError_t e = cudaMemcpyAsync(&st, ws, sizeof(st), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (st != 0) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyAsync(ws, &zero, sizeof(zero), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return static_cast<ds4moe_status>(st);
+}
+
+}  // extern "C"

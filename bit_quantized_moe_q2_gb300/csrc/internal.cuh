@@ -1,0 +1,102 @@
+// Internal declarations shared by the ds4moe translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ds4moe.h"
+
+namespace ds4 {
+
+// ------------------------------------------------------------ formats
+constexpr int kQ41Vals = 32, kQ41Bytes = 20;
+constexpr int kQ2KVals = 256, kQ2KBytes = 84;
+
+__host__ __device__ inline int block_vals(int q) {
+  return q == DS4MOE_Q4_1 ? kQ41Vals : q == DS4MOE_Q2_K ? kQ2KVals : 0;
+}
+__host__ __device__ inline int block_bytes(int q) {
+  return q == DS4MOE_Q4_1 ? kQ41Bytes : q == DS4MOE_Q2_K ? kQ2KBytes : 0;
+}
+__host__ __device__ inline int64_t row_bytes(int q, int cols) {
+  return (int64_t)(cols / block_vals(q)) * block_bytes(q);
+}
+
+// ---------------------------------------------------------- workspace
+// Every region starts on a 256-byte boundary.  The header holds the sticky
+// device status word and small counters.
+struct WsHeader {
+  uint32_t status;     // 0 or a ds4moe_status recorded by a kernel
+  int32_t n_active;    // experts with >= 1 routed pair (set by bucketing)
+  uint32_t route_done; // last-block counter of the fused router
+  uint32_t pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
+
+struct WsLayout {
+  size_t hdr, logits, counts, offs, active, perm, inv, lrank, h, y, total;
+};
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(const ds4moe_layer &L, int T, int k, int /*prefill*/) {
+  WsLayout w{};
+  size_t o = 0;
+  const size_t E = (size_t)L.n_expert, P = (size_t)T * (size_t)k;
+  w.hdr = o;     o += align256(sizeof(WsHeader));
+  w.logits = o;  o += align256(sizeof(float) * (size_t)T * E);
+  w.counts = o;  o += align256(sizeof(int32_t) * E);
+  w.offs = o;    o += align256(sizeof(int32_t) * (E + 1));
+  w.active = o;  o += align256(sizeof(int32_t) * E);
+  w.perm = o;    o += align256(sizeof(int32_t) * P);
+  w.inv = o;     o += align256(sizeof(int32_t) * P);
+  w.lrank = o;   o += align256(sizeof(int32_t) * P);
+  w.h = o;       o += align256(sizeof(uint16_t) * P * (size_t)L.d_ff);
+  w.y = o;       o += align256(sizeof(float) * P * (size_t)L.d_model);
+  w.total = o;
+  return w;
+}
+
+template <typename T>
+inline T *ws_ptr(void *ws, size_t off) { return reinterpret_cast<T *>(static_cast<char *>(ws) + off); }
+
+// ------------------------------------------------------- device helpers
+__device__ __forceinline__ float f16_bits_to_f32(uint32_t h) {
+  return __half2float(__ushort_as_half((unsigned short)h));
+}
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ void record_status(WsHeader *hdr, uint32_t code) {
+  atomicCAS(&hdr->status, 0u, code);
+}
+
+// Round-to-nearest-even fp32 -> bf16 bit pattern (hardware conversion).
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// ------------------------------------------------------- launch entry points
+// (defined in ffn_decode.cu / ffn_prefill.cu; called from ds4moe_abi.cu)
+struct FfnArgs {
+  ds4moe_layer L;
+  const uint16_t *x;
+  const float *w;
+  int T, k;
+  float *out;
+  WsHeader *hdr;
+  const int32_t *offs, *active, *perm, *inv;
+  uint16_t *h;
+  float *y;
+};
+
+cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s);
+cudaError_t launch_ffn_prefill(const FfnArgs &a, cudaStream_t s);
+cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace ds4

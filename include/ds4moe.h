@@ -1,0 +1,211 @@
+/*
+ * ds4moe -- routed-MoE expert FFN over low-bit block-quantized weights
+ * (Q4_1 and Q2_K) for one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Plain pointers and sizes only; no CUDA, PyTorch or C++ types cross
+ * this boundary.  A "stream" argument is a cudaStream_t passed as void*
+ * (NULL = the legacy default stream).  Device pointers must come from
+ * cudaMalloc-class allocations on the current device.
+ *
+ * Sources of the operations (web pages):
+ *  [DS4-1] molayo1419.me, "ds4.c 해독하기 1/8": DeepSeek V4 Flash shape --
+ *          256 routed experts per layer, 6 used per token, 43 layers.
+ *  [DS4-2] molayo1419.me, "【#2】ds4.c 해독하기": the routed-expert-only
+ *          2-bit recipe (w1 = gate, w2 = down, w3 = up; expert matrices
+ *          4096 x 2048); the Q2_K type trait (256 values / 84 bytes), its
+ *          layout table and its qs packing expression.
+ *  [Q41]   thakicloud.com, "자체 저비트 포맷을 llama.cpp로 옮기기: 복원값이
+ *          비트까지 같은 GGUF Q4_1 재부호화": the Q4_1 block ("Q4_1 블록이 어떻게
+ *          생겼나"), the lossless re-encode and its two conditions ("무손실이
+ *          성립하는 조건 두 개", "실제로 돌린 코드"), explicit bits/group ("비트
+ *          폭과 그룹 크기는 메타데이터에서만 읽습니다"), block order along the
+ *          input dimension ("텐서 이름과 KV 메타데이터").
+ *
+ * Conventions
+ *  - The caller owns every buffer.  Nothing here allocates device memory on
+ *    the compute path; scratch lives in a caller-provided workspace whose size
+ *    ds4moe_workspace_bytes() returns.
+ *  - Device entry points are asynchronous on `stream`.  Errors that the host
+ *    can see (bad sizes, NULL or misaligned pointers, unsupported formats,
+ *    too small a workspace) return before anything is launched.  Errors that
+ *    only the device can see (an expert id out of range, a bounded wait that
+ *    gave up) are recorded in a status word inside the workspace and reported
+ *    by ds4moe_stream_status(); kernels never trap.
+ *  - Alignment: every device pointer must be 16-byte aligned.
+ *  - Weight tensors are experts-major: expert e of a [rows x cols] matrix
+ *    starts at byte e * rows * row_bytes, row r at + r * row_bytes, and a row
+ *    is cols / block_values consecutive blocks along the input axis.
+ *    gate (w1) and up (w3) are [d_ff x d_model], down (w2) is [d_model x d_ff].
+ *  - Activations x are bf16 bit patterns (uint16_t), row-major [T, d_model].
+ *  - T == 0 is a no-op that returns DS4MOE_OK.
+ */
+#ifndef DS4MOE_H
+#define DS4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DS4MOE_OK = 0,
+  DS4MOE_EINVAL = 1,       /* invalid argument (host-detected, nothing launched) */
+  DS4MOE_EBLOCKER = 2,     /* lossless re-encode condition violated ([Q41]) */
+  DS4MOE_EUNSUPPORTED = 3, /* block format not supported (e.g. IQ2_XXS) */
+  DS4MOE_ECUDA = 4,        /* a CUDA runtime call failed */
+  DS4MOE_ETIMEOUT = 5,     /* a bounded device-side wait gave up */
+  DS4MOE_EDEVICE = 6,      /* device-detected data error (expert id out of range) */
+  DS4MOE_ESPACE = 7        /* workspace smaller than ds4moe_workspace_bytes() */
+} ds4moe_status;
+
+/* Block formats.  These ids are this library's own, not ggml's. */
+typedef enum {
+  DS4MOE_Q4_1 = 1,   /* 32 values in 20 bytes: fp16 d @0, fp16 m @2, qs[16] @4;
+                        value j = low nibble of qs[j], value j+16 = high nibble;
+                        y = d*q + m  ([Q41] "Q4_1 블록이 어떻게 생겼나") */
+  DS4MOE_Q2_K = 2,   /* 256 values in 84 bytes: scales[16] @0 (sc | mn << 4 per
+                        16 values), qs[64] @16, fp16 d @80, fp16 dmin @82;
+                        value i: code (qs[32*(i/128) + i%32] >> 2*((i%128)/32)) & 3,
+                        y = d*sc*q - dmin*mn  ([DS4-2] layout table and packing) */
+  DS4MOE_IQ2_XXS = 3 /* named by [DS4-2]; its grid codebook is not given there:
+                        every entry point returns DS4MOE_EUNSUPPORTED */
+} ds4moe_qtype;
+
+/* One routed-MoE layer's expert weights (device pointers, 16-byte aligned). */
+typedef struct {
+  int32_t d_model;   /* D: input/output width (multiple of the gate/up block size) */
+  int32_t d_ff;      /* F: hidden width (multiple of the down block size and of 16) */
+  int32_t n_expert;  /* E: routed experts in this layer, 1..1024 */
+  int32_t q_gate, q_up, q_down;  /* ds4moe_qtype of each matrix */
+  const void *gate;  /* [E][F rows][D/bv * bb bytes]  w1 */
+  const void *up;    /* [E][F rows][D/bv * bb bytes]  w3 */
+  const void *down;  /* [E][D rows][F/bv * bb bytes]  w2 */
+} ds4moe_layer;
+
+/* Values and bytes per block of a format (0 if unknown). */
+int32_t ds4moe_block_values(int32_t qtype);
+int32_t ds4moe_block_bytes(int32_t qtype);
+
+/* Human-readable name of a status code (static string). */
+const char *ds4moe_status_string(int32_t status);
+
+/*
+ * ds4moe_quantize_ref -- HOST, synchronous.  Packs integer codes and their
+ * scales into blocks; nothing is recomputed or rounded.
+ *
+ * out_type == DS4MOE_Q4_1: the lossless re-encode of [Q41] ("무손실이
+ *   성립하는 조건 두 개", "실제로 돌린 코드").  `codes` holds n_values codes,
+ *   one per byte, each < 2^bits; scale_f16[g] / min_f16[g] are the fp16 bit
+ *   patterns of group g (n_values / group entries each).  Each 32-value block
+ *   copies its group's (scale, min) into (d, m) and folds its codes into
+ *   nibbles.  bits and group are explicit and never inferred from a byte
+ *   count ([Q41] "비트 폭과 그룹 크기는 메타데이터에서만 읽습니다").
+ *   Returns DS4MOE_EBLOCKER if group % 32 != 0, bits > 4 or any code >=
+ *   2^bits (no fallback); DS4MOE_EINVAL if bits < 1, group < 1, n_values %
+ *   group != 0 or a pointer is NULL.  sub_sc / sub_mn must be NULL.
+ * out_type == DS4MOE_Q2_K: packs 2-bit codes ([DS4-2] layout table and qs
+ *   packing).  bits must be 2 and group 256; scale_f16 / min_f16 hold d and
+ *   dmin per 256 values; sub_sc / sub_mn hold the 4-bit scale and min of each
+ *   16-value sub-block (n_values / 16 entries, one per byte).  Codes > 3 or
+ *   nibbles > 15 return DS4MOE_EBLOCKER.
+ * out_type == DS4MOE_IQ2_XXS: DS4MOE_EUNSUPPORTED.
+ * out_bytes must be at least n_values / block_values * block_bytes
+ * (DS4MOE_ESPACE otherwise).  `out_blocks` is host memory.
+ */
+ds4moe_status ds4moe_quantize_ref(int32_t out_type, int32_t bits, int32_t group,
+                                  const uint8_t *codes, const uint16_t *scale_f16,
+                                  const uint16_t *min_f16, const uint8_t *sub_sc,
+                                  const uint8_t *sub_mn, int64_t n_values,
+                                  void *out_blocks, size_t out_bytes);
+
+/*
+ * ds4moe_dequant -- DEVICE.  Decodes n_values values of `blocks` (device,
+ * qtype layout above) into fp32 `out` (device).  The result is the single
+ * fp32 rounding of the exact decoded value (d*q + m, or d*sc*q - dmin*mn),
+ * so it is unique bit for bit.  n_values must be a multiple of the block
+ * size.
+ */
+ds4moe_status ds4moe_dequant(int32_t qtype, const void *blocks, int64_t n_values,
+                             float *out, void *stream);
+
+/*
+ * ds4moe_workspace_bytes -- bytes of device workspace needed by
+ * ds4moe_route_topk + ds4moe_ffn_decode / ds4moe_ffn_prefill for this layer
+ * shape, T tokens and top-k (one workspace serves all three calls).  Returns
+ * 0 for invalid arguments.  `prefill` selects the prefill path's layout.
+ */
+size_t ds4moe_workspace_bytes(const ds4moe_layer *L, int32_t T, int32_t k,
+                              int32_t prefill);
+
+/*
+ * ds4moe_workspace_init -- DEVICE.  Clears the status word and the
+ * persistent counters of a fresh workspace.  Call once after allocating it
+ * (and after any ds4moe_stream_status that reported an error).
+ */
+ds4moe_status ds4moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * ds4moe_route_topk -- DEVICE.  Router of one layer ([DS4-1] model shape:
+ * top-6 of 256 experts per token; scoring per the library's reading: plain
+ * logits with a softmax over the selected experts).
+ *   logits[t,e] = sum_j x[t,j] * Wr[e,j] (+ bias[e]), computed with a
+ *     compensated (twice-working-precision) dot product and rounded once to
+ *     fp32;
+ *   idx[t, 0..k) = the k largest logits, descending, ties to the lower
+ *     expert id, NaN below -inf;
+ *   w[t,i] = exp(l_i - l_0) / sum_j exp(l_j - l_0) over the k selected.
+ * x: bf16 [T, d_model]; Wr: fp32 [n_expert, d_model]; bias: fp32 [n_expert]
+ * or NULL; idx: int32 [T, k]; w: fp32 [T, k]; logits: fp32 [T, n_expert] or
+ * NULL.  1 <= k <= min(n_expert, 32), d_model % 4 == 0.  `ws` is the layer
+ * workspace (ds4moe_workspace_bytes).
+ */
+ds4moe_status ds4moe_route_topk(const uint16_t *x, const float *Wr, const float *bias,
+                                int32_t T, int32_t d_model, int32_t n_expert, int32_t k,
+                                int32_t *idx, float *w, float *logits, void *ws,
+                                size_t ws_bytes, void *stream);
+
+/*
+ * ds4moe_ffn_decode -- DEVICE.  Routed expert FFN + combine for a decode
+ * batch (small T):
+ *   for each (t, i): e = idx[t,i];
+ *     g = W1[e] x_t, u = W3[e] x_t  (dequant fused into the contraction),
+ *     h = bf16(silu(g) * u), silu(z) = z / (1 + exp(-z)),
+ *     y_{t,i} = W2[e] h;
+ *   out[t] = sum_{i<k} w[t,i] * y_{t,i}, summed in rank order i = 0..k-1.
+ * x: bf16 [T, d_model]; idx: int32 [T, k] (from ds4moe_route_topk or the
+ * caller); w: fp32 [T, k]; out: fp32 [T, d_model].  Pairs whose expert id is
+ * out of range are skipped and flag DS4MOE_EDEVICE in the workspace status.
+ * Accuracy: fp32 accumulation over exact integer codes; max |err| <=
+ * 2e-3 * max |exact| (tested against a double-precision oracle).
+ */
+ds4moe_status ds4moe_ffn_decode(const ds4moe_layer *L, const uint16_t *x,
+                                const int32_t *idx, const float *w, int32_t T,
+                                int32_t k, float *out, void *ws, size_t ws_bytes,
+                                void *stream);
+
+/*
+ * ds4moe_ffn_prefill -- DEVICE.  Same contract as ds4moe_ffn_decode for a
+ * prefill chunk (large T, e.g. the 4096-token chunk of [DS4-1]'s distributed
+ * prefill): tokens are bucketed per expert and each expert runs as a grouped
+ * GEMM.
+ */
+ds4moe_status ds4moe_ffn_prefill(const ds4moe_layer *L, const uint16_t *x,
+                                 const int32_t *idx, const float *w, int32_t T,
+                                 int32_t k, float *out, void *ws, size_t ws_bytes,
+                                 void *stream);
+
+/*
+ * ds4moe_stream_status -- synchronizes `stream`, then reads and clears the
+ * device status word of `ws`.  Returns DS4MOE_OK, the recorded device error
+ * (DS4MOE_EDEVICE, DS4MOE_ETIMEOUT) or DS4MOE_ECUDA if the stream itself
+ * failed.
+ */
+ds4moe_status ds4moe_stream_status(void *ws, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS4MOE_H */

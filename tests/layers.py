@@ -64,3 +64,27 @@ def oracle_forward(L: Layer, x_bf16: np.ndarray):
     out = oracle.moe_ffn(w.d_model, w.d_ff, w.n_expert, L.qg, L.gate, L.qu, L.up, L.qd, L.down,
                          x_bf16, idx, wt)
     return out, idx, wt, logits
+
+
+# ---------------------------------------------------------------- GPU side
+def to_device(L: Layer):
+    """Upload a host layer's block bytes (made by the oracle's packer) for
+    the CUDA path."""
+    import bit_quantized_moe_q2_gb300 as M
+    from bit_quantized_moe_q2_gb300.device import DeviceLayer
+    w = L.w
+    return DeviceLayer.from_host(w.d_model, w.d_ff, w.n_expert, M.QTYPES[w.gate.qtype], M.QTYPES[w.up.qtype],
+                                 M.QTYPES[w.down.qtype], L.gate, L.up, L.down)
+
+
+_cache = {}
+
+
+def cached_layer(w: synth.Workload, layer: int = 0):
+    """(host Layer, DeviceLayer) built once per test session."""
+    key = (w, layer)
+    if key not in _cache:
+        L = build_layer(w, layer)
+        _cache.clear()          # keep at most one full layer resident
+        _cache[key] = (L, to_device(L))
+    return _cache[key]
