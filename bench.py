@@ -1,0 +1,480 @@
+#!/usr/bin/env python
+"""Benchmark of the routed-MoE expert FFN (route + gate/up + SwiGLU + down +
+combine) on one GB300, through the libds4moe C ABI.
+
+Workload (default): one DeepSeek-V4-Flash-shaped routed-MoE layer at decode
+batch 1 -- d_model 4096, d_ff 2048, 256 experts, top-6 with a softmax over
+the selected, gate/up/down all Q2_K, synthetic seeded weights and tokens.
+A step is one pass of the whole path over one token.  Weights are
+replicated into 8 device copies and tokens come from 16 pre-staged slots;
+step i uses copy i % 8 and slot i % 16, so consecutive steps never re-read
+bytes still resident in L2 (8 copies x 2.1 GB >> 129 MB of L2).
+
+Printed JSON line: tokens/s (value), weight-stream GB/s and its fraction of
+the measured HBM peak, the dominant kernel's roofline (gate/up GEMV, timed
+with CUDA events on its launch stream), the CPU oracle as a baseline, the
+end-to-end number through the C ABI with host buffers, and SM clocks sampled
+during the timed region.
+
+`--impl reference` times the CPU oracle itself (the program the CUDA path is
+checked against) on the same metric, each step a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from datetime import datetime
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+N_COPIES = 8
+N_SLOTS = 16
+METRIC = "routed-MoE tokens/s"
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", type=int, default=1, help="workload id in synth.WORKLOADS (decode: 0, 1, 2)")
+    ap.add_argument("--cpu-tokens", type=int, default=0, help="tokens in the CPU-baseline sample (0: 2 x cores)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------ distribution
+def dist_env():
+    """(rank, world, local_rank) from torchrun's environment (1 process if unset)."""
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def rank_batch_offset(rank: int) -> int:
+    """Each rank draws its own tokens (weak scaling: fixed work per GPU)."""
+    return 1000 * rank
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max over ranks (the slowest rank sets the job's time)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons."""
+
+    def __init__(self, gpu_index: int, period_ms: int = 20):
+        self.cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                    "-i", str(gpu_index), "-lms", str(period_ms)]
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = datetime.now()
+        else:
+            self.t1 = datetime.now()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                continue
+            rows.append((ts, f))
+        inside = [f for ts, f in rows if self.t0 and self.t1 and self.t0 <= ts <= self.t1]
+        use = inside if inside else [f for _, f in rows]
+        sm = [float(f[2]) for f in use if f[2].replace(".", "").isdigit()]
+        smax = [float(f[3]) for f in use if f[3].replace(".", "").isdigit()]
+        reasons = set()
+        for f in use:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), f[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(use), "samples_in_region": len(inside)}
+
+
+# --------------------------------------------------------------- workload
+def host_layer_blocks(w: synth.Workload, layer: int, experts, packer):
+    """Experts-major block bytes of the listed experts (others zero) via `packer`."""
+    out = {}
+    for t in (synth.T_GATE, synth.T_UP, synth.T_DOWN):
+        rows, cols = synth.matrix_shape(w, t)
+        q = synth.recipe(w, t)
+        per = rows * cols // (256 if q.qtype == synth.Q2_K else 32) * (84 if q.qtype == synth.Q2_K else 20)
+        buf = np.zeros(w.n_expert * per, np.uint8)
+        for e in experts:
+            buf[e * per:(e + 1) * per] = packer(synth.matrix_fields(w, layer, t, e))
+        out[t] = buf
+    return out
+
+
+def product_packer(M):
+    def pack(f):
+        if f.qtype == synth.Q4_1:
+            return M.ds4moe_quantize_ref(M.DS4MOE_Q4_1, f.bits, f.group, f.codes, f.scale, f.minv)
+        return M.ds4moe_quantize_ref(M.DS4MOE_Q2_K, 2, 256, f.codes, f.scale, f.minv, f.sc, f.mn)
+    return pack
+
+
+def device_layer(w: synth.Workload, M, torch):
+    """All experts of layer 0 packed by the library's host packer, uploaded."""
+    from bit_quantized_moe_q2_gb300.device import DeviceLayer
+    qid = {synth.Q4_1: M.DS4MOE_Q4_1, synth.Q2_K: M.DS4MOE_Q2_K}
+    dev = DeviceLayer.empty(w.d_model, w.d_ff, w.n_expert, qid[w.gate.qtype], qid[w.up.qtype], qid[w.down.qtype])
+    pack = product_packer(M)
+    names = {synth.T_GATE: "gate", synth.T_UP: "up", synth.T_DOWN: "down"}
+    pinned = {}
+    for e in range(w.n_expert):
+        blocks = {name: pack(synth.matrix_fields(w, 0, t, e)) for t, name in names.items()}
+        torch.cuda.current_stream().synchronize()      # previous expert's copies are done
+        for name, b in blocks.items():
+            if name not in pinned:
+                pinned[name] = torch.empty(b.size, dtype=torch.uint8).pin_memory()
+            pinned[name].numpy()[:] = b
+            dev.expert_slice(name, e).copy_(pinned[name], non_blocking=True)
+    torch.cuda.synchronize()
+    return dev
+
+
+def expert_bytes(w: synth.Workload) -> int:
+    tot = 0
+    for t in (synth.T_GATE, synth.T_UP, synth.T_DOWN):
+        rows, cols = synth.matrix_shape(w, t)
+        q = synth.recipe(w, t)
+        tot += rows * cols // (256 if q.qtype == synth.Q2_K else 32) * (84 if q.qtype == synth.Q2_K else 20)
+    return tot
+
+
+def gate_up_bytes(w: synth.Workload) -> int:
+    tot = 0
+    for t in (synth.T_GATE, synth.T_UP):
+        rows, cols = synth.matrix_shape(w, t)
+        q = synth.recipe(w, t)
+        tot += rows * cols // (256 if q.qtype == synth.Q2_K else 32) * (84 if q.qtype == synth.Q2_K else 20)
+    return tot
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def cores_available() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------ CPU oracle
+def cpu_baseline(w: synth.Workload, n_tokens: int, batch0: int) -> dict:
+    """The oracle (plain C, fp64) on a bounded sample of tokens, all host cores."""
+    import oracle
+    cores = cores_available()
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    Wr, bias = synth.router(w)
+    x = synth.activations(w, T=n_tokens, batch=batch0)
+    idx, wt, _ = oracle.route(x, Wr, bias, w.k)
+    blocks = host_layer_blocks(w, 0, sorted(set(idx.ravel().tolist())), oracle.pack_fields)
+    qg, qu, qd = (oracle.QTYPES[w.gate.qtype], oracle.QTYPES[w.up.qtype], oracle.QTYPES[w.down.qtype])
+    t0 = time.perf_counter()
+    idx, wt, _ = oracle.route(x, Wr, bias, w.k)
+    oracle.moe_ffn(w.d_model, w.d_ff, w.n_expert, qg, blocks[synth.T_GATE], qu, blocks[synth.T_UP], qd,
+                   blocks[synth.T_DOWN], x, idx, wt)
+    dt = time.perf_counter() - t0
+    return {"value": n_tokens / dt, "unit": "tokens/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"{n_tokens} tokens: route + all selected expert FFNs + combine (fp64 C oracle, OpenMP over tokens)"}
+
+
+# ------------------------------------------------------- reference (oracle)
+def run_reference(args, w: synth.Workload):
+    """The CPU oracle as the reference arm: K timed steps, each a bounded
+    sample of the per-token work (rows of the selected experts' gate, up and
+    down matrices), extrapolated to tokens/s by weight values processed."""
+    import oracle
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    cores = 1  # the row-slice sample runs on one thread
+    Wr, bias = synth.router(w)
+    n_tok = 4
+    x = synth.activations(w, T=n_tok, batch=0)
+    idx, wt, _ = oracle.route(x, Wr, bias, w.k)
+    qg, qu, qd = (oracle.QTYPES[w.gate.qtype], oracle.QTYPES[w.up.qtype], oracle.QTYPES[w.down.qtype])
+    experts = sorted(set(idx.ravel().tolist()))
+    blocks = host_layer_blocks(w, 0, experts, oracle.pack_fields)
+    D, F = w.d_model, w.d_ff
+    per_g = blocks[synth.T_GATE].size // w.n_expert
+    per_u = blocks[synth.T_UP].size // w.n_expert
+    per_d = blocks[synth.T_DOWN].size // w.n_expert
+    xs = oracle.bf16_to_f32(x).astype(np.float64)
+    hs = {}
+    for t in range(n_tok):
+        for i in range(w.k):
+            e = int(idx[t, i])
+            _, h, _, _ = oracle.expert_ffn(D, F, qg, blocks[synth.T_GATE], qu, blocks[synth.T_UP], qd,
+                                           blocks[synth.T_DOWN], e, x[t])
+            hs[(t, i)] = oracle.bf16_to_f32(h).astype(np.float64)
+    values_per_token = w.k * 3 * D * F
+    # size the per-step sample so that warmup + steps take ~100 s
+    budget = 100.0 / max(args.steps + args.warmup, 1)
+    t0 = time.perf_counter()
+    oracle.matvec_rows(qg, blocks[synth.T_GATE][idx[0, 0] * per_g:(idx[0, 0] + 1) * per_g], F, D, 0, 8, xs[0])
+    t_row = (time.perf_counter() - t0) / 8          # one gate row (D values)
+    R = int(max(1, min(F // 2, budget / (4 * t_row))))
+
+    def step(s):
+        t, i = (s // w.k) % n_tok, s % w.k
+        e = int(idx[t, i])
+        r0 = (s * R) % (F - R + 1)
+        oracle.matvec_rows(qg, blocks[synth.T_GATE][e * per_g:(e + 1) * per_g], F, D, r0, R, xs[t])
+        oracle.matvec_rows(qu, blocks[synth.T_UP][e * per_u:(e + 1) * per_u], F, D, r0, R, xs[t])
+        d0 = (s * 2 * R) % (D - 2 * R + 1)
+        oracle.matvec_rows(qd, blocks[synth.T_DOWN][e * per_d:(e + 1) * per_d], D, F, d0, 2 * R, hs[(t, i)])
+        return 2 * R * D + 2 * R * F
+
+    for s in range(args.warmup):
+        step(s)
+    done = 0
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        done += step(s)
+    dt = time.perf_counter() - t0
+    tokens = done / values_per_token
+    value = tokens / dt if dt > 0 else 0.0
+    sample = (f"per step {R} rows of gate, {R} of up and {2 * R} of down of one selected expert "
+              f"(fp64 C oracle, one thread); tokens/s extrapolated at {values_per_token} weight values "
+              f"per token (router < 1% of the work, not sampled)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / max(args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w: synth.Workload) -> dict:
+    return {"workload": w.name, "d_model": w.d_model, "d_ff": w.d_ff, "n_expert": w.n_expert, "top_k": w.k,
+            "tokens_per_step": w.T, "gate": w.gate.qtype, "up": w.up.qtype, "down": w.down.qtype,
+            "seed": w.seed, "l2": f"{N_COPIES} device copies of the layer x {N_SLOTS} token slots rotate per step: "
+                                  "no step re-reads bytes an earlier step left in L2"}
+
+
+# --------------------------------------------------------------- our arm
+def run_ours(args, w: synth.Workload):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    from bit_quantized_moe_q2_gb300 import _build
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier(world)
+    import bit_quantized_moe_q2_gb300 as M
+    from bit_quantized_moe_q2_gb300.device import check_status, workspace
+
+    dev = device_layer(w, M, torch)
+    copies = [dev] + [type(dev)(dev.d_model, dev.d_ff, dev.n_expert, dev.q_gate, dev.q_up, dev.q_down,
+                                dev.gate.clone(), dev.up.clone(), dev.down.clone()) for _ in range(N_COPIES - 1)]
+    Wr, bias = synth.router(w)
+    Wr_d = torch.from_numpy(Wr).cuda()
+    b_d = None if bias is None else torch.from_numpy(bias).cuda()
+    T, k, D = w.T, w.k, w.d_model
+    xs_host = [synth.activations(w, T=T, batch=rank_batch_offset(rank) + s) for s in range(N_SLOTS)]
+    xs = [torch.from_numpy(x.view(np.int16)).cuda() for x in xs_host]
+    idx = [torch.empty((T, k), dtype=torch.int32, device="cuda") for _ in range(N_SLOTS)]
+    wt = [torch.empty((T, k), dtype=torch.float32, device="cuda") for _ in range(N_SLOTS)]
+    out = [torch.empty((T, D), dtype=torch.float32, device="cuda") for _ in range(N_SLOTS)]
+    ws = workspace(dev, T, k)
+    stream = torch.cuda.Stream()
+
+    def step(i, s=None):
+        j = i % N_SLOTS
+        c = copies[i % N_COPIES]
+        M.ds4moe_route_topk(xs[j], Wr_d, b_d, k, idx[j], wt[j], None, ws, s)
+        M.ds4moe_ffn_decode(c.abi, xs[j], idx[j], wt[j], out[j], ws, s)
+
+    with torch.cuda.stream(stream):
+        for i in range(2 * N_SLOTS):
+            step(i)
+    check_status(ws, stream)
+    # per-slot unique experts (algorithmic bytes)
+    uniq = [len(set(idx[j].cpu().numpy().ravel().tolist())) for j in range(N_SLOTS)]
+
+    # one CUDA graph per step position (slot j uses copy j % N_COPIES)
+    graphs = []
+    for j in range(N_SLOTS):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(j)
+        graphs.append(g)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % N_SLOTS].replay()
+    stream.synchronize()
+    check_status(ws, stream)
+
+    # ---- timed region: exactly K steps
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.mark(True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            graphs[i % N_SLOTS].replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    barrier(world)
+    clocks = sampler.stop()
+    ms = reduce_max(ev0.elapsed_time(ev1), world)
+    check_status(ws, stream)
+
+    tokens = world * args.steps * T
+    value = tokens / (ms / 1000.0)
+    ms_per_step = ms / args.steps
+    eb = expert_bytes(w)
+    algo_step = [u * eb + Wr.nbytes + (0 if bias is None else bias.nbytes) + T * D * 2 + T * D * 4 for u in uniq]
+    algo_bytes = sum(algo_step[i % N_SLOTS] for i in range(args.steps))
+    stream_gbs = algo_bytes / (ms / 1000.0) / 1e9 / 1.0 * 1.0
+    peak, peak_kind = measured_peaks()
+
+    # ---- per-kernel roofline: same steps, eager ABI calls with the library's
+    # event profiling on (CUDA events on the launch stream around each kernel)
+    kp = min(args.steps, 2000)
+    M.ds4moe_profile_enable(True)
+    with torch.cuda.stream(stream):
+        for i in range(kp):
+            step(i, stream)
+    stream.synchronize()
+    prof = M.ds4moe_profile_read()
+    M.ds4moe_profile_enable(False)
+    launches_per_step = sum(n for _, n in prof.values()) / kp
+    gu_ms, gu_n = prof.get("gate_up", (float("nan"), 1))
+    gu_algo = sum(uniq[i % N_SLOTS] * gate_up_bytes(w) + T * D * 2 + T * k * w.d_ff * 2 for i in range(kp)) / kp
+    gu_avg_s = gu_ms / gu_n / 1000.0
+    roofline = {"kernel": "gate_up (fused dequant GEMV + SwiGLU)", "bound": "hbm",
+                "achieved": gu_algo / gu_avg_s / 1e9, "peak": peak, "unit": "GB/s",
+                "frac": gu_algo / gu_avg_s / 1e9 / peak, "traffic": None,
+                "algorithmic_bytes_per_launch": int(gu_algo), "avg_launch_us": gu_avg_s * 1e6,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else
+                               "fallback 6.8 TB/s"}
+    kernels = {n: {"avg_us": 1000 * t / c, "launches_per_step": c / kp} for n, (t, c) in prof.items()}
+
+    # ---- end to end through the C ABI with host buffers
+    ke = min(args.steps, 2000)
+    xh = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs_host]
+    oh = torch.empty((T, D), dtype=torch.float32).pin_memory()
+    x_in = torch.empty((T, D), dtype=torch.int16, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(ke):
+            x_in.copy_(xh[i % N_SLOTS], non_blocking=True)
+            c = copies[i % N_COPIES]
+            M.ds4moe_route_topk(x_in, Wr_d, b_d, k, idx[0], wt[0], None, ws, stream)
+            M.ds4moe_ffn_decode(c.abi, x_in, idx[0], wt[0], out[0], ws, stream)
+            oh.copy_(out[0], non_blocking=True)
+            stream.synchronize()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world)
+    e2e = {"value": world * ke * T / (e2e_ms / 1000.0), "unit": "tokens/s", "steps": ke,
+           "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 4,
+           "path": "pinned H2D x, ds4moe_route_topk + ds4moe_ffn_decode (eager), D2H out, stream sync per step"}
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        n = args.cpu_tokens or 2 * cores_available()
+        cpu = cpu_baseline(w, n, batch0=50_000)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 accumulate over exact 2-bit codes and bf16 activations",
+            "data": "synthetic", "config": workload_config(w),
+            "weight_stream_gbs": stream_gbs, "hbm_frac": stream_gbs / peak,
+            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(round(launches_per_step * args.steps)), "clocks": clocks}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    w = synth.WORKLOADS[args.workload]
+    if w.path != "decode":
+        raise SystemExit("bench.py times the decode workloads (0, 1, 2)")
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

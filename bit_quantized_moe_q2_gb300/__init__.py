@@ -25,6 +25,7 @@ EXPORTS = (
     "ds4moe_block_values", "ds4moe_block_bytes", "ds4moe_status_string", "ds4moe_quantize_ref",
     "ds4moe_dequant", "ds4moe_workspace_bytes", "ds4moe_workspace_init", "ds4moe_route_topk",
     "ds4moe_ffn_decode", "ds4moe_ffn_prefill", "ds4moe_stream_status",
+    "ds4moe_profile_enable", "ds4moe_profile_count", "ds4moe_profile_entry",
 )
 
 
@@ -67,6 +68,10 @@ def lib():
         L.ds4moe_ffn_decode.argtypes = [ctypes.POINTER(Layer), p, p, p, i32, i32, p, p, sz, p]
         L.ds4moe_ffn_prefill.argtypes = [ctypes.POINTER(Layer), p, p, p, i32, i32, p, p, sz, p]
         L.ds4moe_stream_status.argtypes = [p, p]
+        L.ds4moe_profile_enable.argtypes = [i32]
+        L.ds4moe_profile_count.argtypes = []
+        L.ds4moe_profile_entry.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_int64)]
         for name in EXPORTS:
             if name not in ("ds4moe_block_values", "ds4moe_block_bytes", "ds4moe_status_string",
                             "ds4moe_workspace_bytes"):
@@ -164,6 +169,21 @@ def ds4moe_ffn_prefill(layer: Layer, x, idx, w, out, ws, stream=None):
     _check(lib().ds4moe_ffn_prefill(ctypes.byref(layer), _ptr(x), _ptr(idx), _ptr(w), T, k, _ptr(out),
                                     _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "ds4moe_ffn_prefill")
+
+
+def ds4moe_profile_enable(on: bool):
+    _check(lib().ds4moe_profile_enable(int(bool(on))), "ds4moe_profile_enable")
+
+
+def ds4moe_profile_read() -> dict:
+    """{kernel name: (total_ms, launches)} since the last ds4moe_profile_enable."""
+    L = lib()
+    out = {}
+    for i in range(L.ds4moe_profile_count()):
+        name, ms, n = ctypes.c_char_p(), ctypes.c_double(), ctypes.c_int64()
+        _check(L.ds4moe_profile_entry(i, ctypes.byref(name), ctypes.byref(ms), ctypes.byref(n)), "ds4moe_profile_entry")
+        out[name.value.decode()] = (ms.value, n.value)
+    return out
 
 
 def ds4moe_stream_status(ws, stream=None) -> int:

@@ -346,9 +346,12 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
     cudaFuncSetAttribute(k_bucket, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
     attr_set = true;
   }
-  k_bucket<<<1, 1024, smem, s>>>(idx, P, E, a.hdr, ws_ptr<int32_t>(ws, lay.counts), ws_ptr<int32_t>(ws, lay.offs),
-                                 ws_ptr<int32_t>(ws, lay.active), ws_ptr<int32_t>(ws, lay.perm),
-                                 ws_ptr<int32_t>(ws, lay.inv), ws_ptr<int32_t>(ws, lay.lrank));
+  {
+    ProfScope prof("bucket", s);
+    k_bucket<<<1, 1024, smem, s>>>(idx, P, E, a.hdr, ws_ptr<int32_t>(ws, lay.counts), ws_ptr<int32_t>(ws, lay.offs),
+                                   ws_ptr<int32_t>(ws, lay.active), ws_ptr<int32_t>(ws, lay.perm),
+                                   ws_ptr<int32_t>(ws, lay.inv), ws_ptr<int32_t>(ws, lay.lrank));
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_status(e);
   e = prefill ? launch_ffn_prefill(a, s) : launch_ffn_decode(a, s);
@@ -392,6 +395,7 @@ ds4moe_status ds4moe_dequant(int32_t qtype, const void *blocks, int64_t n_values
   const int threads = 256;
   const int64_t want = (work + threads - 1) / threads;
   const int grid = (int)(want < (int64_t)num_sms() * 32 ? want : (int64_t)num_sms() * 32);
+  ProfScope prof("dequant", s);
   if (qtype == DS4MOE_Q4_1)
     k_dequant_q41<<<grid, threads, 0, s>>>(static_cast<const uint8_t *>(blocks), nb, out);
   else
@@ -432,10 +436,16 @@ ds4moe_status ds4moe_route_topk(const uint16_t *x, const float *Wr, const float 
   float *lg = logits ? logits : ws_ptr<float>(ws, lay.logits);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t warps = (int64_t)T * n_expert;
-  k_router_logits<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(x, Wr, bias, T, d_model, n_expert, lg);
+  {
+    ProfScope prof("router_logits", s);
+    k_router_logits<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(x, Wr, bias, T, d_model, n_expert, lg);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_status(e);
-  k_topk_softmax<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(lg, T, n_expert, k, idx, w);
+  {
+    ProfScope prof("topk_softmax", s);
+    k_topk_softmax<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(lg, T, n_expert, k, idx, w);
+  }
   return cuda_status(cudaGetLastError());
 }
 

@@ -157,17 +157,26 @@ __global__ void k_combine(FfnArgs a) {
 
 cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s) {
   const int grid = num_sms() * 8;
-  k_gate_up_simt<<<grid, 256, 0, s>>>(a);
+  {
+    ProfScope p("gate_up", s);
+    k_gate_up_simt<<<grid, 256, 0, s>>>(a);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_down_simt<<<grid, 256, 0, s>>>(a);
+  {
+    ProfScope p("down", s);
+    k_down_simt<<<grid, 256, 0, s>>>(a);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s) {
   const int64_t n4 = (int64_t)a.T * a.L.d_model / 4;
   const int grid = (int)((n4 + 255) / 256 < num_sms() * 16 ? (n4 + 255) / 256 : num_sms() * 16);
-  k_combine<<<grid, 256, 0, s>>>(a);
+  {
+    ProfScope p("combine", s);
+    k_combine<<<grid, 256, 0, s>>>(a);
+  }
   return cudaGetLastError();
 }
 

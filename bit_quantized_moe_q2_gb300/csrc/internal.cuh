@@ -99,4 +99,19 @@ cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s);
 
 int num_sms();
 
+// Brackets one kernel launch with CUDA events while profiling is enabled
+// (ds4moe_profile_enable); a no-op otherwise and during stream capture.
+class ProfScope {
+ public:
+  ProfScope(const char *name, cudaStream_t s);
+  ~ProfScope();
+  ProfScope(const ProfScope &) = delete;
+  ProfScope &operator=(const ProfScope &) = delete;
+
+ private:
+  const char *name_;
+  cudaStream_t s_;
+  cudaEvent_t a_ = nullptr, b_ = nullptr;
+};
+
 }  // namespace ds4

@@ -204,6 +204,21 @@ ds4moe_status ds4moe_ffn_prefill(const ds4moe_layer *L, const uint16_t *x,
  */
 ds4moe_status ds4moe_stream_status(void *ws, void *stream);
 
+/*
+ * Per-kernel timing (tracing aid).  ds4moe_profile_enable(1) clears the
+ * totals and, until ds4moe_profile_enable(0), brackets every kernel the
+ * library launches with a pair of CUDA events recorded on the launch stream
+ * (skipped while that stream is being captured into a CUDA graph).
+ * ds4moe_profile_count() synchronizes on the pending events and returns the
+ * number of distinct kernels seen; ds4moe_profile_entry(i, ...) returns the
+ * i-th kernel's name (static storage, valid until the next enable), total
+ * milliseconds and launch count.
+ */
+ds4moe_status ds4moe_profile_enable(int32_t on);
+int32_t ds4moe_profile_count(void);
+ds4moe_status ds4moe_profile_entry(int32_t i, const char **name, double *total_ms,
+                                   int64_t *launches);
+
 #ifdef __cplusplus
 }
 #endif

@@ -61,6 +61,7 @@ def _L():
         lib.orc_dequant.argtypes = [i32, p, i64, p]
         lib.orc_router_logits.argtypes = [p, p, p, i32, i32, i32, p]
         lib.orc_topk_softmax.argtypes = [p, i32, i32, i32, p, p]
+        lib.orc_matvec_rows.argtypes = [i32, p, i32, i32, i32, i32, p, p]
         lib.orc_expert_ffn.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, p, p, p, p, p]
         lib.orc_moe_ffn.argtypes = [i32, i32, i32, i32, p, i32, p, i32, p, p, p, p, i32, i32, p]
         _lib = lib
@@ -213,6 +214,17 @@ def route(x_bf16, Wr, bias, k: int):
 
 
 # ---------------------------------------------------------------------- FFN
+def matvec_rows(qtype, mat, rows, cols, row0, nrows, vec) -> np.ndarray:
+    """Rows [row0, row0+nrows) of W @ vec for one [rows x cols] block matrix."""
+    mat = _c(mat, np.uint8)
+    vec = _c(vec, np.float64)
+    out = np.empty(nrows, np.float64)
+    st = _L().orc_matvec_rows(qtype, mat.ctypes.data, rows, cols, row0, nrows, vec.ctypes.data, out.ctypes.data)
+    if st:
+        raise OracleError(st, "matvec_rows")
+    return out
+
+
 def expert_ffn(D, F, qg, gate, qu, up, qd, down, e, x_bf16):
     """One (token, expert): returns (y fp64 [D], h bf16 [F], g fp64 [F], u fp64 [F])."""
     x = _c(x_bf16, np.uint16)

@@ -327,16 +327,24 @@ static int64_t row_bytes(int qtype, int cols) {
   return (int64_t)cols / orc_block_values(qtype) * orc_block_bytes(qtype);
 }
 
-/* out[r] = sum_j W[r, j] * in[j] in double over the exact fp32 weights. */
-static void matvec(int qtype, const uint8_t *mat, int rows, int cols,
-                   const double *in, double *out, float *rowbuf) {
+/* out[r - row0] = sum_j W[r, j] * in[j] for r in [row0, row0 + nrows), in
+ * double over the exact fp32 weights (one row dequantised at a time). */
+int orc_matvec_rows(int qtype, const uint8_t *mat, int rows, int cols, int row0,
+                    int nrows, const double *in, double *out) {
+  if (!orc_block_values(qtype)) return ORC_EUNSUPPORTED;
+  if (cols <= 0 || cols % orc_block_values(qtype) || row0 < 0 || nrows < 0 ||
+      row0 + nrows > rows)
+    return ORC_EINVAL;
   int64_t rb = row_bytes(qtype, cols);
-  for (int r = 0; r < rows; ++r) {
+  float *rowbuf = (float *)malloc(sizeof(float) * (size_t)cols);
+  for (int r = row0; r < row0 + nrows; ++r) {
     orc_dequant(qtype, mat + (int64_t)r * rb, cols, rowbuf);
     double acc = 0.0;
     for (int j = 0; j < cols; ++j) acc += (double)rowbuf[j] * in[j];
-    out[r] = acc;
+    out[r - row0] = acc;
   }
+  free(rowbuf);
+  return ORC_OK;
 }
 
 /* One (token, expert) pair: g = Wg x, u = Wu x, h = bf16(silu(g) * u) with
@@ -354,10 +362,9 @@ int orc_expert_ffn(int D, int F, int qg, const uint8_t *gate, int qu,
   double *g = (double *)malloc(sizeof(double) * (size_t)F);
   double *u = (double *)malloc(sizeof(double) * (size_t)F);
   double *h = (double *)malloc(sizeof(double) * (size_t)F);
-  float *rowbuf = (float *)malloc(sizeof(float) * (size_t)(D > F ? D : F));
   for (int j = 0; j < D; ++j) xin[j] = orc_bf16(x[j]);
-  matvec(qg, gate + (int64_t)e * F * row_bytes(qg, D), F, D, xin, g, rowbuf);
-  matvec(qu, up + (int64_t)e * F * row_bytes(qu, D), F, D, xin, u, rowbuf);
+  orc_matvec_rows(qg, gate + (int64_t)e * F * row_bytes(qg, D), F, D, 0, F, xin, g);
+  orc_matvec_rows(qu, up + (int64_t)e * F * row_bytes(qu, D), F, D, 0, F, xin, u);
   for (int r = 0; r < F; ++r) {
     double silu = g[r] / (1.0 + exp(-g[r]));
     uint16_t hb = orc_round_bf16(silu * u[r]);
@@ -366,8 +373,8 @@ int orc_expert_ffn(int D, int F, int qg, const uint8_t *gate, int qu,
   }
   if (g_out) memcpy(g_out, g, sizeof(double) * (size_t)F);
   if (u_out) memcpy(u_out, u, sizeof(double) * (size_t)F);
-  matvec(qd, down + (int64_t)e * D * row_bytes(qd, F), D, F, h, y, rowbuf);
-  free(xin); free(g); free(u); free(h); free(rowbuf);
+  orc_matvec_rows(qd, down + (int64_t)e * D * row_bytes(qd, F), D, F, 0, D, h, y);
+  free(xin); free(g); free(u); free(h);
   return ORC_OK;
 }
 
