@@ -5,6 +5,7 @@
 // ffn_prefill.cu.
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "internal.cuh"
 
@@ -478,3 +479,73 @@ ds4moe_status ds4moe_stream_status(void *ws, void *stream) {
 }
 
 }  // extern "C"
+
+// ======================================================= allocation-free
+// ds4moe_ffn_decode_noalloc: the decode FFN for callers that cannot allocate
+// device memory themselves (see include/ds4moe.h).  Its scratch is this
+// file-scope device array instead of a caller-provided workspace.  Host code
+// must not pass the array's name to a kernel: on the host it is only a
+// stand-in for the device symbol, so the device address is looked up once
+// per device with cudaGetSymbolAddress and cached.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 4u << 20;  // DS4MOE_NOALLOC_SCRATCH_BYTES
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kMaxDevices] = {};
+
+ds4moe_status noalloc_scratch(void **out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= kMaxDevices) return DS4MOE_ECUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (!p) return DS4MOE_ECUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return DS4MOE_OK;
+}
+
+}  // namespace
+
+extern "C" ds4moe_status ds4moe_ffn_decode_noalloc(const ds4moe_layer *L, const uint16_t *x,
+                                                   const int32_t *idx, const float *w, int32_t T,
+                                                   int32_t k, float *out, int32_t *status_out,
+                                                   void *stream) {
+  ds4moe_status st = check_layer(L);
+  if (st != DS4MOE_OK) return st;
+  if (T < 0 || k < 1 || k > 32 || k > L->n_expert) return DS4MOE_EINVAL;
+  if (T == 0) return DS4MOE_OK;
+  const size_t need = ws_layout(*L, T, k, 0).total;
+  if (need > kNoAllocScratchBytes) {
+    fprintf(stderr,
+            "ds4moe_ffn_decode_noalloc: T=%d k=%d d_model=%d d_ff=%d n_expert=%d needs %zu bytes of "
+            "scratch, above the fixed %zu-byte array; use ds4moe_ffn_decode with a workspace\n",
+            T, k, L->d_model, L->d_ff, L->n_expert, need, kNoAllocScratchBytes);
+    return DS4MOE_ESPACE;
+  }
+  void *scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != DS4MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's bytes: the status word and counters
+  // in its header must start at zero; every other region is written before
+  // it is read within a call
+  cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(WsHeader), s);
+  if (e != cudaSuccess) return cuda_status(e);
+  st = run_ffn(false, L, x, idx, w, T, k, out, scratch, kNoAllocScratchBytes, stream);
+  if (st != DS4MOE_OK) return st;
+  if (status_out) {
+    e = cudaMemcpyAsync(status_out, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return DS4MOE_OK;
+}
+

@@ -205,6 +205,43 @@ ds4moe_status ds4moe_ffn_prefill(const ds4moe_layer *L, const uint16_t *x,
 ds4moe_status ds4moe_stream_status(void *ws, void *stream);
 
 /*
+ * ds4moe_ffn_decode_noalloc -- DEVICE.  The same computation and arguments
+ * as ds4moe_ffn_decode, for callers that cannot allocate device memory or
+ * hand the library a workspace: an application whose memory is owned by a
+ * host framework's own pool or arena (an allocation behind its back breaks
+ * its accounting and out-of-memory handling), a per-token decode loop that
+ * cannot afford cudaMalloc's implicit device synchronisation and unbounded
+ * latency, or a fixed plug-in interface with no place to pass a workspace
+ * pointer.  (The paper has no counterpart; this is a property of this
+ * library's interface only.)
+ *
+ * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.  Its scratch is one fixed device array of
+ * DS4MOE_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library, which every GPU
+ * that loads the library holds until the process exits.  A call whose
+ * sizes need more scratch than that (ds4moe_workspace_bytes(L, T, k, 0) >
+ * DS4MOE_NOALLOC_SCRATCH_BYTES; e.g. the 4096 x 2048, 256-expert, top-6
+ * shape fits up to 16 tokens) returns DS4MOE_ESPACE, prints why on stderr
+ * and launches nothing.
+ *
+ * All calls on a device share that one array and it keeps the previous
+ * call's contents; each call clears the part that must start at zero.
+ * Calls whose work can overlap on the GPU (different streams, or different
+ * host threads without ordering) race on the array: order them on one
+ * stream.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture.
+ *
+ * status_out: optional device int32; receives this call's device status
+ * (0 or DS4MOE_EDEVICE for an expert id out of range), asynchronously.
+ */
+#define DS4MOE_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+ds4moe_status ds4moe_ffn_decode_noalloc(const ds4moe_layer *L, const uint16_t *x,
+                                        const int32_t *idx, const float *w, int32_t T,
+                                        int32_t k, float *out, int32_t *status_out,
+                                        void *stream);
+
+/*
  * Per-kernel timing (tracing aid).  ds4moe_profile_enable(1) clears the
  * totals and, until ds4moe_profile_enable(0), brackets every kernel the
  * library launches with a pair of CUDA events recorded on the launch stream
