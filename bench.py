@@ -54,6 +54,10 @@ def parse_args(argv=None):
     ap.add_argument("--workload", type=int, default=1, help="workload id in synth.WORKLOADS (decode: 0, 1, 2)")
     ap.add_argument("--cpu-tokens", type=int, default=0, help="tokens in the CPU-baseline sample (0: 2 x cores)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--copies", type=int, default=N_COPIES,
+                    help="device copies of the layer rotated across steps (profiling runs use 1)")
+    ap.add_argument("--timed-only", action="store_true",
+                    help="skip the per-kernel, end-to-end and CPU passes (for profiler captures)")
     return ap.parse_args(argv)
 
 
@@ -305,10 +309,10 @@ def run_reference(args, w: synth.Workload):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(w: synth.Workload) -> dict:
+def workload_config(w: synth.Workload, n_copies: int = N_COPIES) -> dict:
     return {"workload": w.name, "d_model": w.d_model, "d_ff": w.d_ff, "n_expert": w.n_expert, "top_k": w.k,
             "tokens_per_step": w.T, "gate": w.gate.qtype, "up": w.up.qtype, "down": w.down.qtype,
-            "seed": w.seed, "l2": f"{N_COPIES} device copies of the layer x {N_SLOTS} token slots rotate per step: "
+            "seed": w.seed, "l2": f"{n_copies} device copies of the layer x {N_SLOTS} token slots rotate per step: "
                                   "no step re-reads bytes an earlier step left in L2"}
 
 
@@ -330,8 +334,9 @@ def run_ours(args, w: synth.Workload):
     from bit_quantized_moe_q2_gb300.device import check_status, workspace
 
     dev = device_layer(w, M, torch)
+    n_copies = max(1, args.copies)
     copies = [dev] + [type(dev)(dev.d_model, dev.d_ff, dev.n_expert, dev.q_gate, dev.q_up, dev.q_down,
-                                dev.gate.clone(), dev.up.clone(), dev.down.clone()) for _ in range(N_COPIES - 1)]
+                                dev.gate.clone(), dev.up.clone(), dev.down.clone()) for _ in range(n_copies - 1)]
     Wr, bias = synth.router(w)
     Wr_d = torch.from_numpy(Wr).cuda()
     b_d = None if bias is None else torch.from_numpy(bias).cuda()
@@ -346,7 +351,7 @@ def run_ours(args, w: synth.Workload):
 
     def step(i, s=None):
         j = i % N_SLOTS
-        c = copies[i % N_COPIES]
+        c = copies[i % n_copies]
         M.ds4moe_route_topk(xs[j], Wr_d, b_d, k, idx[j], wt[j], None, ws, s)
         M.ds4moe_ffn_decode(c.abi, xs[j], idx[j], wt[j], out[j], ws, s)
 
@@ -401,6 +406,12 @@ def run_ours(args, w: synth.Workload):
     stream_gbs = algo_bytes / (ms / 1000.0) / 1e9 / 1.0 * 1.0
     peak, peak_kind = measured_peaks()
 
+    if args.timed_only:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": world * args.steps * T / (ms / 1000.0), "unit": "tokens/s",
+                              "ms_per_step": ms / args.steps, "steps": args.steps, "note": "timed-only run"}),
+                  flush=True)
+        return
     # ---- per-kernel roofline: same steps, eager ABI calls with the library's
     # event profiling on (CUDA events on the launch stream around each kernel)
     kp = min(args.steps, 2000)
@@ -434,7 +445,7 @@ def run_ours(args, w: synth.Workload):
     with torch.cuda.stream(stream):
         for i in range(ke):
             x_in.copy_(xh[i % N_SLOTS], non_blocking=True)
-            c = copies[i % N_COPIES]
+            c = copies[i % n_copies]
             M.ds4moe_route_topk(x_in, Wr_d, b_d, k, idx[0], wt[0], None, ws, stream)
             M.ds4moe_ffn_decode(c.abi, x_in, idx[0], wt[0], out[0], ws, stream)
             oh.copy_(out[0], non_blocking=True)
@@ -455,7 +466,7 @@ def run_ours(args, w: synth.Workload):
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 accumulate over exact 2-bit codes and bf16 activations",
-            "data": "synthetic", "config": workload_config(w),
+            "data": "synthetic", "config": workload_config(w, n_copies),
             "weight_stream_gbs": stream_gbs, "hbm_frac": stream_gbs / peak,
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(round(launches_per_step * args.steps)), "clocks": clocks}
