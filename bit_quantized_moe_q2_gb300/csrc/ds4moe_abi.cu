@@ -141,14 +141,60 @@ __device__ __forceinline__ bool ranks_before(float va, int a, float vb, int b) {
   return a < b;
 }
 
-// One warp per token: k rounds of a warp arg-max, then a softmax over the k
-// selected logits in double, summed in rank order.
+// Top-k + softmax of one token's E <= 256 logits held in registers by one
+// warp (entry lane + 32 j in v[j]); shared by the fused router and the
+// stand-alone top-k kernel.
+__device__ __forceinline__ void topk_softmax_warp(const float (&v)[8], int E, int k, int32_t *__restrict__ idx,
+                                                  float *__restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  uint32_t taken = 0;
+  float my_v = 0.f;
+  int my_e = -1;
+  for (int i = 0; i < k; ++i) {
+    float bv = 0.f;
+    int be = -1;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && !(taken & (1u << j)) && ranks_before(v[j], e, bv, be)) {
+        bv = v[j];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (ranks_before(ov, oe, bv, be)) { bv = ov; be = oe; }
+    }
+    if (be >= 0 && (be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == i) { my_v = bv; my_e = be; }
+  }
+  const double m = (double)__shfl_sync(0xffffffffu, my_v, 0);
+  const double ex = lane < k ? exp((double)my_v - m) : 0.0;
+  double sum = 0.0;
+  for (int i = 0; i < k; ++i) sum += __shfl_sync(0xffffffffu, ex, i);
+  if (lane < k) {
+    idx[lane] = my_e;
+    w[lane] = (float)(ex / sum);
+  }
+}
+
+// One warp per token: top-k + softmax over logits already in memory
+// (E <= 256 in registers; larger E re-reads its row each round).
 __global__ void k_topk_softmax(const float *__restrict__ logits, int T, int E, int k,
                                int32_t *__restrict__ idx, float *__restrict__ w) {
   const int t = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   const float *l = logits + (int64_t)t * E;
+  if (E <= 256) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = lane + 32 * j < E ? l[lane + 32 * j] : 0.f;
+    topk_softmax_warp(v, E, k, idx + (int64_t)t * k, w + (int64_t)t * k);
+    return;
+  }
   uint32_t taken = 0;  // bit j: entry lane + 32 j already selected
   float my_v = 0.f;
   int my_e = -1;
@@ -179,6 +225,98 @@ __global__ void k_topk_softmax(const float *__restrict__ logits, int T, int E, i
   }
 }
 
+// Decode router (T <= 256, E <= 256, d_model <= 8192): one CTA per expert.
+// Its 256 threads hold the expert's router row in registers (NI float4 per
+// thread) and compute, for every token, a compensated (Dot2) partial over
+// their slice; partials are merged across lanes and warps with TwoSum in a
+// fixed order, the bias is added with TwoSum, and the result rounded once.
+// The last CTA to finish (ticket counter in the workspace header) runs the
+// top-k and softmax for all tokens.
+template <int NI>
+__global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict__ x, const float *__restrict__ Wr,
+                                                     const float *__restrict__ bias, int T, int D, int E, int k,
+                                                     float *__restrict__ logits, int32_t *__restrict__ idx,
+                                                     float *__restrict__ w, WsHeader *__restrict__ hdr) {
+  __shared__ float ps[8][32], pc[8][32];
+  __shared__ uint32_t ticket;
+  const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  float4 wv[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int j = 4 * (tid + 256 * i);
+    wv[i] = j < D ? *reinterpret_cast<const float4 *>(Wr + (int64_t)e * D + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int t0 = 0; t0 < T; t0 += 32) {
+    const int nt = min(32, T - t0);
+    for (int tt = 0; tt < nt; ++tt) {
+      const uint16_t *xr = x + (int64_t)(t0 + tt) * D;
+      float s = 0.f, c = 0.f;
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int j = 4 * (tid + 256 * i);
+        if (j < D) {
+          const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(xr + j));
+          const float xs[4] = {bf16_bits_to_f32(xv.x & 0xFFFFu), bf16_bits_to_f32(xv.x >> 16),
+                               bf16_bits_to_f32(xv.y & 0xFFFFu), bf16_bits_to_f32(xv.y >> 16)};
+          const float ws4[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float p, pe, se;
+            two_prod(xs[q], ws4[q], p, pe);
+            two_sum(s, p, s, se);
+            c = __fadd_rn(c, __fadd_rn(pe, se));
+          }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        const float so = __shfl_xor_sync(0xffffffffu, s, off);
+        const float co = __shfl_xor_sync(0xffffffffu, c, off);
+        float se;
+        two_sum(s, so, s, se);
+        c = __fadd_rn(c, __fadd_rn(co, se));
+      }
+      if (lane == 0) {
+        ps[wid][tt] = s;
+        pc[wid][tt] = c;
+      }
+    }
+    __syncthreads();
+    if (wid == 0 && lane < nt) {
+      float s = ps[0][lane], c = pc[0][lane];
+      for (int ww = 1; ww < 8; ++ww) {
+        float se;
+        two_sum(s, ps[ww][lane], s, se);
+        c = __fadd_rn(c, __fadd_rn(pc[ww][lane], se));
+      }
+      if (bias) {
+        float se;
+        two_sum(s, bias[e], s, se);
+        c = __fadd_rn(c, se);
+      }
+      logits[(int64_t)(t0 + lane) * E + e] = __fadd_rn(s, c);
+    }
+    __syncthreads();
+  }
+  // the last CTA to finish ranks the experts of every token
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) ticket = atomicAdd(&hdr->route_done, 1u);
+  __syncthreads();
+  if (ticket != (uint32_t)E - 1u) return;
+  __threadfence();
+  for (int t = wid; t < T; t += 8) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int ee = lane + 32 * j;
+      v[j] = ee < E ? __ldcg(logits + (int64_t)t * E + ee) : 0.f;
+    }
+    topk_softmax_warp(v, E, k, idx + (int64_t)t * k, w + (int64_t)t * k);
+  }
+  if (tid == 0) hdr->route_done = 0u;
+}
+
 // ---------------------------------------------------------------- bucketing
 // One CTA of 1024 threads.  Pairs p = t*k + i are grouped by expert, stable
 // in p (hence in token order).  Phase A: warp w walks its contiguous slice of
@@ -189,7 +327,9 @@ __global__ void __launch_bounds__(1024) k_bucket(const int32_t *__restrict__ idx
                                                  WsHeader *__restrict__ hdr, int32_t *__restrict__ counts,
                                                  int32_t *__restrict__ offs, int32_t *__restrict__ active,
                                                  int32_t *__restrict__ perm, int32_t *__restrict__ inv,
-                                                 int32_t *__restrict__ lrank) {
+                                                 int32_t *__restrict__ lrank, Group *__restrict__ groups,
+                                                 const uint16_t *__restrict__ x, int T, int D,
+                                                 uint8_t *__restrict__ xs16, float *__restrict__ xs32) {
   extern __shared__ int32_t sm[];
   int32_t *wcnt = sm;              // [32][E]
   int32_t *soff = sm + 32 * E;     // [E + 1]
@@ -275,8 +415,61 @@ __global__ void __launch_bounds__(1024) k_bucket(const int32_t *__restrict__ idx
     }
     __syncthreads();
     if (f) active[warp_tot[wid] + fi - 1] = tid;
+    __syncthreads();
+    // token groups: ceil(count / kGroup) per expert, numbered in expert order
+    const int ng = (v + kGroup - 1) / kGroup;
+    int gi = ng;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, gi, off);
+      if (lane >= off) gi += o;
+    }
+    if (lane == 31) warp_tot[wid] = gi;
+    __syncthreads();
+    if (wid == 0) {
+      int wt = warp_tot[lane], wi = wt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, wi, off);
+        if (lane >= off) wi += o;
+      }
+      warp_tot[lane] = wi - wt;
+      if (lane == 31) hdr->n_groups = wi;
+    }
+    __syncthreads();
+    if (tid < E) {
+      const int g0 = warp_tot[wid] + gi - ng;
+      for (int j = 0; j < ng; ++j) groups[g0 + j] = Group{tid, excl + kGroup * j, min(kGroup, v - kGroup * j), 0};
+    }
   }
   __syncthreads();
+  // sub-block (16-value) and block (32-value) sums of x for the tensor-core
+  // decode kernels
+  if (xs16) {
+    const int n32 = D / 32;
+    for (int i = tid; i < T * n32; i += 1024) {
+      const int t = i / n32, b32 = i % n32;
+      const uint16_t *xr = x + (int64_t)t * D + 32 * b32;
+      float s[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          a0 += bf16_bits_to_f32(xr[16 * hh + j]);
+          a1 += bf16_bits_to_f32(xr[16 * hh + 8 + j]);
+        }
+        s[hh] = a0 + a1;
+        const int n16 = 2 * b32 + hh;
+        const uint16_t hi = f32_to_bf16_bits(s[hh]);
+        const uint16_t lo = f32_to_bf16_bits(s[hh] - bf16_bits_to_f32(hi));
+        uint16_t *rec = reinterpret_cast<uint16_t *>(xs16 + ((int64_t)t * (D / 256 + 1) + n16 / 16) * 64);
+        rec[sums_slot(n16 & 15)] = hi;
+        rec[16 + sums_slot(n16 & 15)] = lo;
+      }
+      xs32[(int64_t)t * n32 + b32] = s[0] + s[1];
+    }
+  }
   // Phase C: scatter
   for (int p = tid; p < P; p += 1024) {
     const int r = lrank[p];
@@ -340,6 +533,11 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
   a.inv = ws_ptr<int32_t>(ws, lay.inv);
   a.h = ws_ptr<uint16_t>(ws, lay.h);
   a.y = ws_ptr<float>(ws, lay.y);
+  a.groups = ws_ptr<Group>(ws, lay.groups);
+  a.xs16 = ws_ptr<uint8_t>(ws, lay.xs16);
+  a.xs32 = ws_ptr<float>(ws, lay.xs32);
+  a.hs16 = ws_ptr<uint8_t>(ws, lay.hs16);
+  const bool sums = decode_mma_ok(*L);
   const int E = L->n_expert, P = T * k;
   const size_t smem = sizeof(int32_t) * (32 * (size_t)E + E + 1);
   static bool attr_set = false;
@@ -351,7 +549,10 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
     ProfScope prof("bucket", s);
     k_bucket<<<1, 1024, smem, s>>>(idx, P, E, a.hdr, ws_ptr<int32_t>(ws, lay.counts), ws_ptr<int32_t>(ws, lay.offs),
                                    ws_ptr<int32_t>(ws, lay.active), ws_ptr<int32_t>(ws, lay.perm),
-                                   ws_ptr<int32_t>(ws, lay.inv), ws_ptr<int32_t>(ws, lay.lrank));
+                                   ws_ptr<int32_t>(ws, lay.inv), ws_ptr<int32_t>(ws, lay.lrank),
+                                   ws_ptr<Group>(ws, lay.groups), x, T, L->d_model,
+                                   sums ? ws_ptr<uint8_t>(ws, lay.xs16) : nullptr,
+                                   sums ? ws_ptr<float>(ws, lay.xs32) : nullptr);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_status(e);
@@ -436,6 +637,16 @@ ds4moe_status ds4moe_route_topk(const uint16_t *x, const float *Wr, const float 
   if (ws_bytes < need) return DS4MOE_ESPACE;
   float *lg = logits ? logits : ws_ptr<float>(ws, lay.logits);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T <= 256 && n_expert <= 256 && d_model <= 8192) {
+    WsHeader *hdr = static_cast<WsHeader *>(ws);
+    ProfScope prof("route_topk", s);
+    const int ni = (d_model + 1023) / 1024;
+    if (ni <= 1) k_route_small<1><<<n_expert, 256, 0, s>>>(x, Wr, bias, T, d_model, n_expert, k, lg, idx, w, hdr);
+    else if (ni <= 2) k_route_small<2><<<n_expert, 256, 0, s>>>(x, Wr, bias, T, d_model, n_expert, k, lg, idx, w, hdr);
+    else if (ni <= 4) k_route_small<4><<<n_expert, 256, 0, s>>>(x, Wr, bias, T, d_model, n_expert, k, lg, idx, w, hdr);
+    else k_route_small<8><<<n_expert, 256, 0, s>>>(x, Wr, bias, T, d_model, n_expert, k, lg, idx, w, hdr);
+    return cuda_status(cudaGetLastError());
+  }
   const int64_t warps = (int64_t)T * n_expert;
   {
     ProfScope prof("router_logits", s);

@@ -31,12 +31,27 @@ struct WsHeader {
   uint32_t status;     // 0 or a ds4moe_status recorded by a kernel
   int32_t n_active;    // experts with >= 1 routed pair (set by bucketing)
   uint32_t route_done; // last-block counter of the fused router
-  uint32_t pad[61];
+  int32_t n_groups;    // token groups (<= kGroup pairs of one expert each)
+  uint32_t pad[60];
 };
+
+// A token group: up to kGroup consecutive expert-sorted pairs of one expert.
+constexpr int kGroup = 8;
+struct Group {
+  int32_t e, p0, nt, pad;
+};
+
+// Sub-block sums of an activation row in the order the tensor-core kernels
+// read them: per 256-value block a 64-byte record, first 16 bf16 "hi" parts
+// then 16 bf16 "lo" parts (sum ~= hi + lo); within each half, lane quad c
+// owns 8 bytes holding sub-blocks (2c, 2c+1, 2c+8, 2c+9).
+__host__ __device__ inline int sums_slot(int n) {  // bf16 index of sub-block n within a half
+  return 4 * ((n & 7) >> 1) + (n & 1) + 2 * (n >> 3);
+}
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
 struct WsLayout {
-  size_t hdr, logits, counts, offs, active, perm, inv, lrank, h, y, total;
+  size_t hdr, logits, counts, offs, active, perm, inv, lrank, groups, xs16, xs32, hs16, h, y, total;
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -53,6 +68,10 @@ inline WsLayout ws_layout(const ds4moe_layer &L, int T, int k, int /*prefill*/) 
   w.perm = o;    o += align256(sizeof(int32_t) * P);
   w.inv = o;     o += align256(sizeof(int32_t) * P);
   w.lrank = o;   o += align256(sizeof(int32_t) * P);
+  w.groups = o;  o += align256(sizeof(Group) * P);
+  w.xs16 = o;    o += align256((size_t)T * (size_t)(L.d_model / 256 + 1) * 64);
+  w.xs32 = o;    o += align256(sizeof(float) * (size_t)T * (size_t)(L.d_model / 32 + 1));
+  w.hs16 = o;    o += align256(P * (size_t)(L.d_ff / 256 + 1) * 64);
   w.h = o;       o += align256(sizeof(uint16_t) * P * (size_t)L.d_ff);
   w.y = o;       o += align256(sizeof(float) * P * (size_t)L.d_model);
   w.total = o;
@@ -89,6 +108,10 @@ struct FfnArgs {
   float *out;
   WsHeader *hdr;
   const int32_t *offs, *active, *perm, *inv;
+  const Group *groups;
+  const uint8_t *xs16;  // [T][D/256][64 B] sub-block sums of x
+  const float *xs32;    // [T][D/32] block sums of x
+  uint8_t *hs16;        // [P][F/256][64 B] sub-block sums of h
   uint16_t *h;
   float *y;
 };
@@ -96,6 +119,7 @@ struct FfnArgs {
 cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_ffn_prefill(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s);
+bool decode_mma_ok(const ds4moe_layer &L);
 
 int num_sms();
 

@@ -70,6 +70,12 @@ REDUCED = [
     synth.WORKLOADS[1].replace(d_model=768, d_ff=512, n_expert=16, k=6, T=21, seed=102),
     synth.WORKLOADS[2].replace(d_model=1024, d_ff=256, n_expert=5, k=3, T=40, seed=103),
     synth.WORKLOADS[3].replace(d_model=512, d_ff=768, n_expert=12, k=4, T=97, seed=104),
+    # shapes whose rows split into 16-byte bulk copies (tensor-core decode path)
+    synth.WORKLOADS[1].replace(d_model=1024, d_ff=1024, n_expert=12, k=4, T=37, seed=105),
+    synth.WORKLOADS[2].replace(d_model=2048, d_ff=1024, n_expert=10, k=3, T=50, seed=106),
+    synth.WORKLOADS[0].replace(d_model=2048, d_ff=1024, n_expert=6, k=2, T=19, seed=107,
+                               gate=synth.Q2K, up=synth.Q41_4BIT),
+    synth.WORKLOADS[3].replace(d_model=4096, d_ff=2048, n_expert=9, k=6, T=11, seed=108),
 ]
 
 
@@ -88,9 +94,10 @@ def test_reduced_layers_all_tokens(M, wi, prefill):
     assert rel_err(out, ref) <= TOL
 
 
-def test_one_expert_takes_every_token_and_k_1(M):
-    # n_e = T for one expert (many passes over its token list); k = 1
-    w = REDUCED[0].replace(T=45, k=1)
+@pytest.mark.parametrize("wi", [0, 4])
+def test_one_expert_takes_every_token_and_k_1(M, wi):
+    # n_e = T for one expert (many token groups); k = 1
+    w = REDUCED[wi].replace(T=45, k=1)
     L = build_layer(w)
     dev = to_device(L)
     x = synth.activations(w)
