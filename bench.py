@@ -352,8 +352,7 @@ def run_ours(args, w: synth.Workload):
     def step(i, s=None):
         j = i % N_SLOTS
         c = copies[i % n_copies]
-        M.ds4moe_route_topk(xs[j], Wr_d, b_d, k, idx[j], wt[j], None, ws, s)
-        M.ds4moe_ffn_decode(c.abi, xs[j], idx[j], wt[j], out[j], ws, s)
+        M.ds4moe_moe_decode(c.abi, xs[j], Wr_d, b_d, k, out[j], idx[j], wt[j], ws, s)
 
     with torch.cuda.stream(stream):
         for i in range(2 * N_SLOTS):
@@ -423,7 +422,7 @@ def run_ours(args, w: synth.Workload):
     prof = M.ds4moe_profile_read()
     M.ds4moe_profile_enable(False)
     launches_per_step = sum(n for _, n in prof.values()) / kp
-    gu_ms, gu_n = prof.get("gate_up", (float("nan"), 1))
+    gu_ms, gu_n = prof.get("gate_up", prof.get("gate_up_simt", (float("nan"), 1)))
     gu_algo = sum(uniq[i % N_SLOTS] * gate_up_bytes(w) + T * D * 2 + T * k * w.d_ff * 2 for i in range(kp)) / kp
     gu_avg_s = gu_ms / gu_n / 1000.0
     roofline = {"kernel": "gate_up (fused dequant GEMV + SwiGLU)", "bound": "hbm",
@@ -446,8 +445,7 @@ def run_ours(args, w: synth.Workload):
         for i in range(ke):
             x_in.copy_(xh[i % N_SLOTS], non_blocking=True)
             c = copies[i % n_copies]
-            M.ds4moe_route_topk(x_in, Wr_d, b_d, k, idx[0], wt[0], None, ws, stream)
-            M.ds4moe_ffn_decode(c.abi, x_in, idx[0], wt[0], out[0], ws, stream)
+            M.ds4moe_moe_decode(c.abi, x_in, Wr_d, b_d, k, out[0], idx[0], wt[0], ws, stream)
             oh.copy_(out[0], non_blocking=True)
             stream.synchronize()
     e1.record(stream)
@@ -455,7 +453,7 @@ def run_ours(args, w: synth.Workload):
     e2e_ms = reduce_max(e0.elapsed_time(e1), world)
     e2e = {"value": world * ke * T / (e2e_ms / 1000.0), "unit": "tokens/s", "steps": ke,
            "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 4,
-           "path": "pinned H2D x, ds4moe_route_topk + ds4moe_ffn_decode (eager), D2H out, stream sync per step"}
+           "path": "pinned H2D x, ds4moe_moe_decode (eager C-ABI call), D2H out, stream sync per step"}
 
     if rank != 0:
         return

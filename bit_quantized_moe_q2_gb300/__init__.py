@@ -26,7 +26,7 @@ EXPORTS = (
     "ds4moe_dequant", "ds4moe_workspace_bytes", "ds4moe_workspace_init", "ds4moe_route_topk",
     "ds4moe_ffn_decode", "ds4moe_ffn_prefill", "ds4moe_stream_status",
     "ds4moe_profile_enable", "ds4moe_profile_count", "ds4moe_profile_entry",
-    "ds4moe_ffn_decode_noalloc",
+    "ds4moe_ffn_decode_noalloc", "ds4moe_moe_decode",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -71,6 +71,7 @@ def lib():
         L.ds4moe_ffn_prefill.argtypes = [ctypes.POINTER(Layer), p, p, p, i32, i32, p, p, sz, p]
         L.ds4moe_stream_status.argtypes = [p, p]
         L.ds4moe_ffn_decode_noalloc.argtypes = [ctypes.POINTER(Layer), p, p, p, i32, i32, p, p, p]
+        L.ds4moe_moe_decode.argtypes = [ctypes.POINTER(Layer), p, p, p, i32, i32, p, p, p, p, sz, p]
         L.ds4moe_profile_enable.argtypes = [i32]
         L.ds4moe_profile_count.argtypes = []
         L.ds4moe_profile_entry.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
@@ -172,6 +173,14 @@ def ds4moe_ffn_prefill(layer: Layer, x, idx, w, out, ws, stream=None):
     _check(lib().ds4moe_ffn_prefill(ctypes.byref(layer), _ptr(x), _ptr(idx), _ptr(w), T, k, _ptr(out),
                                     _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "ds4moe_ffn_prefill")
+
+
+def ds4moe_moe_decode(layer: Layer, x, Wr, bias, k, out, idx, w, ws, stream=None):
+    """Route + expert FFN + combine of one decode step (writes idx, w, out)."""
+    T = x.shape[0]
+    _check(lib().ds4moe_moe_decode(ctypes.byref(layer), _ptr(x), _ptr(Wr), _ptr(bias), T, k, _ptr(out), _ptr(idx),
+                                   _ptr(w), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "ds4moe_moe_decode")
 
 
 def ds4moe_ffn_decode_noalloc(layer: Layer, x, idx, w, out, status_out=None, stream=None):

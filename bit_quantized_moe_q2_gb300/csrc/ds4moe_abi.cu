@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "internal.cuh"
+#include "ptx.cuh"
 
 using namespace ds4;
 
@@ -232,7 +233,7 @@ __global__ void k_topk_softmax(const float *__restrict__ logits, int T, int E, i
 // fixed order, the bias is added with TwoSum, and the result rounded once.
 // The last CTA to finish (ticket counter in the workspace header) runs the
 // top-k and softmax for all tokens.
-template <int NI>
+template <int NI, bool TOPK>
 __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict__ x, const float *__restrict__ Wr,
                                                      const float *__restrict__ bias, int T, int D, int E, int k,
                                                      float *__restrict__ logits, int32_t *__restrict__ idx,
@@ -240,22 +241,26 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict_
   __shared__ float ps[8][32], pc[8][32];
   __shared__ uint32_t ticket;
   const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  // the router row is constant: fetch it before waiting for x
   float4 wv[NI];
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
     const int j = 4 * (tid + 256 * i);
-    wv[i] = j < D ? *reinterpret_cast<const float4 *>(Wr + (int64_t)e * D + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    wv[i] = j < D ? __ldg(reinterpret_cast<const float4 *>(Wr + (int64_t)e * D + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
   for (int t0 = 0; t0 < T; t0 += 32) {
     const int nt = min(32, T - t0);
     for (int tt = 0; tt < nt; ++tt) {
       const uint16_t *xr = x + (int64_t)(t0 + tt) * D;
-      float s = 0.f, c = 0.f;
+      // four independent compensated chains (one per float4 component)
+      float s4[4] = {0.f, 0.f, 0.f, 0.f}, c4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < NI; ++i) {
         const int j = 4 * (tid + 256 * i);
         if (j < D) {
-          const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(xr + j));
+          const uint2 xv = __ldcg(reinterpret_cast<const uint2 *>(xr + j));
           const float xs[4] = {bf16_bits_to_f32(xv.x & 0xFFFFu), bf16_bits_to_f32(xv.x >> 16),
                                bf16_bits_to_f32(xv.y & 0xFFFFu), bf16_bits_to_f32(xv.y >> 16)};
           const float ws4[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
@@ -263,10 +268,17 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict_
           for (int q = 0; q < 4; ++q) {
             float p, pe, se;
             two_prod(xs[q], ws4[q], p, pe);
-            two_sum(s, p, s, se);
-            c = __fadd_rn(c, __fadd_rn(pe, se));
+            two_sum(s4[q], p, s4[q], se);
+            c4[q] = __fadd_rn(c4[q], __fadd_rn(pe, se));
           }
         }
+      }
+      float s = s4[0], c = __fadd_rn(c4[0], __fadd_rn(c4[1], __fadd_rn(c4[2], c4[3])));
+#pragma unroll
+      for (int q = 1; q < 4; ++q) {
+        float se;
+        two_sum(s, s4[q], s, se);
+        c = __fadd_rn(c, se);
       }
 #pragma unroll
       for (int off = 16; off; off >>= 1) {
@@ -298,6 +310,7 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict_
     }
     __syncthreads();
   }
+  if (!TOPK) return;  // ranking done by the bucketing kernel of the fused decode path
   // the last CTA to finish ranks the experts of every token
   __threadfence();
   __syncthreads();
@@ -323,19 +336,127 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict_
 // pairs 32 at a time and ranks each pair among same-expert pairs of the slice
 // (__match_any_sync); Phase B: per-expert totals, exclusive offsets and
 // per-warp bases; Phase C: scatter.  Also builds the list of active experts.
-__global__ void __launch_bounds__(1024) k_bucket(const int32_t *__restrict__ idx, int P, int E,
+__global__ void __launch_bounds__(1024) k_bucket(int32_t *__restrict__ idx, int P, int E,
                                                  WsHeader *__restrict__ hdr, int32_t *__restrict__ counts,
                                                  int32_t *__restrict__ offs, int32_t *__restrict__ active,
                                                  int32_t *__restrict__ perm, int32_t *__restrict__ inv,
                                                  int32_t *__restrict__ lrank, Group *__restrict__ groups,
                                                  const uint16_t *__restrict__ x, int T, int D,
-                                                 uint8_t *__restrict__ xs16, float *__restrict__ xs32) {
+                                                 uint16_t *__restrict__ x16, uint8_t *__restrict__ xs16,
+                                                 float *__restrict__ xs32, const float *__restrict__ logits, int k,
+                                                 float *__restrict__ w, int32_t *__restrict__ nvalid,
+                                                 float *__restrict__ out) {
   extern __shared__ int32_t sm[];
   int32_t *wcnt = sm;              // [32][E]
   int32_t *soff = sm + 32 * E;     // [E + 1]
   __shared__ int32_t warp_tot[32];
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  for (int i = tid; i < 32 * E; i += 1024) wcnt[i] = 0;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nthr = blockDim.x;
+  ptx::pdl_wait();  // idx (or the logits) and x come from the preceding grids
+  ptx::pdl_launch_dependents();
+  // fused decode path: rank the experts of every token here (E <= 256)
+  if (logits) {
+    for (int t = wid; t < T; t += nthr / 32) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int e = lane + 32 * j;
+        v[j] = e < E ? __ldcg(logits + (int64_t)t * E + e) : 0.f;
+      }
+      topk_softmax_warp(v, E, k, idx + (int64_t)t * k, w + (int64_t)t * k);
+    }
+    __syncthreads();
+  }
+  // valid experts per token (for the fused combine); a token without any
+  // gets a zero output row here
+  for (int t = tid; t < T; t += nthr) {
+    int nv = 0;
+    for (int i = 0; i < k; ++i) {
+      const int e = __ldcg(idx + (int64_t)t * k + i);
+      nv += e >= 0 && e < E;
+    }
+    nvalid[t] = nv;
+    if (nv == 0)
+      for (int c = 0; c < D; ++c) out[(int64_t)t * D + c] = 0.f;
+  }
+  // fp16 copy of x and its sub-block (16-value) / block (32-value) sums for
+  // the tensor-core decode kernels.  bf16 -> fp16 is exact for |x| in
+  // [2^-14, 65504]; larger magnitudes are flagged as a data error.
+  if (xs16) {
+    const int n32 = D / 32;
+    for (int i = tid; i < T * n32; i += nthr) {
+      const int t = i / n32, b32 = i % n32;
+      const uint4 *xr = reinterpret_cast<const uint4 *>(x + (int64_t)t * D + 32 * b32);
+      uint4 *x16r = reinterpret_cast<uint4 *>(x16 + (int64_t)t * D + 32 * b32);
+      float s[2] = {0.f, 0.f};
+      bool big = false;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = __ldcg(xr + q);
+        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float lo = bf16_bits_to_f32(wd[r] & 0xFFFFu), hi = bf16_bits_to_f32(wd[r] >> 16);
+          big |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+          o[r] = (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
+          s[q >> 1] += lo + hi;
+        }
+        x16r[q] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int n16 = 2 * b32 + hh;
+        const __half hi = __float2half_rn(s[hh]);
+        const __half lo = __float2half_rn(s[hh] - __half2float(hi));
+        uint16_t *rec = reinterpret_cast<uint16_t *>(xs16 + ((int64_t)t * (D / 256 + 1) + n16 / 16) * 64);
+        rec[n16 & 15] = __half_as_ushort(hi);
+        rec[16 + (n16 & 15)] = __half_as_ushort(lo);
+        big |= fabsf(s[hh]) > 65504.f;
+      }
+      if (big) record_status(hdr, DS4MOE_EDEVICE);
+      xs32[(int64_t)t * n32 + b32] = s[0] + s[1];
+    }
+  }
+  if (P <= 32) {
+    // small batch: one warp ranks the pairs by (expert, pair index)
+    if (wid == 0) {
+      int e = -1;
+      if (lane < P) {
+        e = __ldcg(idx + lane);
+        if (e < 0 || e >= E) { record_status(hdr, DS4MOE_EDEVICE); e = -1; }
+      }
+      const int key = e >= 0 ? e * 32 + lane : 0x7FFFFFFF;
+      int rank = 0;
+      for (int q = 0; q < 32; ++q) rank += __shfl_sync(0xffffffffu, key, q) < key;
+      const unsigned valid = __ballot_sync(0xffffffffu, e >= 0);
+      if (lane < P) inv[lane] = e >= 0 ? rank : -1;
+      if (e >= 0) perm[rank] = lane;
+      // sorted view: lane r holds the expert of the r-th pair
+      __shared__ int32_t sorted_e[32];
+      if (e >= 0) sorted_e[rank] = e;
+      __syncwarp();
+      const int nv = __popc(valid);
+      const int er = lane < nv ? sorted_e[lane] : -1;
+      const int eprev = __shfl_up_sync(0xffffffffu, er, 1);
+      const bool run_start = lane < nv && (lane == 0 || eprev != er);
+      const unsigned starts = __ballot_sync(0xffffffffu, run_start);
+      const int rs = 31 - __clz(starts & (0xffffffffu >> (31 - lane)));   // start of this lane's run
+      const bool gstart = lane < nv && ((lane - rs) % kGroup == 0);
+      const unsigned gmask = __ballot_sync(0xffffffffu, gstart);
+      if (gstart) {
+        int run_end = nv;
+        const unsigned later = starts & ~(0xffffffffu >> (31 - lane));
+        if (later) run_end = __ffs(later) - 1;
+        groups[__popc(gmask & ((1u << lane) - 1u))] = Group{er, lane, min(kGroup, run_end - lane), 0};
+      }
+      if (lane == 0) {
+        hdr->n_groups = __popc(gmask);
+        hdr->n_active = __popc(starts);
+      }
+    }
+    return;
+  }
+  for (int i = tid; i < 32 * E; i += nthr) wcnt[i] = 0;
   __syncthreads();
   const int R = (P + 31) / 32;
   const int p0 = wid * R, p1 = min(P, p0 + R);
@@ -443,33 +564,6 @@ __global__ void __launch_bounds__(1024) k_bucket(const int32_t *__restrict__ idx
     }
   }
   __syncthreads();
-  // sub-block (16-value) and block (32-value) sums of x for the tensor-core
-  // decode kernels
-  if (xs16) {
-    const int n32 = D / 32;
-    for (int i = tid; i < T * n32; i += 1024) {
-      const int t = i / n32, b32 = i % n32;
-      const uint16_t *xr = x + (int64_t)t * D + 32 * b32;
-      float s[2];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          a0 += bf16_bits_to_f32(xr[16 * hh + j]);
-          a1 += bf16_bits_to_f32(xr[16 * hh + 8 + j]);
-        }
-        s[hh] = a0 + a1;
-        const int n16 = 2 * b32 + hh;
-        const uint16_t hi = f32_to_bf16_bits(s[hh]);
-        const uint16_t lo = f32_to_bf16_bits(s[hh] - bf16_bits_to_f32(hi));
-        uint16_t *rec = reinterpret_cast<uint16_t *>(xs16 + ((int64_t)t * (D / 256 + 1) + n16 / 16) * 64);
-        rec[sums_slot(n16 & 15)] = hi;
-        rec[16 + sums_slot(n16 & 15)] = lo;
-      }
-      xs32[(int64_t)t * n32 + b32] = s[0] + s[1];
-    }
-  }
   // Phase C: scatter
   for (int p = tid; p < P; p += 1024) {
     const int r = lrank[p];
@@ -479,14 +573,6 @@ __global__ void __launch_bounds__(1024) k_bucket(const int32_t *__restrict__ idx
     const int pos = soff[e] + wcnt[wslice * E + e] + r;
     perm[pos] = p;
     inv[p] = pos;
-  }
-}
-
-__global__ void k_clear_header(WsHeader *hdr) {
-  if (threadIdx.x == 0) {
-    hdr->status = 0;
-    hdr->n_active = 0;
-    hdr->route_done = 0;
   }
 }
 
@@ -505,9 +591,11 @@ ds4moe_status check_layer(const ds4moe_layer *L) {
   return DS4MOE_OK;
 }
 
+// Bucketing, expert FFN and combine.  With `logits` (fused decode path) the
+// bucketing kernel first ranks the experts of every token and writes idx / w.
 ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, const int32_t *idx,
                       const float *w, int32_t T, int32_t k, float *out, void *ws, size_t ws_bytes,
-                      void *stream) {
+                      void *stream, const float *logits = nullptr) {
   ds4moe_status st = check_layer(L);
   if (st != DS4MOE_OK) return st;
   if (T < 0 || k < 1 || k > 32 || k > L->n_expert) return DS4MOE_EINVAL;
@@ -534,10 +622,13 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
   a.h = ws_ptr<uint16_t>(ws, lay.h);
   a.y = ws_ptr<float>(ws, lay.y);
   a.groups = ws_ptr<Group>(ws, lay.groups);
+  a.x16 = ws_ptr<uint16_t>(ws, lay.x16);
   a.xs16 = ws_ptr<uint8_t>(ws, lay.xs16);
   a.xs32 = ws_ptr<float>(ws, lay.xs32);
   a.hs16 = ws_ptr<uint8_t>(ws, lay.hs16);
+  a.nvalid = ws_ptr<int32_t>(ws, lay.nvalid);
   const bool sums = decode_mma_ok(*L);
+  a.cnt = sums ? ws_ptr<int32_t>(ws, lay.cnt) : nullptr;
   const int E = L->n_expert, P = T * k;
   const size_t smem = sizeof(int32_t) * (32 * (size_t)E + E + 1);
   static bool attr_set = false;
@@ -545,16 +636,17 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
     cudaFuncSetAttribute(k_bucket, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
     attr_set = true;
   }
+  cudaError_t e = cudaSuccess;
   {
     ProfScope prof("bucket", s);
-    k_bucket<<<1, 1024, smem, s>>>(idx, P, E, a.hdr, ws_ptr<int32_t>(ws, lay.counts), ws_ptr<int32_t>(ws, lay.offs),
-                                   ws_ptr<int32_t>(ws, lay.active), ws_ptr<int32_t>(ws, lay.perm),
-                                   ws_ptr<int32_t>(ws, lay.inv), ws_ptr<int32_t>(ws, lay.lrank),
-                                   ws_ptr<Group>(ws, lay.groups), x, T, L->d_model,
-                                   sums ? ws_ptr<uint8_t>(ws, lay.xs16) : nullptr,
-                                   sums ? ws_ptr<float>(ws, lay.xs32) : nullptr);
+    const int threads = P <= 32 ? 256 : 1024;
+    e = launch_pdl(k_bucket, dim3(1), dim3(threads), P <= 32 ? 0 : smem, s, const_cast<int32_t *>(idx), P, E, a.hdr,
+                   ws_ptr<int32_t>(ws, lay.counts), ws_ptr<int32_t>(ws, lay.offs), ws_ptr<int32_t>(ws, lay.active),
+                   ws_ptr<int32_t>(ws, lay.perm), ws_ptr<int32_t>(ws, lay.inv), ws_ptr<int32_t>(ws, lay.lrank),
+                   ws_ptr<Group>(ws, lay.groups), x, (int)T, (int)L->d_model, ws_ptr<uint16_t>(ws, lay.x16),
+                   sums ? ws_ptr<uint8_t>(ws, lay.xs16) : nullptr, sums ? ws_ptr<float>(ws, lay.xs32) : nullptr,
+                   logits, (int)k, const_cast<float *>(w), ws_ptr<int32_t>(ws, lay.nvalid), out);
   }
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_status(e);
   e = prefill ? launch_ffn_prefill(a, s) : launch_ffn_decode(a, s);
   if (e != cudaSuccess) return cuda_status(e);
@@ -612,8 +704,7 @@ size_t ds4moe_workspace_bytes(const ds4moe_layer *L, int32_t T, int32_t k, int32
 
 ds4moe_status ds4moe_workspace_init(void *ws, size_t ws_bytes, void *stream) {
   if (!ws || !aligned16(ws) || ws_bytes < sizeof(WsHeader)) return DS4MOE_EINVAL;
-  k_clear_header<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<WsHeader *>(ws));
-  return cuda_status(cudaGetLastError());
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
 }
 
 ds4moe_status ds4moe_route_topk(const uint16_t *x, const float *Wr, const float *bias, int32_t T,
@@ -641,11 +732,12 @@ ds4moe_status ds4moe_route_topk(const uint16_t *x, const float *Wr, const float 
     WsHeader *hdr = static_cast<WsHeader *>(ws);
     ProfScope prof("route_topk", s);
     const int ni = (d_model + 1023) / 1024;
-    if (ni <= 1) k_route_small<1><<<n_expert, 256, 0, s>>>(x, Wr, bias, T, d_model, n_expert, k, lg, idx, w, hdr);
-    else if (ni <= 2) k_route_small<2><<<n_expert, 256, 0, s>>>(x, Wr, bias, T, d_model, n_expert, k, lg, idx, w, hdr);
-    else if (ni <= 4) k_route_small<4><<<n_expert, 256, 0, s>>>(x, Wr, bias, T, d_model, n_expert, k, lg, idx, w, hdr);
-    else k_route_small<8><<<n_expert, 256, 0, s>>>(x, Wr, bias, T, d_model, n_expert, k, lg, idx, w, hdr);
-    return cuda_status(cudaGetLastError());
+    auto kern = ni <= 1   ? k_route_small<1, true>
+                : ni <= 2 ? k_route_small<2, true>
+                : ni <= 4 ? k_route_small<4, true>
+                          : k_route_small<8, true>;
+    return cuda_status(launch_pdl(kern, dim3(n_expert), dim3(256), 0, s, x, Wr, bias, (int)T, (int)d_model,
+                                  (int)n_expert, (int)k, lg, idx, w, hdr));
   }
   const int64_t warps = (int64_t)T * n_expert;
   {
@@ -671,6 +763,42 @@ ds4moe_status ds4moe_ffn_prefill(const ds4moe_layer *L, const uint16_t *x, const
                                  const float *w, int32_t T, int32_t k, float *out, void *ws,
                                  size_t ws_bytes, void *stream) {
   return run_ffn(true, L, x, idx, w, T, k, out, ws, ws_bytes, stream);
+}
+
+ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const float *Wr, const float *bias,
+                               int32_t T, int32_t k, float *out, int32_t *idx, float *w, void *ws,
+                               size_t ws_bytes, void *stream) {
+  ds4moe_status st = check_layer(L);
+  if (st != DS4MOE_OK) return st;
+  const int E = L->n_expert, D = L->d_model;
+  if (T < 0 || k < 1 || k > 32 || k > E) return DS4MOE_EINVAL;
+  if (T == 0) return DS4MOE_OK;
+  if (!x || !Wr || !out || !idx || !w || !ws) return DS4MOE_EINVAL;
+  if (!aligned16(x) || !aligned16(Wr) || !aligned16(out) || !aligned16(idx) || !aligned16(w) || !aligned16(ws) ||
+      (bias && !aligned16(bias)))
+    return DS4MOE_EINVAL;
+  const WsLayout lay = ws_layout(*L, T, k, 0);
+  if (ws_bytes < lay.total) return DS4MOE_ESPACE;
+  if (T > 256 || E > 256 || D > 8192 || D % 8) {
+    // the two-call path gives the same results for shapes the fused router does not cover
+    st = ds4moe_route_topk(x, Wr, bias, T, D, E, k, idx, w, nullptr, ws, ws_bytes, stream);
+    if (st != DS4MOE_OK) return st;
+    return run_ffn(false, L, x, idx, w, T, k, out, ws, ws_bytes, stream);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float *lg = ws_ptr<float>(ws, lay.logits);
+  {
+    ProfScope prof("route", s);
+    const int ni = (D + 1023) / 1024;
+    auto kern = ni <= 1   ? k_route_small<1, false>
+                : ni <= 2 ? k_route_small<2, false>
+                : ni <= 4 ? k_route_small<4, false>
+                          : k_route_small<8, false>;
+    cudaError_t e = launch_pdl(kern, dim3(E), dim3(256), 0, s, x, Wr, bias, (int)T, (int)D, (int)E, (int)k, lg, idx,
+                               w, static_cast<WsHeader *>(ws));
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return run_ffn(false, L, x, idx, w, T, k, out, ws, ws_bytes, stream, lg);
 }
 
 ds4moe_status ds4moe_stream_status(void *ws, void *stream) {

@@ -23,10 +23,7 @@
 namespace ds4 {
 namespace {
 
-constexpr int kTok = kGroup;            // tokens per pass (= MMA n)
-constexpr uint32_t kMagic = 0x43004300u;  // bf16x2 (128, 128)
-constexpr uint32_t kOne = 0x3F803F80u;    // bf16x2 (1, 1)
-constexpr uint32_t kNeg128 = 0xC300C300u; // bf16x2 (-128, -128)
+constexpr int kTok = kGroup;  // tokens per pass (= MMA n)
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -40,91 +37,119 @@ __device__ __forceinline__ float warp_sum(float v) {
 // (2c, 2c+1) hold values 4c, 4c+1 of a 16-value run and slots (2c+8, 2c+9)
 // values 4c+2, 4c+3, so B is a natural-order 64-bit load of 4 activations.
 
-// Q2_K scale folding constants for code position s' (the code sits at bit
-// 2 s' of each bf16 half, i.e. the operand is 128 + 4^s' q):
-//   s1 = sc * 4^-s',  s0 = -128 * sc * 4^-s'  from v = 128 + sc:
-//   s1 = v * 4^-s' - 128 * 4^-s',  s0 = v * (-128 * 4^-s') + 16384 * 4^-s'.
-__device__ __forceinline__ void q2k_consts(uint32_t v, int sp, uint32_t &s1, uint32_t &s0) {
-  const uint32_t f1 = sp == 0 ? 0x3F803F80u : sp == 1 ? 0x3E803E80u : 0x3D803D80u;   // 4^-s'
-  const uint32_t f0 = sp == 0 ? 0xC300C300u : sp == 1 ? 0xC200C200u : 0xC100C100u;   // -128 * 4^-s'
-  const uint32_t g0 = sp == 0 ? 0x46804680u : sp == 1 ? 0x45804580u : 0x44804480u;   // 16384 * 4^-s'
-  s1 = ptx::fma_bf16x2(v, f1, f0);
-  s0 = ptx::fma_bf16x2(v, f0, g0);
+// fp16x2 constants
+constexpr uint32_t kMagicH = 0x64006400u;    // (1024, 1024)
+constexpr uint32_t kOneH = 0x3C003C00u;      // (1, 1)
+constexpr uint32_t kNeg1024H = 0xE400E400u;  // (-1024, -1024)
+constexpr uint32_t kSixteenthH = 0x2C002C00u; // (1/16, 1/16)
+constexpr uint32_t kNeg64H = 0xD400D400u;    // (-64, -64)
+
+// Per-lane Q2_K constants.  Lane quad c walks the four 16-value sub-blocks
+// 4c .. 4c+3 of every 256-value block (one sub-block per 4 consecutive MMAs,
+// values 4j .. 4j+3 in MMA j); those sub-blocks sit in qs half c/2 at code
+// positions s = 2 (c & 1) (sub-blocks 4c, 4c+1) and s + 1 (4c+2, 4c+3).
+// A code at position s becomes the fp16 operand 1024 + 4^s q (one OR with
+// the magic exponent), and the scale fold is exact:
+//   (1024 + 4^s q) * (sc 4^-s) + (-1024 sc 4^-s) = sc q  (<= 45).
+struct Q2kLane {
+  uint32_t mask[2];  // code field of position s, s + 1 in both fp16 lanes
+  uint32_t f1[2];    // 4^-s
+  uint32_t f0[2];    // -1024 * 4^-s
+};
+
+__device__ __forceinline__ Q2kLane q2k_lane(int c) {
+  Q2kLane k;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int s = 2 * (c & 1) + i;
+    k.mask[i] = 0x00030003u << (2 * s);
+    const uint32_t p = (uint32_t)(15 - 2 * s);            // fp16 exponent field of 4^-s
+    k.f1[i] = (p << 10) | (p << 26);
+    const uint32_t q = (uint32_t)(25 - 2 * s) | 0x20u;    // -(1024 * 4^-s): sign + exponent 25 - 2s
+    k.f0[i] = (q << 10) | (q << 26);
+  }
+  return k;
 }
 
-// This lane's activations for one 256-value segment: the B fragments of the
-// 16 sixteen-value runs (token g, values 16n + 4c .. 16n + 4c + 3) and, for
-// Q2_K mins, the sub-block-sum fragments (hi and lo parts).
+// This lane's activations (fp16) for one 256-value segment.
+// Q2_K mapping: bx[4i + j] = values 64c + 16i + 4j .. +3 (contiguous per lane);
+// shi / slo = hi and lo parts of the sums of sub-blocks 4c .. 4c+3.
+// Q4_1 mapping: bx[2b + h] = values 32b + 16h + 4c .. +3.
 struct SegIn {
   uint2 bx[16];
   uint2 shi, slo;
 };
 
+template <int Q>
 __device__ __forceinline__ void load_seg(SegIn &in, const uint16_t *__restrict__ xb,
                                          const uint8_t *__restrict__ sums, int c) {
+  if constexpr (Q == DS4MOE_Q2_K) {
 #pragma unroll
-  for (int n = 0; n < 16; ++n) in.bx[n] = xb ? ptx::ldg_nc_v2(xb + 16 * n + 4 * c) : make_uint2(0u, 0u);
-  in.shi = sums ? ptx::ldg_nc_v2(sums + 8 * c) : make_uint2(0u, 0u);
-  in.slo = sums ? ptx::ldg_nc_v2(sums + 32 + 8 * c) : make_uint2(0u, 0u);
+    for (int u = 0; u < 8; ++u) {
+      uint4 t = make_uint4(0u, 0u, 0u, 0u);
+      if (xb) t = *reinterpret_cast<const uint4 *>(xb + 64 * c + 8 * u);
+      in.bx[2 * u] = make_uint2(t.x, t.y);
+      in.bx[2 * u + 1] = make_uint2(t.z, t.w);
+    }
+    in.shi = sums ? *reinterpret_cast<const uint2 *>(sums + 8 * c) : make_uint2(0u, 0u);
+    in.slo = sums ? *reinterpret_cast<const uint2 *>(sums + 32 + 8 * c) : make_uint2(0u, 0u);
+  } else {
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+      in.bx[n] = xb ? *reinterpret_cast<const uint2 *>(xb + 32 * (n >> 1) + 16 * (n & 1) + 4 * c)
+                    : make_uint2(0u, 0u);
+    in.shi = in.slo = make_uint2(0u, 0u);
+  }
 }
 
 // One Q2_K 256-value block of 16 staged rows (row g at blk_a, g + 8 at
 // blk_b): acc += d * (sum sc*q*x) - dmin * (sum mn*xsum).
 __device__ __forceinline__ void q2k_block(const uint8_t *__restrict__ blk_a, const uint8_t *__restrict__ blk_b,
-                                          const SegIn &in, int c, float (&acc)[4]) {
-  uint32_t qa[4], qb[4], sa[4], sb[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    qa[j] = ptx::lds32(blk_a + 16 + 4 * (4 * j + c));
-    qb[j] = ptx::lds32(blk_b + 16 + 4 * (4 * j + c));
-    sa[j] = ptx::lds32(blk_a + 4 * j);
-    sb[j] = ptx::lds32(blk_b + 4 * j);
-  }
+                                          const SegIn &in, const Q2kLane &kl, int c, float (&acc)[4]) {
+  const uint8_t *qsa = blk_a + 16 + 32 * (c >> 1), *qsb = blk_b + 16 + 32 * (c >> 1);
+  const uint32_t swa = ptx::lds32(blk_a + 4 * c), swb = ptx::lds32(blk_b + 4 * c);
   const uint32_t dda = ptx::lds32(blk_a + 80), ddb = ptx::lds32(blk_b + 80);
-  uint32_t scma[4], scmb[4];
+  const uint32_t scma = swa & 0x0F0F0F0Fu, scmb = swb & 0x0F0F0F0Fu;
+  // scale folding constants of sub-blocks 4c + i, rows a and b
+  uint32_t s1a[4], s0a[4], s1b[4], s0b[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    scma[j] = sa[j] & 0x0F0F0F0Fu;
-    scmb[j] = sb[j] & 0x0F0F0F0Fu;
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t sel = 0x4040u | ((uint32_t)i << 8) | (uint32_t)i;   // (1024 + sc, 1024 + sc)
+    s1a[i] = ptx::fma_f16x2(__byte_perm(scma, 0x64646464u, sel), kl.f1[i >> 1], kl.f0[i >> 1]);
+    s1b[i] = ptx::fma_f16x2(__byte_perm(scmb, 0x64646464u, sel), kl.f1[i >> 1], kl.f0[i >> 1]);
+    s0a[i] = ptx::mul_f16x2(s1a[i], kNeg1024H);
+    s0b[i] = ptx::mul_f16x2(s1b[i], kNeg1024H);
   }
   float dm[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t a01 = __byte_perm(qa[j], 0, 0x4140), a23 = __byte_perm(qa[j], 0, 0x4342);
-    const uint32_t b01 = __byte_perm(qb[j], 0, 0x4140), b23 = __byte_perm(qb[j], 0, 0x4342);
-    const uint32_t a01s = __byte_perm(qa[j] >> 2, 0, 0x4140), a23s = __byte_perm(qa[j] >> 2, 0, 0x4342);
-    const uint32_t b01s = __byte_perm(qb[j] >> 2, 0, 0x4140), b23s = __byte_perm(qb[j] >> 2, 0, 0x4342);
+  for (int wi = 0; wi < 8; ++wi) {            // qs word (4 consecutive values) of this lane
+    const uint32_t qa = ptx::lds32(qsa + 4 * wi), qb = ptx::lds32(qsb + 4 * wi);
+    const uint32_t a01 = __byte_perm(qa, 0, 0x4140), a23 = __byte_perm(qa, 0, 0x4342);
+    const uint32_t b01 = __byte_perm(qb, 0, 0x4140), b23 = __byte_perm(qb, 0, 0x4342);
+    const int j = wi & 3;
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const int n = 8 * (j >> 1) + 2 * s + (j & 1);  // 16-value sub-block of this MMA
-      const int sp = s < 3 ? s : 2;                   // s = 3 is read from the >> 2 copy
-      const uint32_t mask = 0x00030003u << (2 * sp);
-      const uint32_t sel = 0x4040u | ((uint32_t)(n & 3) << 8) | (uint32_t)(n & 3);
-      uint32_t s1a, s0a, s1b, s0b;
-      q2k_consts(__byte_perm(scma[n >> 2], 0x43434343u, sel), sp, s1a, s0a);
-      q2k_consts(__byte_perm(scmb[n >> 2], 0x43434343u, sel), sp, s1b, s0b);
+    for (int si = 0; si < 2; ++si) {          // code position s + si -> sub-block i
+      const int i = (wi >> 2) + 2 * si;
       uint32_t A[4];
-      A[0] = ptx::fma_bf16x2(ptx::and_or(s < 3 ? a01 : a01s, mask, kMagic), s1a, s0a);
-      A[1] = ptx::fma_bf16x2(ptx::and_or(s < 3 ? b01 : b01s, mask, kMagic), s1b, s0b);
-      A[2] = ptx::fma_bf16x2(ptx::and_or(s < 3 ? a23 : a23s, mask, kMagic), s1a, s0a);
-      A[3] = ptx::fma_bf16x2(ptx::and_or(s < 3 ? b23 : b23s, mask, kMagic), s1b, s0b);
-      ptx::mma_bf16(dm[j & 1], A, in.bx[n].x, in.bx[n].y);
+      A[0] = ptx::fma_f16x2(ptx::and_or(a01, kl.mask[si], kMagicH), s1a[i], s0a[i]);
+      A[1] = ptx::fma_f16x2(ptx::and_or(b01, kl.mask[si], kMagicH), s1b[i], s0b[i]);
+      A[2] = ptx::fma_f16x2(ptx::and_or(a23, kl.mask[si], kMagicH), s1a[i], s0a[i]);
+      A[3] = ptx::fma_f16x2(ptx::and_or(b23, kl.mask[si], kMagicH), s1b[i], s0b[i]);
+      ptx::mma_f16(dm[j & 1], A, in.bx[4 * i + j].x, in.bx[4 * i + j].y);
     }
   }
-  // mins: D_min[r][t] = sum_n mn[r][n] * xsum[n][t] (xsum = hi + lo); lane
-  // quad c takes scale bytes 2c, 2c+1 and 2c+8, 2c+9, high nibble = min
+  // mins: D_min[r][t] = sum over sub-blocks 4c..4c+3 (K slots 2c, 2c+1,
+  // 2c+8, 2c+9) of mn[r][n] * xsum[n][t], xsum = hi + lo
   float dn[4] = {0.f, 0.f, 0.f, 0.f};
   {
-    const uint32_t sel = (c & 1) ? 0x4342u : 0x4140u;
+    const uint32_t ma = (swa >> 4) & 0x0F0F0F0Fu, mb = (swb >> 4) & 0x0F0F0F0Fu;
     uint32_t Am[4];
-    Am[0] = ptx::fma_bf16x2(ptx::and_or(__byte_perm(sa[c >> 1], 0, sel) >> 4, 0x000F000Fu, kMagic), kOne, kNeg128);
-    Am[1] = ptx::fma_bf16x2(ptx::and_or(__byte_perm(sb[c >> 1], 0, sel) >> 4, 0x000F000Fu, kMagic), kOne, kNeg128);
-    Am[2] = ptx::fma_bf16x2(ptx::and_or(__byte_perm(sa[2 + (c >> 1)], 0, sel) >> 4, 0x000F000Fu, kMagic), kOne,
-                            kNeg128);
-    Am[3] = ptx::fma_bf16x2(ptx::and_or(__byte_perm(sb[2 + (c >> 1)], 0, sel) >> 4, 0x000F000Fu, kMagic), kOne,
-                            kNeg128);
-    ptx::mma_bf16(dn, Am, in.shi.x, in.shi.y);
-    ptx::mma_bf16(dn, Am, in.slo.x, in.slo.y);
+    Am[0] = ptx::fma_f16x2(__byte_perm(ma, 0, 0x4140) | kMagicH, kOneH, kNeg1024H);
+    Am[1] = ptx::fma_f16x2(__byte_perm(mb, 0, 0x4140) | kMagicH, kOneH, kNeg1024H);
+    Am[2] = ptx::fma_f16x2(__byte_perm(ma, 0, 0x4342) | kMagicH, kOneH, kNeg1024H);
+    Am[3] = ptx::fma_f16x2(__byte_perm(mb, 0, 0x4342) | kMagicH, kOneH, kNeg1024H);
+    ptx::mma_f16(dn, Am, in.shi.x, in.shi.y);
+    ptx::mma_f16(dn, Am, in.slo.x, in.slo.y);
   }
   const float da = f16_bits_to_f32(dda & 0xFFFFu), dmina = f16_bits_to_f32(dda >> 16);
   const float db = f16_bits_to_f32(ddb & 0xFFFFu), dminb = f16_bits_to_f32(ddb >> 16);
@@ -135,8 +160,9 @@ __device__ __forceinline__ void q2k_block(const uint8_t *__restrict__ blk_a, con
 }
 
 // Eight Q4_1 blocks (one 256-value segment): per block
-// acc += d * (sum q*x) + m * (sum x).  xs_a / xs_b: the 8 block sums of
-// tokens 2c and 2c + 1 (or nullptr).
+// acc += d * (sum q*x) + m * (sum x).  Low nibbles -> 1024 + q, high
+// nibbles -> 1024 + 16 q, both turned into exact q by one packed FMA.
+// xs_a / xs_b: the 8 block sums of tokens 2c and 2c + 1 (or nullptr).
 __device__ __forceinline__ void q41_seg(const uint8_t *__restrict__ seg_a, const uint8_t *__restrict__ seg_b,
                                         const SegIn &in, const float *__restrict__ xs_a,
                                         const float *__restrict__ xs_b, int c, float (&acc)[4]) {
@@ -154,17 +180,17 @@ __device__ __forceinline__ void q41_seg(const uint8_t *__restrict__ seg_a, const
     const uint32_t a01 = __byte_perm(qa, 0, 0x4140), a23 = __byte_perm(qa, 0, 0x4342);
     const uint32_t b01 = __byte_perm(qb, 0, 0x4140), b23 = __byte_perm(qb, 0, 0x4342);
     uint32_t lo[4], hi[4];
-    lo[0] = ptx::fma_bf16x2(ptx::and_or(a01, 0x000F000Fu, kMagic), kOne, kNeg128);
-    lo[1] = ptx::fma_bf16x2(ptx::and_or(b01, 0x000F000Fu, kMagic), kOne, kNeg128);
-    lo[2] = ptx::fma_bf16x2(ptx::and_or(a23, 0x000F000Fu, kMagic), kOne, kNeg128);
-    lo[3] = ptx::fma_bf16x2(ptx::and_or(b23, 0x000F000Fu, kMagic), kOne, kNeg128);
-    hi[0] = ptx::fma_bf16x2(ptx::and_or(a01 >> 4, 0x000F000Fu, kMagic), kOne, kNeg128);
-    hi[1] = ptx::fma_bf16x2(ptx::and_or(b01 >> 4, 0x000F000Fu, kMagic), kOne, kNeg128);
-    hi[2] = ptx::fma_bf16x2(ptx::and_or(a23 >> 4, 0x000F000Fu, kMagic), kOne, kNeg128);
-    hi[3] = ptx::fma_bf16x2(ptx::and_or(b23 >> 4, 0x000F000Fu, kMagic), kOne, kNeg128);
+    lo[0] = ptx::fma_f16x2(ptx::and_or(a01, 0x000F000Fu, kMagicH), kOneH, kNeg1024H);
+    lo[1] = ptx::fma_f16x2(ptx::and_or(b01, 0x000F000Fu, kMagicH), kOneH, kNeg1024H);
+    lo[2] = ptx::fma_f16x2(ptx::and_or(a23, 0x000F000Fu, kMagicH), kOneH, kNeg1024H);
+    lo[3] = ptx::fma_f16x2(ptx::and_or(b23, 0x000F000Fu, kMagicH), kOneH, kNeg1024H);
+    hi[0] = ptx::fma_f16x2(ptx::and_or(a01, 0x00F000F0u, kMagicH), kSixteenthH, kNeg64H);
+    hi[1] = ptx::fma_f16x2(ptx::and_or(b01, 0x00F000F0u, kMagicH), kSixteenthH, kNeg64H);
+    hi[2] = ptx::fma_f16x2(ptx::and_or(a23, 0x00F000F0u, kMagicH), kSixteenthH, kNeg64H);
+    hi[3] = ptx::fma_f16x2(ptx::and_or(b23, 0x00F000F0u, kMagicH), kSixteenthH, kNeg64H);
     float d[4] = {0.f, 0.f, 0.f, 0.f};
-    ptx::mma_bf16(d, lo, in.bx[2 * bb].x, in.bx[2 * bb].y);
-    ptx::mma_bf16(d, hi, in.bx[2 * bb + 1].x, in.bx[2 * bb + 1].y);
+    ptx::mma_f16(d, lo, in.bx[2 * bb].x, in.bx[2 * bb].y);
+    ptx::mma_f16(d, hi, in.bx[2 * bb + 1].x, in.bx[2 * bb + 1].y);
     const float da = f16_bits_to_f32(dma & 0xFFFFu), ma = f16_bits_to_f32(dma >> 16);
     const float db = f16_bits_to_f32(dmb & 0xFFFFu), mb = f16_bits_to_f32(dmb >> 16);
     acc[0] = fmaf(da, d[0], fmaf(ma, xsa[bb], acc[0]));
@@ -179,9 +205,9 @@ template <int Q>
 constexpr int seg_bytes() { return Q == DS4MOE_Q2_K ? kQ2KBytes : 8 * kQ41Bytes; }
 
 template <int Q>
-__device__ __forceinline__ void seg_rows(const uint8_t *ra, const uint8_t *rb, const SegIn &in,
+__device__ __forceinline__ void seg_rows(const uint8_t *ra, const uint8_t *rb, const SegIn &in, const Q2kLane &kl,
                                          const float *xs_a, const float *xs_b, int c, float (&acc)[4]) {
-  if constexpr (Q == DS4MOE_Q2_K) q2k_block(ra, rb, in, c, acc);
+  if constexpr (Q == DS4MOE_Q2_K) q2k_block(ra, rb, in, kl, c, acc);
   else q41_seg(ra, rb, in, xs_a, xs_b, c, acc);
 }
 
@@ -200,18 +226,40 @@ __device__ __forceinline__ void stage_rows(uint8_t *dst, const uint8_t *src, int
   if (r >= 0 && r < 16) ptx::bulk_g2s(dst + r * chunk, src + r * stride, chunk, bar);
 }
 
+// ============================================================ tile driver
+// One staged 16-row tile chunk (row g at buf + g * ch) against this lane's
+// token activations: nseg 256-value segments.
+template <int Q>
+__device__ __forceinline__ void tile_rows(const uint8_t *buf, uint32_t ch, int nseg, const uint16_t *xb,
+                                          const uint8_t *sums, const float *xs_a, const float *xs_b,
+                                          const Q2kLane &kl, int g, int c, float (&acc)[4]) {
+  const uint8_t *ra = buf + g * ch, *rb = buf + (g + 8) * ch;
+  for (int sg = 0; sg < nseg; ++sg) {
+    SegIn in;
+    load_seg<Q>(in, xb ? xb + 256 * sg : nullptr, sums ? sums + 64 * sg : nullptr, c);
+    seg_rows<Q>(ra + seg_bytes<Q>() * sg, rb + seg_bytes<Q>() * sg, in, kl, xs_a ? xs_a + 8 * sg : nullptr,
+                xs_b ? xs_b + 8 * sg : nullptr, c, acc);
+  }
+}
+
 // ============================================================ gate / up
-// CTA = kp warps; warp w owns K chunk w of both matrices.  Shared memory per
-// warp: two stages of [16 gate rows | 16 up rows] x chunk bytes.
+// CTA = 2 kp warps: warp w < kp computes K chunk w of the gate tile, warp
+// kp + w the same chunk of the up tile.  Each warp stages its 16 rows x chunk
+// bytes in two shared-memory stages; the K partials are summed in shared
+// memory in a fixed order, then h = bf16(silu(g) * u) and the tile's
+// sub-block sums of h are written.
 template <int QG, int QU>
-__global__ void __launch_bounds__(256) k_gate_up_mma(FfnArgs a, int kp, uint32_t chg, uint32_t chu) {
+__global__ void __launch_bounds__(512) k_gate_up_mma(FfnArgs a, int kp, uint32_t chg, uint32_t chu) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
   const int D = a.L.d_model, F = a.L.d_ff;
-  const uint32_t stage_bytes = 16u * (chg + chu);
-  uint8_t *wbuf = smem + (size_t)w * 2 * stage_bytes;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)kp * 2 * stage_bytes);  // [kp][2]
-  float *red = reinterpret_cast<float *>(bars + 2 * kp);                              // [kp][32][8]
+  const bool is_up = w >= kp;
+  const int part = is_up ? w - kp : w;
+  const uint32_t ch = is_up ? chu : chg;
+  const uint32_t stage_bytes = 16u * ch;
+  uint8_t *wbuf = smem + (is_up ? (size_t)kp * 32 * chg + (size_t)part * 32 * chu : (size_t)part * 32 * chg);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)kp * 32 * (chg + chu));  // [2 kp][2]
+  float *red = reinterpret_cast<float *>(bars + 4 * kp);                              // [2 kp][32][4]
   uint64_t *mybar = bars + 2 * w;
   if (lane == 0) {
     ptx::mbar_init(&mybar[0], 1);
@@ -219,94 +267,89 @@ __global__ void __launch_bounds__(256) k_gate_up_mma(FfnArgs a, int kp, uint32_t
     ptx::fence_mbar_init();
   }
   __syncwarp();
+  const Q2kLane kl = q2k_lane(c);
+  // groups, permutation, fp16 x and its sums come from the bucketing grid
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
   const int ntile = F / 16;
-  const int U = a.hdr->n_groups * ntile;
-  const int64_t rbg = row_bytes(QG, D), rbu = row_bytes(QU, D);
-  const int kvals = D / kp;  // values per K chunk (same for gate and up)
-  const uint8_t *gate = static_cast<const uint8_t *>(a.L.gate);
-  const uint8_t *up = static_cast<const uint8_t *>(a.L.up);
+  const int U = __ldcg(&a.hdr->n_groups) * ntile;
+  const int64_t rb = is_up ? row_bytes(QU, D) : row_bytes(QG, D);
+  const uint8_t *mat = static_cast<const uint8_t *>(is_up ? a.L.up : a.L.gate);
+  const int kvals = D / kp, k0 = part * kvals;
 
+  auto load_group = [&](int u) {
+    const int4 v = __ldcg(reinterpret_cast<const int4 *>(a.groups + u / ntile));
+    return Group{v.x, v.y, v.z, v.w};
+  };
   auto issue = [&](int u, int st) {
-    const Group grp = a.groups[u / ntile];
+    const Group grp = load_group(u);
     const int row0 = (u % ntile) * 16;
-    uint8_t *dst = wbuf + (size_t)st * stage_bytes;
     if (lane == 0) ptx::mbar_arrive_expect_tx(&mybar[st], stage_bytes);
     __syncwarp();
-    const uint8_t *gs = gate + ((int64_t)grp.e * F + row0) * rbg + (int64_t)w * chg;
-    const uint8_t *us = up + ((int64_t)grp.e * F + row0) * rbu + (int64_t)w * chu;
-    stage_rows(dst, gs, rbg, chg, &mybar[st], 0);
-    stage_rows(dst + 16 * chg, us, rbu, chu, &mybar[st], 16);
+    stage_rows(wbuf + (size_t)st * stage_bytes, mat + ((int64_t)grp.e * F + row0) * rb + (int64_t)part * ch, rb,
+               ch, &mybar[st], 0);
   };
 
-  uint32_t phase[2] = {0u, 0u};
+  uint32_t phase = 0u;  // bit st: parity of stage st
   int u = blockIdx.x;
   if (u < U) issue(u, 0);
   if (u + (int)gridDim.x < U) issue(u + gridDim.x, 1);
   bool timed_out = false;
   for (int it = 0; u < U; u += gridDim.x, ++it) {
     const int st = it & 1;
-    const Group grp = a.groups[u / ntile];
+    const Group grp = load_group(u);
     const int row0 = (u % ntile) * 16;
-    if (!timed_out && !ptx::mbar_wait(&mybar[st], phase[st])) {
+    if (!timed_out && !ptx::mbar_wait(&mybar[st], (phase >> st) & 1u)) {
       record_status(a.hdr, DS4MOE_ETIMEOUT);
       timed_out = true;
     }
-    phase[st] ^= 1u;
-    const uint8_t *buf = wbuf + (size_t)st * stage_bytes;
+    phase ^= 1u << st;
     // this lane's token (B column g) and the tokens of its D columns 2c, 2c+1
-    const int k0 = w * kvals;
     const uint16_t *xb = nullptr;
     const uint8_t *sums = nullptr;
     const float *xs_a = nullptr, *xs_b = nullptr;
     if (g < grp.nt) {
-      const int t = a.perm[grp.p0 + g] / a.k;
-      xb = a.x + (int64_t)t * D + k0;
+      const int t = __ldcg(a.perm + grp.p0 + g) / a.k;
+      xb = a.x16 + (int64_t)t * D + k0;
       sums = a.xs16 + ((int64_t)t * (D / 256 + 1) + k0 / 256) * 64;
     }
-    if (2 * c < grp.nt) xs_a = a.xs32 + (int64_t)(a.perm[grp.p0 + 2 * c] / a.k) * (D / 32) + k0 / 32;
-    if (2 * c + 1 < grp.nt) xs_b = a.xs32 + (int64_t)(a.perm[grp.p0 + 2 * c + 1] / a.k) * (D / 32) + k0 / 32;
-    float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
+    if (2 * c < grp.nt) xs_a = a.xs32 + (int64_t)(__ldcg(a.perm + grp.p0 + 2 * c) / a.k) * (D / 32) + k0 / 32;
+    if (2 * c + 1 < grp.nt) xs_b = a.xs32 + (int64_t)(__ldcg(a.perm + grp.p0 + 2 * c + 1) / a.k) * (D / 32) + k0 / 32;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (!timed_out) {
-      const uint8_t *ga = buf + g * chg, *gb = buf + (g + 8) * chg;
-      const uint8_t *ua = buf + 16 * chg + g * chu, *ub = buf + 16 * chg + (g + 8) * chu;
-      for (int sg = 0; sg < kvals / 256; ++sg) {
-        SegIn in;
-        load_seg(in, xb ? xb + 256 * sg : nullptr, sums ? sums + 64 * sg : nullptr, c);
-        const float *xa = xs_a ? xs_a + 8 * sg : nullptr, *xbb = xs_b ? xs_b + 8 * sg : nullptr;
-        seg_rows<QG>(ga + seg_bytes<QG>() * sg, gb + seg_bytes<QG>() * sg, in, xa, xbb, c, ag);
-        seg_rows<QU>(ua + seg_bytes<QU>() * sg, ub + seg_bytes<QU>() * sg, in, xa, xbb, c, au);
-      }
+      const uint8_t *buf = wbuf + (size_t)st * stage_bytes;
+      if (is_up) tile_rows<QU>(buf, ch, kvals / 256, xb, sums, xs_a, xs_b, kl, g, c, acc);
+      else tile_rows<QG>(buf, ch, kvals / 256, xb, sums, xs_a, xs_b, kl, g, c, acc);
     }
     __syncwarp();
     if (u + 2 * (int)gridDim.x < U && !timed_out) issue(u + 2 * gridDim.x, st);
-    // K-slice partials -> shared, summed in fixed warp order
-    float *r = red + ((size_t)w * 32 + lane) * 8;
+    float *r = red + ((size_t)w * 32 + lane) * 4;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      r[i] = ag[i];
-      r[4 + i] = au[i];
-    }
+    for (int i = 0; i < 4; ++i) r[i] = acc[i];
     __syncthreads();
     if (w == 0) {
       float gs[4] = {0.f, 0.f, 0.f, 0.f}, us[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int ww = 0; ww < kp; ++ww) {
-        const float *q = red + ((size_t)ww * 32 + lane) * 8;
+      for (int p = 0; p < kp; ++p) {
+        const float *qg = red + ((size_t)p * 32 + lane) * 4, *qu = red + ((size_t)(kp + p) * 32 + lane) * 4;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          gs[i] += q[i];
-          us[i] += q[4 + i];
+          gs[i] += qg[i];
+          us[i] += qu[i];
         }
       }
-      // h for rows (g, g+8) x tokens (2c, 2c+1); zero for absent tokens
+      // h for rows (g, g+8) x tokens (2c, 2c+1)
       float hsum[2] = {0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int row = row0 + g + 8 * (i >> 1);
         const int tok = 2 * c + (i & 1);
         if (tok < grp.nt) {
-          const uint16_t hb = f32_to_bf16_bits(silu(gs[i]) * us[i]);
-          a.h[(int64_t)(grp.p0 + tok) * F + row] = hb;
-          hsum[i & 1] += bf16_bits_to_f32(hb);
+          // h is rounded to bf16 (the definition), then stored as the fp16
+          // operand of the down kernel (exact for |h| in [2^-14, 65504])
+          const float hv = bf16_bits_to_f32(f32_to_bf16_bits(silu(gs[i]) * us[i]));
+          if (fabsf(hv) > 65504.f) record_status(a.hdr, DS4MOE_EDEVICE);
+          a.h[(int64_t)(grp.p0 + tok) * F + row] = __half_as_ushort(__float2half_rn(hv));
+          hsum[i & 1] += hv;
         }
       }
       // sub-block sums of h over the tile's 16 rows (for the down kernel's mins)
@@ -322,12 +365,12 @@ __global__ void __launch_bounds__(256) k_gate_up_mma(FfnArgs a, int kp, uint32_t
         for (int i = 0; i < 2; ++i) {
           const int tok = 2 * c + i;
           if (tok < grp.nt) {
-            const uint16_t hi = f32_to_bf16_bits(hsum[i]);
-            const uint16_t lo = f32_to_bf16_bits(hsum[i] - bf16_bits_to_f32(hi));
+            const __half hi = __float2half_rn(hsum[i]);
+            const __half lo = __float2half_rn(hsum[i] - __half2float(hi));
             uint16_t *rec = reinterpret_cast<uint16_t *>(
                 a.hs16 + ((int64_t)(grp.p0 + tok) * (F / 256 + 1) + n16 / 16) * 64);
-            rec[sums_slot(n16 & 15)] = hi;
-            rec[16 + sums_slot(n16 & 15)] = lo;
+            rec[n16 & 15] = __half_as_ushort(hi);
+            rec[16 + (n16 & 15)] = __half_as_ushort(lo);
           }
         }
       }
@@ -336,57 +379,101 @@ __global__ void __launch_bounds__(256) k_gate_up_mma(FfnArgs a, int kp, uint32_t
   }
   // no copy may still be landing in shared memory when the CTA exits
   if (timed_out) {
-    for (int st = 0; st < 2; ++st) ptx::mbar_wait(&mybar[st], phase[st], 1u << 20);
+    for (int st = 0; st < 2; ++st) ptx::mbar_wait(&mybar[st], (phase >> st) & 1u, 1u << 20);
   }
 }
 
 // ================================================================ down
-// One warp per (token group, 16-row tile) over the full K (= d_ff); CTA of
-// `nw` independent warps, two stages each.
-template <int QD>
+// Weighted combine fused into the down kernel: each warp counts, per token of
+// its group, one arrival at (token, 16-row tile); the warp that brings the
+// count to the token's number of valid experts sums that tile of
+// out[t] = sum_{i<k} w[t,i] * y[inv[t,i]] in rank order (so the result does
+// not depend on which warp finishes last) and resets the counter.
+__device__ __forceinline__ void combine_tile(const FfnArgs &a, const Group &grp, int tile, int ntile) {
+  const int lane = threadIdx.x & 31;
+  const int D = a.L.d_model, k = a.k;
+  __threadfence();  // this lane's y stores are visible before it is counted
+  __syncwarp();
+  int tok = -1;
+  bool last = false;
+  if (lane < grp.nt) {
+    tok = __ldcg(a.perm + grp.p0 + lane) / k;
+    const int old = atomicAdd(a.cnt + (int64_t)tok * ntile + tile, 1);
+    last = old == __ldcg(a.nvalid + tok) - 1;
+    if (last) a.cnt[(int64_t)tok * ntile + tile] = 0;
+  }
+  unsigned lm = __ballot_sync(0xffffffffu, last);
+  while (lm) {
+    const int src = __ffs(lm) - 1;
+    lm &= lm - 1u;
+    const int t = __shfl_sync(0xffffffffu, tok, src);
+    __threadfence();  // the other experts' y tiles are visible after the count
+    if (lane < 16) {
+      const int row = tile * 16 + lane;
+      float acc = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const int pos = __ldcg(a.inv + (int64_t)t * k + j);
+        if (pos < 0) continue;
+        acc = fmaf(__ldcg(a.w + (int64_t)t * k + j), __ldcg(a.y + (int64_t)pos * D + row), acc);
+      }
+      a.out[(int64_t)t * D + row] = acc;
+    }
+  }
+}
+
+// One warp per (token group, 16-row tile) over the full K (= d_ff), NST
+// shared-memory stages per warp.  The first tiles are prefetched before the
+// dependency wait: the token groups were complete before the gate/up grid
+// (whose h this kernel reads) launched it.
+template <int NST>
 __global__ void __launch_bounds__(256) k_down_mma(FfnArgs a, uint32_t chd) {
-  static_assert(QD == DS4MOE_Q2_K, "the tensor-core down kernel reads Q2_K rows");
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
   const int nw = blockDim.x >> 5;
   const int D = a.L.d_model, F = a.L.d_ff;
+  const Q2kLane kl = q2k_lane(c);
   const uint32_t stage_bytes = 16u * chd;
-  uint8_t *wbuf = smem + (size_t)w * 2 * stage_bytes;
-  uint64_t *mybar = reinterpret_cast<uint64_t *>(smem + (size_t)nw * 2 * stage_bytes) + 2 * w;
+  uint8_t *wbuf = smem + (size_t)w * NST * stage_bytes;
+  uint64_t *mybar = reinterpret_cast<uint64_t *>(smem + (size_t)nw * NST * stage_bytes) + NST * w;
   if (lane == 0) {
-    ptx::mbar_init(&mybar[0], 1);
-    ptx::mbar_init(&mybar[1], 1);
+    for (int st = 0; st < NST; ++st) ptx::mbar_init(&mybar[st], 1);
     ptx::fence_mbar_init();
   }
   __syncwarp();
   const int ntile = D / 16;
-  const int U = a.hdr->n_groups * ntile;
-  const int64_t rbd = row_bytes(QD, F);
+  const int U = __ldcg(&a.hdr->n_groups) * ntile;
+  const int64_t rbd = row_bytes(DS4MOE_Q2_K, F);
   const uint8_t *down = static_cast<const uint8_t *>(a.L.down);
   const int gw = blockIdx.x * nw + w, nwarps = gridDim.x * nw;
 
+  auto load_group = [&](int u) {
+    const int4 v = __ldcg(reinterpret_cast<const int4 *>(a.groups + u / ntile));
+    return Group{v.x, v.y, v.z, v.w};
+  };
   auto issue = [&](int u, int st) {
-    const Group grp = a.groups[u / ntile];
+    const Group grp = load_group(u);
     const int row0 = (u % ntile) * 16;
     if (lane == 0) ptx::mbar_arrive_expect_tx(&mybar[st], stage_bytes);
     __syncwarp();
     stage_rows(wbuf + (size_t)st * stage_bytes, down + ((int64_t)grp.e * D + row0) * rbd, rbd, chd, &mybar[st], 0);
   };
 
-  uint32_t phase[2] = {0u, 0u};
+  uint32_t phase = 0u;
   int u = gw;
-  if (u < U) issue(u, 0);
-  if (u + nwarps < U) issue(u + nwarps, 1);
+  for (int st = 0; st < NST; ++st)
+    if (u + st * nwarps < U) issue(u + st * nwarps, st);
+  ptx::pdl_wait();  // h and its sums come from the gate/up grid
+  ptx::pdl_launch_dependents();
   bool timed_out = false;
   for (int it = 0; u < U; u += nwarps, ++it) {
-    const int st = it & 1;
-    const Group grp = a.groups[u / ntile];
+    const int st = NST == 1 ? 0 : it % NST;
+    const Group grp = load_group(u);
     const int row0 = (u % ntile) * 16;
-    if (!timed_out && !ptx::mbar_wait(&mybar[st], phase[st])) {
+    if (!timed_out && !ptx::mbar_wait(&mybar[st], (phase >> st) & 1u)) {
       record_status(a.hdr, DS4MOE_ETIMEOUT);
       timed_out = true;
     }
-    phase[st] ^= 1u;
+    phase ^= 1u << st;
     const uint16_t *xb = nullptr;
     const uint8_t *sums = nullptr;
     if (g < grp.nt) {
@@ -394,26 +481,20 @@ __global__ void __launch_bounds__(256) k_down_mma(FfnArgs a, uint32_t chd) {
       sums = a.hs16 + (int64_t)(grp.p0 + g) * (F / 256 + 1) * 64;
     }
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (!timed_out) {
-      const uint8_t *rows = wbuf + (size_t)st * stage_bytes;
-      const uint8_t *ra = rows + g * chd, *rb = rows + (g + 8) * chd;
-      for (int sg = 0; sg < F / 256; ++sg) {
-        SegIn in;
-        load_seg(in, xb ? xb + 256 * sg : nullptr, sums ? sums + 64 * sg : nullptr, c);
-        q2k_block(ra + kQ2KBytes * sg, rb + kQ2KBytes * sg, in, c, acc);
-      }
-    }
+    if (!timed_out) tile_rows<DS4MOE_Q2_K>(wbuf + (size_t)st * stage_bytes, chd, F / 256, xb, sums, nullptr, nullptr,
+                                          kl, g, c, acc);
     __syncwarp();
-    if (u + 2 * nwarps < U && !timed_out) issue(u + 2 * nwarps, st);
+    if (u + NST * nwarps < U && !timed_out) issue(u + NST * nwarps, st);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int tok = 2 * c + (i & 1);
       if (tok < grp.nt) a.y[(int64_t)(grp.p0 + tok) * D + row0 + g + 8 * (i >> 1)] = acc[i];
     }
+    if (a.cnt) combine_tile(a, grp, u % ntile, ntile);
   }
   // no copy may still be landing in shared memory when the CTA exits
   if (timed_out) {
-    for (int st = 0; st < 2; ++st) ptx::mbar_wait(&mybar[st], phase[st], 1u << 20);
+    for (int st = 0; st < NST; ++st) ptx::mbar_wait(&mybar[st], (phase >> st) & 1u, 1u << 20);
   }
 }
 
@@ -521,6 +602,7 @@ __global__ void __launch_bounds__(256) k_down_simt(FfnArgs a) {
 
 // out[t, c] = sum_{i<k} w[t,i] * y[inv[t,i], c], in rank order.
 __global__ void k_combine(FfnArgs a) {
+  ptx::pdl_wait();  // y comes from the down grid
   const int D = a.L.d_model, k = a.k;
   const int64_t n4 = (int64_t)a.T * D / 4;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
@@ -528,10 +610,10 @@ __global__ void k_combine(FfnArgs a) {
     const int c = (int)((i * 4) % D);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
-      const int pos = a.inv[t * k + j];
+      const int pos = __ldcg(a.inv + t * k + j);
       if (pos < 0) continue;
       const float wt = a.w[t * k + j];
-      const float4 yv = *reinterpret_cast<const float4 *>(a.y + (int64_t)pos * D + c);
+      const float4 yv = __ldcg(reinterpret_cast<const float4 *>(a.y + (int64_t)pos * D + c));
       acc.x = fmaf(wt, yv.x, acc.x);
       acc.y = fmaf(wt, yv.y, acc.y);
       acc.z = fmaf(wt, yv.z, acc.z);
@@ -564,26 +646,26 @@ cudaError_t launch_gate_up_mma(const FfnArgs &a, cudaStream_t s, int kp) {
   const int D = a.L.d_model;
   const uint32_t chg = (uint32_t)(D / kp / block_vals(QG) * block_bytes(QG));
   const uint32_t chu = (uint32_t)(D / kp / block_vals(QU) * block_bytes(QU));
-  const size_t smem = (size_t)kp * 2 * 16 * (chg + chu) + 16 * kp + (size_t)kp * 32 * 8 * sizeof(float);
+  const size_t smem = (size_t)kp * 32 * (chg + chu) + 32 * kp + (size_t)2 * kp * 32 * 4 * sizeof(float);
   auto kern = k_gate_up_mma<QG, QU>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kp * 32, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 2 * kp * 32, smem);
   if (e != cudaSuccess) return e;
   const int grid = num_sms() * (per_sm > 0 ? per_sm : 1);
   ProfScope p("gate_up", s);
-  kern<<<grid, kp * 32, smem, s>>>(a, kp, chg, chu);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(2 * kp * 32), smem, s, a, kp, chg, chu);
 }
 
-template <int QD>
 cudaError_t launch_down_mma(const FfnArgs &a, cudaStream_t s) {
   const int F = a.L.d_ff;
-  const uint32_t chd = (uint32_t)row_bytes(QD, F);
-  const int nw = 4;
-  const size_t smem = (size_t)nw * 2 * 16 * chd + 16 * nw;
-  auto kern = k_down_mma<QD>;
+  const uint32_t chd = (uint32_t)row_bytes(DS4MOE_Q2_K, F);
+  // one stage per warp and as many warps as shared memory allows: every
+  // tile of a small batch is in flight at once
+  const int nw = 8;
+  const size_t smem = (size_t)nw * 16 * chd + 8 * nw;
+  auto kern = k_down_mma<1>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -591,8 +673,7 @@ cudaError_t launch_down_mma(const FfnArgs &a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int grid = num_sms() * (per_sm > 0 ? per_sm : 1);
   ProfScope p("down", s);
-  kern<<<grid, nw * 32, smem, s>>>(a, chd);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(nw * 32), smem, s, a, chd);
 }
 
 }  // namespace
@@ -600,12 +681,13 @@ cudaError_t launch_down_mma(const FfnArgs &a, cudaStream_t s) {
 // The tensor-core kernels need rows that split into 16-byte-multiple bulk
 // copies and stages that fit in shared memory; other shapes use SIMT.
 bool decode_mma_ok(const ds4moe_layer &L) {
+  if (L.d_model % 16) return false;
   const int kp = pick_kp(L.d_model, L.q_gate, L.q_up);
   if (kp == 0) return false;
   const int64_t st = 16 * (row_bytes(L.q_gate, L.d_model) + row_bytes(L.q_up, L.d_model)) / kp;
   if (2 * st * kp > 200 * 1024) return false;
   const int64_t rbd = row_bytes(L.q_down, L.d_ff);
-  return L.q_down == DS4MOE_Q2_K && L.d_ff % 256 == 0 && rbd % 16 == 0 && 2 * 16 * 4 * rbd <= 200 * 1024;
+  return L.q_down == DS4MOE_Q2_K && L.d_ff % 256 == 0 && rbd % 16 == 0 && 8 * 16 * rbd <= 200 * 1024;
 }
 
 cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s) {
@@ -618,7 +700,7 @@ cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s) {
     else if (L.q_gate == DS4MOE_Q2_K) e = launch_gate_up_mma<DS4MOE_Q2_K, DS4MOE_Q4_1>(a, s, kp);
     else e = launch_gate_up_mma<DS4MOE_Q4_1, DS4MOE_Q2_K>(a, s, kp);
     if (e != cudaSuccess) return e;
-    return launch_down_mma<DS4MOE_Q2_K>(a, s);
+    return launch_down_mma(a, s);
   }
   const int grid = num_sms() * 8;
   {
@@ -635,13 +717,11 @@ cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s) {
+  if (a.cnt) return cudaSuccess;  // fused into the down kernel
   const int64_t n4 = (int64_t)a.T * a.L.d_model / 4;
   const int grid = (int)((n4 + 255) / 256 < num_sms() * 16 ? (n4 + 255) / 256 : num_sms() * 16);
-  {
-    ProfScope p("combine", s);
-    k_combine<<<grid, 256, 0, s>>>(a);
-  }
-  return cudaGetLastError();
+  ProfScope p("combine", s);
+  return launch_pdl(k_combine, dim3(grid), dim3(256), 0, s, a);
 }
 
 }  // namespace ds4

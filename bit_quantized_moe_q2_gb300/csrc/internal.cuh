@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/ds4moe.h"
 
 namespace ds4 {
@@ -41,17 +43,14 @@ struct Group {
   int32_t e, p0, nt, pad;
 };
 
-// Sub-block sums of an activation row in the order the tensor-core kernels
-// read them: per 256-value block a 64-byte record, first 16 bf16 "hi" parts
-// then 16 bf16 "lo" parts (sum ~= hi + lo); within each half, lane quad c
-// owns 8 bytes holding sub-blocks (2c, 2c+1, 2c+8, 2c+9).
-__host__ __device__ inline int sums_slot(int n) {  // bf16 index of sub-block n within a half
-  return 4 * ((n & 7) >> 1) + (n & 1) + 2 * (n >> 3);
-}
+// Sub-block sums of an activation row for the tensor-core kernels: per
+// 256-value block a 64-byte record of 16 fp16 "hi" parts then 16 fp16 "lo"
+// parts (sum of sub-block n ~= hi[n] + lo[n]), in sub-block order.
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
 struct WsLayout {
-  size_t hdr, logits, counts, offs, active, perm, inv, lrank, groups, xs16, xs32, hs16, h, y, total;
+  size_t hdr, logits, counts, offs, active, perm, inv, lrank, groups, x16, xs16, xs32, hs16, h, y, nvalid, cnt,
+      total;
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -69,11 +68,14 @@ inline WsLayout ws_layout(const ds4moe_layer &L, int T, int k, int /*prefill*/) 
   w.inv = o;     o += align256(sizeof(int32_t) * P);
   w.lrank = o;   o += align256(sizeof(int32_t) * P);
   w.groups = o;  o += align256(sizeof(Group) * P);
+  w.x16 = o;     o += align256(sizeof(uint16_t) * (size_t)T * (size_t)L.d_model);
   w.xs16 = o;    o += align256((size_t)T * (size_t)(L.d_model / 256 + 1) * 64);
   w.xs32 = o;    o += align256(sizeof(float) * (size_t)T * (size_t)(L.d_model / 32 + 1));
   w.hs16 = o;    o += align256(P * (size_t)(L.d_ff / 256 + 1) * 64);
   w.h = o;       o += align256(sizeof(uint16_t) * P * (size_t)L.d_ff);
   w.y = o;       o += align256(sizeof(float) * P * (size_t)L.d_model);
+  w.nvalid = o;  o += align256(sizeof(int32_t) * (size_t)T);
+  w.cnt = o;     o += align256(sizeof(int32_t) * (size_t)T * (size_t)(L.d_model / 16));
   w.total = o;
   return w;
 }
@@ -109,11 +111,14 @@ struct FfnArgs {
   WsHeader *hdr;
   const int32_t *offs, *active, *perm, *inv;
   const Group *groups;
+  const uint16_t *x16;  // [T][D] x as fp16 (tensor-core path)
   const uint8_t *xs16;  // [T][D/256][64 B] sub-block sums of x
   const float *xs32;    // [T][D/32] block sums of x
   uint8_t *hs16;        // [P][F/256][64 B] sub-block sums of h
-  uint16_t *h;
+  uint16_t *h;          // [P][F] hidden: fp16 (tensor-core path) or bf16 (SIMT)
   float *y;
+  const int32_t *nvalid;  // [T] experts in range per token
+  int32_t *cnt;           // [T][D/16] arrival counters of the fused combine (nullptr: separate combine)
 };
 
 cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s);
@@ -122,6 +127,25 @@ cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s);
 bool decode_mma_ok(const ds4moe_layer &L);
 
 int num_sms();
+
+// Launch with programmatic stream serialization (the kernel overlaps the
+// tail of the preceding grid and must call ptx::pdl_wait before consuming
+// its outputs).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Brackets one kernel launch with CUDA events while profiling is enabled
 // (ds4moe_profile_enable); a no-op otherwise and during stream capture.

@@ -54,11 +54,21 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+// ------------------------------------------------------- dependent launch
+// Programmatic dependent launch: wait until the preceding grid in the stream
+// has completed and its writes are visible (a no-op without the launch
+// attribute); allow the next grid to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------- loads
 // Plain C++ loads so the compiler can schedule them; the mbarrier wait's
 // memory clobber keeps shared-memory reads after the copy completes.
 __device__ __forceinline__ uint32_t lds32(const void *p) { return *static_cast<const uint32_t *>(p); }
 __device__ __forceinline__ uint2 ldg_nc_v2(const void *p) { return __ldg(static_cast<const uint2 *>(p)); }
+// L2-only loads for data written by the preceding grid of a dependent launch.
+__device__ __forceinline__ uint2 ldcg_v2(const void *p) { return __ldcg(static_cast<const uint2 *>(p)); }
+__device__ __forceinline__ uint4 ldcg_v4(const void *p) { return __ldcg(static_cast<const uint4 *>(p)); }
 
 // ------------------------------------------------------------------ math
 // D += A * B, m16n8k16, bf16 inputs, fp32 accumulate.
@@ -68,6 +78,26 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D += A * B, m16n8k16, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Packed fp16x2 fused multiply-add / multiply, one rounding per lane.
+__device__ __forceinline__ uint32_t fma_f16x2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // Packed bf16x2 fused multiply-add, one rounding per lane.

@@ -140,9 +140,9 @@ size_t ds4moe_workspace_bytes(const ds4moe_layer *L, int32_t T, int32_t k,
                               int32_t prefill);
 
 /*
- * ds4moe_workspace_init -- DEVICE.  Clears the status word and the
- * persistent counters of a fresh workspace.  Call once after allocating it
- * (and after any ds4moe_stream_status that reported an error).
+ * ds4moe_workspace_init -- DEVICE.  Zeroes the workspace (status word and
+ * the counters the kernels leave at zero after every call).  Call once after
+ * allocating it, and again after any call that reported an error.
  */
 ds4moe_status ds4moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
@@ -195,6 +195,20 @@ ds4moe_status ds4moe_ffn_prefill(const ds4moe_layer *L, const uint16_t *x,
                                  const int32_t *idx, const float *w, int32_t T,
                                  int32_t k, float *out, void *ws, size_t ws_bytes,
                                  void *stream);
+
+/*
+ * ds4moe_moe_decode -- DEVICE.  One decode step of a routed-MoE layer in
+ * one call: ds4moe_route_topk followed by ds4moe_ffn_decode, with the same
+ * results (idx / w are written as outputs), but scheduled as one chain of
+ * kernels: the router's ranking runs inside the bucketing kernel and the
+ * weighted combine inside the down projection.  Same arguments and
+ * constraints as those two calls; `ws` must hold
+ * ds4moe_workspace_bytes(L, T, k, 0) bytes.
+ */
+ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const float *Wr,
+                                const float *bias, int32_t T, int32_t k, float *out,
+                                int32_t *idx, float *w, void *ws, size_t ws_bytes,
+                                void *stream);
 
 /*
  * ds4moe_stream_status -- synchronizes `stream`, then reads and clears the

@@ -45,6 +45,21 @@ def gpu_forward(M, dev, x, Wr, bias, k, prefill=False, idx_override=None, w_over
     return out.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy(), st
 
 
+def gpu_moe_decode(M, dev, x, Wr, bias, k):
+    """The fused decode entry point: (out, idx, w, status)."""
+    import torch
+    from bit_quantized_moe_q2_gb300.device import workspace
+    T = x.shape[0]
+    idx = torch.full((T, k), -5, dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    out = torch.full((T, dev.d_model), float("nan"), dtype=torch.float32, device="cuda")
+    ws = workspace(dev, T, k)
+    M.ds4moe_moe_decode(dev.abi, torch_bf16_bits(x), torch.from_numpy(Wr).cuda(),
+                        None if bias is None else torch.from_numpy(bias).cuda(), k, out, idx, w, ws)
+    st = M.ds4moe_stream_status(ws)
+    return out.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy(), st
+
+
 def oracle_out(L, x, idx, w):
     ww = L.w
     return oracle.moe_ffn(ww.d_model, ww.d_ff, ww.n_expert, L.qg, L.gate, L.qu, L.up, L.qd, L.down, x, idx, w)
@@ -92,6 +107,23 @@ def test_reduced_layers_all_tokens(M, wi, prefill):
     assert np.array_equal(idx, ridx)
     ref = oracle_out(L, x, ridx, rw)
     assert rel_err(out, ref) <= TOL
+
+
+@pytest.mark.parametrize("wi", range(len(REDUCED)))
+def test_fused_decode_entry_point(M, wi):
+    w = REDUCED[wi]
+    L = build_layer(w)
+    dev = to_device(L)
+    x = synth.activations(w)
+    out, idx, wt, st = gpu_moe_decode(M, dev, x, L.Wr, L.bias, w.k)
+    assert st == M.DS4MOE_OK
+    ridx, rw, _ = oracle.route(x, L.Wr, L.bias, w.k)
+    assert np.array_equal(idx, ridx)
+    assert np.abs(wt.view(np.int32).astype(np.int64) - rw.view(np.int32)).max() <= 2
+    assert rel_err(out, oracle_out(L, x, ridx, rw)) <= TOL
+    # and twice in a row on the same workspace-free call pattern gives the same bits
+    out2, idx2, _, _ = gpu_moe_decode(M, dev, x, L.Wr, L.bias, w.k)
+    assert np.array_equal(out2.view(np.uint32), out.view(np.uint32)) and np.array_equal(idx2, idx)
 
 
 @pytest.mark.parametrize("wi", [0, 4])
@@ -150,6 +182,18 @@ def _sample_tokens(idx, n_expert, n):
     for e in light:
         pick |= set(np.nonzero((idx == e).any(1))[0][:4].tolist())
     return np.array(sorted(pick))
+
+
+def test_full_workload_fused_decode_t1(M):
+    w = synth.WORKLOADS[1]
+    L, dev = cached_layer(w)
+    for batch in (0, 1, 2):
+        x = synth.activations(w, batch=batch)
+        out, idx, wt, st = gpu_moe_decode(M, dev, x, L.Wr, L.bias, w.k)
+        assert st == M.DS4MOE_OK
+        ridx, rw, _ = oracle.route(x, L.Wr, L.bias, w.k)
+        assert np.array_equal(idx, ridx)
+        assert rel_err(out, oracle_out(L, x, ridx, rw)) <= TOL
 
 
 @pytest.mark.parametrize("wid,prefill", [(0, False), (1, False), (2, False), (3, True)])
