@@ -142,15 +142,13 @@ __device__ __forceinline__ bool ranks_before(float va, int a, float vb, int b) {
   return a < b;
 }
 
-// Top-k + softmax of one token's E <= 256 logits held in registers by one
-// warp (entry lane + 32 j in v[j]); shared by the fused router and the
-// stand-alone top-k kernel.
-__device__ __forceinline__ void topk_softmax_warp(const float (&v)[8], int E, int k, int32_t *__restrict__ idx,
-                                                  float *__restrict__ w) {
+// Top-k of one token's E <= 256 logits held in registers by one warp (entry
+// lane + 32 j in v[j]): lane i < k receives the i-th selected (logit, id).
+__device__ __forceinline__ void topk_select_warp(const float (&v)[8], int E, int k, float &my_v, int &my_e) {
   const int lane = threadIdx.x & 31;
   uint32_t taken = 0;
-  float my_v = 0.f;
-  int my_e = -1;
+  my_v = 0.f;
+  my_e = -1;
   for (int i = 0; i < k; ++i) {
     float bv = 0.f;
     int be = -1;
@@ -171,13 +169,29 @@ __device__ __forceinline__ void topk_softmax_warp(const float (&v)[8], int E, in
     if (be >= 0 && (be & 31) == lane) taken |= 1u << (be >> 5);
     if (lane == i) { my_v = bv; my_e = be; }
   }
+}
+
+// Softmax over the k selected logits (lane i < k holds the i-th): in
+// double, summed in rank order, rounded once to fp32.
+__device__ __forceinline__ float softmax_selected_warp(float my_v, int k) {
+  const int lane = threadIdx.x & 31;
   const double m = (double)__shfl_sync(0xffffffffu, my_v, 0);
   const double ex = lane < k ? exp((double)my_v - m) : 0.0;
   double sum = 0.0;
   for (int i = 0; i < k; ++i) sum += __shfl_sync(0xffffffffu, ex, i);
+  return (float)(ex / sum);
+}
+
+__device__ __forceinline__ void topk_softmax_warp(const float (&v)[8], int E, int k, int32_t *__restrict__ idx,
+                                                  float *__restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  float my_v;
+  int my_e;
+  topk_select_warp(v, E, k, my_v, my_e);
+  const float wi = softmax_selected_warp(my_v, k);
   if (lane < k) {
     idx[lane] = my_e;
-    w[lane] = (float)(ex / sum);
+    w[lane] = wi;
   }
 }
 
@@ -330,6 +344,51 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict_
   if (tid == 0) hdr->route_done = 0u;
 }
 
+// fp16 copy of x and its sub-block (16-value) / block (32-value) sums for
+// the tensor-core decode kernels, by `n` threads numbered from `i0`.
+// bf16 -> fp16 is exact for |x| in [2^-14, 65504]; larger magnitudes are
+// flagged as a data error.
+__device__ __forceinline__ void convert_x(const uint16_t *__restrict__ x, int T, int D, uint16_t *__restrict__ x16,
+                                          uint8_t *__restrict__ xs16, float *__restrict__ xs32,
+                                          WsHeader *__restrict__ hdr, int i0, int n) {
+  const int n32 = D / 32;
+  for (int i = i0; i < T * n32; i += n) {
+    const int t = i / n32, b32 = i % n32;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + (int64_t)t * D + 32 * b32);
+    uint4 *x16r = reinterpret_cast<uint4 *>(x16 + (int64_t)t * D + 32 * b32);
+    uint4 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = __ldcg(xr + q);
+    float s[2] = {0.f, 0.f};
+    bool big = false;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t wd[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float lo = bf16_bits_to_f32(wd[r] & 0xFFFFu), hi = bf16_bits_to_f32(wd[r] >> 16);
+        big |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+        o[r] = (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
+        s[q >> 1] += lo + hi;
+      }
+      x16r[q] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int n16 = 2 * b32 + hh;
+      const __half hi = __float2half_rn(s[hh]);
+      const __half lo = __float2half_rn(s[hh] - __half2float(hi));
+      uint16_t *rec = reinterpret_cast<uint16_t *>(xs16 + ((int64_t)t * (D / 256 + 1) + n16 / 16) * 64);
+      rec[n16 & 15] = __half_as_ushort(hi);
+      rec[16 + (n16 & 15)] = __half_as_ushort(lo);
+      big |= fabsf(s[hh]) > 65504.f;
+    }
+    if (big) record_status(hdr, DS4MOE_EDEVICE);
+    xs32[(int64_t)t * n32 + b32] = s[0] + s[1];
+  }
+}
+
 // ---------------------------------------------------------------- bucketing
 // One CTA of 1024 threads.  Pairs p = t*k + i are grouped by expert, stable
 // in p (hence in token order).  Phase A: warp w walks its contiguous slice of
@@ -353,6 +412,87 @@ __global__ void __launch_bounds__(1024) k_bucket(int32_t *__restrict__ idx, int 
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nthr = blockDim.x;
   ptx::pdl_wait();  // idx (or the logits) and x come from the preceding grids
   ptx::pdl_launch_dependents();
+  if (P <= 32) {
+    // Small batch (decode): warp 0 ranks (fused path) and sorts the pairs by
+    // (expert, pair index) from shared memory, warp 1 computes the routing
+    // weights, the other warps convert x -- concurrently.
+    __shared__ int32_t s_idx[32];
+    __shared__ float s_val[32];
+    __shared__ int32_t sorted_e[32];
+    if (wid == 0) {
+      if (logits) {
+        for (int t = 0; t < T; ++t) {
+          float v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int e = lane + 32 * j;
+            v[j] = e < E ? __ldcg(logits + (int64_t)t * E + e) : 0.f;
+          }
+          float my_v;
+          int my_e;
+          topk_select_warp(v, E, k, my_v, my_e);
+          if (lane < k) {
+            s_idx[t * k + lane] = my_e;
+            s_val[t * k + lane] = my_v;
+            idx[(int64_t)t * k + lane] = my_e;
+          }
+        }
+        __syncwarp();
+        asm volatile("bar.arrive 1, 64;" ::: "memory");  // hand the selected logits to warp 1
+      } else if (lane < P) {
+        s_idx[lane] = __ldcg(idx + lane);
+      }
+      __syncwarp();
+      int e = -1;
+      if (lane < P) {
+        e = s_idx[lane];
+        if (e < 0 || e >= E) { record_status(hdr, DS4MOE_EDEVICE); e = -1; }
+      }
+      const unsigned valid = __ballot_sync(0xffffffffu, e >= 0);
+      // valid experts per token (for the fused combine); a token without any
+      // gets a zero output row
+      if (lane < T) {
+        const int nvt = __popc(valid & (uint32_t)(((1ull << k) - 1ull) << (lane * k)));
+        nvalid[lane] = nvt;
+        if (nvt == 0)
+          for (int c = 0; c < D; ++c) out[(int64_t)lane * D + c] = 0.f;
+      }
+      const int key = e >= 0 ? e * 32 + lane : 0x7FFFFFFF;
+      int rank = 0;
+      for (int q = 0; q < 32; ++q) rank += __shfl_sync(0xffffffffu, key, q) < key;
+      if (lane < P) inv[lane] = e >= 0 ? rank : -1;
+      if (e >= 0) perm[rank] = lane;
+      // sorted view: lane r holds the expert of the r-th pair
+      if (e >= 0) sorted_e[rank] = e;
+      __syncwarp();
+      const int nv = __popc(valid);
+      const int er = lane < nv ? sorted_e[lane] : -1;
+      const int eprev = __shfl_up_sync(0xffffffffu, er, 1);
+      const bool run_start = lane < nv && (lane == 0 || eprev != er);
+      const unsigned starts = __ballot_sync(0xffffffffu, run_start);
+      const int rs = 31 - __clz(starts & (0xffffffffu >> (31 - lane)));   // start of this lane's run
+      const bool gstart = lane < nv && ((lane - rs) % kGroup == 0);
+      const unsigned gmask = __ballot_sync(0xffffffffu, gstart);
+      if (gstart) {
+        int run_end = nv;
+        const unsigned later = starts & ~(0xffffffffu >> (31 - lane));
+        if (later) run_end = __ffs(later) - 1;
+        groups[__popc(gmask & ((1u << lane) - 1u))] = Group{er, lane, min(kGroup, run_end - lane), 0};
+      }
+      if (lane == 0) {
+        hdr->n_groups = __popc(gmask);
+        hdr->n_active = __popc(starts);
+      }
+    } else if (wid == 1 && logits) {
+      asm volatile("bar.sync 1, 64;" ::: "memory");
+      for (int t = 0; t < T; ++t) {
+        const float wi = softmax_selected_warp(lane < k ? s_val[t * k + lane] : 0.f, k);
+        if (lane < k) w[(int64_t)t * k + lane] = wi;
+      }
+    }
+    if (wid >= 2 && xs16) convert_x(x, T, D, x16, xs16, xs32, hdr, tid - 64, nthr - 64);
+    return;
+  }
   // fused decode path: rank the experts of every token here (E <= 256)
   if (logits) {
     for (int t = wid; t < T; t += nthr / 32) {
@@ -378,84 +518,7 @@ __global__ void __launch_bounds__(1024) k_bucket(int32_t *__restrict__ idx, int 
     if (nv == 0)
       for (int c = 0; c < D; ++c) out[(int64_t)t * D + c] = 0.f;
   }
-  // fp16 copy of x and its sub-block (16-value) / block (32-value) sums for
-  // the tensor-core decode kernels.  bf16 -> fp16 is exact for |x| in
-  // [2^-14, 65504]; larger magnitudes are flagged as a data error.
-  if (xs16) {
-    const int n32 = D / 32;
-    for (int i = tid; i < T * n32; i += nthr) {
-      const int t = i / n32, b32 = i % n32;
-      const uint4 *xr = reinterpret_cast<const uint4 *>(x + (int64_t)t * D + 32 * b32);
-      uint4 *x16r = reinterpret_cast<uint4 *>(x16 + (int64_t)t * D + 32 * b32);
-      float s[2] = {0.f, 0.f};
-      bool big = false;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 v = __ldcg(xr + q);
-        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const float lo = bf16_bits_to_f32(wd[r] & 0xFFFFu), hi = bf16_bits_to_f32(wd[r] >> 16);
-          big |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
-          o[r] = (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
-          s[q >> 1] += lo + hi;
-        }
-        x16r[q] = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int n16 = 2 * b32 + hh;
-        const __half hi = __float2half_rn(s[hh]);
-        const __half lo = __float2half_rn(s[hh] - __half2float(hi));
-        uint16_t *rec = reinterpret_cast<uint16_t *>(xs16 + ((int64_t)t * (D / 256 + 1) + n16 / 16) * 64);
-        rec[n16 & 15] = __half_as_ushort(hi);
-        rec[16 + (n16 & 15)] = __half_as_ushort(lo);
-        big |= fabsf(s[hh]) > 65504.f;
-      }
-      if (big) record_status(hdr, DS4MOE_EDEVICE);
-      xs32[(int64_t)t * n32 + b32] = s[0] + s[1];
-    }
-  }
-  if (P <= 32) {
-    // small batch: one warp ranks the pairs by (expert, pair index)
-    if (wid == 0) {
-      int e = -1;
-      if (lane < P) {
-        e = __ldcg(idx + lane);
-        if (e < 0 || e >= E) { record_status(hdr, DS4MOE_EDEVICE); e = -1; }
-      }
-      const int key = e >= 0 ? e * 32 + lane : 0x7FFFFFFF;
-      int rank = 0;
-      for (int q = 0; q < 32; ++q) rank += __shfl_sync(0xffffffffu, key, q) < key;
-      const unsigned valid = __ballot_sync(0xffffffffu, e >= 0);
-      if (lane < P) inv[lane] = e >= 0 ? rank : -1;
-      if (e >= 0) perm[rank] = lane;
-      // sorted view: lane r holds the expert of the r-th pair
-      __shared__ int32_t sorted_e[32];
-      if (e >= 0) sorted_e[rank] = e;
-      __syncwarp();
-      const int nv = __popc(valid);
-      const int er = lane < nv ? sorted_e[lane] : -1;
-      const int eprev = __shfl_up_sync(0xffffffffu, er, 1);
-      const bool run_start = lane < nv && (lane == 0 || eprev != er);
-      const unsigned starts = __ballot_sync(0xffffffffu, run_start);
-      const int rs = 31 - __clz(starts & (0xffffffffu >> (31 - lane)));   // start of this lane's run
-      const bool gstart = lane < nv && ((lane - rs) % kGroup == 0);
-      const unsigned gmask = __ballot_sync(0xffffffffu, gstart);
-      if (gstart) {
-        int run_end = nv;
-        const unsigned later = starts & ~(0xffffffffu >> (31 - lane));
-        if (later) run_end = __ffs(later) - 1;
-        groups[__popc(gmask & ((1u << lane) - 1u))] = Group{er, lane, min(kGroup, run_end - lane), 0};
-      }
-      if (lane == 0) {
-        hdr->n_groups = __popc(gmask);
-        hdr->n_active = __popc(starts);
-      }
-    }
-    return;
-  }
+  if (xs16) convert_x(x, T, D, x16, xs16, xs32, hdr, tid, nthr);
   for (int i = tid; i < 32 * E; i += nthr) wcnt[i] = 0;
   __syncthreads();
   const int R = (P + 31) / 32;
@@ -633,7 +696,14 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
   const size_t smem = sizeof(int32_t) * (32 * (size_t)E + E + 1);
   static bool attr_set = false;
   if (!attr_set) {
+    // one shared-memory carveout for every kernel of the chain: consecutive
+    // grids then never wait for an SM to reconfigure its L1/shared split
     cudaFuncSetAttribute(k_bucket, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    cudaFuncSetAttribute(k_bucket, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    for (auto kern : {k_route_small<1, false>, k_route_small<2, false>, k_route_small<4, false>,
+                      k_route_small<8, false>, k_route_small<1, true>, k_route_small<2, true>,
+                      k_route_small<4, true>, k_route_small<8, true>})
+      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     attr_set = true;
   }
   cudaError_t e = cudaSuccess;

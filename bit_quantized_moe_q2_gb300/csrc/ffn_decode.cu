@@ -650,6 +650,8 @@ cudaError_t launch_gate_up_mma(const FfnArgs &a, cudaStream_t s, int kp) {
   auto kern = k_gate_up_mma<QG, QU>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return e;
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 2 * kp * 32, smem);
   if (e != cudaSuccess) return e;
@@ -667,6 +669,8 @@ cudaError_t launch_down_mma(const FfnArgs &a, cudaStream_t s) {
   const size_t smem = (size_t)nw * 16 * chd + 8 * nw;
   auto kern = k_down_mma<1>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, nw * 32, smem);
