@@ -390,7 +390,8 @@ __device__ __forceinline__ void convert_x(const uint16_t *__restrict__ x, int T,
 }
 
 // ---------------------------------------------------------------- bucketing
-// One CTA of 1024 threads.  Pairs p = t*k + i are grouped by expert, stable
+// One CTA (256 threads for the decode batch path, P <= 32, which leaves the
+// expert offsets unwritten; else 1024).  Pairs p = t*k + i are grouped by expert, stable
 // in p (hence in token order).  Phase A: warp w walks its contiguous slice of
 // pairs 32 at a time and ranks each pair among same-expert pairs of the slice
 // (__match_any_sync); Phase B: per-expert totals, exclusive offsets and
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(1024) k_bucket(int32_t *__restrict__ idx, int 
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nthr = blockDim.x;
   ptx::pdl_wait();  // idx (or the logits) and x come from the preceding grids
   ptx::pdl_launch_dependents();
-  if (P <= 32) {
+  if (nthr <= 256) {  // the host picks 256 threads only for P <= 32
     // Small batch (decode): warp 0 ranks (fused path) and sorts the pairs by
     // (expert, pair index) from shared memory, warp 1 computes the routing
     // weights, the other warps convert x -- concurrently.
@@ -690,7 +691,14 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
   a.xs32 = ws_ptr<float>(ws, lay.xs32);
   a.hs16 = ws_ptr<uint8_t>(ws, lay.hs16);
   a.nvalid = ws_ptr<int32_t>(ws, lay.nvalid);
-  const bool sums = decode_mma_ok(*L);
+  const bool tc = prefill && prefill_tc_ok(*L);
+  if (tc) {
+    a.xp = ws_ptr<uint16_t>(ws, lay.xp);
+    a.chunks_gu = ws_ptr<Chunk>(ws, lay.chunks_gu);
+    a.chunks_dn = ws_ptr<Chunk>(ws, lay.chunks_dn);
+    a.nchunks = ws_ptr<int32_t>(ws, lay.nchunks);
+  }
+  const bool sums = !tc && decode_mma_ok(*L);
   a.cnt = sums ? ws_ptr<int32_t>(ws, lay.cnt) : nullptr;
   const int E = L->n_expert, P = T * k;
   const size_t smem = sizeof(int32_t) * (32 * (size_t)E + E + 1);
@@ -709,8 +717,9 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
   cudaError_t e = cudaSuccess;
   {
     ProfScope prof("bucket", s);
-    const int threads = P <= 32 ? 256 : 1024;
-    e = launch_pdl(k_bucket, dim3(1), dim3(threads), P <= 32 ? 0 : smem, s, const_cast<int32_t *>(idx), P, E, a.hdr,
+    // the tensor-core prefill reads the expert offsets: always the full path
+    const int threads = P <= 32 && !tc ? 256 : 1024;
+    e = launch_pdl(k_bucket, dim3(1), dim3(threads), threads == 256 ? 0 : smem, s, const_cast<int32_t *>(idx), P, E, a.hdr,
                    ws_ptr<int32_t>(ws, lay.counts), ws_ptr<int32_t>(ws, lay.offs), ws_ptr<int32_t>(ws, lay.active),
                    ws_ptr<int32_t>(ws, lay.perm), ws_ptr<int32_t>(ws, lay.inv), ws_ptr<int32_t>(ws, lay.lrank),
                    ws_ptr<Group>(ws, lay.groups), x, (int)T, (int)L->d_model, ws_ptr<uint16_t>(ws, lay.x16),

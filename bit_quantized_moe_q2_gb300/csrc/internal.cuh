@@ -48,14 +48,25 @@ struct Group {
 // parts (sum of sub-block n ~= hi[n] + lo[n]), in sub-block order.
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
+// A token chunk of the prefill grouped GEMMs: n <= BN consecutive
+// expert-sorted pairs p0 .. p0+n-1, all routed to expert e.
+struct Chunk {
+  int32_t e, p0, n, pad;
+};
+// Token-chunk widths of the prefill kernels (gate/up and down).
+constexpr int kChunkGateUp = 128, kChunkDown = 256;
+// Row length of the gathered prefill activations: D fp16 values, then the
+// hi/lo fp16 parts of the D/32 block sums.
+inline int64_t xp_cols(int64_t D) { return D + D / 16; }
+
 struct WsLayout {
   size_t hdr, logits, counts, offs, active, perm, inv, lrank, groups, x16, xs16, xs32, hs16, h, y, nvalid, cnt,
-      total;
+      xp, chunks_gu, chunks_dn, nchunks, total;
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-inline WsLayout ws_layout(const ds4moe_layer &L, int T, int k, int /*prefill*/) {
+inline WsLayout ws_layout(const ds4moe_layer &L, int T, int k, int prefill) {
   WsLayout w{};
   size_t o = 0;
   const size_t E = (size_t)L.n_expert, P = (size_t)T * (size_t)k;
@@ -76,6 +87,13 @@ inline WsLayout ws_layout(const ds4moe_layer &L, int T, int k, int /*prefill*/) 
   w.y = o;       o += align256(sizeof(float) * P * (size_t)L.d_model);
   w.nvalid = o;  o += align256(sizeof(int32_t) * (size_t)T);
   w.cnt = o;     o += align256(sizeof(int32_t) * (size_t)T * (size_t)(L.d_model / 16));
+  if (prefill) {  // tensor-core prefill: x gathered in pair order, token chunks
+    const size_t ne = E < P ? E : P;
+    w.xp = o;        o += align256(sizeof(uint16_t) * P * (size_t)xp_cols(L.d_model));
+    w.chunks_gu = o; o += align256(sizeof(Chunk) * (ne + P / kChunkGateUp + 1));
+    w.chunks_dn = o; o += align256(sizeof(Chunk) * (ne + P / kChunkDown + 1));
+    w.nchunks = o;   o += align256(2 * sizeof(int32_t));
+  }
   w.total = o;
   return w;
 }
@@ -119,12 +137,17 @@ struct FfnArgs {
   float *y;
   const int32_t *nvalid;  // [T] experts in range per token
   int32_t *cnt;           // [T][D/16] arrival counters of the fused combine (nullptr: separate combine)
+  // tensor-core prefill only (nullptr otherwise)
+  uint16_t *xp;           // [P][D] x of each sorted pair, fp16
+  Chunk *chunks_gu, *chunks_dn;
+  int32_t *nchunks;       // [2]: chunk counts of chunks_gu / chunks_dn
 };
 
 cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_ffn_prefill(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s);
 bool decode_mma_ok(const ds4moe_layer &L);
+bool prefill_tc_ok(const ds4moe_layer &L);
 
 int num_sms();
 
