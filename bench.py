@@ -16,6 +16,11 @@ with CUDA events on its launch stream), the CPU oracle as a baseline, the
 end-to-end number through the C ABI with host buffers, and SM clocks sampled
 during the timed region.
 
+`--workload 3` times the prefill chunk instead: 4096 tokens per step (router
+with bias, top-6 of 256, Q4_1 gate/up, Q2_K down) through ds4moe_route_topk +
+ds4moe_ffn_prefill, reported as tokens/s and TFLOP/s with the tensor-core
+roofline of the gate/up grouped GEMM.
+
 `--impl reference` times the CPU oracle itself (the program the CUDA path is
 checked against) on the same metric, each step a bounded sample.
 """
@@ -51,7 +56,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", type=int, default=1, help="workload id in synth.WORKLOADS (decode: 0, 1, 2)")
+    ap.add_argument("--workload", type=int, default=1,
+                    help="workload id in synth.WORKLOADS (decode: 0, 1, 2; prefill: 3)")
     ap.add_argument("--cpu-tokens", type=int, default=0, help="tokens in the CPU-baseline sample (0: 2 x cores)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--copies", type=int, default=N_COPIES,
@@ -211,6 +217,24 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return 6800.0, "fallback"
+
+
+def measured_tensor_peak(sustained: bool):
+    """Dense bf16 TFLOP/s (kind::f16 runs at the same rate)."""
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)[key]), "measured"
+    except (OSError, KeyError, ValueError):
+        return (1700.0 if sustained else 1900.0), "fallback"
+
+
+def prefill_flops(w: synth.Workload) -> tuple[float, float]:
+    """(whole step, gate/up kernel) algorithmic FLOPs: 2 * 3 * D * F per
+    (token, selected expert) plus the router's 2 * D * E per token."""
+    pairs = w.T * w.k
+    ffn = 2.0 * 3 * w.d_model * w.d_ff * pairs
+    return ffn + 2.0 * w.d_model * w.n_expert * w.T, 2.0 * 2 * w.d_model * w.d_ff * pairs
 
 
 def cores_available() -> int:
@@ -474,13 +498,151 @@ def run_ours(args, w: synth.Workload):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------- prefill chunk arm
+def run_ours_prefill(args, w: synth.Workload):
+    """Prefill: route (with bias) + tensor-core expert FFN over T tokens per
+    step.  Inputs (3.4 GB of weights) far exceed L2, so no flush is needed."""
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    from bit_quantized_moe_q2_gb300 import _build
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier(world)
+    import bit_quantized_moe_q2_gb300 as M
+    from bit_quantized_moe_q2_gb300.device import check_status, workspace
+
+    dev = device_layer(w, M, torch)
+    Wr, bias = synth.router(w)
+    Wr_d = torch.from_numpy(Wr).cuda()
+    b_d = None if bias is None else torch.from_numpy(bias).cuda()
+    T, k, D = w.T, w.k, w.d_model
+    n_slots = 2
+    xs_host = [synth.activations(w, T=T, batch=rank_batch_offset(rank) + s) for s in range(n_slots)]
+    xs = [torch.from_numpy(x.view(np.int16)).cuda() for x in xs_host]
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    out = torch.empty((T, D), dtype=torch.float32, device="cuda")
+    ws = workspace(dev, T, k, prefill=True)
+    stream = torch.cuda.Stream()
+
+    def step(i, x=None):
+        xin = xs[i % n_slots] if x is None else x
+        M.ds4moe_route_topk(xin, Wr_d, b_d, k, idx, wt, None, ws, stream)
+        M.ds4moe_ffn_prefill(dev.abi, xin, idx, wt, out, ws, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    stream.synchronize()
+    check_status(ws, stream)
+    counts = np.bincount(idx.cpu().numpy().ravel(), minlength=w.n_expert)
+
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.mark(True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    barrier(world)
+    clocks = sampler.stop()
+    ms = reduce_max(ev0.elapsed_time(ev1), world)
+    check_status(ws, stream)
+    flops_step, flops_gu = prefill_flops(w)
+    value = world * args.steps * T / (ms / 1000.0)
+    tflops = world * args.steps * flops_step / (ms / 1000.0) / 1e12
+    if args.timed_only:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": "tokens/s", "tflops": tflops,
+                              "ms_per_step": ms / args.steps, "steps": args.steps, "note": "timed-only run"}),
+                  flush=True)
+        return
+
+    # per-kernel times (CUDA events around each launch on its stream)
+    kp = min(args.steps, 10)
+    M.ds4moe_profile_enable(True)
+    with torch.cuda.stream(stream):
+        for i in range(kp):
+            step(i)
+    stream.synchronize()
+    prof = M.ds4moe_profile_read()
+    M.ds4moe_profile_enable(False)
+    launches_per_step = sum(n for _, n in prof.values()) / kp
+    kernels = {n: {"avg_us": 1000 * t / c, "launches_per_step": c / kp} for n, (t, c) in prof.items()}
+    gu_ms, gu_n = prof.get("gate_up_tc", (float("nan"), 1))
+    gu_s = gu_ms / gu_n / 1000.0
+    peak, peak_kind = measured_tensor_peak(sustained=True)
+    roofline = {"kernel": "gate_up_tc (tcgen05 grouped GEMM, fused Q4_1 dequant + SwiGLU)", "bound": "tensor",
+                "achieved": flops_gu / gu_s / 1e12, "peak": peak, "unit": "TFLOP/s",
+                "frac": flops_gu / gu_s / 1e12 / peak, "traffic": None,
+                "algorithmic_flops_per_launch": flops_gu, "avg_launch_us": gu_s * 1e6,
+                "peak_source": f"{peak_kind} bf16_tflops_sustained (kind::f16 runs at the bf16 rate)"}
+
+    # end to end with host buffers: pinned x in, out back, per step
+    ke = min(args.steps, 5)
+    xh = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs_host]
+    oh = torch.empty((T, D), dtype=torch.float32).pin_memory()
+    x_in = torch.empty((T, D), dtype=torch.int16, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(ke):
+            x_in.copy_(xh[i % n_slots], non_blocking=True)
+            step(i, x_in)
+            oh.copy_(out, non_blocking=True)
+            stream.synchronize()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world)
+    e2e = {"value": world * ke * T / (e2e_ms / 1000.0), "unit": "tokens/s", "steps": ke,
+           "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 4,
+           "path": "pinned H2D x, ds4moe_route_topk + ds4moe_ffn_prefill (C-ABI calls), D2H out, sync per step"}
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        n = args.cpu_tokens or 2 * cores_available()
+        cpu = cpu_baseline(w, n, batch0=50_000)
+    cfg = workload_config(w, 1)
+    cfg["l2"] = "inputs larger than L2: every step streams 3.4 GB of expert weights"
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16 tensor-core operands (exact gate/up split), f32 accumulate",
+            "data": "synthetic", "config": cfg, "tflops": tflops,
+            "tensor_frac": tflops / peak, "roofline": roofline, "kernels": kernels,
+            "expert_load": {"max": int(counts.max()), "min": int(counts.min()), "empty": int((counts == 0).sum())},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(round(launches_per_step * args.steps)),
+            "clocks": clocks}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
     w = synth.WORKLOADS[args.workload]
-    if w.path != "decode":
-        raise SystemExit("bench.py times the decode workloads (0, 1, 2)")
+    if w.path not in ("decode", "prefill") or w.n_layers != 1:
+        raise SystemExit("bench.py times the one-layer workloads (decode: 0, 1, 2; prefill: 3)")
     if args.impl == "reference":
         run_reference(args, w)
+    elif w.path == "prefill":
+        run_ours_prefill(args, w)
     else:
         run_ours(args, w)
 

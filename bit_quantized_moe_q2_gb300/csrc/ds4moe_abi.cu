@@ -87,18 +87,13 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
-// One warp per (t, e): Dot2 over d_model, lanes own interleaved float4
-// slices, the (sum, error) pairs are merged across lanes with TwoSum, the
-// bias is added with TwoSum, and the result is rounded once.
-__global__ void k_router_logits(const uint16_t *__restrict__ x, const float *__restrict__ Wr,
-                                const float *__restrict__ bias, int T, int D, int E,
-                                float *__restrict__ logits) {
-  const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+// One warp computes x_t . Wr_e (+ bias) with Dot2: lanes own interleaved
+// float4 slices, the (sum, error) pairs are merged across lanes with TwoSum,
+// the bias is added with TwoSum, and the result is rounded once.  Every lane
+// returns the same value.
+__device__ __forceinline__ float dot2_row_warp(const uint16_t *__restrict__ xr, const float *__restrict__ wr, int D,
+                                               const float *bias_e) {
   const int lane = threadIdx.x & 31;
-  if (gw >= (int64_t)T * E) return;
-  const int t = (int)(gw / E), e = (int)(gw % E);
-  const uint16_t *xr = x + (int64_t)t * D;
-  const float *wr = Wr + (int64_t)e * D;
   float s = 0.f, c = 0.f;
   for (int j = 4 * lane; j < D; j += 128) {
     const float4 wv = *reinterpret_cast<const float4 *>(wr + j);
@@ -122,13 +117,27 @@ __global__ void k_router_logits(const uint16_t *__restrict__ x, const float *__r
     two_sum(s, so, s, se);
     c = __fadd_rn(c, __fadd_rn(co, se));
   }
-  if (lane == 0) {
-    if (bias) {
-      float se;
-      two_sum(s, bias[e], s, se);
-      c = __fadd_rn(c, se);
-    }
-    logits[(int64_t)t * E + e] = __fadd_rn(s, c);
+  if (bias_e) {
+    float se;
+    two_sum(s, *bias_e, s, se);
+    c = __fadd_rn(c, se);
+  }
+  return __fadd_rn(s, c);
+}
+
+// One warp per (t, e) (or per (listed token, e) when `list` is given, for
+// the tokens the certified fast path handed back): exact logits.
+__global__ void k_router_logits(const uint16_t *__restrict__ x, const float *__restrict__ Wr,
+                                const float *__restrict__ bias, int T, int D, int E,
+                                float *__restrict__ logits, const int32_t *__restrict__ list = nullptr,
+                                const int32_t *__restrict__ count = nullptr) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n = list ? (int64_t)*count * E : (int64_t)T * E;
+  for (int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; gw < n;
+       gw += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int t = list ? list[gw / E] : (int)(gw / E), e = (int)(gw % E);
+    const float v = dot2_row_warp(x + (int64_t)t * D, Wr + (int64_t)e * D, D, bias ? bias + e : nullptr);
+    if (lane == 0) logits[(int64_t)t * E + e] = v;
   }
 }
 
@@ -197,11 +206,9 @@ __device__ __forceinline__ void topk_softmax_warp(const float (&v)[8], int E, in
 
 // One warp per token: top-k + softmax over logits already in memory
 // (E <= 256 in registers; larger E re-reads its row each round).
-__global__ void k_topk_softmax(const float *__restrict__ logits, int T, int E, int k,
-                               int32_t *__restrict__ idx, float *__restrict__ w) {
-  const int t = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+__device__ __forceinline__ void topk_softmax_row(const float *__restrict__ logits, int t, int E, int k,
+                                                 int32_t *__restrict__ idx, float *__restrict__ w) {
   const int lane = threadIdx.x & 31;
-  if (t >= T) return;
   const float *l = logits + (int64_t)t * E;
   if (E <= 256) {
     float v[8];
@@ -237,6 +244,201 @@ __global__ void k_topk_softmax(const float *__restrict__ logits, int T, int E, i
   if (lane < k) {
     idx[(int64_t)t * k + lane] = my_e;
     w[(int64_t)t * k + lane] = (float)(ex / sum);
+  }
+}
+
+// With `list`, only the listed tokens (count of them).
+__global__ void k_topk_softmax(const float *__restrict__ logits, int T, int E, int k,
+                               int32_t *__restrict__ idx, float *__restrict__ w,
+                               const int32_t *__restrict__ list = nullptr, const int32_t *__restrict__ count = nullptr) {
+  const int n = list ? *count : T;
+  for (int gw = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5); gw < n;
+       gw += (int)(((int64_t)gridDim.x * blockDim.x) >> 5))
+    topk_softmax_row(logits, list ? list[gw] : gw, E, k, idx, w);
+}
+
+// ------------------------------------------------- certified router (large T)
+// Approximate logits (no bias) for the certified fast path: a tiled fp32
+// GEMM, 64 tokens x 64 experts per CTA and 4 x 4 outputs per thread.  Each
+// output is a sum of 64-term FMA chains over consecutive 64-value chunks of
+// K, each chunk started from zero and then added to the running total, so
+// it carries at most 64 + D/64 roundings: |error| <= gamma_n * sum_j
+// |x_j w_j| with gamma_n = n u / (1 - n u), u = 2^-24 (Higham, "Accuracy and
+// Stability of Numerical Algorithms", 2nd ed., section 3.1).
+constexpr int kRT = 64, kRK = 32;
+__global__ void __launch_bounds__(256) k_router_approx(const uint16_t *__restrict__ x, const float *__restrict__ Wr,
+                                                       int T, int D, int E, float *__restrict__ lg) {
+  __shared__ __align__(16) float Xs[kRK][kRT + 4];
+  __shared__ __align__(16) float Ws[kRK][kRT + 4];
+  const int t0 = blockIdx.y * kRT, e0 = blockIdx.x * kRT;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int lr = tid >> 2, lc = (tid & 3) * 8;  // staging: row lr, k lc .. lc + 7
+  float tot[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tot[i][j] = 0.f;
+  for (int k0 = 0; k0 < D; k0 += 64) {
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int kc = k0; kc < k0 + 64; kc += kRK) {
+      {
+        const int t = t0 + lr;
+        const uint4 v = t < T ? *reinterpret_cast<const uint4 *>(x + (int64_t)t * D + kc + lc) : make_uint4(0, 0, 0, 0);
+        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          Xs[lc + 2 * q][lr] = bf16_bits_to_f32(wd[q] & 0xFFFFu);
+          Xs[lc + 2 * q + 1][lr] = bf16_bits_to_f32(wd[q] >> 16);
+        }
+        const int e = e0 + lr;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+        if (e < E) {
+          a = *reinterpret_cast<const float4 *>(Wr + (int64_t)e * D + kc + lc);
+          b = *reinterpret_cast<const float4 *>(Wr + (int64_t)e * D + kc + lc + 4);
+        }
+        Ws[lc + 0][lr] = a.x; Ws[lc + 1][lr] = a.y; Ws[lc + 2][lr] = a.z; Ws[lc + 3][lr] = a.w;
+        Ws[lc + 4][lr] = b.x; Ws[lc + 5][lr] = b.y; Ws[lc + 6][lr] = b.z; Ws[lc + 7][lr] = b.w;
+      }
+      __syncthreads();
+#pragma unroll 8
+      for (int kk = 0; kk < kRK; ++kk) {
+        const float4 xv = *reinterpret_cast<const float4 *>(&Xs[kk][ty * 4]);
+        const float4 wv = *reinterpret_cast<const float4 *>(&Ws[kk][tx * 4]);
+        const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xa[i], wa[j], acc[i][j]);
+      }
+      __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tot[i][j] = __fadd_rn(tot[i][j], acc[i][j]);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) lg[(int64_t)t * E + e] = tot[i][j];
+    }
+  }
+}
+
+// Euclidean norms of the T rows of x and the E rows of Wr (one warp per
+// row), rounded up so that |x_t . w_e| sums are bounded by xn[t] * wn[e]
+// (Cauchy-Schwarz).
+__global__ void k_row_norms(const uint16_t *__restrict__ x, int T, const float *__restrict__ Wr, int E, int D,
+                            float *__restrict__ xn, float *__restrict__ wn) {
+  const int lane = threadIdx.x & 31;
+  for (int r = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5); r < T + E;
+       r += (int)(((int64_t)gridDim.x * blockDim.x) >> 5)) {
+    float ss = 0.f;
+    if (r < T) {
+      const uint16_t *xr = x + (int64_t)r * D;
+      for (int j = 2 * lane; j < D; j += 64) {
+        const uint32_t v = *reinterpret_cast<const uint32_t *>(xr + j);
+        const float a = bf16_bits_to_f32(v & 0xFFFFu), b = bf16_bits_to_f32(v >> 16);
+        ss = fmaf(a, a, fmaf(b, b, ss));
+      }
+    } else {
+      const float *wr = Wr + (int64_t)(r - T) * D;
+      for (int j = lane; j < D; j += 32) ss = fmaf(wr[j], wr[j], ss);
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    // the fp32 sum of squares is within (D/32 + 6) u of exact; 1 + 2^-10 covers it
+    const float nv = sqrtf(ss) * (1.f + 0x1p-10f);
+    if (lane == 0) (r < T ? xn[r] : wn[r - T]) = nv;
+  }
+}
+
+// One warp per token: top-k over the approximate logits (+ bias); if every
+// selected value minus its error bound stays above every unselected value
+// plus its bound, the selected set is that of the exact logits, and only
+// the k selected logits are recomputed exactly (Dot2) to order them and
+// weight them.  Otherwise the token is handed back (list) for an exact pass
+// over all E logits.
+__global__ void k_topk_cert(const float *__restrict__ lg, const float *__restrict__ bias,
+                            const float *__restrict__ xn, const float *__restrict__ wn,
+                            const uint16_t *__restrict__ x, const float *__restrict__ Wr, int T, int D, int E,
+                            int k, float gam, int32_t *__restrict__ idx, float *__restrict__ w,
+                            int32_t *__restrict__ list, int32_t *__restrict__ count) {
+  const int lane = threadIdx.x & 31;
+  for (int t = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5); t < T;
+       t += (int)(((int64_t)gridDim.x * blockDim.x) >> 5)) {
+    float v[8], bd[8];
+    bool finite = true;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = 0.f;
+      bd[j] = 0.f;
+      if (e < E) {
+        v[j] = __fadd_rn(lg[(int64_t)t * E + e], bias ? bias[e] : 0.f);
+        bd[j] = gam * xn[t] * wn[e] + 0x1p-21f * fabsf(v[j]) + 0x1p-126f;
+        finite &= isfinite(v[j]) && isfinite(bd[j]);
+      }
+    }
+    float my_v;
+    int my_e;
+    topk_select_warp(v, E, k, my_v, my_e);
+    uint32_t selm = 0;
+    for (int i = 0; i < k; ++i) {
+      const int se = __shfl_sync(0xffffffffu, my_e, i);
+      if (se >= 0 && (se & 31) == lane) selm |= 1u << (se >> 5);
+    }
+    float lo = INFINITY, hi = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (lane + 32 * j >= E) continue;
+      if ((selm >> j) & 1u) lo = fminf(lo, v[j] - bd[j]);
+      else hi = fmaxf(hi, v[j] + bd[j]);
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+    }
+    finite = __all_sync(0xffffffffu, finite);
+    if (!finite || !(lo > hi)) {
+      if (lane == 0) list[atomicAdd(count, 1)] = t;
+      continue;
+    }
+    // exact logits of the selected experts, then order them exactly
+    float ex = 0.f;
+    for (int i = 0; i < k; ++i) {
+      const int se = __shfl_sync(0xffffffffu, my_e, i);
+      const float val = dot2_row_warp(x + (int64_t)t * D, Wr + (int64_t)se * D, D, bias ? bias + se : nullptr);
+      if (lane == i) ex = val;
+    }
+    int rank = 0;
+    for (int j = 0; j < k; ++j) {
+      const float ov = __shfl_sync(0xffffffffu, ex, j);
+      const int oe = __shfl_sync(0xffffffffu, my_e, j);
+      if (lane < k && j != lane && ranks_before(ov, oe, ex, my_e)) ++rank;
+    }
+    float rv = 0.f;
+    int re = -1;
+    for (int r = 0; r < k; ++r) {
+      const int src = __ffs(__ballot_sync(0xffffffffu, lane < k && rank == r)) - 1;
+      const float vv = __shfl_sync(0xffffffffu, ex, src);
+      const int ee = __shfl_sync(0xffffffffu, my_e, src);
+      if (lane == r) { rv = vv; re = ee; }
+    }
+    const float wi = softmax_selected_warp(rv, k);
+    if (lane < k) {
+      idx[(int64_t)t * k + lane] = re;
+      w[(int64_t)t * k + lane] = wi;
+    }
   }
 }
 
@@ -803,7 +1005,13 @@ ds4moe_status ds4moe_route_topk(const uint16_t *x, const float *Wr, const float 
   shape.d_ff = 16;
   shape.n_expert = n_expert;
   const WsLayout lay = ws_layout(shape, T, k, 0);
-  const size_t need = logits ? sizeof(WsHeader) : lay.logits + align256(sizeof(float) * (size_t)T * n_expert);
+  // Large batches without a logits output take the certified fast path
+  // (approximate fp32 GEMM + error bounds; exact Dot2 for the selected
+  // experts and for tokens whose top-k boundary is within the bounds).
+  const bool fast = !logits && T > 256 && n_expert <= 256 && d_model % 64 == 0;
+  const size_t need = fast     ? lay.rlist + align256(sizeof(int32_t) * ((size_t)T + 64))
+                      : logits ? sizeof(WsHeader)
+                               : lay.logits + align256(sizeof(float) * (size_t)T * n_expert);
   if (ws_bytes < need) return DS4MOE_ESPACE;
   float *lg = logits ? logits : ws_ptr<float>(ws, lay.logits);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -817,6 +1025,38 @@ ds4moe_status ds4moe_route_topk(const uint16_t *x, const float *Wr, const float 
                           : k_route_small<8, true>;
     return cuda_status(launch_pdl(kern, dim3(n_expert), dim3(256), 0, s, x, Wr, bias, (int)T, (int)d_model,
                                   (int)n_expert, (int)k, lg, idx, w, hdr));
+  }
+  if (fast) {
+    float *xn = ws_ptr<float>(ws, lay.rnorm), *wn = xn + T;
+    int32_t *cnt = ws_ptr<int32_t>(ws, lay.rlist), *list = cnt + 64;
+    const int n_chain = 64 + d_model / 64 + 2;
+    const float gam = (float)(n_chain * 0x1p-24 / (1.0 - n_chain * 0x1p-24));
+    cudaError_t e;
+    {
+      ProfScope prof("router_norms", s);
+      k_row_norms<<<num_sms() * 4, 256, 0, s>>>(x, T, Wr, n_expert, d_model, xn, wn);
+      if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
+    }
+    {
+      ProfScope prof("router_approx", s);
+      k_router_approx<<<dim3((n_expert + kRT - 1) / kRT, (T + kRT - 1) / kRT), 256, 0, s>>>(x, Wr, T, d_model,
+                                                                                         n_expert, lg);
+      if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
+    }
+    if ((e = cudaMemsetAsync(cnt, 0, sizeof(int32_t), s)) != cudaSuccess) return cuda_status(e);
+    {
+      ProfScope prof("topk_cert", s);
+      const int grid = (T + 7) / 8 < num_sms() * 8 ? (T + 7) / 8 : num_sms() * 8;
+      k_topk_cert<<<grid, 256, 0, s>>>(lg, bias, xn, wn, x, Wr, T, d_model, n_expert, k, gam, idx, w, list, cnt);
+      if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
+    }
+    {
+      ProfScope prof("router_exact_tail", s);
+      k_router_logits<<<num_sms() * 8, 256, 0, s>>>(x, Wr, bias, T, d_model, n_expert, lg, list, cnt);
+      if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
+      k_topk_softmax<<<num_sms() * 2, 256, 0, s>>>(lg, T, n_expert, k, idx, w, list, cnt);
+    }
+    return cuda_status(cudaGetLastError());
   }
   const int64_t warps = (int64_t)T * n_expert;
   {

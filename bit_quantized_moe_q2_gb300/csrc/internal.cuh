@@ -60,7 +60,7 @@ constexpr int kChunkGateUp = 128, kChunkDown = 256;
 inline int64_t xp_cols(int64_t D) { return D + D / 16; }
 
 struct WsLayout {
-  size_t hdr, logits, counts, offs, active, perm, inv, lrank, groups, x16, xs16, xs32, hs16, h, y, nvalid, cnt,
+  size_t hdr, logits, rnorm, rlist, counts, offs, active, perm, inv, lrank, groups, x16, xs16, xs32, hs16, h, y, nvalid, cnt,
       xp, chunks_gu, chunks_dn, nchunks, total;
 };
 
@@ -72,6 +72,8 @@ inline WsLayout ws_layout(const ds4moe_layer &L, int T, int k, int prefill) {
   const size_t E = (size_t)L.n_expert, P = (size_t)T * (size_t)k;
   w.hdr = o;     o += align256(sizeof(WsHeader));
   w.logits = o;  o += align256(sizeof(float) * (size_t)T * E);
+  w.rnorm = o;   o += align256(sizeof(float) * ((size_t)T + E));    // router fast path: row norms of x, Wr
+  w.rlist = o;   o += align256(sizeof(int32_t) * ((size_t)T + 64)); // count, then tokens handed back
   w.counts = o;  o += align256(sizeof(int32_t) * E);
   w.offs = o;    o += align256(sizeof(int32_t) * (E + 1));
   w.active = o;  o += align256(sizeof(int32_t) * E);

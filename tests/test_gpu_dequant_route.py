@@ -144,3 +144,53 @@ def test_route_with_bias_large_t(M):
     w = synth.WORKLOADS[3].replace(T=1000, seed=31)
     Wr, bias = synth.router(w)
     _check_route(M, synth.activations(w), Wr, bias, 6)
+
+
+# ------------------------------------------- routing without a logits output
+# Batches above 256 tokens then take the certified fast path: approximate
+# fp32 logits with a rigorous error bound select the top-k; only the selected
+# logits are recomputed exactly, and tokens whose boundary is within the
+# bound are recomputed exactly in full.  Indices must still match bit for bit.
+def _gpu_route_no_logits(M, x, Wr, bias, k):
+    import torch
+    T = x.shape[0]
+    idx = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    w = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(T * Wr.shape[0] * 4 + 8 * (T + Wr.shape[0]) + (1 << 20), dtype=torch.uint8, device="cuda")
+    M.ds4moe_route_topk(torch_bf16_bits(x), torch.from_numpy(np.ascontiguousarray(Wr)).cuda(),
+                        None if bias is None else torch.from_numpy(bias).cuda(), k, idx, w, None, ws)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), w.cpu().numpy()
+
+
+@pytest.mark.parametrize("wid", [2, 3])
+def test_route_without_logits_output_matches_oracle(M, wid):
+    w = synth.WORKLOADS[wid]
+    Wr, bias = synth.router(w)
+    x = synth.activations(w)
+    idx, wt = _gpu_route_no_logits(M, x, Wr, bias, w.k)
+    ridx, rw, _ = oracle.route(x, Wr, bias, w.k)
+    assert np.array_equal(idx, ridx)
+    assert ulp_diff_f32(wt, rw).max() <= 2
+
+
+def test_route_fast_path_hands_back_tied_tokens(M):
+    """Half the tokens carry a large x[0]; experts 0-4 weigh x[0] heavily and
+    experts 9, 17, 21 share one row that weighs it less, so for those tokens
+    the 6th choice is an exact three-way tie (resolved to expert 9), which no
+    error bound can certify: those tokens must go through the exact pass."""
+    rng = np.random.default_rng(41)
+    E, D, T, k = 32, 1024, 300, 6
+    Wr = (rng.standard_normal((E, D)) * 0.02).astype(np.float32)
+    Wr[0:5, 0] = 1.0
+    Wr[9, 0] = 0.5
+    Wr[17] = Wr[9]
+    Wr[21] = Wr[9]
+    xf = rng.standard_normal((T, D))
+    xf[::2, 0] = 8.0
+    x = oracle.round_bf16(xf)
+    idx, wt = _gpu_route_no_logits(M, x, Wr, None, k)
+    ridx, rw, _ = oracle.route(x, Wr, None, k)
+    assert np.array_equal(idx, ridx)
+    assert (ridx[::2, 5] == 9).all() and set(ridx[::2, :5].ravel().tolist()) == {0, 1, 2, 3, 4}
+    assert ulp_diff_f32(wt, rw).max() <= 2
