@@ -21,6 +21,11 @@ with bias, top-6 of 256, Q4_1 gate/up, Q2_K down) through ds4moe_route_topk +
 ds4moe_ffn_prefill, reported as tokens/s and TFLOP/s with the tensor-core
 roofline of the gate/up grouped GEMM.
 
+`--workload 4` times the 43-layer decode stack (every layer with its own
+router and 256 Q2_K experts, 91 GB resident; residual in fp32, each layer fed
+bf16 of the RMS-normalised residual) through ds4moe_stack_decode, one CUDA graph per step; the
+weights are generated on all host cores into shared memory, layer by layer.
+
 `--impl reference` times the CPU oracle itself (the program the CUDA path is
 checked against) on the same metric, each step a bounded sample.
 """
@@ -64,6 +69,10 @@ def parse_args(argv=None):
                     help="device copies of the layer rotated across steps (profiling runs use 1)")
     ap.add_argument("--timed-only", action="store_true",
                     help="skip the per-kernel, end-to-end and CPU passes (for profiler captures)")
+    ap.add_argument("--n-expert", type=int, default=0,
+                    help="override the workload's expert count (smaller cases for profiler captures)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's tokens per step (smaller cases for profiler captures)")
     return ap.parse_args(argv)
 
 
@@ -294,7 +303,7 @@ def run_reference(args, w: synth.Workload):
             _, h, _, _ = oracle.expert_ffn(D, F, qg, blocks[synth.T_GATE], qu, blocks[synth.T_UP], qd,
                                            blocks[synth.T_DOWN], e, x[t])
             hs[(t, i)] = oracle.bf16_to_f32(h).astype(np.float64)
-    values_per_token = w.k * 3 * D * F
+    values_per_token = w.k * 3 * D * F * w.n_layers
     # size the per-step sample so that warmup + steps take ~100 s
     budget = 100.0 / max(args.steps + args.warmup, 1)
     t0 = time.perf_counter()
@@ -323,7 +332,7 @@ def run_reference(args, w: synth.Workload):
     value = tokens / dt if dt > 0 else 0.0
     sample = (f"per step {R} rows of gate, {R} of up and {2 * R} of down of one selected expert "
               f"(fp64 C oracle, one thread); tokens/s extrapolated at {values_per_token} weight values "
-              f"per token (router < 1% of the work, not sampled)")
+              f"per token ({w.n_layers} layer(s); router < 1% of the work, not sampled)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / max(args.steps, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -634,13 +643,224 @@ def run_ours_prefill(args, w: synth.Workload):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------- decode stack arm
+_POOL_M = None
+
+
+def _pool_init():
+    global _POOL_M
+    import bit_quantized_moe_q2_gb300 as M
+    M.lib()
+    _POOL_M = M
+
+
+def _pack_expert(job):
+    """Pack expert e of one layer into the shared-memory tensors (worker)."""
+    from multiprocessing import shared_memory
+    w, layer, e, names, per = job
+    pack = product_packer(_POOL_M)
+    for t, name in zip((synth.T_GATE, synth.T_UP, synth.T_DOWN), names):
+        shm = shared_memory.SharedMemory(name=name)
+        try:
+            shm.buf[e * per[t]:(e + 1) * per[t]] = pack(synth.matrix_fields(w, layer, t, e)).tobytes()
+        finally:
+            shm.close()
+    return e
+
+
+def tensor_bytes(w: synth.Workload, t: int) -> int:
+    rows, cols = synth.matrix_shape(w, t)
+    q = synth.recipe(w, t)
+    return rows * cols // (256 if q.qtype == synth.Q2_K else 32) * (84 if q.qtype == synth.Q2_K else 20)
+
+
+def run_ours_stack(args, w: synth.Workload):
+    import multiprocessing as mp
+    from multiprocessing import shared_memory
+    rank, world, local = dist_env()
+    from bit_quantized_moe_q2_gb300 import _build
+    if rank == 0 or world == 1:
+        _build.build()
+    # the generator pool starts (spawn) before the first GPU call
+    per = {t: tensor_bytes(w, t) for t in (synth.T_GATE, synth.T_UP, synth.T_DOWN)}
+    shms = [shared_memory.SharedMemory(create=True, size=w.n_expert * per[t])
+            for t in (synth.T_GATE, synth.T_UP, synth.T_DOWN)]
+    pool = mp.get_context("spawn").Pool(max(1, cores_available()), initializer=_pool_init)
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    barrier(world)
+    import bit_quantized_moe_q2_gb300 as M
+    from bit_quantized_moe_q2_gb300.device import DeviceLayer, check_status, workspace
+    qid = {synth.Q4_1: M.DS4MOE_Q4_1, synth.Q2_K: M.DS4MOE_Q2_K}
+    t_gen = time.perf_counter()
+    devs, Wrs, biases = [], [], []
+    names = [sh.name for sh in shms]
+    try:
+        for layer in range(w.n_layers):
+            pool.map(_pack_expert, [(w, layer, e, names, per) for e in range(w.n_expert)], chunksize=4)
+            dev = DeviceLayer.empty(w.d_model, w.d_ff, w.n_expert, qid[w.gate.qtype], qid[w.up.qtype],
+                                    qid[w.down.qtype])
+            for sh, dst in zip(shms, (dev.gate, dev.up, dev.down)):
+                dst.copy_(torch.frombuffer(sh.buf, dtype=torch.uint8, count=dst.numel()))
+            Wr, b = synth.router(w, layer)
+            devs.append(dev)
+            Wrs.append(torch.from_numpy(Wr).cuda())
+            biases.append(None if b is None else torch.from_numpy(b).cuda())
+    finally:
+        pool.close()
+        pool.join()
+        for sh in shms:
+            sh.close()
+            sh.unlink()
+    t_gen = time.perf_counter() - t_gen
+    T, k, D, L = w.T, w.k, w.d_model, w.n_layers
+    bias_arg = None if biases[0] is None else biases
+    x0 = [torch.from_numpy(oracle_free_bf16_to_f32(synth.activations(w, T=T, batch=rank_batch_offset(rank) + s)))
+          .cuda() for s in range(N_SLOTS)]
+    x_res = torch.empty((T, D), dtype=torch.float32, device="cuda")
+    xb = torch.empty((T, D), dtype=torch.int16, device="cuda")
+    out = torch.empty((T, D), dtype=torch.float32, device="cuda")
+    idx = torch.empty((L, M.stack_ldk(T, k)), dtype=torch.int32, device="cuda")
+    wt = torch.empty((L, M.stack_ldk(T, k)), dtype=torch.float32, device="cuda")
+    ws = workspace(devs[0], T, k)
+    abis = [d.abi for d in devs]
+    stream = torch.cuda.Stream()
+
+    def step(j, s=None):
+        x_res.copy_(x0[j], non_blocking=True)
+        M.ds4moe_stack_decode(abis, Wrs, bias_arg, k, x_res, xb, out, idx, wt, ws, stream=s)
+
+    with torch.cuda.stream(stream):
+        for j in range(N_SLOTS):
+            step(j, stream)
+    check_status(ws, stream)
+    uniq = [len(set(idx[l, :T * k].cpu().numpy().ravel().tolist())) for l in range(L)]
+    graphs = []
+    for j in range(N_SLOTS):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(j, stream)
+        graphs.append(g)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % N_SLOTS].replay()
+    stream.synchronize()
+    check_status(ws, stream)
+
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.mark(True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            graphs[i % N_SLOTS].replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    barrier(world)
+    clocks = sampler.stop()
+    ms = reduce_max(ev0.elapsed_time(ev1), world)
+    check_status(ws, stream)
+    value = world * args.steps * T / (ms / 1000.0)
+    eb = expert_bytes(w)
+    algo_step = sum(u * eb for u in uniq) + L * (w.n_expert * D * 4) + T * D * 4 * 2
+    stream_gbs = algo_step / (ms / args.steps / 1000.0) / 1e9
+    peak, peak_kind = measured_peaks()
+    if args.timed_only:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": "tokens/s", "ms_per_step": ms / args.steps,
+                              "steps": args.steps, "note": "timed-only run"}), flush=True)
+        return
+    kp = min(args.steps, 50)
+    M.ds4moe_profile_enable(True)
+    with torch.cuda.stream(stream):
+        for i in range(kp):
+            step(i % N_SLOTS, stream)
+    stream.synchronize()
+    prof = M.ds4moe_profile_read()
+    M.ds4moe_profile_enable(False)
+    launches_per_step = sum(n for _, n in prof.values()) / kp
+    kernels = {n: {"avg_us": 1000 * t / c, "launches_per_step": c / kp} for n, (t, c) in prof.items()}
+    gu_ms, gu_n = prof.get("gate_up", prof.get("gate_up_simt", (float("nan"), 1)))
+    gu_algo = (sum(uniq) / L) * gate_up_bytes(w) + T * D * 2 + T * k * w.d_ff * 2
+    gu_s = gu_ms / gu_n / 1000.0
+    roofline = {"kernel": "gate_up (fused dequant GEMV + SwiGLU), per layer", "bound": "hbm",
+                "achieved": gu_algo / gu_s / 1e9, "peak": peak, "unit": "GB/s", "frac": gu_algo / gu_s / 1e9 / peak,
+                "traffic": None, "algorithmic_bytes_per_launch": int(gu_algo), "avg_launch_us": gu_s * 1e6,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else
+                               "fallback 6.8 TB/s"}
+    # end to end: pinned x in, x_res out, per step
+    ke = min(args.steps, 50)
+    xh = [x.cpu().pin_memory() for x in x0]
+    oh = torch.empty((T, D), dtype=torch.float32).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(ke):
+            x_res.copy_(xh[i % N_SLOTS], non_blocking=True)
+            M.ds4moe_stack_decode(abis, Wrs, bias_arg, k, x_res, xb, out, idx, wt, ws, stream=stream)
+            oh.copy_(x_res, non_blocking=True)
+            stream.synchronize()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world)
+    e2e = {"value": world * ke * T / (e2e_ms / 1000.0), "unit": "tokens/s", "steps": ke,
+           "h2d_bytes_per_step": T * D * 4, "d2h_bytes_per_step": T * D * 4,
+           "path": "pinned H2D x_res, ds4moe_stack_decode (eager C-ABI call, 43 layers), D2H x_res, sync per step"}
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        n = args.cpu_tokens or max(2, cores_available() // 2)
+        cpu = cpu_baseline(w, n, batch0=50_000)
+        cpu["value"] /= L
+        cpu["sample"] = (f"{n} tokens through layer 0 (route + selected expert FFNs + combine, fp64 C oracle, "
+                         f"OpenMP over tokens), tokens/s divided by the {L} layers")
+    cfg = workload_config(w, 1)
+    cfg["n_layers"] = L
+    cfg["l2"] = f"inputs larger than L2: every step streams {L} layers of expert weights"
+    cfg["weights_generated_s"] = round(t_gen, 1)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 accumulate over exact 2-bit codes and bf16 activations",
+            "data": "synthetic", "config": cfg, "weight_stream_gbs": stream_gbs, "hbm_frac": stream_gbs / peak,
+            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(round(launches_per_step * args.steps)), "clocks": clocks}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def oracle_free_bf16_to_f32(b: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (a bit shift; no method arithmetic)."""
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
 def main(argv=None):
     args = parse_args(argv)
     w = synth.WORKLOADS[args.workload]
-    if w.path not in ("decode", "prefill") or w.n_layers != 1:
-        raise SystemExit("bench.py times the one-layer workloads (decode: 0, 1, 2; prefill: 3)")
+    if args.n_expert:
+        w = w.replace(n_expert=args.n_expert)
+    if args.tokens:
+        w = w.replace(T=args.tokens)
+    if w.path not in ("decode", "prefill"):
+        raise SystemExit("bench.py times workloads 0-4")
     if args.impl == "reference":
         run_reference(args, w)
+    elif w.n_layers > 1:
+        run_ours_stack(args, w)
     elif w.path == "prefill":
         run_ours_prefill(args, w)
     else:

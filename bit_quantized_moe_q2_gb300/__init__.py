@@ -26,7 +26,7 @@ EXPORTS = (
     "ds4moe_dequant", "ds4moe_workspace_bytes", "ds4moe_workspace_init", "ds4moe_route_topk",
     "ds4moe_ffn_decode", "ds4moe_ffn_prefill", "ds4moe_stream_status",
     "ds4moe_profile_enable", "ds4moe_profile_count", "ds4moe_profile_entry",
-    "ds4moe_ffn_decode_noalloc", "ds4moe_moe_decode",
+    "ds4moe_ffn_decode_noalloc", "ds4moe_moe_decode", "ds4moe_residual_norm", "ds4moe_stack_decode",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -72,6 +72,9 @@ def lib():
         L.ds4moe_stream_status.argtypes = [p, p]
         L.ds4moe_ffn_decode_noalloc.argtypes = [ctypes.POINTER(Layer), p, p, p, i32, i32, p, p, p]
         L.ds4moe_moe_decode.argtypes = [ctypes.POINTER(Layer), p, p, p, i32, i32, p, p, p, p, sz, p]
+        L.ds4moe_residual_norm.argtypes = [p, p, p, i32, i32, ctypes.c_float, p]
+        L.ds4moe_stack_decode.argtypes = [ctypes.POINTER(Layer), ctypes.POINTER(p), ctypes.POINTER(p), i32, i32,
+                                          i32, ctypes.c_float, p, p, p, p, p, p, sz, p]
         L.ds4moe_profile_enable.argtypes = [i32]
         L.ds4moe_profile_count.argtypes = []
         L.ds4moe_profile_entry.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
@@ -181,6 +184,34 @@ def ds4moe_moe_decode(layer: Layer, x, Wr, bias, k, out, idx, w, ws, stream=None
     _check(lib().ds4moe_moe_decode(ctypes.byref(layer), _ptr(x), _ptr(Wr), _ptr(bias), T, k, _ptr(out), _ptr(idx),
                                    _ptr(w), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "ds4moe_moe_decode")
+
+
+STACK_RMS_EPS = 1e-6
+
+
+def ds4moe_residual_norm(x_res, out, x_next, eps=STACK_RMS_EPS, stream=None):
+    """x_res += out (fp32; out None: skip), x_next = bf16(x_res / rms(x_res))."""
+    T, D = x_res.shape
+    _check(lib().ds4moe_residual_norm(_ptr(x_res), _ptr(out), _ptr(x_next), T, D, float(eps), _stream(stream)),
+           "ds4moe_residual_norm")
+
+
+def stack_ldk(T: int, k: int) -> int:
+    """Per-layer stride of ds4moe_stack_decode's idx / w outputs."""
+    return (T * k + 3) // 4 * 4
+
+
+def ds4moe_stack_decode(layers, Wr, bias, k, x_res, x_bf16, out, idx, w, ws, eps=STACK_RMS_EPS, stream=None):
+    """One decode step through len(layers) layers (x_res updated in place;
+    idx / w [n_layers, stack_ldk(T, k)] receive every layer's routing)."""
+    n = len(layers)
+    T = x_res.shape[0]
+    arr = (Layer * n)(*layers)
+    wr = (ctypes.c_void_p * n)(*[_ptr(t) for t in Wr])
+    bs = None if bias is None else (ctypes.c_void_p * n)(*[_ptr(t) for t in bias])
+    _check(lib().ds4moe_stack_decode(arr, wr, bs, n, T, k, float(eps), _ptr(x_res), _ptr(x_bf16), _ptr(out),
+                                     _ptr(idx), _ptr(w), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "ds4moe_stack_decode")
 
 
 def ds4moe_ffn_decode_noalloc(layer: Layer, x, idx, w, out, status_out=None, stream=None):

@@ -842,6 +842,51 @@ __global__ void __launch_bounds__(1024) k_bucket(int32_t *__restrict__ idx, int 
   }
 }
 
+// ------------------------------------------------------------- residual
+// One CTA per token: x_res += out (fp32; out == nullptr: skip), then
+// x_next = bf16_RNE(x_res * r), r = 1 / sqrt(mean(x_res^2) + eps), the sum of
+// squares reduced in a fixed order (thread, warp, CTA).
+constexpr int kNormThreads = 256;
+__global__ void __launch_bounds__(kNormThreads) k_residual_norm(float *__restrict__ x_res, const float *__restrict__ out,
+                                                               uint16_t *__restrict__ x_next, int D, float eps) {
+  ptx::pdl_wait();  // out comes from the preceding grid
+  ptx::pdl_launch_dependents();
+  __shared__ float s_part[kNormThreads / 32];
+  const int t = blockIdx.x, tid = threadIdx.x;
+  float4 *xr = reinterpret_cast<float4 *>(x_res + (int64_t)t * D);
+  const float4 *orow = out ? reinterpret_cast<const float4 *>(out + (int64_t)t * D) : nullptr;
+  float ss = 0.f;
+  for (int i = tid; i < D / 4; i += kNormThreads) {
+    float4 v = xr[i];
+    if (orow) {
+      const float4 o = __ldcg(orow + i);
+      v.x = __fadd_rn(v.x, o.x);
+      v.y = __fadd_rn(v.y, o.y);
+      v.z = __fadd_rn(v.z, o.z);
+      v.w = __fadd_rn(v.w, o.w);
+      xr[i] = v;
+    }
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((tid & 31) == 0) s_part[tid >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kNormThreads / 32; ++w) tot += s_part[w];
+  const float r = 1.0f / sqrtf(tot / (float)D + eps);
+  uint2 *xn = reinterpret_cast<uint2 *>(x_next + (int64_t)t * D);
+  for (int i = tid; i < D / 4; i += kNormThreads) {
+    const float4 v = xr[i];
+    xn[i] = make_uint2((uint32_t)f32_to_bf16_bits(v.x * r) | ((uint32_t)f32_to_bf16_bits(v.y * r) << 16),
+                       (uint32_t)f32_to_bf16_bits(v.z * r) | ((uint32_t)f32_to_bf16_bits(v.w * r) << 16));
+  }
+}
+
 // ------------------------------------------------------------- validation
 ds4moe_status check_layer(const ds4moe_layer *L) {
   if (!L) return DS4MOE_EINVAL;
@@ -1118,6 +1163,42 @@ ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const 
     if (e != cudaSuccess) return cuda_status(e);
   }
   return run_ffn(false, L, x, idx, w, T, k, out, ws, ws_bytes, stream, lg);
+}
+
+ds4moe_status ds4moe_residual_norm(float *x_res, const float *out, uint16_t *x_next, int32_t T, int32_t d_model,
+                                   float eps, void *stream) {
+  if (T < 0 || d_model <= 0 || d_model % 4 || !(eps >= 0.f)) return DS4MOE_EINVAL;
+  if (T == 0) return DS4MOE_OK;
+  if (!x_res || !x_next || !aligned16(x_res) || !aligned16(x_next) || (out && !aligned16(out)))
+    return DS4MOE_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProfScope prof("residual_norm", s);
+  return cuda_status(launch_pdl(k_residual_norm, dim3(T), dim3(kNormThreads), 0, s, x_res, out, x_next,
+                                (int)d_model, eps));
+}
+
+ds4moe_status ds4moe_stack_decode(const ds4moe_layer *layers, const float *const *Wr, const float *const *bias,
+                                  int32_t n_layers, int32_t T, int32_t k, float eps, float *x_res, uint16_t *x_bf16,
+                                  float *out, int32_t *idx, float *w, void *ws, size_t ws_bytes, void *stream) {
+  if (!layers || !Wr || n_layers < 1) return DS4MOE_EINVAL;
+  if (T < 0 || k < 1 || k > 32) return DS4MOE_EINVAL;
+  for (int l = 0; l < n_layers; ++l) {  // validate everything before launching anything
+    const ds4moe_status st = check_layer(&layers[l]);
+    if (st != DS4MOE_OK) return st;
+    if (layers[l].d_model != layers[0].d_model || !Wr[l] || k > layers[l].n_expert) return DS4MOE_EINVAL;
+    if (ws_bytes < ws_layout(layers[l], T, k, 0).total) return DS4MOE_ESPACE;
+  }
+  if (T == 0) return DS4MOE_OK;
+  if (!idx || !w || !aligned16(idx) || !aligned16(w)) return DS4MOE_EINVAL;
+  const int D = layers[0].d_model;
+  const size_t ldk = ((size_t)T * k + 3) & ~size_t(3);
+  ds4moe_status st = ds4moe_residual_norm(x_res, nullptr, x_bf16, T, D, eps, stream);
+  for (int l = 0; l < n_layers && st == DS4MOE_OK; ++l) {
+    st = ds4moe_moe_decode(&layers[l], x_bf16, Wr[l], bias ? bias[l] : nullptr, T, k, out, idx + l * ldk,
+                           w + l * ldk, ws, ws_bytes, stream);
+    if (st == DS4MOE_OK) st = ds4moe_residual_norm(x_res, out, x_bf16, T, D, eps, stream);
+  }
+  return st;
 }
 
 ds4moe_status ds4moe_stream_status(void *ws, void *stream) {

@@ -211,6 +211,48 @@ ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const 
                                 void *stream);
 
 /*
+ * ds4moe_residual_norm -- DEVICE.  The step between layers of a decode
+ * stack ([DS4-1]: 43 routed-MoE layers): per token t,
+ *   x_res[t] += out[t]                 (fp32, one rounding per element),
+ *   x_next[t] = bf16_RNE(x_res[t] / sqrt(mean_j x_res[t,j]^2 + eps)),
+ * the next layer's input.  With out == NULL only the normalisation runs.
+ * x_res / out: fp32 [T, d_model]; x_next: bf16 bit patterns [T, d_model].
+ * The normalisation (an RMS norm with unit weight) is this library's reading
+ * of the stack: the pages give only x += moe(x), and with their weight
+ * distributions an unnormalised residual overflows within a few layers.
+ * The sum of squares is an fp32 reduction in a fixed order, so x_next may
+ * differ from an exact evaluation by one bf16 ulp where x / rms lies within
+ * ~1e-6 relative of a rounding boundary.
+ */
+#define DS4MOE_STACK_RMS_EPS 1e-6f
+ds4moe_status ds4moe_residual_norm(float *x_res, const float *out, uint16_t *x_next,
+                                   int32_t T, int32_t d_model, float eps, void *stream);
+
+/*
+ * ds4moe_stack_decode -- DEVICE.  One decode step through n_layers routed-MoE
+ * layers: x_bf16 = norm(x_res) (ds4moe_residual_norm with out = NULL); then
+ * for each layer l, ds4moe_moe_decode(layers[l], x_bf16, Wr[l], bias[l]) ->
+ * out and ds4moe_residual_norm(x_res, out, x_bf16).  Exactly the kernels and
+ * results of making those calls one by one (no host synchronisation;
+ * capturable into a CUDA graph).
+ *   layers, Wr, bias: HOST arrays of n_layers entries (layer descriptors and
+ *     device pointers; bias[l] may be NULL, bias itself may be NULL);
+ *   x_res: fp32 [T, d_model], updated in place;
+ *   x_bf16: bf16 [T, d_model] and out: fp32 [T, d_model], scratch that hold
+ *     the normalised input after the last layer / its output on return;
+ *   idx, w: int32 / fp32 [n_layers][ldk], ldk = T * k rounded up to a
+ *     multiple of 4 (so every layer's slice stays 16-byte aligned), each
+ *     layer's routing [T, k] at the start of its slice.
+ * All layers share one workspace of max_l ds4moe_workspace_bytes(layers[l],
+ * T, k, 0) bytes.  Same constraints as ds4moe_moe_decode for every layer.
+ */
+ds4moe_status ds4moe_stack_decode(const ds4moe_layer *layers, const float *const *Wr,
+                                  const float *const *bias, int32_t n_layers, int32_t T,
+                                  int32_t k, float eps, float *x_res, uint16_t *x_bf16,
+                                  float *out, int32_t *idx, float *w, void *ws,
+                                  size_t ws_bytes, void *stream);
+
+/*
  * ds4moe_stream_status -- synchronizes `stream`, then reads and clears the
  * device status word of `ws`.  Returns DS4MOE_OK, the recorded device error
  * (DS4MOE_EDEVICE, DS4MOE_ETIMEOUT) or DS4MOE_ECUDA if the stream itself

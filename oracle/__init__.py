@@ -51,6 +51,7 @@ def _L():
         lib.orc_round_bf16.restype = ctypes.c_uint16
         lib.orc_round_bf16.argtypes = [ctypes.c_double]
         lib.orc_round_bf16_array.argtypes = [p, i64, p]
+        lib.orc_rmsnorm_bf16.argtypes = [p, i64, i64, ctypes.c_double, p]
         lib.orc_q41_pack.argtypes = [p, p, p, i64, p]
         lib.orc_q41_unpack.argtypes = [p, i64, p, p, p]
         lib.orc_q41_dequant.argtypes = [p, i64, p]
@@ -102,6 +103,16 @@ def round_bf16(v) -> np.ndarray:
     v = _c(v, np.float64)
     out = np.empty(v.shape, dtype=np.uint16)
     _L().orc_round_bf16_array(v.ctypes.data, v.size, out.ctypes.data)
+    return out
+
+
+def rmsnorm_bf16(x_res, eps: float) -> np.ndarray:
+    """Layer input of the decode stack: bf16 bits of x / sqrt(mean(x^2) + eps)
+    per row of the fp32 residual x_res [T, D] (fp64 arithmetic)."""
+    x = _c(x_res, np.float32)
+    T, D = x.shape
+    out = np.empty((T, D), dtype=np.uint16)
+    _L().orc_rmsnorm_bf16(x.ctypes.data, T, D, float(eps), out.ctypes.data)
     return out
 
 

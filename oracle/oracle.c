@@ -30,7 +30,10 @@
  * dot product (+ optional bias) with a softmax over the k selected experts;
  * top-k ties go to the lower expert id and NaN ranks below -inf; the FFN is
  * SwiGLU, silu(gate) * up, with the hidden activation rounded to bf16;
- * expert tensors are experts-major.
+ * expert tensors are experts-major; in the 43-layer stack ([DS4-1]) the
+ * residual stream stays fp32 (x += moe(..) with one fp32 rounding) and each
+ * layer reads bf16(x / rms(x)), an RMS normalisation with unit weight --
+ * without it the stated weight distributions overflow within a few layers.
  *
  * Pins: every function here is checked by tests/test_oracle_*.py against
  * facts the pages fix or mathematics fixes (hand-derived golden blocks,
@@ -405,4 +408,18 @@ int orc_moe_ffn(int D, int F, int E, int qg, const uint8_t *gate, int qu,
     free(acc); free(y);
   }
   return ORC_OK;
+}
+
+/* ----------------------------------------------------------- layer stack */
+/* [DS4-1] stacks 43 routed-MoE layers.  Reading (see header): the residual
+ * x_res stays fp32, x_res += out rounds once to fp32 (done by the caller in
+ * fp32), and a layer's input is bf16_RNE(x_res / sqrt(mean(x_res^2) + eps)),
+ * evaluated here in fp64 per token. */
+void orc_rmsnorm_bf16(const float *x, int64_t T, int64_t D, double eps, uint16_t *out) {
+  for (int64_t t = 0; t < T; ++t) {
+    double ss = 0.0;
+    for (int64_t j = 0; j < D; ++j) ss += (double)x[t * D + j] * (double)x[t * D + j];
+    const double r = 1.0 / sqrt(ss / (double)D + eps);
+    for (int64_t j = 0; j < D; ++j) out[t * D + j] = orc_round_bf16((double)x[t * D + j] * r);
+  }
 }

@@ -247,3 +247,30 @@ def test_rejects_out_of_range_expert_ids(small_layer):
     with pytest.raises(oracle.OracleError):
         oracle.moe_ffn(w.d_model, w.d_ff, w.n_expert, L.qg, L.gate, L.qu, L.up, L.qd, L.down,
                        x, np.array([[0, w.n_expert]], np.int32), np.ones((1, 2), np.float32))
+
+
+# ----------------------------------------------------------- layer stack
+def test_rmsnorm_layer_input_closed_forms():
+    """bf16(x / sqrt(mean(x^2) + eps)): a constant row maps to +-1 (eps = 0);
+    scaling a row by a power of two leaves it unchanged (eps = 0, exact);
+    the result's mean square is 1 within bf16 rounding; eps damps tiny rows
+    by exactly sqrt(ms / (ms + eps))."""
+    import oracle
+    D = 256
+    x = np.full((2, D), 3.0, dtype=np.float32)
+    x[1] = -0.125
+    y = oracle.bf16_to_f32(oracle.rmsnorm_bf16(x, 0.0))
+    assert (y[0] == 1.0).all() and (y[1] == -1.0).all()
+    rng = np.random.default_rng(3)
+    r = rng.standard_normal((5, D)).astype(np.float32)
+    a = oracle.rmsnorm_bf16(r, 0.0)
+    assert np.array_equal(a, oracle.rmsnorm_bf16(r * np.float32(64.0), 0.0))
+    assert np.array_equal(a, oracle.rmsnorm_bf16(r * np.float32(2.0 ** -20), 0.0))
+    ms = (oracle.bf16_to_f32(a).astype(np.float64) ** 2).mean(axis=1)
+    assert np.abs(ms - 1.0).max() < 2 ** -7
+    # constant row c with eps: value = c / sqrt(c^2 + eps), rounded to bf16
+    c, eps = np.float32(0.001), 3e-6
+    got = oracle.bf16_to_f32(oracle.rmsnorm_bf16(np.full((1, D), c, np.float32), eps))[0, 0]
+    want = float(c) / np.sqrt(float(c) ** 2 + eps)
+    assert abs(got - want) <= abs(want) * 2 ** -8
+    assert got < 1.0
