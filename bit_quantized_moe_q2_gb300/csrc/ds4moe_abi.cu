@@ -151,32 +151,50 @@ __device__ __forceinline__ bool ranks_before(float va, int a, float vb, int b) {
   return a < b;
 }
 
+// Ranking key of (logit, expert): a larger key ranks first.  The logit maps
+// monotonically onto 32 bits with NaN lowest (below -inf) and -0 == +0; ties
+// go to the lower expert id.
+__device__ __forceinline__ uint64_t rank_key(float v, int e) {
+  const uint32_t u = __float_as_uint(v) == 0x80000000u ? 0u : __float_as_uint(v);
+  const uint32_t o = isnan(v) ? 0u : (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((uint64_t)o << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e);
+}
+
+__device__ __forceinline__ float key_value(uint64_t key) {
+  const uint32_t o = (uint32_t)(key >> 32);
+  if (o == 0u) return __uint_as_float(0x7FC00000u);  // NaN
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
 // Top-k of one token's E <= 256 logits held in registers by one warp (entry
 // lane + 32 j in v[j]): lane i < k receives the i-th selected (logit, id).
+// k rounds of a warp-wide maximum of the ranking keys.
 __device__ __forceinline__ void topk_select_warp(const float (&v)[8], int E, int k, float &my_v, int &my_e) {
   const int lane = threadIdx.x & 31;
-  uint32_t taken = 0;
+  uint64_t key[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) key[j] = lane + 32 * j < E ? rank_key(v[j], lane + 32 * j) : 0ull;
   my_v = 0.f;
   my_e = -1;
   for (int i = 0; i < k; ++i) {
-    float bv = 0.f;
-    int be = -1;
+    uint64_t best = key[0];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E && !(taken & (1u << j)) && ranks_before(v[j], e, bv, be)) {
-        bv = v[j];
-        be = e;
-      }
-    }
+    for (int j = 1; j < 8; ++j) best = key[j] > best ? key[j] : best;
 #pragma unroll
     for (int off = 16; off; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (ranks_before(ov, oe, bv, be)) { bv = ov; be = oe; }
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
+      best = o > best ? o : best;
     }
-    if (be >= 0 && (be & 31) == lane) taken |= 1u << (be >> 5);
-    if (lane == i) { my_v = bv; my_e = be; }
+    const int be = (int)(0xFFFFFFFFu - (uint32_t)best);
+    if ((be & 31) == lane) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j == (be >> 5)) key[j] = 0ull;
+    }
+    if (lane == i) {
+      my_v = key_value(best);
+      my_e = be;
+    }
   }
 }
 
@@ -442,18 +460,169 @@ __global__ void k_topk_cert(const float *__restrict__ lg, const float *__restric
   }
 }
 
+// fp16 copy of x and its sub-block (16-value) / block (32-value) sums for
+// the tensor-core decode kernels, by `n` threads numbered from `i0`.
+// bf16 -> fp16 is exact for |x| in [2^-14, 65504]; larger magnitudes are
+// flagged as a data error.
+__device__ __forceinline__ void convert_x(const uint16_t *__restrict__ x, int T, int D, uint16_t *__restrict__ x16,
+                                          uint8_t *__restrict__ xs16, float *__restrict__ xs32,
+                                          WsHeader *__restrict__ hdr, int i0, int n) {
+  const int n32 = D / 32;
+  for (int i = i0; i < T * n32; i += n) {
+    const int t = i / n32, b32 = i % n32;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + (int64_t)t * D + 32 * b32);
+    uint4 *x16r = reinterpret_cast<uint4 *>(x16 + (int64_t)t * D + 32 * b32);
+    uint4 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = __ldcg(xr + q);
+    float s[2] = {0.f, 0.f};
+    bool big = false;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t wd[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float lo = bf16_bits_to_f32(wd[r] & 0xFFFFu), hi = bf16_bits_to_f32(wd[r] >> 16);
+        big |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+        o[r] = (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
+        s[q >> 1] += lo + hi;
+      }
+      x16r[q] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int n16 = 2 * b32 + hh;
+      const __half hi = __float2half_rn(s[hh]);
+      const __half lo = __float2half_rn(s[hh] - __half2float(hi));
+      uint16_t *rec = reinterpret_cast<uint16_t *>(xs16 + ((int64_t)t * (D / 256 + 1) + n16 / 16) * 64);
+      rec[n16 & 15] = __half_as_ushort(hi);
+      rec[16 + (n16 & 15)] = __half_as_ushort(lo);
+      big |= fabsf(s[hh]) > 65504.f;
+    }
+    if (big) record_status(hdr, DS4MOE_EDEVICE);
+    xs32[(int64_t)t * n32 + b32] = s[0] + s[1];
+  }
+}
+
+// Outputs of the bucketing step (pairs p = t*k + i grouped by expert).
+struct BucketArgs {
+  int32_t *idx;
+  int P, E, T, D, k;
+  WsHeader *hdr;
+  int32_t *counts, *offs, *active, *perm, *inv, *lrank;
+  Group *groups;
+  const uint16_t *x;
+  uint16_t *x16;
+  uint8_t *xs16;
+  float *xs32;
+  float *w;
+  int32_t *nvalid;
+  float *out;
+};
+
+// Bucketing of a decode batch (P <= 32 pairs) by a CTA of 256 threads
+// (E <= 256): with `logits`, every thread ranks one expert of each token
+// against all others (the expert is selected iff fewer than k rank above it,
+// and its rank is its position), writing idx; warp 1 turns the selected
+// logits into routing weights while warp 0 sorts the pairs by (expert, pair
+// index) and cuts them into groups of <= kGroup.  Ends with the CTA
+// converged only for warps 0 and 1's own work.
+__device__ __forceinline__ void bucket_small_warps(const BucketArgs &b, const float *__restrict__ logits) {
+  __shared__ int32_t s_idx[32];
+  __shared__ float s_val[32];
+  __shared__ int32_t sorted_e[32];
+  __shared__ uint64_t s_key[256];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int P = b.P, E = b.E, T = b.T, k = b.k;
+  if (logits) {
+    for (int t = 0; t < T; ++t) {
+      const float v = tid < E ? __ldcg(logits + (int64_t)t * E + tid) : 0.f;
+      const uint64_t key = rank_key(v, tid);
+      if (tid < E) s_key[tid] = key;
+      __syncthreads();
+      if (tid < E) {
+        int rank = 0;
+#pragma unroll 8
+        for (int j = 0; j < E; ++j) rank += s_key[j] > key;
+        if (rank < k) {
+          s_idx[t * k + rank] = tid;
+          s_val[t * k + rank] = v;
+          b.idx[(int64_t)t * k + rank] = tid;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (wid == 0) {
+    if (!logits && lane < P) s_idx[lane] = __ldcg(b.idx + lane);
+    __syncwarp();
+    int e = -1;
+    if (lane < P) {
+      e = s_idx[lane];
+      if (e < 0 || e >= E) { record_status(b.hdr, DS4MOE_EDEVICE); e = -1; }
+    }
+    const unsigned valid = __ballot_sync(0xffffffffu, e >= 0);
+    // valid experts per token (for the fused combine); a token without any
+    // gets a zero output row
+    if (lane < T) {
+      const int nvt = __popc(valid & (uint32_t)(((1ull << k) - 1ull) << (lane * k)));
+      b.nvalid[lane] = nvt;
+      if (nvt == 0)
+        for (int c = 0; c < b.D; ++c) b.out[(int64_t)lane * b.D + c] = 0.f;
+    }
+    const int key = e >= 0 ? e * 32 + lane : 0x7FFFFFFF;
+    int rank = 0;
+    for (int q = 0; q < 32; ++q) rank += __shfl_sync(0xffffffffu, key, q) < key;
+    if (lane < P) b.inv[lane] = e >= 0 ? rank : -1;
+    if (e >= 0) b.perm[rank] = lane;
+    // sorted view: lane r holds the expert of the r-th pair
+    if (e >= 0) sorted_e[rank] = e;
+    __syncwarp();
+    const int nv = __popc(valid);
+    const int er = lane < nv ? sorted_e[lane] : -1;
+    const int eprev = __shfl_up_sync(0xffffffffu, er, 1);
+    const bool run_start = lane < nv && (lane == 0 || eprev != er);
+    const unsigned starts = __ballot_sync(0xffffffffu, run_start);
+    const int rs = 31 - __clz(starts & (0xffffffffu >> (31 - lane)));   // start of this lane's run
+    const bool gstart = lane < nv && ((lane - rs) % kGroup == 0);
+    const unsigned gmask = __ballot_sync(0xffffffffu, gstart);
+    if (gstart) {
+      int run_end = nv;
+      const unsigned later = starts & ~(0xffffffffu >> (31 - lane));
+      if (later) run_end = __ffs(later) - 1;
+      b.groups[__popc(gmask & ((1u << lane) - 1u))] = Group{er, lane, min(kGroup, run_end - lane), 0};
+    }
+    if (lane == 0) {
+      b.hdr->n_groups = __popc(gmask);
+      b.hdr->n_active = __popc(starts);
+    }
+  } else if (wid == 1 && logits) {
+    for (int t = 0; t < T; ++t) {
+      const float wi = softmax_selected_warp(lane < k ? s_val[t * k + lane] : 0.f, k);
+      if (lane < k) b.w[(int64_t)t * k + lane] = wi;
+    }
+  }
+}
+
 // Decode router (T <= 256, E <= 256, d_model <= 8192): one CTA per expert.
 // Its 256 threads hold the expert's router row in registers (NI float4 per
 // thread) and compute, for every token, a compensated (Dot2) partial over
 // their slice; partials are merged across lanes and warps with TwoSum in a
 // fixed order, the bias is added with TwoSum, and the result rounded once.
-// The last CTA to finish (ticket counter in the workspace header) runs the
-// top-k and softmax for all tokens.
-template <int NI, bool TOPK>
+// MODE kRouteLogits only writes the logits (the bucketing kernel ranks
+// them).  Otherwise the last CTA to finish (ticket counter in the workspace
+// header) ranks the experts of every token: kRouteTopk writes idx and w;
+// kRouteBucket (decode batches of <= 32 pairs) also sorts the pairs into
+// expert groups for the FFN kernels, and every CTA first converts its slice
+// of x for them -- the whole bucketing step without a kernel of its own.
+enum { kRouteLogits = 0, kRouteTopk = 1, kRouteBucket = 2 };
+template <int NI, int MODE>
 __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict__ x, const float *__restrict__ Wr,
                                                      const float *__restrict__ bias, int T, int D, int E, int k,
                                                      float *__restrict__ logits, int32_t *__restrict__ idx,
-                                                     float *__restrict__ w, WsHeader *__restrict__ hdr) {
+                                                     float *__restrict__ w, WsHeader *__restrict__ hdr,
+                                                     BucketArgs bk) {
   __shared__ float ps[8][32], pc[8][32];
   __shared__ uint32_t ticket;
   const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -466,6 +635,8 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict_
   }
   ptx::pdl_wait();
   ptx::pdl_launch_dependents();
+  if (MODE == kRouteBucket && bk.xs16)
+    convert_x(x, T, D, bk.x16, bk.xs16, bk.xs32, hdr, blockIdx.x * 256 + tid, gridDim.x * 256);
   for (int t0 = 0; t0 < T; t0 += 32) {
     const int nt = min(32, T - t0);
     for (int tt = 0; tt < nt; ++tt) {
@@ -526,7 +697,7 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict_
     }
     __syncthreads();
   }
-  if (!TOPK) return;  // ranking done by the bucketing kernel of the fused decode path
+  if (MODE == kRouteLogits) return;  // ranking done by the bucketing kernel
   // the last CTA to finish ranks the experts of every token
   __threadfence();
   __syncthreads();
@@ -534,61 +705,20 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict_
   __syncthreads();
   if (ticket != (uint32_t)E - 1u) return;
   __threadfence();
-  for (int t = wid; t < T; t += 8) {
-    float v[8];
+  if (MODE == kRouteBucket) {
+    bucket_small_warps(bk, logits);
+  } else {
+    for (int t = wid; t < T; t += 8) {
+      float v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int ee = lane + 32 * j;
-      v[j] = ee < E ? __ldcg(logits + (int64_t)t * E + ee) : 0.f;
+      for (int j = 0; j < 8; ++j) {
+        const int ee = lane + 32 * j;
+        v[j] = ee < E ? __ldcg(logits + (int64_t)t * E + ee) : 0.f;
+      }
+      topk_softmax_warp(v, E, k, idx + (int64_t)t * k, w + (int64_t)t * k);
     }
-    topk_softmax_warp(v, E, k, idx + (int64_t)t * k, w + (int64_t)t * k);
   }
   if (tid == 0) hdr->route_done = 0u;
-}
-
-// fp16 copy of x and its sub-block (16-value) / block (32-value) sums for
-// the tensor-core decode kernels, by `n` threads numbered from `i0`.
-// bf16 -> fp16 is exact for |x| in [2^-14, 65504]; larger magnitudes are
-// flagged as a data error.
-__device__ __forceinline__ void convert_x(const uint16_t *__restrict__ x, int T, int D, uint16_t *__restrict__ x16,
-                                          uint8_t *__restrict__ xs16, float *__restrict__ xs32,
-                                          WsHeader *__restrict__ hdr, int i0, int n) {
-  const int n32 = D / 32;
-  for (int i = i0; i < T * n32; i += n) {
-    const int t = i / n32, b32 = i % n32;
-    const uint4 *xr = reinterpret_cast<const uint4 *>(x + (int64_t)t * D + 32 * b32);
-    uint4 *x16r = reinterpret_cast<uint4 *>(x16 + (int64_t)t * D + 32 * b32);
-    uint4 v[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) v[q] = __ldcg(xr + q);
-    float s[2] = {0.f, 0.f};
-    bool big = false;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t wd[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-      uint32_t o[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float lo = bf16_bits_to_f32(wd[r] & 0xFFFFu), hi = bf16_bits_to_f32(wd[r] >> 16);
-        big |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
-        o[r] = (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
-        s[q >> 1] += lo + hi;
-      }
-      x16r[q] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int n16 = 2 * b32 + hh;
-      const __half hi = __float2half_rn(s[hh]);
-      const __half lo = __float2half_rn(s[hh] - __half2float(hi));
-      uint16_t *rec = reinterpret_cast<uint16_t *>(xs16 + ((int64_t)t * (D / 256 + 1) + n16 / 16) * 64);
-      rec[n16 & 15] = __half_as_ushort(hi);
-      rec[16 + (n16 & 15)] = __half_as_ushort(lo);
-      big |= fabsf(s[hh]) > 65504.f;
-    }
-    if (big) record_status(hdr, DS4MOE_EDEVICE);
-    xs32[(int64_t)t * n32 + b32] = s[0] + s[1];
-  }
 }
 
 // ---------------------------------------------------------------- bucketing
@@ -616,83 +746,11 @@ __global__ void __launch_bounds__(1024) k_bucket(int32_t *__restrict__ idx, int 
   ptx::pdl_wait();  // idx (or the logits) and x come from the preceding grids
   ptx::pdl_launch_dependents();
   if (nthr <= 256) {  // the host picks 256 threads only for P <= 32
-    // Small batch (decode): warp 0 ranks (fused path) and sorts the pairs by
-    // (expert, pair index) from shared memory, warp 1 computes the routing
-    // weights, the other warps convert x -- concurrently.
-    __shared__ int32_t s_idx[32];
-    __shared__ float s_val[32];
-    __shared__ int32_t sorted_e[32];
-    if (wid == 0) {
-      if (logits) {
-        for (int t = 0; t < T; ++t) {
-          float v[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int e = lane + 32 * j;
-            v[j] = e < E ? __ldcg(logits + (int64_t)t * E + e) : 0.f;
-          }
-          float my_v;
-          int my_e;
-          topk_select_warp(v, E, k, my_v, my_e);
-          if (lane < k) {
-            s_idx[t * k + lane] = my_e;
-            s_val[t * k + lane] = my_v;
-            idx[(int64_t)t * k + lane] = my_e;
-          }
-        }
-        __syncwarp();
-        asm volatile("bar.arrive 1, 64;" ::: "memory");  // hand the selected logits to warp 1
-      } else if (lane < P) {
-        s_idx[lane] = __ldcg(idx + lane);
-      }
-      __syncwarp();
-      int e = -1;
-      if (lane < P) {
-        e = s_idx[lane];
-        if (e < 0 || e >= E) { record_status(hdr, DS4MOE_EDEVICE); e = -1; }
-      }
-      const unsigned valid = __ballot_sync(0xffffffffu, e >= 0);
-      // valid experts per token (for the fused combine); a token without any
-      // gets a zero output row
-      if (lane < T) {
-        const int nvt = __popc(valid & (uint32_t)(((1ull << k) - 1ull) << (lane * k)));
-        nvalid[lane] = nvt;
-        if (nvt == 0)
-          for (int c = 0; c < D; ++c) out[(int64_t)lane * D + c] = 0.f;
-      }
-      const int key = e >= 0 ? e * 32 + lane : 0x7FFFFFFF;
-      int rank = 0;
-      for (int q = 0; q < 32; ++q) rank += __shfl_sync(0xffffffffu, key, q) < key;
-      if (lane < P) inv[lane] = e >= 0 ? rank : -1;
-      if (e >= 0) perm[rank] = lane;
-      // sorted view: lane r holds the expert of the r-th pair
-      if (e >= 0) sorted_e[rank] = e;
-      __syncwarp();
-      const int nv = __popc(valid);
-      const int er = lane < nv ? sorted_e[lane] : -1;
-      const int eprev = __shfl_up_sync(0xffffffffu, er, 1);
-      const bool run_start = lane < nv && (lane == 0 || eprev != er);
-      const unsigned starts = __ballot_sync(0xffffffffu, run_start);
-      const int rs = 31 - __clz(starts & (0xffffffffu >> (31 - lane)));   // start of this lane's run
-      const bool gstart = lane < nv && ((lane - rs) % kGroup == 0);
-      const unsigned gmask = __ballot_sync(0xffffffffu, gstart);
-      if (gstart) {
-        int run_end = nv;
-        const unsigned later = starts & ~(0xffffffffu >> (31 - lane));
-        if (later) run_end = __ffs(later) - 1;
-        groups[__popc(gmask & ((1u << lane) - 1u))] = Group{er, lane, min(kGroup, run_end - lane), 0};
-      }
-      if (lane == 0) {
-        hdr->n_groups = __popc(gmask);
-        hdr->n_active = __popc(starts);
-      }
-    } else if (wid == 1 && logits) {
-      asm volatile("bar.sync 1, 64;" ::: "memory");
-      for (int t = 0; t < T; ++t) {
-        const float wi = softmax_selected_warp(lane < k ? s_val[t * k + lane] : 0.f, k);
-        if (lane < k) w[(int64_t)t * k + lane] = wi;
-      }
-    }
+    // Small batch (decode): warps 0 and 1 rank, weight and sort, the other
+    // warps convert x -- concurrently.
+    BucketArgs b{idx, P, E, T, D, k, hdr, counts, offs, active, perm, inv, lrank, groups, x, x16, xs16, xs32, w,
+                 nvalid, out};
+    bucket_small_warps(b, logits);
     if (wid >= 2 && xs16) convert_x(x, T, D, x16, xs16, xs32, hdr, tid - 64, nthr - 64);
     return;
   }
@@ -902,11 +960,23 @@ ds4moe_status check_layer(const ds4moe_layer *L) {
   return DS4MOE_OK;
 }
 
+// The bucketing outputs inside a workspace laid out by ws_layout.
+BucketArgs bucket_args(const ds4moe_layer &L, void *ws, const WsLayout &lay, const uint16_t *x, int32_t *idx,
+                       float *w, int T, int k, float *out, bool sums) {
+  return BucketArgs{idx, T * k, L.n_expert, T, L.d_model, k, ws_ptr<WsHeader>(ws, lay.hdr),
+                    ws_ptr<int32_t>(ws, lay.counts), ws_ptr<int32_t>(ws, lay.offs), ws_ptr<int32_t>(ws, lay.active),
+                    ws_ptr<int32_t>(ws, lay.perm), ws_ptr<int32_t>(ws, lay.inv), ws_ptr<int32_t>(ws, lay.lrank),
+                    ws_ptr<Group>(ws, lay.groups), x, ws_ptr<uint16_t>(ws, lay.x16),
+                    sums ? ws_ptr<uint8_t>(ws, lay.xs16) : nullptr, sums ? ws_ptr<float>(ws, lay.xs32) : nullptr, w,
+                    ws_ptr<int32_t>(ws, lay.nvalid), out};
+}
+
 // Bucketing, expert FFN and combine.  With `logits` (fused decode path) the
-// bucketing kernel first ranks the experts of every token and writes idx / w.
+// bucketing kernel first ranks the experts of every token and writes idx / w;
+// with `bucketed` the router kernel has already done the whole bucketing step.
 ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, const int32_t *idx,
                       const float *w, int32_t T, int32_t k, float *out, void *ws, size_t ws_bytes,
-                      void *stream, const float *logits = nullptr) {
+                      void *stream, const float *logits = nullptr, bool bucketed = false) {
   ds4moe_status st = check_layer(L);
   if (st != DS4MOE_OK) return st;
   if (T < 0 || k < 1 || k > 32 || k > L->n_expert) return DS4MOE_EINVAL;
@@ -955,14 +1025,15 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
     // grids then never wait for an SM to reconfigure its L1/shared split
     cudaFuncSetAttribute(k_bucket, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
     cudaFuncSetAttribute(k_bucket, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    for (auto kern : {k_route_small<1, false>, k_route_small<2, false>, k_route_small<4, false>,
-                      k_route_small<8, false>, k_route_small<1, true>, k_route_small<2, true>,
-                      k_route_small<4, true>, k_route_small<8, true>})
+    for (auto kern : {k_route_small<1, kRouteLogits>, k_route_small<2, kRouteLogits>, k_route_small<4, kRouteLogits>,
+                      k_route_small<8, kRouteLogits>, k_route_small<1, kRouteTopk>, k_route_small<2, kRouteTopk>,
+                      k_route_small<4, kRouteTopk>, k_route_small<8, kRouteTopk>, k_route_small<1, kRouteBucket>,
+                      k_route_small<2, kRouteBucket>, k_route_small<4, kRouteBucket>, k_route_small<8, kRouteBucket>})
       cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     attr_set = true;
   }
   cudaError_t e = cudaSuccess;
-  {
+  if (!bucketed) {
     ProfScope prof("bucket", s);
     // the tensor-core prefill reads the expert offsets: always the full path
     const int threads = P <= 32 && !tc ? 256 : 1024;
@@ -1064,12 +1135,12 @@ ds4moe_status ds4moe_route_topk(const uint16_t *x, const float *Wr, const float 
     WsHeader *hdr = static_cast<WsHeader *>(ws);
     ProfScope prof("route_topk", s);
     const int ni = (d_model + 1023) / 1024;
-    auto kern = ni <= 1   ? k_route_small<1, true>
-                : ni <= 2 ? k_route_small<2, true>
-                : ni <= 4 ? k_route_small<4, true>
-                          : k_route_small<8, true>;
+    auto kern = ni <= 1   ? k_route_small<1, kRouteTopk>
+                : ni <= 2 ? k_route_small<2, kRouteTopk>
+                : ni <= 4 ? k_route_small<4, kRouteTopk>
+                          : k_route_small<8, kRouteTopk>;
     return cuda_status(launch_pdl(kern, dim3(n_expert), dim3(256), 0, s, x, Wr, bias, (int)T, (int)d_model,
-                                  (int)n_expert, (int)k, lg, idx, w, hdr));
+                                  (int)n_expert, (int)k, lg, idx, w, hdr, BucketArgs{}));
   }
   if (fast) {
     float *xn = ws_ptr<float>(ws, lay.rnorm), *wn = xn + T;
@@ -1151,18 +1222,30 @@ ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const 
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float *lg = ws_ptr<float>(ws, lay.logits);
+  // up to 32 pairs: the router's last CTA also does the bucketing
+  const bool fused = T * k <= 32;
   {
-    ProfScope prof("route", s);
+    ProfScope prof(fused ? "route_bucket" : "route", s);
     const int ni = (D + 1023) / 1024;
-    auto kern = ni <= 1   ? k_route_small<1, false>
-                : ni <= 2 ? k_route_small<2, false>
-                : ni <= 4 ? k_route_small<4, false>
-                          : k_route_small<8, false>;
-    cudaError_t e = launch_pdl(kern, dim3(E), dim3(256), 0, s, x, Wr, bias, (int)T, (int)D, (int)E, (int)k, lg, idx,
-                               w, static_cast<WsHeader *>(ws));
+    cudaError_t e;
+    if (fused) {
+      auto kern = ni <= 1   ? k_route_small<1, kRouteBucket>
+                  : ni <= 2 ? k_route_small<2, kRouteBucket>
+                  : ni <= 4 ? k_route_small<4, kRouteBucket>
+                            : k_route_small<8, kRouteBucket>;
+      e = launch_pdl(kern, dim3(E), dim3(256), 0, s, x, Wr, bias, (int)T, (int)D, (int)E, (int)k, lg, idx, w,
+                     static_cast<WsHeader *>(ws), bucket_args(*L, ws, lay, x, idx, w, T, k, out, decode_mma_ok(*L)));
+    } else {
+      auto kern = ni <= 1   ? k_route_small<1, kRouteLogits>
+                  : ni <= 2 ? k_route_small<2, kRouteLogits>
+                  : ni <= 4 ? k_route_small<4, kRouteLogits>
+                            : k_route_small<8, kRouteLogits>;
+      e = launch_pdl(kern, dim3(E), dim3(256), 0, s, x, Wr, bias, (int)T, (int)D, (int)E, (int)k, lg, idx, w,
+                     static_cast<WsHeader *>(ws), BucketArgs{});
+    }
     if (e != cudaSuccess) return cuda_status(e);
   }
-  return run_ffn(false, L, x, idx, w, T, k, out, ws, ws_bytes, stream, lg);
+  return run_ffn(false, L, x, idx, w, T, k, out, ws, ws_bytes, stream, lg, fused);
 }
 
 ds4moe_status ds4moe_residual_norm(float *x_res, const float *out, uint16_t *x_next, int32_t T, int32_t d_model,
