@@ -5,10 +5,13 @@
 // Q4_1 / Q2_K block layouts of the ggml quantization notes) is, per expert e
 // and its sorted token pairs P_e:
 //   H[p] = bf16(silu(Wg_e x_p) * (Wu_e x_p)),   Y[p] = Wd_e H[p].
-// With weights as the MMA's A operand (M = 128 weight rows per tile) and the
-// expert's tokens as B (N = up to 128 / 256 tokens), each weight byte is
-// dequantized once per token chunk and multiplied against every token of the
-// chunk.
+// Each weight byte is dequantized once per token chunk and multiplied
+// against every token of the chunk.  A tcgen05.mma with M = 128 and K = 16
+// costs the tensor pipe about the same time for any N up to 256 (measured),
+// so the operands are oriented to fill N: gate/up take the chunk's tokens as
+// A (M = 128) and 128 gate rows + the same 128 up rows as B (N = 256), one
+// MMA producing g and u side by side; down takes 128 weight rows as A and
+// the chunk's tokens (up to 256) as B.
 //
 // One persistent CTA per SM, warp-specialised:
 //   warps 0-7   dequantize the staged blocks into fp16 A tiles (K-major,
@@ -76,7 +79,7 @@ struct TcCfg {
   static constexpr int kSB = NMAT == 2 ? 3 : 2;
   static constexpr int kSQ = QA == DS4MOE_Q2_K ? 2 : (NMAT == 2 ? 2 : 4);
   static constexpr int kATile = kTileM * kStepK * 2;
-  static constexpr int kTiles = NMAT == 2 ? 4 : 1;  // gate hi, gate lo, up hi, up lo
+  static constexpr int kTiles = NMAT == 2 ? 4 : 1;  // gate hi, up hi, gate -lo, up -lo
   static constexpr int kASlot = kTiles * kATile;
   static constexpr int kBSlot = BN * kStepK * 2;
   static constexpr int kQMat = kTileM * QFmt<QA>::kBytes;
@@ -303,8 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait_all(&aempty[aslot], ((ait / C::kSA) & 1) ^ 1)) { ok = false; break; }
             uint8_t *tile = sA + aslot * C::kASlot;
             const int b = 2 * (kk & 1) + hb;
-            mg[kk] = dq_q41_exact(qrow + 20 * b, tile, tile + C::kATile, r, hb, big);
-            mu[kk] = dq_q41_exact(qrow + C::kQMat + 20 * b, tile + 2 * C::kATile, tile + 3 * C::kATile, r, hb, big);
+            // B tiles of 256 rows: gate rows 0..127 then up rows 128..255, hi then lo
+            mg[kk] = dq_q41_exact(qrow + 20 * b, tile, tile + 2 * C::kATile, r, hb, big);
+            mu[kk] = dq_q41_exact(qrow + C::kQMat + 20 * b, tile + C::kATile, tile + 3 * C::kATile, r, hb, big);
             publish(aslot);
             ++ait;
             if (kk & 1) {
@@ -328,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               u4[i] = mu[4 * c + i] | (mu[4 * c + i] << 16);
             }
             sts128(tile + sw128_off(r, 4 * hb + c), g4[0], g4[1], g4[2], g4[3]);
-            sts128(tile + 2 * C::kATile + sw128_off(r, 4 * hb + c), u4[0], u4[1], u4[2], u4[3]);
+            sts128(tile + C::kATile + sw128_off(r, 4 * hb + c), u4[0], u4[1], u4[2], u4[3]);
           }
           publish(aslot);
           ++ait;
@@ -370,20 +374,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(32 * sub) << 16) + (uint32_t)(tb * NMAT * BN);
       const int64_t grow = (int64_t)mt * kTileM + row;
-      for (int j0 = 0; j0 < ch.n; j0 += 32) {
-        if constexpr (NMAT == 2) {
+      if constexpr (NMAT == 2) {
+        // lane = token of the chunk; columns 0..127 = g, 128..255 = u of the
+        // tile's 128 rows: 256 contiguous bytes of h per token
+        const int tok = row;
+        uint4 *H = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + (int64_t)(ch.p0 + tok) * a.rows +
+                                             (int64_t)mt * kTileM);
+#pragma unroll 1
+        for (int c0 = 0; c0 < kTileM; c0 += 32) {
           uint32_t g[32], v[32];
-          ptx::tmem_ld32x2_wait(tbase + j0, tbase + BN + j0, g, v);
-          uint16_t *H = static_cast<uint16_t *>(a.out);
+          ptx::tmem_ld32x2_wait(tbase + c0, tbase + kTileM + c0, g, v);
+          if (tok < ch.n) {
+            uint32_t hp[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (j0 + j < ch.n) {
-              const float hv = bf16_bits_to_f32(f32_to_bf16_bits(silu(__uint_as_float(g[j])) * __uint_as_float(v[j])));
-              big |= !(fabsf(hv) <= 65504.f);
-              H[(int64_t)(ch.p0 + j0 + j) * a.rows + grow] = __half_as_ushort(__float2half_rn(hv));
+            for (int j = 0; j < 32; j += 2) {
+              const float h0 = bf16_bits_to_f32(f32_to_bf16_bits(silu(__uint_as_float(g[j])) * __uint_as_float(v[j])));
+              const float h1 =
+                  bf16_bits_to_f32(f32_to_bf16_bits(silu(__uint_as_float(g[j + 1])) * __uint_as_float(v[j + 1])));
+              big |= !(fabsf(h0) <= 65504.f) || !(fabsf(h1) <= 65504.f);
+              hp[j >> 1] = (uint32_t)__half_as_ushort(__float2half_rn(h0)) |
+                           ((uint32_t)__half_as_ushort(__float2half_rn(h1)) << 16);
             }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) H[c0 / 8 + q] = make_uint4(hp[4 * q], hp[4 * q + 1], hp[4 * q + 2], hp[4 * q + 3]);
           }
-        } else {
+        }
+      }
+      for (int j0 = 0; NMAT == 1 && j0 < ch.n; j0 += 32) {
+        {
           uint32_t y[32];
           ptx::tmem_ld32_wait(tbase + j0, y);
           float *Y = static_cast<float *>(a.out);
@@ -457,6 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++tit) {
         const Chunk ch = a.chunks[u / MT];
         const uint32_t idesc = f16_idesc(kTileM, (ch.n + 15) & ~15);
+        const uint32_t idesc_gu = f16_idesc(kTileM, 2 * kTileM);  // M = 128 tokens, N = 256 rows
         const int tb = tit % C::kNB;
         if (!ptx::mbar_wait_or_abort(&tempty[tb], ((tit / C::kNB) & 1) ^ 1, abort_flag)) { ok = false; break; }
         ptx::tc_fence_after();
@@ -470,16 +489,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::tc_fence_after();
           const uint32_t a0 = ptx::smem_u32(sA + aslot * C::kASlot), b0 = ptx::smem_u32(sB + bslot * C::kBSlot);
-          const bool lo_too = NMAT == 2 && !is_min_step(s);
+          if constexpr (NMAT == 2) {
+            // tokens (the B ring's tile) as A, the 256 weight rows as B
+            const bool lo_too = !is_min_step(s);
 #pragma unroll
-          for (int kk = 0; kk < kStepK / 16; ++kk) {
-            const uint64_t bd = sw128_desc(b0 + 32 * kk);
-#pragma unroll
-            for (int m = 0; m < NMAT; ++m) {
-              const uint32_t at = a0 + (NMAT == 2 ? 2 * m : m) * C::kATile + 32 * kk;
-              ptx::umma_f16(dcol + m * BN, sw128_desc(at), bd, idesc, (s | kk) != 0);
-              if (lo_too) ptx::umma_f16(dcol + m * BN, sw128_desc(at + C::kATile), bd, idesc, 1);
+            for (int kk = 0; kk < kStepK / 16; ++kk) {
+              const uint64_t xd = sw128_desc(b0 + 32 * kk);
+              ptx::umma_f16(dcol, xd, sw128_desc(a0 + 32 * kk), idesc_gu, (s | kk) != 0);
+              if (lo_too) ptx::umma_f16(dcol, xd, sw128_desc(a0 + 2 * C::kATile + 32 * kk), idesc_gu, 1);
             }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kStepK / 16; ++kk)
+              ptx::umma_f16(dcol, sw128_desc(a0 + 32 * kk), sw128_desc(b0 + 32 * kk), idesc, (s | kk) != 0);
           }
           issued = true;
           ptx::umma_commit(&aempty[aslot]);
