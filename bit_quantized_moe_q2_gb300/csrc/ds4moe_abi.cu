@@ -168,7 +168,9 @@ __device__ __forceinline__ float key_value(uint64_t key) {
 
 // Top-k of one token's E <= 256 logits held in registers by one warp (entry
 // lane + 32 j in v[j]): lane i < k receives the i-th selected (logit, id).
-// k rounds of a warp-wide maximum of the ranking keys.
+// k rounds of a warp-wide maximum of the ranking keys: the maximum of the
+// high (logit) halves, then of the low (id) halves among the lanes holding
+// that logit, each one warp reduction.
 __device__ __forceinline__ void topk_select_warp(const float (&v)[8], int E, int k, float &my_v, int &my_e) {
   const int lane = threadIdx.x & 31;
   uint64_t key[8];
@@ -177,15 +179,13 @@ __device__ __forceinline__ void topk_select_warp(const float (&v)[8], int E, int
   my_v = 0.f;
   my_e = -1;
   for (int i = 0; i < k; ++i) {
-    uint64_t best = key[0];
+    uint64_t lb = key[0];
 #pragma unroll
-    for (int j = 1; j < 8; ++j) best = key[j] > best ? key[j] : best;
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-      const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
-      best = o > best ? o : best;
-    }
-    const int be = (int)(0xFFFFFFFFu - (uint32_t)best);
+    for (int j = 1; j < 8; ++j) lb = key[j] > lb ? key[j] : lb;
+    const uint32_t bh = __reduce_max_sync(0xffffffffu, (uint32_t)(lb >> 32));
+    const uint32_t bl = __reduce_max_sync(0xffffffffu, (uint32_t)(lb >> 32) == bh ? (uint32_t)lb : 0u);
+    const uint64_t best = ((uint64_t)bh << 32) | bl;
+    const int be = (int)(0xFFFFFFFFu - bl);
     if ((be & 31) == lane) {
 #pragma unroll
       for (int j = 0; j < 8; ++j)
@@ -522,94 +522,91 @@ struct BucketArgs {
 };
 
 // Bucketing of a decode batch (P <= 32 pairs) by a CTA of 256 threads
-// (E <= 256): with `logits`, every thread ranks one expert of each token
-// against all others (the expert is selected iff fewer than k rank above it,
-// and its rank is its position), writing idx; warp 1 turns the selected
-// logits into routing weights while warp 0 sorts the pairs by (expert, pair
-// index) and cuts them into groups of <= kGroup.  Ends with the CTA
-// converged only for warps 0 and 1's own work.
+// (E <= 256).  With `logits`, warp w ranks the experts of tokens w, w + 8,
+// ... (writing idx, and the k selected logits to w: the routing weights are
+// their softmax, computed later off the critical path by
+// finish_routing_weights); then warp 0 sorts the pairs by (expert, pair
+// index) with ballot-based radix ranking and cuts them into groups of
+// <= kGroup.
 __device__ __forceinline__ void bucket_small_warps(const BucketArgs &b, const float *__restrict__ logits) {
   __shared__ int32_t s_idx[32];
-  __shared__ float s_val[32];
   __shared__ int32_t sorted_e[32];
-  __shared__ uint64_t s_key[256];
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
   const int P = b.P, E = b.E, T = b.T, k = b.k;
   if (logits) {
-    for (int t = 0; t < T; ++t) {
-      const float v = tid < E ? __ldcg(logits + (int64_t)t * E + tid) : 0.f;
-      const uint64_t key = rank_key(v, tid);
-      if (tid < E) s_key[tid] = key;
-      __syncthreads();
-      if (tid < E) {
-        int rank = 0;
-#pragma unroll 8
-        for (int j = 0; j < E; ++j) rank += s_key[j] > key;
-        if (rank < k) {
-          s_idx[t * k + rank] = tid;
-          s_val[t * k + rank] = v;
-          b.idx[(int64_t)t * k + rank] = tid;
-        }
+    for (int t = wid; t < T; t += nw) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int e = lane + 32 * j;
+        v[j] = e < E ? __ldcg(logits + (int64_t)t * E + e) : 0.f;
       }
-      __syncthreads();
+      float my_v;
+      int my_e;
+      topk_select_warp(v, E, k, my_v, my_e);
+      if (lane < k) {
+        s_idx[t * k + lane] = my_e;
+        b.idx[(int64_t)t * k + lane] = my_e;
+        b.w[(int64_t)t * k + lane] = my_v;
+      }
     }
+    __syncthreads();
   }
-  if (wid == 0) {
-    if (!logits && lane < P) s_idx[lane] = __ldcg(b.idx + lane);
-    __syncwarp();
-    int e = -1;
-    if (lane < P) {
-      e = s_idx[lane];
-      if (e < 0 || e >= E) { record_status(b.hdr, DS4MOE_EDEVICE); e = -1; }
-    }
-    const unsigned valid = __ballot_sync(0xffffffffu, e >= 0);
-    // valid experts per token (for the fused combine); a token without any
-    // gets a zero output row
-    if (lane < T) {
-      const int nvt = __popc(valid & (uint32_t)(((1ull << k) - 1ull) << (lane * k)));
-      b.nvalid[lane] = nvt;
-      if (nvt == 0)
-        for (int c = 0; c < b.D; ++c) b.out[(int64_t)lane * b.D + c] = 0.f;
-    }
-    const int key = e >= 0 ? e * 32 + lane : 0x7FFFFFFF;
-    int rank = 0;
-    for (int q = 0; q < 32; ++q) rank += __shfl_sync(0xffffffffu, key, q) < key;
-    if (lane < P) b.inv[lane] = e >= 0 ? rank : -1;
-    if (e >= 0) b.perm[rank] = lane;
-    // sorted view: lane r holds the expert of the r-th pair
-    if (e >= 0) sorted_e[rank] = e;
-    __syncwarp();
-    const int nv = __popc(valid);
-    const int er = lane < nv ? sorted_e[lane] : -1;
-    const int eprev = __shfl_up_sync(0xffffffffu, er, 1);
-    const bool run_start = lane < nv && (lane == 0 || eprev != er);
-    const unsigned starts = __ballot_sync(0xffffffffu, run_start);
-    const int rs = 31 - __clz(starts & (0xffffffffu >> (31 - lane)));   // start of this lane's run
-    const bool gstart = lane < nv && ((lane - rs) % kGroup == 0);
-    const unsigned gmask = __ballot_sync(0xffffffffu, gstart);
-    if (gstart) {
-      int run_end = nv;
-      const unsigned later = starts & ~(0xffffffffu >> (31 - lane));
-      if (later) run_end = __ffs(later) - 1;
-      b.groups[__popc(gmask & ((1u << lane) - 1u))] = Group{er, lane, min(kGroup, run_end - lane), 0};
-    }
-    if (lane == 0) {
-      b.hdr->n_groups = __popc(gmask);
-      b.hdr->n_active = __popc(starts);
-    }
-  } else if (wid == 1 && logits) {
-    for (int t = 0; t < T; ++t) {
-      const float wi = softmax_selected_warp(lane < k ? s_val[t * k + lane] : 0.f, k);
-      if (lane < k) b.w[(int64_t)t * k + lane] = wi;
-    }
+  if (wid != 0) return;
+  if (!logits && lane < P) s_idx[lane] = __ldcg(b.idx + lane);
+  __syncwarp();
+  int e = -1;
+  if (lane < P) {
+    e = s_idx[lane];
+    if (e < 0 || e >= E) { record_status(b.hdr, DS4MOE_EDEVICE); e = -1; }
+  }
+  const unsigned valid = __ballot_sync(0xffffffffu, e >= 0);
+  // valid experts per token (for the fused combine); a token without any
+  // gets a zero output row
+  if (lane < T) {
+    const int nvt = __popc(valid & (uint32_t)(((1ull << k) - 1ull) << (lane * k)));
+    b.nvalid[lane] = nvt;
+    if (nvt == 0)
+      for (int c = 0; c < b.D; ++c) b.out[(int64_t)lane * b.D + c] = 0.f;
+  }
+  // rank of (expert, pair) among the 32 lanes, invalid pairs last (as
+  // expert E): radix ranking over the keys (expert << 5 | lane), one ballot
+  // per key bit, most significant first
+  const uint32_t key = ((uint32_t)(e >= 0 ? e : E) << 5) | (uint32_t)lane;
+  const int nbits = 5 + 32 - __clz(E);
+  int rank = 0;
+  uint32_t same = 0xffffffffu;
+  for (int bit = nbits - 1; bit >= 0; --bit) {
+    const uint32_t mine = (key >> bit) & 1u;
+    const uint32_t ones = __ballot_sync(0xffffffffu, mine);
+    if (mine) rank += __popc(same & ~ones);
+    same &= mine ? ones : ~ones;
+  }
+  if (lane < P) b.inv[lane] = e >= 0 ? rank : -1;
+  if (e >= 0) b.perm[rank] = lane;
+  // sorted view: lane r holds the expert of the r-th pair
+  if (e >= 0) sorted_e[rank] = e;
+  __syncwarp();
+  const int nv = __popc(valid);
+  const int er = lane < nv ? sorted_e[lane] : -1;
+  const int eprev = __shfl_up_sync(0xffffffffu, er, 1);
+  const bool run_start = lane < nv && (lane == 0 || eprev != er);
+  const unsigned starts = __ballot_sync(0xffffffffu, run_start);
+  const int rs = 31 - __clz(starts & (0xffffffffu >> (31 - lane)));   // start of this lane's run
+  const bool gstart = lane < nv && ((lane - rs) % kGroup == 0);
+  const unsigned gmask = __ballot_sync(0xffffffffu, gstart);
+  if (gstart) {
+    int run_end = nv;
+    const unsigned later = starts & ~(0xffffffffu >> (31 - lane));
+    if (later) run_end = __ffs(later) - 1;
+    b.groups[__popc(gmask & ((1u << lane) - 1u))] = Group{er, lane, min(kGroup, run_end - lane), 0};
+  }
+  if (lane == 0) {
+    b.hdr->n_groups = __popc(gmask);
+    b.hdr->n_active = __popc(starts);
   }
 }
 
-// Decode router (T <= 256, E <= 256, d_model <= 8192): one CTA per expert.
-// Its 256 threads hold the expert's router row in registers (NI float4 per
-// thread) and compute, for every token, a compensated (Dot2) partial over
-// their slice; partials are merged across lanes and warps with TwoSum in a
-// fixed order, the bias is added with TwoSum, and the result rounded once.
 // MODE kRouteLogits only writes the logits (the bucketing kernel ranks
 // them).  Otherwise the last CTA to finish (ticket counter in the workspace
 // header) ranks the experts of every token: kRouteTopk writes idx and w;
@@ -1018,6 +1015,7 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
   const bool sums = !tc && decode_mma_ok(*L);
   a.cnt = sums ? ws_ptr<int32_t>(ws, lay.cnt) : nullptr;
   const int E = L->n_expert, P = T * k;
+  a.w_logits = logits != nullptr && P <= 32;  // the small bucketing path leaves raw selected logits in w
   const size_t smem = sizeof(int32_t) * (32 * (size_t)E + E + 1);
   static bool attr_set = false;
   if (!attr_set) {

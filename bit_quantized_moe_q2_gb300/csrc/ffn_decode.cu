@@ -248,7 +248,7 @@ __device__ __forceinline__ void tile_rows(const uint8_t *buf, uint32_t ch, int n
 // bytes in two shared-memory stages; the K partials are summed in shared
 // memory in a fixed order, then h = bf16(silu(g) * u) and the tile's
 // sub-block sums of h are written.
-template <int QG, int QU>
+template <int QG, int QU, bool FIN>
 __global__ void __launch_bounds__(512) k_gate_up_mma(FfnArgs a, int kp, uint32_t chg, uint32_t chu) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
@@ -271,6 +271,7 @@ __global__ void __launch_bounds__(512) k_gate_up_mma(FfnArgs a, int kp, uint32_t
   // groups, permutation, fp16 x and its sums come from the bucketing grid
   ptx::pdl_wait();
   ptx::pdl_launch_dependents();
+  if (FIN && blockIdx.x == 0 && w == 0) finish_routing_weights(const_cast<float *>(a.w), a.T, a.k);
   const int ntile = F / 16;
   const int U = __ldcg(&a.hdr->n_groups) * ntile;
   const int64_t rb = is_up ? row_bytes(QU, D) : row_bytes(QG, D);
@@ -556,6 +557,7 @@ __global__ void __launch_bounds__(256) k_gate_up_simt(FfnArgs a) {
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t items = (int64_t)a.hdr->n_groups * F;
   const int64_t rbg = row_bytes(a.L.q_gate, D), rbu = row_bytes(a.L.q_up, D);
+  if (a.w_logits && gw == 0) finish_routing_weights(const_cast<float *>(a.w), a.T, k);
   for (int64_t item = gw; item < items; item += nw) {
     const Group grp = a.groups[item / F];
     const int r = (int)(item % F);
@@ -647,7 +649,9 @@ cudaError_t launch_gate_up_mma(const FfnArgs &a, cudaStream_t s, int kp) {
   const uint32_t chg = (uint32_t)(D / kp / block_vals(QG) * block_bytes(QG));
   const uint32_t chu = (uint32_t)(D / kp / block_vals(QU) * block_bytes(QU));
   const size_t smem = (size_t)kp * 32 * (chg + chu) + 32 * kp + (size_t)2 * kp * 32 * 4 * sizeof(float);
-  auto kern = k_gate_up_mma<QG, QU>;
+  // a separate instantiation for the batches whose routing weights are still
+  // logits keeps the main loop's code of the other one untouched
+  auto kern = a.w_logits ? k_gate_up_mma<QG, QU, true> : k_gate_up_mma<QG, QU, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);

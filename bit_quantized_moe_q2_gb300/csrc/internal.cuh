@@ -120,6 +120,21 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// Routing weights of a decode batch of P = T * k <= 32 pairs, by one warp:
+// w[t*k + i] holds the i-th selected logit of token t (descending), and is
+// replaced by exp(l_i - l_0) / sum_j exp(l_j - l_0), in double, summed in
+// rank order, rounded once to fp32 -- one lane per pair.
+__device__ __forceinline__ void finish_routing_weights(float *w, int T, int k) {
+  const int lane = threadIdx.x & 31, P = T * k;
+  const int base = lane < P ? lane - lane % k : 0;
+  const float v = lane < P ? w[lane] : 0.f;
+  const double m = (double)__shfl_sync(0xffffffffu, v, base);
+  const double ex = lane < P ? exp((double)v - m) : 0.0;
+  double sum = 0.0;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, base + j < 32 ? base + j : 0);
+  if (lane < P) w[lane] = (float)(ex / sum);
+}
+
 // ------------------------------------------------------- launch entry points
 // (defined in ffn_decode.cu / ffn_prefill.cu; called from ds4moe_abi.cu)
 struct FfnArgs {
@@ -139,6 +154,7 @@ struct FfnArgs {
   float *y;
   const int32_t *nvalid;  // [T] experts in range per token
   int32_t *cnt;           // [T][D/16] arrival counters of the fused combine (nullptr: separate combine)
+  int w_logits;           // w holds the k selected logits per token: the gate/up grid turns them into weights
   // tensor-core prefill only (nullptr otherwise)
   uint16_t *xp;           // [P][D] x of each sorted pair, fp16
   Chunk *chunks_gu, *chunks_dn;
