@@ -499,6 +499,460 @@ __global__ void __launch_bounds__(256) k_down_mma(FfnArgs a, uint32_t chd) {
   }
 }
 
+// ================================================== single-token decode
+// With one token (T = 1) every expert group holds one pair, and the n = 8
+// side of the MMA is better spent on eight Q2_K sub-blocks than on tokens.
+// Per 128-value half of a 256-value block, K slots 2n, 2n+1 of every MMA
+// carry two values of sub-block n, and the activation operand is placed
+// block-diagonally (column n sees only K slots 2n, 2n+1), so after the eight
+// MMAs of a half, D[row][n] is the code-dot of sub-block n alone.  The
+// per-(row, sub-block) scale is then one fp32 FMA per 16 weights in the
+// epilogue, and the mins one more MMA per block (mn codes x sub-block sums).
+//
+// Codes enter as fp16 subnormals: masking the 2-bit field at bit 2p of the
+// low byte of each fp16 half leaves q * 2^(2p - 24) exactly, one LOP per
+// operand register; the power of two is folded into the block scale.  Lane
+// quad c handles sub-blocks c and c + 4 of a half, which share the qs bytes
+// 16 (c & 1) .. +15 at code positions c / 2 and c / 2 + 2, and D columns
+// 2c, 2c+1, which both sit at code position c.
+//
+// Each consumer warp owns one 256-value block column of K and keeps its
+// activation operands in registers; a producer warp streams 16-row tiles
+// into a ring of shared-memory stages with bulk copies.
+struct T1Lane {
+  uint32_t m1, m2;  // code fields at positions c/2 and c/2 + 2, both fp16 halves
+  uint32_t qoff;    // this lane's 16 qs bytes within a 32-byte half
+  uint32_t rot;     // word order rotation of lanes with odd c (spreads banks)
+  uint32_t soff;    // scale word holding bytes 2c, 2c+1 of a half
+  uint32_t ssel;    // PRMT selector: (byte 2c, 0, byte 2c+1, 0)
+  float kd;         // 2^(48 - 2c): undoes sc's 2^-24 and the columns' 2^(2c-24)
+};
+
+__device__ __forceinline__ T1Lane t1_lane(int c) {
+  T1Lane L;
+  L.m1 = 0x00030003u << (2 * (c >> 1));
+  L.m2 = L.m1 << 4;
+  L.qoff = 16u * (c & 1);
+  L.rot = 2u * (c & 1);
+  L.soff = 4u * (c >> 1);
+  const uint32_t b = 2u * (c & 1);
+  L.ssel = b | (4u << 4) | ((b + 1u) << 8) | (4u << 12);
+  L.kd = __uint_as_float((uint32_t)(127 + 48 - 2 * c) << 23);
+  return L;
+}
+
+// Activation operands of one 256-value block of one token: x[h][s] for the
+// eight MMAs of half h, m for the mins MMA (columns 0 / 1: hi / lo parts of
+// the 16 sub-block sums).
+struct T1B {
+  uint32_t x[2][8][2];
+  uint32_t m[2];
+};
+
+__device__ __forceinline__ uint32_t pack_h2(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
+
+// src: the block's 256 activations, bf16 (BF16 = true) or fp16 bits.
+template <bool BF16>
+__device__ __forceinline__ void t1_load_b(T1B &B, const uint16_t *__restrict__ src, int g, int c) {
+  const bool own0 = g == c, own1 = g == c + 4;
+  uint16_t shi[2], slo[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    // sub-block 8h + g of the block, natural order
+    const uint4 v0 = __ldcg(reinterpret_cast<const uint4 *>(src + 16 * (8 * h + g)));
+    const uint4 v1 = __ldcg(reinterpret_cast<const uint4 *>(src + 16 * (8 * h + g)) + 1);
+    const uint32_t wd[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint16_t f[16];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t bits = (wd[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
+      float v;
+      if (BF16) {
+        v = bf16_bits_to_f32(bits);
+        f[i] = __half_as_ushort(__float2half_rn(v));
+      } else {
+        v = f16_bits_to_f32(bits);
+        f[i] = (uint16_t)bits;
+      }
+      s += v;
+    }
+    // K step 2 wd + beta: values 4 (wd ^ rot) + beta and + 2
+#pragma unroll
+    for (int wdi = 0; wdi < 4; ++wdi) {
+#pragma unroll
+      for (int beta = 0; beta < 2; ++beta) {
+        const uint32_t p0 = pack_h2(f[4 * wdi + beta], f[4 * wdi + 2 + beta]);
+        const uint32_t p1 = pack_h2(f[4 * (wdi ^ 2) + beta], f[4 * (wdi ^ 2) + 2 + beta]);
+        const uint32_t p = (c & 1) ? p1 : p0;
+        B.x[h][2 * wdi + beta][0] = own0 ? p : 0u;
+        B.x[h][2 * wdi + beta][1] = own1 ? p : 0u;
+      }
+    }
+    const __half hi = __float2half_rn(s);
+    shi[h] = __half_as_ushort(hi);
+    slo[h] = __half_as_ushort(__float2half_rn(s - __half2float(hi)));
+  }
+  // mins operand: K slots 2c, 2c+1 = sub-blocks 2c, 2c+1 (half 0) and
+  // 2c+8, 2c+9 (half 1); their sums live in lanes 4 (2c) and 4 (2c + 1)
+  uint32_t mv[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint16_t h0 = (uint16_t)__shfl_sync(0xffffffffu, (uint32_t)shi[h], 8 * c);
+    const uint16_t h1 = (uint16_t)__shfl_sync(0xffffffffu, (uint32_t)shi[h], 8 * c + 4);
+    const uint16_t l0 = (uint16_t)__shfl_sync(0xffffffffu, (uint32_t)slo[h], 8 * c);
+    const uint16_t l1 = (uint16_t)__shfl_sync(0xffffffffu, (uint32_t)slo[h], 8 * c + 4);
+    mv[h] = g == 0 ? pack_h2(h0, h1) : g == 1 ? pack_h2(l0, l1) : 0u;
+  }
+  B.m[0] = mv[0];
+  B.m[1] = mv[1];
+}
+
+// One Q2_K block column of NM matrices of 16 staged rows each (matrix m,
+// row r at sb + (16 m + r) * rs): this lane's share of
+// d * sum(sc * q * x) - dmin * sum(mn * xsum) for rows g and g + 8 of every
+// matrix.  Even and odd K steps accumulate separately, so 2 NM MMA chains
+// are in flight.
+template <int NM>
+__device__ __forceinline__ void t1_block(const uint8_t *__restrict__ sb, uint32_t rs, int g, const T1B &B,
+                                         const T1Lane &L, float (&y)[NM][2]) {
+  const uint8_t *row[NM][2];
+  uint32_t sp[NM][2][2], dd[NM][2];
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      row[m][r] = sb + (size_t)(16 * m + g + 8 * r) * rs;
+      // scale bytes of sub-blocks (2c, 2c+1) of half 0 and (8+2c, 9+2c) of half 1
+      sp[m][r][0] = __byte_perm(ptx::lds32(row[m][r] + L.soff), 0u, L.ssel);
+      sp[m][r][1] = __byte_perm(ptx::lds32(row[m][r] + 8 + L.soff), 0u, L.ssel);
+      dd[m][r] = ptx::lds32(row[m][r] + 80);
+    }
+  }
+  float sacc[NM][2];
+#pragma unroll
+  for (int m = 0; m < NM; ++m) sacc[m][0] = sacc[m][1] = 0.f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t wq[NM][2][4];
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) wq[m][r][i] = ptx::lds32(row[m][r] + 16 + 32 * h + L.qoff + 4 * (i ^ L.rot));
+    float C[NM][2][4];
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) C[m][0][j] = C[m][1][j] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int m = 0; m < NM; ++m) {
+        const uint32_t A[4] = {wq[m][0][i] & L.m1, wq[m][1][i] & L.m1, wq[m][0][i] & L.m2, wq[m][1][i] & L.m2};
+        ptx::mma_f16(C[m][0], A, B.x[h][2 * i][0], B.x[h][2 * i][1]);
+      }
+#pragma unroll
+      for (int m = 0; m < NM; ++m) {
+        const uint32_t ua = wq[m][0][i] >> 8, ub = wq[m][1][i] >> 8;
+        const uint32_t A[4] = {ua & L.m1, ub & L.m1, ua & L.m2, ub & L.m2};
+        ptx::mma_f16(C[m][1], A, B.x[h][2 * i + 1][0], B.x[h][2 * i + 1][1]);
+      }
+    }
+    // sc of sub-blocks 8h + 2c, 8h + 2c + 1 as fp16 subnormals sc * 2^-24
+#pragma unroll
+    for (int m = 0; m < NM; ++m) {
+      const uint32_t sca = sp[m][0][h] & 0x000F000Fu, scb = sp[m][1][h] & 0x000F000Fu;
+      sacc[m][0] = fmaf(f16_bits_to_f32(sca & 0xFFFFu), C[m][0][0] + C[m][1][0], sacc[m][0]);
+      sacc[m][0] = fmaf(f16_bits_to_f32(sca >> 16), C[m][0][1] + C[m][1][1], sacc[m][0]);
+      sacc[m][1] = fmaf(f16_bits_to_f32(scb & 0xFFFFu), C[m][0][2] + C[m][1][2], sacc[m][1]);
+      sacc[m][1] = fmaf(f16_bits_to_f32(scb >> 16), C[m][0][3] + C[m][1][3], sacc[m][1]);
+    }
+  }
+  // mins: mn * 2^-20 (high nibbles) against the sub-block sums
+  const float k20 = 1048576.f;
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+    const uint32_t Am[4] = {sp[m][0][0] & 0x00F000F0u, sp[m][1][0] & 0x00F000F0u, sp[m][0][1] & 0x00F000F0u,
+                            sp[m][1][1] & 0x00F000F0u};
+    float M[4] = {0.f, 0.f, 0.f, 0.f};
+    ptx::mma_f16(M, Am, B.m[0], B.m[1]);
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      y[m][r] = fmaf(f16_bits_to_f32(dd[m][r] & 0xFFFFu) * L.kd, sacc[m][r],
+                     -f16_bits_to_f32(dd[m][r] >> 16) * k20 * (M[2 * r] + M[2 * r + 1]));
+  }
+}
+
+__device__ __forceinline__ float quad_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  return v;
+}
+
+// Last-arriver election over the consumer warps of a stage: every warp
+// publishes its partials, then counts itself; the warp that completes the
+// count returns true (and resets the counter) and may read all partials.
+__device__ __forceinline__ bool t1_last_arriver(int *cnt, int nwarps) {
+  const int lane = threadIdx.x & 31;
+  int last = 0;
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence_block();
+    last = atomicAdd(cnt, 1) == nwarps - 1;
+    if (last) {
+      *cnt = 0;
+      __threadfence_block();
+    }
+  }
+  return __shfl_sync(0xffffffffu, last, 0) != 0;
+}
+
+// Shared-memory row stride of a staged tile: row bytes rounded so that 8
+// consecutive rows fall into 8 distinct 4-bank groups (an odd number of
+// 16-byte units).
+__host__ __device__ constexpr uint32_t t1_row_stride(uint32_t rowb) { return ((rowb / 16) & 1u) ? rowb : rowb + 16; }
+
+// Shared-memory layout of the single-token kernels: nstage stages, then
+// the full / empty barriers, the per-stage partials and the per-stage
+// arrival counters.
+struct T1Smem {
+  uint64_t *full, *empty;
+  float *red;  // [nstage][nwarps][32]
+  int *cnt;    // [nstage]
+};
+__device__ __forceinline__ T1Smem t1_smem(uint8_t *smem, int nstage, uint32_t stage_bytes, int nwarps) {
+  T1Smem t;
+  t.full = reinterpret_cast<uint64_t *>(smem + (size_t)nstage * stage_bytes);
+  t.empty = t.full + nstage;
+  t.red = reinterpret_cast<float *>(t.empty + nstage);
+  t.cnt = reinterpret_cast<int *>(t.red + (size_t)nstage * nwarps * 32);
+  return t;
+}
+__host__ __device__ constexpr size_t t1_smem_bytes(int nstage, uint32_t stage_bytes, int nwarps) {
+  return (size_t)nstage * stage_bytes + 16 * (size_t)nstage + (size_t)nstage * nwarps * 32 * 4 + 4 * (size_t)nstage;
+}
+
+// With one token there are at most k <= 32 groups: every CTA keeps them in
+// shared memory, so no unit waits on a global load for its expert.
+constexpr int kT1MaxGroups = 32;
+__device__ __forceinline__ void t1_load_groups(const FfnArgs &a, Group *s_grp, int *s_ngrp) {
+  if (threadIdx.x < 32) {
+    const int n = __ldcg(&a.hdr->n_groups);
+    if (threadIdx.x < n) {
+      const int4 v = __ldcg(reinterpret_cast<const int4 *>(a.groups + threadIdx.x));
+      s_grp[threadIdx.x] = Group{v.x, v.y, v.z, v.w};
+    }
+    if (threadIdx.x == 0) *s_ngrp = n;
+  }
+  __syncthreads();
+}
+
+// gate/up + SwiGLU for T = 1: warps 0 .. nb-1 consume block w of d_model for
+// the 16 gate and 16 up rows of a tile, warp nb produces.  Units (group,
+// 16-row tile) are split into contiguous ranges, one per CTA; the warp that
+// finishes a unit last sums the blocks and writes h.
+template <bool FIN>
+__global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
+  const int D = a.L.d_model, F = a.L.d_ff, nb = D / 256;
+  const uint32_t rowb = (uint32_t)(kQ2KBytes * nb), rs = t1_row_stride(rowb);
+  const uint32_t stage_bytes = 32u * rs;
+  const T1Smem sm = t1_smem(smem, nstage, stage_bytes, nb);
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < nstage; ++st) {
+      ptx::mbar_init(&sm.full[st], 1);
+      ptx::mbar_init(&sm.empty[st], nb);
+      sm.cnt[st] = 0;
+    }
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  const T1Lane L = t1_lane(c);
+  T1B B;
+  // the activations are the call's input: loaded before the dependency wait
+  if (w < nb) t1_load_b<true>(B, a.x + 256 * w, g, c);
+  ptx::pdl_wait();  // groups come from the routing / bucketing grid
+  ptx::pdl_launch_dependents();
+  const int ntile = F / 16;
+  __shared__ Group s_grp[kT1MaxGroups];
+  __shared__ int s_ngrp;
+  t1_load_groups(a, s_grp, &s_ngrp);
+  const int U = s_ngrp * ntile;
+  const int u0 = (int)((int64_t)U * blockIdx.x / gridDim.x);
+  const int u1 = (int)((int64_t)U * (blockIdx.x + 1) / gridDim.x);
+  auto load_group = [&](int u) { return s_grp[u / ntile]; };
+  if (w == nb) {
+    // producer
+    const uint8_t *gate = static_cast<const uint8_t *>(a.L.gate), *up = static_cast<const uint8_t *>(a.L.up);
+    for (int u = u0, it = 0; u < u1; ++u, ++it) {
+      const int st = it % nstage;
+      if (it >= nstage && !ptx::mbar_wait(&sm.empty[st], ((it / nstage) - 1) & 1)) {
+        record_status(a.hdr, DS4MOE_ETIMEOUT);
+        break;
+      }
+      const Group grp = load_group(u);
+      const int row0 = (u % ntile) * 16;
+      if (lane == 0) ptx::mbar_arrive_expect_tx(&sm.full[st], 32u * rowb);
+      __syncwarp();
+      const uint8_t *src = (lane < 16 ? gate : up) + ((int64_t)grp.e * F + row0 + (lane & 15)) * rowb;
+      ptx::bulk_g2s(smem + (size_t)st * stage_bytes + (size_t)lane * rs, src, rowb, &sm.full[st]);
+      if (FIN && blockIdx.x == 0 && it == nstage - 1) finish_routing_weights(const_cast<float *>(a.w), a.T, a.k);
+    }
+    if (FIN && blockIdx.x == 0 && u1 - u0 < nstage) finish_routing_weights(const_cast<float *>(a.w), a.T, a.k);
+    return;
+  }
+  bool timed_out = false;
+  int it = 0;
+  for (int u = u0; u < u1; ++u, ++it) {
+    const int st = it % nstage;
+    if (!timed_out && !ptx::mbar_wait(&sm.full[st], (it / nstage) & 1)) {
+      record_status(a.hdr, DS4MOE_ETIMEOUT);
+      timed_out = true;
+    }
+    float y[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    if (!timed_out) t1_block<2>(smem + (size_t)st * stage_bytes + kQ2KBytes * w, rs, g, B, L, y);
+    // partials of this block: gate rows g, g+8 at [g], [g+8], up at [16+g], [24+g]
+    float *r = sm.red + ((size_t)st * nb + w) * 32;
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const float v = quad_sum(y[m][q]);
+        if (c == 0) r[16 * m + 8 * q + g] = v;
+      }
+    if (t1_last_arriver(&sm.cnt[st], nb)) {
+      // lane l: gate row l (l < 16) or up row l - 16, blocks summed in order
+      const float *rr = sm.red + (size_t)st * nb * 32 + lane;
+      float sv = 0.f;
+      for (int p = 0; p < nb; ++p) sv += rr[32 * p];
+      const float us = __shfl_down_sync(0xffffffffu, sv, 16);
+      const Group grp = load_group(u);
+      const int row0 = (u % ntile) * 16;
+      float hv = 0.f;
+      if (lane < 16) {
+        // h rounded to bf16 (the definition), stored as the fp16 operand of
+        // the down kernel (exact for |h| in [2^-14, 65504])
+        hv = bf16_bits_to_f32(f32_to_bf16_bits(silu(sv) * us));
+        if (fabsf(hv) > 65504.f) record_status(a.hdr, DS4MOE_EDEVICE);
+        a.h[(int64_t)grp.p0 * F + row0 + lane] = __half_as_ushort(__float2half_rn(hv));
+      }
+#pragma unroll
+      for (int off = 8; off; off >>= 1) hv += __shfl_xor_sync(0xffffffffu, hv, off);
+      if (lane == 0) {
+        const int n16 = row0 / 16;
+        const __half hi = __float2half_rn(hv);
+        const __half lo = __float2half_rn(hv - __half2float(hi));
+        uint16_t *rec = reinterpret_cast<uint16_t *>(a.hs16 + ((int64_t)grp.p0 * (F / 256 + 1) + n16 / 16) * 64);
+        rec[n16 & 15] = __half_as_ushort(hi);
+        rec[16 + (n16 & 15)] = __half_as_ushort(lo);
+      }
+    }
+    // the stage (weights and partials) may be refilled once every warp is here
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&sm.empty[st]);
+  }
+  // no copy may still be landing in shared memory when the CTA exits
+  if (timed_out && lane == 0) {
+    for (int j = it - nstage > 0 ? it - nstage : 0; j < it; ++j)
+      ptx::mbar_wait(&sm.full[j % nstage], (j / nstage) & 1, 1u << 20);
+  }
+}
+
+// down for T = 1: warps 0 .. nb-1 consume block w of d_ff for a 16-row tile
+// of one expert (its h loaded when the group changes), warp nb produces;
+// contiguous unit ranges per CTA, so a CTA sees at most a few groups.  The
+// warp finishing a unit last writes y; the weighted combine is a grid of
+// its own (a fused one would count arrivals per tile across CTAs, and its
+// fences cost more than the launch).
+__global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
+  const int D = a.L.d_model, F = a.L.d_ff, nb = F / 256;
+  const uint32_t rowb = (uint32_t)(kQ2KBytes * nb), rs = t1_row_stride(rowb);
+  const uint32_t stage_bytes = 16u * rs;
+  const T1Smem sm = t1_smem(smem, nstage, stage_bytes, nb);
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < nstage; ++st) {
+      ptx::mbar_init(&sm.full[st], 1);
+      ptx::mbar_init(&sm.empty[st], nb);
+      sm.cnt[st] = 0;
+    }
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  const int ntile = D / 16;
+  // the groups were complete before the gate/up grid launched this one
+  __shared__ Group s_grp[kT1MaxGroups];
+  __shared__ int s_ngrp;
+  t1_load_groups(a, s_grp, &s_ngrp);
+  const int U = s_ngrp * ntile;
+  const int u0 = (int)((int64_t)U * blockIdx.x / gridDim.x);
+  const int u1 = (int)((int64_t)U * (blockIdx.x + 1) / gridDim.x);
+  auto load_group = [&](int u) { return s_grp[u / ntile]; };
+  if (w == nb) {
+    const uint8_t *down = static_cast<const uint8_t *>(a.L.down);
+    for (int u = u0, it = 0; u < u1; ++u, ++it) {
+      const int st = it % nstage;
+      if (it >= nstage && !ptx::mbar_wait(&sm.empty[st], ((it / nstage) - 1) & 1)) {
+        record_status(a.hdr, DS4MOE_ETIMEOUT);
+        break;
+      }
+      const Group grp = load_group(u);
+      const int row0 = (u % ntile) * 16;
+      if (lane == 0) ptx::mbar_arrive_expect_tx(&sm.full[st], 16u * rowb);
+      __syncwarp();
+      if (lane < 16)
+        ptx::bulk_g2s(smem + (size_t)st * stage_bytes + (size_t)lane * rs,
+                      down + ((int64_t)grp.e * D + row0 + lane) * rowb, rowb, &sm.full[st]);
+    }
+    return;
+  }
+  const T1Lane L = t1_lane(c);
+  T1B B;
+  ptx::pdl_wait();  // h comes from the gate/up grid
+  ptx::pdl_launch_dependents();
+  bool timed_out = false;
+  int it = 0, cur = -1;
+  for (int u = u0; u < u1; ++u, ++it) {
+    const int st = it % nstage;
+    const Group grp = load_group(u);
+    if (grp.p0 != cur) {
+      t1_load_b<false>(B, a.h + (int64_t)grp.p0 * F + 256 * w, g, c);
+      cur = grp.p0;
+    }
+    if (!timed_out && !ptx::mbar_wait(&sm.full[st], (it / nstage) & 1)) {
+      record_status(a.hdr, DS4MOE_ETIMEOUT);
+      timed_out = true;
+    }
+    float y[1][2] = {{0.f, 0.f}};
+    if (!timed_out) t1_block<1>(smem + (size_t)st * stage_bytes + kQ2KBytes * w, rs, g, B, L, y);
+    float *r = sm.red + ((size_t)st * nb + w) * 32;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float v = quad_sum(y[0][q]);
+      if (c == 0) r[8 * q + g] = v;
+    }
+    if (t1_last_arriver(&sm.cnt[st], nb)) {
+      const int row0 = (u % ntile) * 16;
+      if (lane < 16) {
+        const float *rr = sm.red + (size_t)st * nb * 32 + lane;
+        float sv = 0.f;
+        for (int p = 0; p < nb; ++p) sv += rr[32 * p];
+        a.y[(int64_t)grp.p0 * D + row0 + lane] = sv;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&sm.empty[st]);
+  }
+  if (timed_out && lane == 0) {
+    for (int j = it - nstage > 0 ? it - nstage : 0; j < it; ++j)
+      ptx::mbar_wait(&sm.full[j % nstage], (j / nstage) & 1, 1u << 20);
+  }
+}
+
 // ============================================================ SIMT path
 template <typename In>
 __device__ __forceinline__ void row_dot_q41(const uint8_t *__restrict__ row, int cols, int nt, In in,
@@ -664,6 +1118,49 @@ cudaError_t launch_gate_up_mma(const FfnArgs &a, cudaStream_t s, int kp) {
   return launch_pdl(kern, dim3(grid), dim3(2 * kp * 32), smem, s, a, kp, chg, chu);
 }
 
+constexpr size_t kT1SmemGateUp = 227 * 1024, kT1SmemDown = 100 * 1024;
+
+cudaError_t launch_gate_up_t1(const FfnArgs &a, cudaStream_t s) {
+  const int nb = a.L.d_model / 256;
+  const uint32_t stage = 32 * t1_row_stride((uint32_t)(kQ2KBytes * nb));
+  int nstage = 6;
+  while (nstage > 2 && t1_smem_bytes(nstage, stage, nb) > kT1SmemGateUp) --nstage;
+  const size_t smem = t1_smem_bytes(nstage, stage, nb);
+  if (smem > kT1SmemGateUp) return cudaErrorInvalidValue;
+  auto kern = a.w_logits ? k_gate_up_t1<true> : k_gate_up_t1<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  ProfScope p("gate_up", s);
+  return launch_pdl(kern, dim3(num_sms()), dim3(32 * (nb + 1)), smem, s, a, nstage);
+}
+
+cudaError_t launch_down_t1(const FfnArgs &a, cudaStream_t s) {
+  const int nb = a.L.d_ff / 256;
+  const uint32_t stage = 16 * t1_row_stride((uint32_t)(kQ2KBytes * nb));
+  int nstage = 8;
+  while (nstage > 2 && t1_smem_bytes(nstage, stage, nb) > kT1SmemDown) --nstage;
+  const size_t smem = t1_smem_bytes(nstage, stage, nb);
+  if (smem > kT1SmemDown) return cudaErrorInvalidValue;
+  auto kern = k_down_t1;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (nb + 1), smem);
+  if (e != cudaSuccess) return e;
+  ProfScope p("down", s);
+  return launch_pdl(kern, dim3(num_sms() * (per_sm > 0 ? per_sm : 1)), dim3(32 * (nb + 1)), smem, s, a, nstage);
+}
+
+// Single-token kernels: Q2_K, one consumer warp per 256-value block of K
+// (at most 16 for gate/up, 8 for down), rows split into 16-byte units.
+bool t1_gate_up_ok(const ds4moe_layer &L) {
+  return L.q_gate == DS4MOE_Q2_K && L.q_up == DS4MOE_Q2_K && L.d_model % 1024 == 0 && L.d_model <= 4096 &&
+         L.d_ff % 16 == 0;
+}
+bool t1_down_ok(const ds4moe_layer &L) {
+  return L.q_down == DS4MOE_Q2_K && L.d_ff % 1024 == 0 && L.d_ff <= 2048 && L.d_model % 16 == 0;
+}
+
 cudaError_t launch_down_mma(const FfnArgs &a, cudaStream_t s) {
   const int F = a.L.d_ff;
   const uint32_t chd = (uint32_t)row_bytes(DS4MOE_Q2_K, F);
@@ -703,12 +1200,13 @@ cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s) {
   if (decode_mma_ok(L)) {
     const int kp = pick_kp(L.d_model, L.q_gate, L.q_up);
     cudaError_t e;
-    if (L.q_gate == DS4MOE_Q2_K && L.q_up == DS4MOE_Q2_K) e = launch_gate_up_mma<DS4MOE_Q2_K, DS4MOE_Q2_K>(a, s, kp);
+    if (a.T == 1 && t1_gate_up_ok(L)) e = launch_gate_up_t1(a, s);
+    else if (L.q_gate == DS4MOE_Q2_K && L.q_up == DS4MOE_Q2_K) e = launch_gate_up_mma<DS4MOE_Q2_K, DS4MOE_Q2_K>(a, s, kp);
     else if (L.q_gate == DS4MOE_Q4_1 && L.q_up == DS4MOE_Q4_1) e = launch_gate_up_mma<DS4MOE_Q4_1, DS4MOE_Q4_1>(a, s, kp);
     else if (L.q_gate == DS4MOE_Q2_K) e = launch_gate_up_mma<DS4MOE_Q2_K, DS4MOE_Q4_1>(a, s, kp);
     else e = launch_gate_up_mma<DS4MOE_Q4_1, DS4MOE_Q2_K>(a, s, kp);
     if (e != cudaSuccess) return e;
-    return launch_down_mma(a, s);
+    return a.T == 1 && t1_down_ok(L) ? launch_down_t1(a, s) : launch_down_mma(a, s);
   }
   const int grid = num_sms() * 8;
   {
@@ -725,7 +1223,7 @@ cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s) {
-  if (a.cnt) return cudaSuccess;  // fused into the down kernel
+  if (a.cnt && !(a.T == 1 && t1_down_ok(a.L))) return cudaSuccess;  // fused into the down kernel
   const int64_t n4 = (int64_t)a.T * a.L.d_model / 4;
   const int grid = (int)((n4 + 255) / 256 < num_sms() * 16 ? (n4 + 255) / 256 : num_sms() * 16);
   ProfScope p("combine", s);
