@@ -19,6 +19,7 @@
 // copies (row bytes not a multiple of 16).
 #include "internal.cuh"
 #include "ptx.cuh"
+#include "t1.cuh"
 
 namespace ds4 {
 namespace {
@@ -499,256 +500,6 @@ __global__ void __launch_bounds__(256) k_down_mma(FfnArgs a, uint32_t chd) {
   }
 }
 
-// ================================================== single-token decode
-// With one token (T = 1) every expert group holds one pair, and the n = 8
-// side of the MMA is better spent on eight Q2_K sub-blocks than on tokens.
-// Per 128-value half of a 256-value block, K slots 2n, 2n+1 of every MMA
-// carry two values of sub-block n, and the activation operand is placed
-// block-diagonally (column n sees only K slots 2n, 2n+1), so after the eight
-// MMAs of a half, D[row][n] is the code-dot of sub-block n alone.  The
-// per-(row, sub-block) scale is then one fp32 FMA per 16 weights in the
-// epilogue, and the mins one more MMA per block (mn codes x sub-block sums).
-//
-// Codes enter as fp16 subnormals: masking the 2-bit field at bit 2p of the
-// low byte of each fp16 half leaves q * 2^(2p - 24) exactly, one LOP per
-// operand register; the power of two is folded into the block scale.  Lane
-// quad c handles sub-blocks c and c + 4 of a half, which share the qs bytes
-// 16 (c & 1) .. +15 at code positions c / 2 and c / 2 + 2, and D columns
-// 2c, 2c+1, which both sit at code position c.
-//
-// Each consumer warp owns one 256-value block column of K and keeps its
-// activation operands in registers; a producer warp streams 16-row tiles
-// into a ring of shared-memory stages with bulk copies.
-struct T1Lane {
-  uint32_t m1, m2;  // code fields at positions c/2 and c/2 + 2, both fp16 halves
-  uint32_t qoff;    // this lane's 16 qs bytes within a 32-byte half
-  uint32_t rot;     // word order rotation of lanes with odd c (spreads banks)
-  uint32_t soff;    // scale word holding bytes 2c, 2c+1 of a half
-  uint32_t ssel;    // PRMT selector: (byte 2c, 0, byte 2c+1, 0)
-  float kd;         // 2^(48 - 2c): undoes sc's 2^-24 and the columns' 2^(2c-24)
-};
-
-__device__ __forceinline__ T1Lane t1_lane(int c) {
-  T1Lane L;
-  L.m1 = 0x00030003u << (2 * (c >> 1));
-  L.m2 = L.m1 << 4;
-  L.qoff = 16u * (c & 1);
-  L.rot = 2u * (c & 1);
-  L.soff = 4u * (c >> 1);
-  const uint32_t b = 2u * (c & 1);
-  L.ssel = b | (4u << 4) | ((b + 1u) << 8) | (4u << 12);
-  L.kd = __uint_as_float((uint32_t)(127 + 48 - 2 * c) << 23);
-  return L;
-}
-
-// Activation operands of one 256-value block of one token: x[h][s] for the
-// eight MMAs of half h, m for the mins MMA (columns 0 / 1: hi / lo parts of
-// the 16 sub-block sums).
-struct T1B {
-  uint32_t x[2][8][2];
-  uint32_t m[2];
-};
-
-__device__ __forceinline__ uint32_t pack_h2(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
-
-// src: the block's 256 activations, bf16 (BF16 = true) or fp16 bits.
-template <bool BF16>
-__device__ __forceinline__ void t1_load_b(T1B &B, const uint16_t *__restrict__ src, int g, int c) {
-  const bool own0 = g == c, own1 = g == c + 4;
-  uint16_t shi[2], slo[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    // sub-block 8h + g of the block, natural order
-    const uint4 v0 = __ldcg(reinterpret_cast<const uint4 *>(src + 16 * (8 * h + g)));
-    const uint4 v1 = __ldcg(reinterpret_cast<const uint4 *>(src + 16 * (8 * h + g)) + 1);
-    const uint32_t wd[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    uint16_t f[16];
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t bits = (wd[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
-      float v;
-      if (BF16) {
-        v = bf16_bits_to_f32(bits);
-        f[i] = __half_as_ushort(__float2half_rn(v));
-      } else {
-        v = f16_bits_to_f32(bits);
-        f[i] = (uint16_t)bits;
-      }
-      s += v;
-    }
-    // K step 2 wd + beta: values 4 (wd ^ rot) + beta and + 2
-#pragma unroll
-    for (int wdi = 0; wdi < 4; ++wdi) {
-#pragma unroll
-      for (int beta = 0; beta < 2; ++beta) {
-        const uint32_t p0 = pack_h2(f[4 * wdi + beta], f[4 * wdi + 2 + beta]);
-        const uint32_t p1 = pack_h2(f[4 * (wdi ^ 2) + beta], f[4 * (wdi ^ 2) + 2 + beta]);
-        const uint32_t p = (c & 1) ? p1 : p0;
-        B.x[h][2 * wdi + beta][0] = own0 ? p : 0u;
-        B.x[h][2 * wdi + beta][1] = own1 ? p : 0u;
-      }
-    }
-    const __half hi = __float2half_rn(s);
-    shi[h] = __half_as_ushort(hi);
-    slo[h] = __half_as_ushort(__float2half_rn(s - __half2float(hi)));
-  }
-  // mins operand: K slots 2c, 2c+1 = sub-blocks 2c, 2c+1 (half 0) and
-  // 2c+8, 2c+9 (half 1); their sums live in lanes 4 (2c) and 4 (2c + 1)
-  uint32_t mv[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint16_t h0 = (uint16_t)__shfl_sync(0xffffffffu, (uint32_t)shi[h], 8 * c);
-    const uint16_t h1 = (uint16_t)__shfl_sync(0xffffffffu, (uint32_t)shi[h], 8 * c + 4);
-    const uint16_t l0 = (uint16_t)__shfl_sync(0xffffffffu, (uint32_t)slo[h], 8 * c);
-    const uint16_t l1 = (uint16_t)__shfl_sync(0xffffffffu, (uint32_t)slo[h], 8 * c + 4);
-    mv[h] = g == 0 ? pack_h2(h0, h1) : g == 1 ? pack_h2(l0, l1) : 0u;
-  }
-  B.m[0] = mv[0];
-  B.m[1] = mv[1];
-}
-
-// One Q2_K block column of NM matrices of 16 staged rows each (matrix m,
-// row r at sb + (16 m + r) * rs): this lane's share of
-// d * sum(sc * q * x) - dmin * sum(mn * xsum) for rows g and g + 8 of every
-// matrix.  Even and odd K steps accumulate separately, so 2 NM MMA chains
-// are in flight.
-template <int NM>
-__device__ __forceinline__ void t1_block(const uint8_t *__restrict__ sb, uint32_t rs, int g, const T1B &B,
-                                         const T1Lane &L, float (&y)[NM][2]) {
-  const uint8_t *row[NM][2];
-  uint32_t sp[NM][2][2], dd[NM][2];
-#pragma unroll
-  for (int m = 0; m < NM; ++m) {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      row[m][r] = sb + (size_t)(16 * m + g + 8 * r) * rs;
-      // scale bytes of sub-blocks (2c, 2c+1) of half 0 and (8+2c, 9+2c) of half 1
-      sp[m][r][0] = __byte_perm(ptx::lds32(row[m][r] + L.soff), 0u, L.ssel);
-      sp[m][r][1] = __byte_perm(ptx::lds32(row[m][r] + 8 + L.soff), 0u, L.ssel);
-      dd[m][r] = ptx::lds32(row[m][r] + 80);
-    }
-  }
-  float sacc[NM][2];
-#pragma unroll
-  for (int m = 0; m < NM; ++m) sacc[m][0] = sacc[m][1] = 0.f;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t wq[NM][2][4];
-#pragma unroll
-    for (int m = 0; m < NM; ++m)
-#pragma unroll
-      for (int r = 0; r < 2; ++r)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) wq[m][r][i] = ptx::lds32(row[m][r] + 16 + 32 * h + L.qoff + 4 * (i ^ L.rot));
-    float C[NM][2][4];
-#pragma unroll
-    for (int m = 0; m < NM; ++m)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) C[m][0][j] = C[m][1][j] = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-      for (int m = 0; m < NM; ++m) {
-        const uint32_t A[4] = {wq[m][0][i] & L.m1, wq[m][1][i] & L.m1, wq[m][0][i] & L.m2, wq[m][1][i] & L.m2};
-        ptx::mma_f16(C[m][0], A, B.x[h][2 * i][0], B.x[h][2 * i][1]);
-      }
-#pragma unroll
-      for (int m = 0; m < NM; ++m) {
-        const uint32_t ua = wq[m][0][i] >> 8, ub = wq[m][1][i] >> 8;
-        const uint32_t A[4] = {ua & L.m1, ub & L.m1, ua & L.m2, ub & L.m2};
-        ptx::mma_f16(C[m][1], A, B.x[h][2 * i + 1][0], B.x[h][2 * i + 1][1]);
-      }
-    }
-    // sc of sub-blocks 8h + 2c, 8h + 2c + 1 as fp16 subnormals sc * 2^-24
-#pragma unroll
-    for (int m = 0; m < NM; ++m) {
-      const uint32_t sca = sp[m][0][h] & 0x000F000Fu, scb = sp[m][1][h] & 0x000F000Fu;
-      sacc[m][0] = fmaf(f16_bits_to_f32(sca & 0xFFFFu), C[m][0][0] + C[m][1][0], sacc[m][0]);
-      sacc[m][0] = fmaf(f16_bits_to_f32(sca >> 16), C[m][0][1] + C[m][1][1], sacc[m][0]);
-      sacc[m][1] = fmaf(f16_bits_to_f32(scb & 0xFFFFu), C[m][0][2] + C[m][1][2], sacc[m][1]);
-      sacc[m][1] = fmaf(f16_bits_to_f32(scb >> 16), C[m][0][3] + C[m][1][3], sacc[m][1]);
-    }
-  }
-  // mins: mn * 2^-20 (high nibbles) against the sub-block sums
-  const float k20 = 1048576.f;
-#pragma unroll
-  for (int m = 0; m < NM; ++m) {
-    const uint32_t Am[4] = {sp[m][0][0] & 0x00F000F0u, sp[m][1][0] & 0x00F000F0u, sp[m][0][1] & 0x00F000F0u,
-                            sp[m][1][1] & 0x00F000F0u};
-    float M[4] = {0.f, 0.f, 0.f, 0.f};
-    ptx::mma_f16(M, Am, B.m[0], B.m[1]);
-#pragma unroll
-    for (int r = 0; r < 2; ++r)
-      y[m][r] = fmaf(f16_bits_to_f32(dd[m][r] & 0xFFFFu) * L.kd, sacc[m][r],
-                     -f16_bits_to_f32(dd[m][r] >> 16) * k20 * (M[2 * r] + M[2 * r + 1]));
-  }
-}
-
-__device__ __forceinline__ float quad_sum(float v) {
-  v += __shfl_xor_sync(0xffffffffu, v, 1);
-  v += __shfl_xor_sync(0xffffffffu, v, 2);
-  return v;
-}
-
-// Last-arriver election over the consumer warps of a stage: every warp
-// publishes its partials, then counts itself; the warp that completes the
-// count returns true (and resets the counter) and may read all partials.
-__device__ __forceinline__ bool t1_last_arriver(int *cnt, int nwarps) {
-  const int lane = threadIdx.x & 31;
-  int last = 0;
-  __syncwarp();
-  if (lane == 0) {
-    __threadfence_block();
-    last = atomicAdd(cnt, 1) == nwarps - 1;
-    if (last) {
-      *cnt = 0;
-      __threadfence_block();
-    }
-  }
-  return __shfl_sync(0xffffffffu, last, 0) != 0;
-}
-
-// Shared-memory row stride of a staged tile: row bytes rounded so that 8
-// consecutive rows fall into 8 distinct 4-bank groups (an odd number of
-// 16-byte units).
-__host__ __device__ constexpr uint32_t t1_row_stride(uint32_t rowb) { return ((rowb / 16) & 1u) ? rowb : rowb + 16; }
-
-// Shared-memory layout of the single-token kernels: nstage stages, then
-// the full / empty barriers, the per-stage partials and the per-stage
-// arrival counters.
-struct T1Smem {
-  uint64_t *full, *empty;
-  float *red;  // [nstage][nwarps][32]
-  int *cnt;    // [nstage]
-};
-__device__ __forceinline__ T1Smem t1_smem(uint8_t *smem, int nstage, uint32_t stage_bytes, int nwarps) {
-  T1Smem t;
-  t.full = reinterpret_cast<uint64_t *>(smem + (size_t)nstage * stage_bytes);
-  t.empty = t.full + nstage;
-  t.red = reinterpret_cast<float *>(t.empty + nstage);
-  t.cnt = reinterpret_cast<int *>(t.red + (size_t)nstage * nwarps * 32);
-  return t;
-}
-__host__ __device__ constexpr size_t t1_smem_bytes(int nstage, uint32_t stage_bytes, int nwarps) {
-  return (size_t)nstage * stage_bytes + 16 * (size_t)nstage + (size_t)nstage * nwarps * 32 * 4 + 4 * (size_t)nstage;
-}
-
-// With one token there are at most k <= 32 groups: every CTA keeps them in
-// shared memory, so no unit waits on a global load for its expert.
-constexpr int kT1MaxGroups = 32;
-__device__ __forceinline__ void t1_load_groups(const FfnArgs &a, Group *s_grp, int *s_ngrp) {
-  if (threadIdx.x < 32) {
-    const int n = __ldcg(&a.hdr->n_groups);
-    if (threadIdx.x < n) {
-      const int4 v = __ldcg(reinterpret_cast<const int4 *>(a.groups + threadIdx.x));
-      s_grp[threadIdx.x] = Group{v.x, v.y, v.z, v.w};
-    }
-    if (threadIdx.x == 0) *s_ngrp = n;
-  }
-  __syncthreads();
-}
-
 // gate/up + SwiGLU for T = 1: warps 0 .. nb-1 consume block w of d_model for
 // the 16 gate and 16 up rows of a tile, warp nb produces.  Units (group,
 // 16-row tile) are split into contiguous ranges, one per CTA; the warp that
@@ -813,7 +564,11 @@ __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage
       timed_out = true;
     }
     float y[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-    if (!timed_out) t1_block<2>(smem + (size_t)st * stage_bytes + kQ2KBytes * w, rs, g, B, L, y);
+    if (!timed_out) {
+      const uint8_t *sb = smem + (size_t)st * stage_bytes + kQ2KBytes * w;
+      const uint8_t *const mats[2] = {sb, sb + 16 * (size_t)rs};
+      t1_block<2>(mats, rs, 0, g, B, L, y);
+    }
     // partials of this block: gate rows g, g+8 at [g], [g+8], up at [16+g], [24+g]
     float *r = sm.red + ((size_t)st * nb + w) * 32;
 #pragma unroll
@@ -871,8 +626,8 @@ __global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
   const int D = a.L.d_model, F = a.L.d_ff, nb = F / 256;
-  const uint32_t rowb = (uint32_t)(kQ2KBytes * nb), rs = t1_row_stride(rowb);
-  const uint32_t stage_bytes = 16u * rs;
+  const uint32_t rowb = (uint32_t)(kQ2KBytes * nb), gap = t1_gap4(rowb);
+  const uint32_t stage_bytes = t1_gap_stage_bytes(rowb);
   const T1Smem sm = t1_smem(smem, nstage, stage_bytes, nb);
   if (threadIdx.x == 0) {
     for (int st = 0; st < nstage; ++st) {
@@ -904,9 +659,10 @@ __global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
       const int row0 = (u % ntile) * 16;
       if (lane == 0) ptx::mbar_arrive_expect_tx(&sm.full[st], 16u * rowb);
       __syncwarp();
-      if (lane < 16)
-        ptx::bulk_g2s(smem + (size_t)st * stage_bytes + (size_t)lane * rs,
-                      down + ((int64_t)grp.e * D + row0 + lane) * rowb, rowb, &sm.full[st]);
+      // four copies of 4 rows (row copies this short are issue-bound)
+      if (lane < 4)
+        ptx::bulk_g2s(smem + (size_t)st * stage_bytes + (size_t)lane * (4u * rowb + gap),
+                      down + ((int64_t)grp.e * D + row0 + 4 * lane) * rowb, 4u * rowb, &sm.full[st]);
     }
     return;
   }
@@ -928,7 +684,10 @@ __global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
       timed_out = true;
     }
     float y[1][2] = {{0.f, 0.f}};
-    if (!timed_out) t1_block<1>(smem + (size_t)st * stage_bytes + kQ2KBytes * w, rs, g, B, L, y);
+    if (!timed_out) {
+      const uint8_t *const mats[1] = {smem + (size_t)st * stage_bytes + kQ2KBytes * w};
+      t1_block<1>(mats, rowb, gap, g, B, L, y);
+    }
     float *r = sm.red + ((size_t)st * nb + w) * 32;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
@@ -1136,7 +895,7 @@ cudaError_t launch_gate_up_t1(const FfnArgs &a, cudaStream_t s) {
 
 cudaError_t launch_down_t1(const FfnArgs &a, cudaStream_t s) {
   const int nb = a.L.d_ff / 256;
-  const uint32_t stage = 16 * t1_row_stride((uint32_t)(kQ2KBytes * nb));
+  const uint32_t stage = t1_gap_stage_bytes((uint32_t)(kQ2KBytes * nb));
   int nstage = 8;
   while (nstage > 2 && t1_smem_bytes(nstage, stage, nb) > kT1SmemDown) --nstage;
   const size_t smem = t1_smem_bytes(nstage, stage, nb);
