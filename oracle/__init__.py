@@ -65,6 +65,11 @@ def _L():
         lib.orc_matvec_rows.argtypes = [i32, p, i32, i32, i32, i32, p, p]
         lib.orc_expert_ffn.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, p, p, p, p, p]
         lib.orc_moe_ffn.argtypes = [i32, i32, i32, i32, p, i32, p, i32, p, p, p, p, i32, i32, p]
+        lib.orc_f32_to_f16.restype = ctypes.c_uint16
+        lib.orc_f32_to_f16.argtypes = [ctypes.c_float]
+        lib.orc_quantize_f32.argtypes = [i32, p, p, i64, i64, p]
+        lib.orc_weighted_sq_error.restype = ctypes.c_double
+        lib.orc_weighted_sq_error.argtypes = [i32, p, p, i64, i64, p]
         _lib = lib
     return _lib
 
@@ -262,3 +267,35 @@ def moe_ffn(D, F, E, qg, gate, qu, up, qd, down, x_bf16, idx, w) -> np.ndarray:
     if st:
         raise OracleError(st, "moe_ffn")
     return out
+
+
+# ------------------------------------------------------ float-input quantizer
+def f32_to_f16(v) -> np.ndarray:
+    """binary32 -> binary16 bit patterns, round to nearest even (own encoder)."""
+    v = np.asarray(v, dtype=np.float32).ravel()
+    return np.array([_L().orc_f32_to_f16(float(a)) for a in v], dtype=np.uint16)
+
+
+def quantize_f32(qtype: int, x, importance=None, cols: int | None = None) -> np.ndarray:
+    """Float-input quantizer ([DS4-2] Q2_K block writer reading; Q4_1 likewise):
+    per-block (Q4_1) or per-sub-block (Q2_K) min / max scales, nearest codes,
+    and with per-column `importance` a small search over neighbouring scales
+    that minimises the weighted squared error.  Returns the block bytes."""
+    x = _c(x, np.float32).ravel()
+    n = x.size
+    bv, bb = block_values(qtype), block_bytes(qtype)
+    out = np.zeros(n // bv * bb if bv else 0, dtype=np.uint8)
+    imp = None if importance is None else _c(importance, np.float32).ravel()
+    c = cols if cols is not None else (imp.size if imp is not None else n)
+    st = _L().orc_quantize_f32(qtype, _ptr(x), _ptr(imp), n, c, _ptr(out))
+    if st != OK:
+        raise OracleError(st, "quantize_f32")
+    return out
+
+
+def weighted_sq_error(qtype: int, x, importance, cols: int, blocks) -> float:
+    """sum over values of importance[col] * (x - dequant)^2 (unit weights when
+    importance is None), in double."""
+    x = _c(x, np.float32).ravel()
+    imp = None if importance is None else _c(importance, np.float32).ravel()
+    return _L().orc_weighted_sq_error(qtype, _ptr(x), _ptr(imp), x.size, cols, _ptr(_c(blocks, np.uint8)))

@@ -423,3 +423,220 @@ void orc_rmsnorm_bf16(const float *x, int64_t T, int64_t D, double eps, uint16_t
     for (int64_t j = 0; j < D; ++j) out[t * D + j] = orc_round_bf16((double)x[t * D + j] * r);
   }
 }
+
+/* ------------------------------------------------ float-input quantizer
+ * [DS4-2], section on the Q2_K block writer: a scale and a minimum are
+ * estimated per 16-value sub-block and every value is rounded to a 2-bit
+ * code 0..3; with an importance matrix the weighted writer scores the
+ * quantisation error with the per-column importance and so changes which
+ * scales and codes are chosen.  The pages give neither search, so this is a
+ * plain reading (the same one the CUDA path implements, decision by
+ * decision in fp32, so that the integer codes can be compared bit for bit):
+ *
+ *   Q2_K, per sub-block s:  lo = min(0, min x), hi = max x,
+ *     a_s = (hi - lo) / 3, b_s = -lo;  d = f16(max a_s / 15),
+ *     dmin = f16(max b_s / 15), sc_s = clamp(rint(a_s / d), 0, 15),
+ *     mn_s = clamp(rint(b_s / dmin), 0, 15), q = clamp(rint((x + dmin mn) /
+ *     (d sc)), 0, 3)  (a zero step gives code 0).
+ *   Q4_1, per 32-value block: d = f16((max - min) / 15), m = f16(min),
+ *     q = clamp(rint((x - m) / d), 0, 15).
+ *   With importance w (one weight per column): every sub-block (Q2_K) tries
+ *   (sc, mn) in {sc-1, sc, sc+1} x {mn-1, mn, mn+1} (Q4_1: d and m each
+ *   also one fp16 step down and up), codes re-chosen for each candidate,
+ *   and keeps the first candidate with the least sum w (x - y)^2 -- the
+ *   plain choice is tried first, so the weighted error never grows.
+ *
+ * All arithmetic is fp32 with one rounding per operation (no contraction);
+ * f16() rounds to nearest even.
+ */
+
+/* IEEE binary32 -> binary16, round to nearest even (finite inputs). */
+uint16_t orc_f32_to_f16(float v) {
+  uint32_t u;
+  memcpy(&u, &v, 4);
+  const uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+  const uint32_t a = u & 0x7FFFFFFFu;
+  if (a >= 0x7F800000u) return (uint16_t)(sign | 0x7C00u | (a > 0x7F800000u ? 0x200u : 0u));
+  const int e = (int)(a >> 23) - 127;
+  uint32_t mant = (a & 0x7FFFFFu) | (a ? 0x800000u : 0u); /* 24-bit significand */
+  if (a == 0) return sign;
+  if (e > 15) return (uint16_t)(sign | 0x7C00u); /* overflow -> inf */
+  /* target exponent field and how many significand bits to drop */
+  int shift;
+  uint32_t exp_field;
+  if (e >= -14) {
+    exp_field = (uint32_t)(e + 15);
+    shift = 13;
+  } else {
+    exp_field = 0;
+    shift = 13 + (-14 - e);
+    if (shift > 24) return sign; /* below half of the smallest subnormal */
+  }
+  uint32_t q = mant >> shift;
+  const uint32_t rem = mant & ((1u << shift) - 1u), half = 1u << (shift - 1);
+  if (rem > half || (rem == half && (q & 1u))) ++q;
+  if (exp_field == 0) return (uint16_t)(sign | q); /* may round up into the normal range: same bits */
+  /* q holds the implicit bit (0x400); a carry out of the significand (q =
+   * 0x800) moves into the exponent field by itself */
+  const uint32_t h = (exp_field << 10) + (q - 0x400u);
+  if (h >= 0x7C00u) return (uint16_t)(sign | 0x7C00u);
+  return (uint16_t)(sign | h);
+}
+
+static float f16f(uint16_t h) { return (float)orc_f16(h); }
+
+/* next representable binary16 above (dir > 0) or below (dir < 0) */
+static uint16_t f16_step(uint16_t h, int dir) {
+  if ((h & 0x7FFFu) == 0) return dir > 0 ? 0x0001u : 0x8001u;
+  const int neg = (h & 0x8000u) != 0;
+  return (uint16_t)((dir > 0) != neg ? h + 1u : h - 1u);
+}
+
+static int clampi(int v, int lo, int hi) { return v < lo ? lo : v > hi ? hi : v; }
+
+static int code_of(float x, float step, float off, int qmax) {
+  /* nearest code for x ~ step * q + off */
+  if (!(step > 0.0f)) return 0;
+  const float t = (x - off) / step;
+  return clampi((int)rintf(t), 0, qmax);
+}
+
+/* Q2_K: codes and weighted error of one sub-block for scale A = d*sc and
+ * offset B = dmin*mn (value = A q - B) */
+static float q2k_sub_err(const float *x, const float *w, float A, float B, uint8_t *q) {
+  float err = 0.0f;
+  for (int i = 0; i < 16; ++i) {
+    const int c = code_of(x[i], A, -B, 3);
+    if (q) q[i] = (uint8_t)c;
+    const float y = A * (float)c - B;
+    const float e = x[i] - y;
+    err = err + (w ? w[i] : 1.0f) * (e * e);
+  }
+  return err;
+}
+
+static void quantize_q2k_block(const float *x, const float *w, uint8_t *blk) {
+  float a[16], b[16];
+  float amax = 0.0f, bmax = 0.0f;
+  for (int s = 0; s < 16; ++s) {
+    float lo = x[16 * s], hi = x[16 * s];
+    for (int i = 1; i < 16; ++i) {
+      const float v = x[16 * s + i];
+      if (v < lo) lo = v;
+      if (v > hi) hi = v;
+    }
+    if (!(lo < 0.0f)) lo = 0.0f;
+    a[s] = (hi - lo) / 3.0f;
+    b[s] = 0.0f - lo;
+    if (a[s] > amax) amax = a[s];
+    if (b[s] > bmax) bmax = b[s];
+  }
+  const uint16_t dh = orc_f32_to_f16(amax / 15.0f), mh = orc_f32_to_f16(bmax / 15.0f);
+  const float d = f16f(dh), dmin = f16f(mh);
+  uint8_t codes[256], sc[16], mn[16];
+  for (int s = 0; s < 16; ++s) {
+    int scs = d > 0.0f ? clampi((int)rintf(a[s] / d), 0, 15) : 0;
+    int mns = dmin > 0.0f ? clampi((int)rintf(b[s] / dmin), 0, 15) : 0;
+    if (w) {
+      float best = q2k_sub_err(x + 16 * s, w + 16 * s, d * (float)scs, dmin * (float)mns, NULL);
+      int bsc = scs, bmn = mns;
+      for (int ds = -1; ds <= 1; ++ds)
+        for (int dm = -1; dm <= 1; ++dm) {
+          const int cs = scs + ds, cm = mns + dm;
+          if ((ds == 0 && dm == 0) || cs < 0 || cs > 15 || cm < 0 || cm > 15) continue;
+          const float e = q2k_sub_err(x + 16 * s, w + 16 * s, d * (float)cs, dmin * (float)cm, NULL);
+          if (e < best) {
+            best = e;
+            bsc = cs;
+            bmn = cm;
+          }
+        }
+      scs = bsc;
+      mns = bmn;
+    }
+    sc[s] = (uint8_t)scs;
+    mn[s] = (uint8_t)mns;
+    q2k_sub_err(x + 16 * s, NULL, d * (float)scs, dmin * (float)mns, codes + 16 * s);
+  }
+  memset(blk, 0, 84);
+  for (int s = 0; s < 16; ++s) blk[s] = (uint8_t)(sc[s] | (mn[s] << 4));
+  for (int i = 0; i < 256; ++i) blk[16 + q2k_qs_index(i)] |= (uint8_t)(codes[i] << q2k_qs_shift(i));
+  put16(blk + 80, dh);
+  put16(blk + 82, mh);
+}
+
+static float q41_err(const float *x, const float *w, float D, float M, uint8_t *q) {
+  float err = 0.0f;
+  for (int j = 0; j < 32; ++j) {
+    const int c = code_of(x[j], D, M, 15);
+    if (q) q[j] = (uint8_t)c;
+    const float y = D * (float)c + M;
+    const float e = x[j] - y;
+    err = err + (w ? w[j] : 1.0f) * (e * e);
+  }
+  return err;
+}
+
+static void quantize_q41_block(const float *x, const float *w, uint8_t *blk) {
+  float lo = x[0], hi = x[0];
+  for (int j = 1; j < 32; ++j) {
+    if (x[j] < lo) lo = x[j];
+    if (x[j] > hi) hi = x[j];
+  }
+  uint16_t dh = orc_f32_to_f16((hi - lo) / 15.0f), mh = orc_f32_to_f16(lo);
+  if (w) {
+    float best = q41_err(x, w, f16f(dh), f16f(mh), NULL);
+    const uint16_t d0 = dh, m0 = mh;
+    for (int dd = -1; dd <= 1; ++dd)
+      for (int dm = -1; dm <= 1; ++dm) {
+        if (dd == 0 && dm == 0) continue;
+        const uint16_t cd = dd ? f16_step(d0, dd) : d0, cm = dm ? f16_step(m0, dm) : m0;
+        const float D = f16f(cd), M = f16f(cm);
+        if (!(D >= 0.0f) || (cd & 0x7C00u) == 0x7C00u || (cm & 0x7C00u) == 0x7C00u) continue;
+        const float e = q41_err(x, w, D, M, NULL);
+        if (e < best) {
+          best = e;
+          dh = cd;
+          mh = cm;
+        }
+      }
+  }
+  uint8_t q[32];
+  q41_err(x, NULL, f16f(dh), f16f(mh), q);
+  put16(blk, dh);
+  put16(blk + 2, mh);
+  for (int j = 0; j < 16; ++j) blk[4 + j] = (uint8_t)(q[j] | (q[j + 16] << 4));
+}
+
+/* x: n_values floats, row-major rows of `cols` values (cols a multiple of
+ * the block size); importance: NULL or `cols` weights, one per column. */
+int orc_quantize_f32(int qtype, const float *x, const float *importance, int64_t n_values, int64_t cols,
+                     uint8_t *out) {
+  const int bv = orc_block_values(qtype), bb = orc_block_bytes(qtype);
+  if (!bv || n_values < 0 || n_values % bv || (importance && (cols <= 0 || cols % bv || n_values % cols)))
+    return ORC_EINVAL;
+  for (int64_t i = 0; i < n_values; ++i)
+    if (!isfinite(x[i])) return ORC_EINVAL;
+  const int64_t nb = n_values / bv;
+  for (int64_t b = 0; b < nb; ++b) {
+    const float *w = importance ? importance + (b * bv) % cols : NULL;
+    if (qtype == ORC_Q2_K) quantize_q2k_block(x + b * bv, w, out + b * bb);
+    else quantize_q41_block(x + b * bv, w, out + b * bb);
+  }
+  return ORC_OK;
+}
+
+/* sum over values of w_col * (x - dequant(x))^2, in double (test helper) */
+double orc_weighted_sq_error(int qtype, const float *x, const float *importance, int64_t n_values, int64_t cols,
+                             const uint8_t *blocks) {
+  float *y = (float *)malloc(sizeof(float) * (size_t)(n_values ? n_values : 1));
+  if (!y) return -1.0;
+  orc_dequant(qtype, blocks, n_values, y);
+  double s = 0.0;
+  for (int64_t i = 0; i < n_values; ++i) {
+    const double e = (double)x[i] - (double)y[i];
+    s += (importance ? (double)importance[i % cols] : 1.0) * e * e;
+  }
+  free(y);
+  return s;
+}
