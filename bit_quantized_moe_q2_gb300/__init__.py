@@ -27,6 +27,7 @@ EXPORTS = (
     "ds4moe_ffn_decode", "ds4moe_ffn_prefill", "ds4moe_stream_status",
     "ds4moe_profile_enable", "ds4moe_profile_count", "ds4moe_profile_entry",
     "ds4moe_ffn_decode_noalloc", "ds4moe_moe_decode", "ds4moe_residual_norm", "ds4moe_stack_decode",
+    "ds4moe_quantize_f32",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -63,6 +64,7 @@ def lib():
         L.ds4moe_status_string.restype = ctypes.c_char_p
         L.ds4moe_quantize_ref.argtypes = [i32, i32, i32, p, p, p, p, p, i64, p, sz]
         L.ds4moe_dequant.argtypes = [i32, p, i64, p, p]
+        L.ds4moe_quantize_f32.argtypes = [i32, p, p, i64, i64, p, ctypes.c_size_t, p, ctypes.c_size_t, p]
         L.ds4moe_workspace_bytes.argtypes = [ctypes.POINTER(Layer), i32, i32, i32]
         L.ds4moe_workspace_bytes.restype = sz
         L.ds4moe_workspace_init.argtypes = [p, sz, p]
@@ -145,6 +147,17 @@ def ds4moe_quantize_ref(out_type, bits, group, codes, scale_f16, min_f16, sub_sc
 
 def ds4moe_dequant(qtype, blocks, n_values, out, stream=None):
     _check(lib().ds4moe_dequant(qtype, _ptr(blocks), n_values, _ptr(out), _stream(stream)), "ds4moe_dequant")
+
+
+def ds4moe_quantize_f32(qtype, x, importance, out, ws, cols=None, stream=None):
+    """x: float32 device tensor (rows of `cols` values; the last dimension by
+    default), importance: None or `cols` float32 weights, out: uint8 device
+    tensor of the block bytes, ws: workspace (device status word)."""
+    n = x.numel()
+    c = int(cols if cols is not None else (x.shape[-1] if x.dim() else n))
+    _check(lib().ds4moe_quantize_f32(qtype, _ptr(x), _ptr(importance), n, c, _ptr(out),
+                                     out.numel() * out.element_size(), _ptr(ws), ws.numel() * ws.element_size(),
+                                     _stream(stream)), "ds4moe_quantize_f32")
 
 
 def ds4moe_workspace_bytes(layer: Layer, T: int, k: int, prefill: bool = False) -> int:

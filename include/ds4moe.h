@@ -121,6 +121,33 @@ ds4moe_status ds4moe_quantize_ref(int32_t out_type, int32_t bits, int32_t group,
                                   void *out_blocks, size_t out_bytes);
 
 /*
+ * ds4moe_quantize_f32 -- DEVICE, asynchronous on `stream`.  Quantizes
+ * n_values fp32 values `x` (device, rows of `cols` values) into Q2_K or Q4_1
+ * blocks `out` (device, out_bytes >= n_values / block_values * block_bytes).
+ * [DS4-2], section on the Q2_K block writer: a scale and a minimum per
+ * 16-value sub-block, values rounded to 2-bit codes; with an importance
+ * matrix the weighted writer scores the error by column importance.  The
+ * pages give no search; this one (fp32, fixed order, deterministic):
+ *   Q2_K  per sub-block lo = min(0, min x), hi = max x, a = (hi - lo) / 3,
+ *         b = -lo; d = f16(max a / 15), dmin = f16(max b / 15); sc = rint(a /
+ *         d), mn = rint(b / dmin) clamped to 0..15; nearest codes 0..3.
+ *   Q4_1  d = f16((max - min) / 15), m = f16(min); nearest codes 0..15.
+ *   importance (device, `cols` fp32 weights, one per column; NULL: none):
+ *         every sub-block tries (sc, mn) +-1 (Q4_1: d and m one binary16
+ *         step each way) and keeps the first candidate with the least
+ *         sum importance * (x - y)^2, the plain choice tried first.
+ * cols must be a multiple of the block size dividing n_values when
+ * importance is given.  Host errors: EUNSUPPORTED (other formats), EINVAL
+ * (sizes, NULL or unaligned pointers), ESPACE (out_bytes, or ws_bytes <
+ * 256).  Device-detected: a block holding a non-finite value is written as
+ * zeros and DS4MOE_EDEVICE is recorded in `ws` (read it with
+ * ds4moe_stream_status).  `ws`: a workspace from ds4moe_workspace_init.
+ */
+ds4moe_status ds4moe_quantize_f32(int32_t qtype, const float *x, const float *importance, int64_t n_values,
+                                  int64_t cols, void *out, size_t out_bytes, void *ws, size_t ws_bytes,
+                                  void *stream);
+
+/*
  * ds4moe_dequant -- DEVICE.  Decodes n_values values of `blocks` (device,
  * qtype layout above) into fp32 `out` (device).  The result is the single
  * fp32 rounding of the exact decoded value (d*q + m, or d*sc*q - dmin*mn),

@@ -495,10 +495,13 @@ static uint16_t f16_step(uint16_t h, int dir) {
 static int clampi(int v, int lo, int hi) { return v < lo ? lo : v > hi ? hi : v; }
 
 static int code_of(float x, float step, float off, int qmax) {
-  /* nearest code for x ~ step * q + off */
+  /* nearest code for x ~ step * q + off; the clamp is done on the float so
+   * that a huge quotient (tiny step) stays well defined */
   if (!(step > 0.0f)) return 0;
-  const float t = (x - off) / step;
-  return clampi((int)rintf(t), 0, qmax);
+  float r = rintf((x - off) / step);
+  if (r < 0.0f) r = 0.0f;
+  if (r > (float)qmax) r = (float)qmax;
+  return (int)r;
 }
 
 /* Q2_K: codes and weighted error of one sub-block for scale A = d*sc and
