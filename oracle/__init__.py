@@ -65,6 +65,7 @@ def _L():
         lib.orc_matvec_rows.argtypes = [i32, p, i32, i32, i32, i32, p, p]
         lib.orc_expert_ffn.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, p, p, p, p, p]
         lib.orc_moe_ffn.argtypes = [i32, i32, i32, i32, p, i32, p, i32, p, p, p, p, i32, i32, p]
+        lib.orc_topk_softmax_selbias.argtypes = [p, p, i32, i32, i32, p, p]
         lib.orc_f32_to_f16.restype = ctypes.c_uint16
         lib.orc_f32_to_f16.argtypes = [ctypes.c_float]
         lib.orc_quantize_f32.argtypes = [i32, p, p, i64, i64, p]
@@ -299,3 +300,17 @@ def weighted_sq_error(qtype: int, x, importance, cols: int, blocks) -> float:
     x = _c(x, np.float32).ravel()
     imp = None if importance is None else _c(importance, np.float32).ravel()
     return _L().orc_weighted_sq_error(qtype, _ptr(x), _ptr(imp), x.size, cols, _ptr(_c(blocks, np.uint8)))
+
+
+# ----------------------------------------------- routing: selection-only bias
+def route_select_bias(x_bf16, Wr, bias, k: int):
+    """Experts ranked by the biased logit, weights = softmax of the selected
+    experts' unbiased logits (bias used for selection only).  Returns
+    (idx, w, unbiased logits, biased logits)."""
+    lu = router_logits(x_bf16, Wr, None)
+    lb = router_logits(x_bf16, Wr, bias)
+    T, E = lu.shape
+    idx = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float32)
+    _L().orc_topk_softmax_selbias(_ptr(_c(lb, np.float32)), _ptr(_c(lu, np.float32)), T, E, k, _ptr(idx), _ptr(w))
+    return idx, w, lu, lb

@@ -643,3 +643,40 @@ double orc_weighted_sq_error(int qtype, const float *x, const float *importance,
   free(y);
   return s;
 }
+
+/* Routing variant with the bias used for selection only (SURVEY next-row
+ * reading, DeepSeek-style): experts are ranked by the biased logit
+ * lb = fp32(x . Wr_e + bias_e) (ties to the lower id, NaN lowest), and the
+ * weights are the softmax of the selected experts' unbiased logits
+ * lu = fp32(x . Wr_e), shifted by their maximum, summed in rank order in
+ * double and rounded once. */
+void orc_topk_softmax_selbias(const float *lb, const float *lu, int T, int E, int k, int32_t *idx, float *w) {
+  char *taken = (char *)malloc((size_t)E);
+  double *ex = (double *)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+  for (int t = 0; t < T; ++t) {
+    const float *l = lb + (int64_t)t * E, *u = lu + (int64_t)t * E;
+    memset(taken, 0, (size_t)E);
+    for (int i = 0; i < k; ++i) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || ranks_before(l[e], e, l[best], best)) best = e;
+      }
+      taken[best] = 1;
+      idx[(int64_t)t * k + i] = best;
+    }
+    double m = -INFINITY;
+    for (int i = 0; i < k; ++i) {
+      const double v = (double)u[idx[(int64_t)t * k + i]];
+      if (v > m) m = v;
+    }
+    double s = 0.0;
+    for (int i = 0; i < k; ++i) {
+      ex[i] = exp((double)u[idx[(int64_t)t * k + i]] - m);
+      s += ex[i];
+    }
+    for (int i = 0; i < k; ++i) w[(int64_t)t * k + i] = (float)(ex[i] / s);
+  }
+  free(taken);
+  free(ex);
+}
