@@ -27,7 +27,7 @@ EXPORTS = (
     "ds4moe_ffn_decode", "ds4moe_ffn_prefill", "ds4moe_stream_status",
     "ds4moe_profile_enable", "ds4moe_profile_count", "ds4moe_profile_entry",
     "ds4moe_ffn_decode_noalloc", "ds4moe_moe_decode", "ds4moe_residual_norm", "ds4moe_stack_decode",
-    "ds4moe_quantize_f32",
+    "ds4moe_quantize_f32", "ds4moe_route_topk_select_bias",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -69,6 +69,7 @@ def lib():
         L.ds4moe_workspace_bytes.restype = sz
         L.ds4moe_workspace_init.argtypes = [p, sz, p]
         L.ds4moe_route_topk.argtypes = [p, p, p, i32, i32, i32, i32, p, p, p, p, sz, p]
+        L.ds4moe_route_topk_select_bias.argtypes = [p, p, p, i32, i32, i32, i32, p, p, p, p, sz, p]
         L.ds4moe_ffn_decode.argtypes = [ctypes.POINTER(Layer), p, p, p, i32, i32, p, p, sz, p]
         L.ds4moe_ffn_prefill.argtypes = [ctypes.POINTER(Layer), p, p, p, i32, i32, p, p, sz, p]
         L.ds4moe_stream_status.argtypes = [p, p]
@@ -167,6 +168,14 @@ def ds4moe_workspace_bytes(layer: Layer, T: int, k: int, prefill: bool = False) 
 def ds4moe_workspace_init(ws, stream=None):
     _check(lib().ds4moe_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "ds4moe_workspace_init")
+
+
+def ds4moe_route_topk_select_bias(x, Wr, bias, k, idx, w, logits, ws, stream=None):
+    T, D = x.shape
+    E = Wr.shape[0]
+    _check(lib().ds4moe_route_topk_select_bias(_ptr(x), _ptr(Wr), _ptr(bias), T, D, E, k, _ptr(idx), _ptr(w),
+                                               _ptr(logits), _ptr(ws), ws.numel() * ws.element_size(),
+                                               _stream(stream)), "ds4moe_route_topk_select_bias")
 
 
 def ds4moe_route_topk(x, Wr, bias, k, idx, w, logits, ws, stream=None):

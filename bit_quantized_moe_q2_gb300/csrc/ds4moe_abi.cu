@@ -206,6 +206,82 @@ __global__ void k_topk_softmax(const float *__restrict__ logits, int T, int E, i
     topk_softmax_row(logits, list ? list[gw] : gw, E, k, idx, w);
 }
 
+// ------------------------------------ routing with a selection-only bias
+// Both logits of (t, e) from one Dot2 pass: the unbiased one rounded from
+// the compensated (sum, error) pair, the biased one after adding the bias
+// with TwoSum -- each equal to what the plain router computes for it.
+__global__ void k_router_logits_both(const uint16_t *__restrict__ x, const float *__restrict__ Wr,
+                                     const float *__restrict__ bias, int T, int D, int E, float *__restrict__ lb,
+                                     float *__restrict__ lu) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n = (int64_t)T * E;
+  for (int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; gw < n;
+       gw += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int t = (int)(gw / E), e = (int)(gw % E);
+    const uint16_t *xr = x + (int64_t)t * D;
+    const float *wr = Wr + (int64_t)e * D;
+    float s = 0.f, c = 0.f;
+    for (int j = 4 * lane; j < D; j += 128) {
+      const float4 wv = *reinterpret_cast<const float4 *>(wr + j);
+      const uint2 xv = *reinterpret_cast<const uint2 *>(xr + j);
+      const float xs[4] = {bf16_bits_to_f32(xv.x & 0xFFFFu), bf16_bits_to_f32(xv.x >> 16),
+                           bf16_bits_to_f32(xv.y & 0xFFFFu), bf16_bits_to_f32(xv.y >> 16)};
+      const float w4[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float p, pe, se;
+        two_prod(xs[q], w4[q], p, pe);
+        two_sum(s, p, s, se);
+        c = __fadd_rn(c, __fadd_rn(pe, se));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      const float so = __shfl_xor_sync(0xffffffffu, s, off);
+      const float co = __shfl_xor_sync(0xffffffffu, c, off);
+      float se;
+      two_sum(s, so, s, se);
+      c = __fadd_rn(c, __fadd_rn(co, se));
+    }
+    const float vu = __fadd_rn(s, c);
+    float sb, se;
+    two_sum(s, bias[e], sb, se);
+    const float vb = __fadd_rn(sb, __fadd_rn(c, se));
+    if (lane == 0) {
+      lu[(int64_t)t * E + e] = vu;
+      lb[(int64_t)t * E + e] = vb;
+    }
+  }
+}
+
+// One warp per token (E <= 256): rank by the biased logits; weights are the
+// softmax of the selected experts' unbiased logits shifted by their maximum,
+// in double, summed in rank order, rounded once.
+__global__ void k_topk_selbias(const float *__restrict__ lb, const float *__restrict__ lu, int T, int E, int k,
+                               int32_t *__restrict__ idx, float *__restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  for (int t = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5); t < T;
+       t += (int)(((int64_t)gridDim.x * blockDim.x) >> 5)) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = lane + 32 * j < E ? lb[(int64_t)t * E + lane + 32 * j] : 0.f;
+    float my_v;
+    int my_e;
+    topk_select_warp(v, E, k, my_v, my_e);
+    const double u = lane < k ? (double)lu[(int64_t)t * E + my_e] : -INFINITY;
+    double m = u;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) m = fmax(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const double ex = lane < k ? exp(u - m) : 0.0;
+    double sum = 0.0;
+    for (int i = 0; i < k; ++i) sum += __shfl_sync(0xffffffffu, ex, i);
+    if (lane < k) {
+      idx[(int64_t)t * k + lane] = my_e;
+      w[(int64_t)t * k + lane] = (float)(ex / sum);
+    }
+  }
+}
+
 // ------------------------------------------------- certified router (large T)
 // Approximate logits (no bias) for the certified fast path: a tiled fp32
 // GEMM, 64 tokens x 64 experts per CTA and 4 x 4 outputs per thread.  Each
@@ -1060,6 +1136,45 @@ ds4moe_status ds4moe_route_topk(const uint16_t *x, const float *Wr, const float 
   {
     ProfScope prof("topk_softmax", s);
     k_topk_softmax<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(lg, T, n_expert, k, idx, w);
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+ds4moe_status ds4moe_route_topk_select_bias(const uint16_t *x, const float *Wr, const float *bias, int32_t T,
+                                            int32_t d_model, int32_t n_expert, int32_t k, int32_t *idx, float *w,
+                                            float *logits, void *ws, size_t ws_bytes, void *stream) {
+  if (T < 0 || d_model <= 0 || d_model % 4 || n_expert < 1 || n_expert > 256 || k < 1 || k > 32 ||
+      k > n_expert)
+    return DS4MOE_EINVAL;
+  if (T == 0) return DS4MOE_OK;
+  if (!x || !Wr || !bias || !idx || !w || !ws) return DS4MOE_EINVAL;
+  if (!aligned16(x) || !aligned16(Wr) || !aligned16(bias) || !aligned16(idx) || !aligned16(w) || !aligned16(ws) ||
+      (logits && !aligned16(logits)))
+    return DS4MOE_EINVAL;
+  if ((int64_t)d_model * 2 % 16) return DS4MOE_EINVAL;
+  ds4moe_layer shape{};
+  shape.d_model = d_model;
+  shape.d_ff = 16;
+  shape.n_expert = n_expert;
+  const WsLayout lay = ws_layout(shape, T, k, 0);
+  const size_t plane = align256(sizeof(float) * (size_t)T * n_expert);
+  if (ws_bytes < lay.logits + (logits ? 1 : 2) * plane) return DS4MOE_ESPACE;
+  float *lb = ws_ptr<float>(ws, lay.logits);
+  float *lu = logits ? logits : ws_ptr<float>(ws, lay.logits + plane);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t warps = (int64_t)T * n_expert;
+  {
+    ProfScope prof("router_logits_both", s);
+    const int64_t blocks = (warps + 7) / 8;
+    k_router_logits_both<<<(unsigned)(blocks < num_sms() * 64 ? blocks : num_sms() * 64), 256, 0, s>>>(
+        x, Wr, bias, T, d_model, n_expert, lb, lu);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_status(e);
+  {
+    ProfScope prof("topk_selbias", s);
+    const int blocks = (T + 7) / 8;
+    k_topk_selbias<<<blocks < num_sms() * 8 ? blocks : num_sms() * 8, 256, 0, s>>>(lb, lu, T, n_expert, k, idx, w);
   }
   return cuda_status(cudaGetLastError());
 }

@@ -194,6 +194,22 @@ ds4moe_status ds4moe_route_topk(const uint16_t *x, const float *Wr, const float 
                                 size_t ws_bytes, void *stream);
 
 /*
+ * ds4moe_route_topk_select_bias -- DEVICE.  Routing variant with the bias
+ * used for selection only (DeepSeek-style): the k experts with the largest
+ * biased logits fp32(x . Wr_e + bias_e) are selected (descending, ties to the
+ * lower id, NaN lowest) and w is the softmax of their UNBIASED logits
+ * fp32(x . Wr_e), shifted by the largest of them, in double, summed in rank
+ * order, rounded once.  Both logits come from one compensated (Dot2) pass
+ * and each equals the plain router's value for it.  Same arguments as
+ * ds4moe_route_topk, except: bias is required; n_expert <= 256; `logits`
+ * (nullable) receives the unbiased logits.  ws must hold the layout's
+ * logits region plus one (with `logits`) or two T x n_expert fp32 planes.
+ */
+ds4moe_status ds4moe_route_topk_select_bias(const uint16_t *x, const float *Wr, const float *bias, int32_t T,
+                                            int32_t d_model, int32_t n_expert, int32_t k, int32_t *idx, float *w,
+                                            float *logits, void *ws, size_t ws_bytes, void *stream);
+
+/*
  * ds4moe_ffn_decode -- DEVICE.  Routed expert FFN + combine for a decode
  * batch (small T):
  *   for each (t, i): e = idx[t,i];
