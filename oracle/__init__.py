@@ -18,8 +18,8 @@ _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
 OK, EINVAL, EBLOCKER, EUNSUPPORTED = 0, 1, 2, 3
-Q4_1, Q2_K = 1, 2
-QTYPES = {"q4_1": Q4_1, "q2_k": Q2_K}
+Q4_1, Q2_K, Q4_K = 1, 2, 4
+QTYPES = {"q4_1": Q4_1, "q2_k": Q2_K, "q4_k": Q4_K}
 
 
 def build(force: bool = False) -> str:
@@ -66,6 +66,9 @@ def _L():
         lib.orc_expert_ffn.argtypes = [i32, i32, i32, p, i32, p, i32, p, i32, p, p, p, p, p]
         lib.orc_moe_ffn.argtypes = [i32, i32, i32, i32, p, i32, p, i32, p, p, p, p, i32, i32, p]
         lib.orc_topk_softmax_selbias.argtypes = [p, p, i32, i32, i32, p, p]
+        lib.orc_q4k_pack.argtypes = [p, p, p, p, p, i64, p]
+        lib.orc_q4k_unpack.argtypes = [p, i64, p, p, p, p, p]
+        lib.orc_q4k_dequant.argtypes = [p, i64, p]
         lib.orc_f32_to_f16.restype = ctypes.c_uint16
         lib.orc_f32_to_f16.argtypes = [ctypes.c_float]
         lib.orc_quantize_f32.argtypes = [i32, p, p, i64, i64, p]
@@ -314,3 +317,29 @@ def route_select_bias(x_bf16, Wr, bias, k: int):
     w = np.empty((T, k), np.float32)
     _L().orc_topk_softmax_selbias(_ptr(_c(lb, np.float32)), _ptr(_c(lu, np.float32)), T, E, k, _ptr(idx), _ptr(w))
     return idx, w, lu, lb
+
+
+# ------------------------------------------------------------------- Q4_K
+def q4k_pack(codes, sc, mn, d, dmin) -> np.ndarray:
+    """codes: 256 per block (0..15); sc, mn: 8 per block (0..63); d, dmin:
+    binary16 bit patterns per block."""
+    codes, sc, mn = _c(codes, np.uint8), _c(sc, np.uint8), _c(mn, np.uint8)
+    d, dmin = _c(d, np.uint16), _c(dmin, np.uint16)
+    nb = codes.size // 256
+    out = np.zeros(nb * 144, dtype=np.uint8)
+    st = _L().orc_q4k_pack(_ptr(codes), _ptr(sc), _ptr(mn), _ptr(d), _ptr(dmin), nb, _ptr(out))
+    if st:
+        raise OracleError(st, "q4k_pack")
+    return out
+
+
+def q4k_unpack(blocks):
+    blocks = _c(blocks, np.uint8)
+    nb = blocks.size // 144
+    codes = np.empty(nb * 256, np.uint8)
+    sc = np.empty(nb * 8, np.uint8)
+    mn = np.empty(nb * 8, np.uint8)
+    d = np.empty(nb, np.uint16)
+    dmin = np.empty(nb, np.uint16)
+    _L().orc_q4k_unpack(_ptr(blocks), nb, _ptr(codes), _ptr(sc), _ptr(mn), _ptr(d), _ptr(dmin))
+    return codes, sc, mn, d, dmin

@@ -45,14 +45,18 @@
 #include <string.h>
 
 enum { ORC_OK = 0, ORC_EINVAL = 1, ORC_EBLOCKER = 2, ORC_EUNSUPPORTED = 3 };
-enum { ORC_Q4_1 = 1, ORC_Q2_K = 2 };
+enum { ORC_Q4_1 = 1, ORC_Q2_K = 2, ORC_Q4_K = 4 };
 
 /* ---------------------------------------------------------------- formats */
 
 /* [DS4-2] type-trait table: Q2_K holds 256 values in 84 bytes.
  * [Q41] "Q4_1 블록이 어떻게 생겼나": Q4_1 holds 32 values in 20 bytes. */
-int orc_block_values(int qtype) { return qtype == ORC_Q4_1 ? 32 : qtype == ORC_Q2_K ? 256 : 0; }
-int orc_block_bytes(int qtype) { return qtype == ORC_Q4_1 ? 20 : qtype == ORC_Q2_K ? 84 : 0; }
+int orc_block_values(int qtype) {
+  return qtype == ORC_Q4_1 ? 32 : qtype == ORC_Q2_K ? 256 : qtype == ORC_Q4_K ? 256 : 0;
+}
+int orc_block_bytes(int qtype) {
+  return qtype == ORC_Q4_1 ? 20 : qtype == ORC_Q2_K ? 84 : qtype == ORC_Q4_K ? 144 : 0;
+}
 
 /* IEEE binary16 -> double, exact (normals, subnormals, inf, NaN). */
 double orc_f16(uint16_t h) {
@@ -249,12 +253,94 @@ void orc_q2k_dequant(const uint8_t *blocks, int64_t nb, float *out) {
     for (int i = 0; i < 256; ++i) out[256 * b + i] = q2k_value(blocks + 84 * b, i);
 }
 
+/* ------------------------------------------------------------------ Q4_K
+ * [DS4-2] type-trait table: Q4_K holds 256 values in 144 bytes; the pages
+ * give no layout.  Reading (the standard k-quant order, as for Q2_K): fp16 d
+ * @0, fp16 dmin @2, scales[12] @4 packing eight 6-bit (scale, min) pairs,
+ * qs[128] @16 holding 4-bit codes.  Sub-block j (values 32j .. 32j+31):
+ * for j < 4 sc = scales[j] & 63, mn = scales[j + 4] & 63; for j >= 4
+ * sc = (scales[j + 4] & 15) | (scales[j - 4] >> 6) << 4,
+ * mn = (scales[j + 4] >> 4) | (scales[j] >> 6) << 4.  Value 64 c + l
+ * (l < 32) is the low nibble of qs[32 c + l], value 64 c + 32 + l its high
+ * nibble.  y = d * sc * q - dmin * mn (one rounding: d * sc * q has at most
+ * 21 significant bits, dmin * mn at most 17). */
+static void q4k_scale_min(const uint8_t *sc12, int j, int *sc, int *mn) {
+  if (j < 4) {
+    *sc = sc12[j] & 63;
+    *mn = sc12[j + 4] & 63;
+  } else {
+    *sc = (sc12[j + 4] & 15) | ((sc12[j - 4] >> 6) << 4);
+    *mn = (sc12[j + 4] >> 4) | ((sc12[j] >> 6) << 4);
+  }
+}
+static int q4k_qs_index(int i) { return 32 * (i / 64) + (i % 32); }
+static int q4k_qs_shift(int i) { return 4 * ((i % 64) / 32); }
+
+int orc_q4k_pack(const uint8_t *codes, const uint8_t *sc, const uint8_t *mn, const uint16_t *d,
+                 const uint16_t *dmin, int64_t nb, uint8_t *out) {
+  for (int64_t b = 0; b < nb; ++b) {
+    uint8_t *blk = out + b * 144;
+    memset(blk, 0, 144);
+    put16(blk, d[b]);
+    put16(blk + 2, dmin[b]);
+    uint8_t *s12 = blk + 4;
+    for (int j = 0; j < 8; ++j) {
+      const int S = sc[b * 8 + j], Mn = mn[b * 8 + j];
+      if (S > 63 || Mn > 63) return ORC_EBLOCKER;
+      if (j < 4) {
+        s12[j] |= (uint8_t)(S & 63);
+        s12[j + 4] |= (uint8_t)(Mn & 63);
+      } else {
+        s12[j + 4] |= (uint8_t)((S & 15) | ((Mn & 15) << 4));
+        s12[j - 4] |= (uint8_t)((S >> 4) << 6);
+        s12[j] |= (uint8_t)((Mn >> 4) << 6);
+      }
+    }
+    for (int i = 0; i < 256; ++i) {
+      const int q = codes[b * 256 + i];
+      if (q > 15) return ORC_EBLOCKER;
+      blk[16 + q4k_qs_index(i)] |= (uint8_t)(q << q4k_qs_shift(i));
+    }
+  }
+  return ORC_OK;
+}
+
+void orc_q4k_unpack(const uint8_t *blocks, int64_t nb, uint8_t *codes, uint8_t *sc, uint8_t *mn, uint16_t *d,
+                    uint16_t *dmin) {
+  for (int64_t b = 0; b < nb; ++b) {
+    const uint8_t *blk = blocks + b * 144;
+    d[b] = get16(blk);
+    dmin[b] = get16(blk + 2);
+    for (int j = 0; j < 8; ++j) {
+      int S, Mn;
+      q4k_scale_min(blk + 4, j, &S, &Mn);
+      sc[b * 8 + j] = (uint8_t)S;
+      mn[b * 8 + j] = (uint8_t)Mn;
+    }
+    for (int i = 0; i < 256; ++i) codes[b * 256 + i] = (uint8_t)((blk[16 + q4k_qs_index(i)] >> q4k_qs_shift(i)) & 15);
+  }
+}
+
+static float q4k_value(const uint8_t *blk, int i) {
+  int S, Mn;
+  q4k_scale_min(blk + 4, i / 32, &S, &Mn);
+  const int q = (blk[16 + q4k_qs_index(i)] >> q4k_qs_shift(i)) & 15;
+  /* exact products in double, one rounding to fp32 */
+  return (float)(orc_f16(get16(blk)) * S * q - orc_f16(get16(blk + 2)) * Mn);
+}
+
+void orc_q4k_dequant(const uint8_t *blocks, int64_t nb, float *out) {
+  for (int64_t b = 0; b < nb; ++b)
+    for (int i = 0; i < 256; ++i) out[b * 256 + i] = q4k_value(blocks + b * 144, i);
+}
+
 int orc_dequant(int qtype, const uint8_t *blocks, int64_t n_values, float *out) {
   int bv = orc_block_values(qtype);
   if (!bv) return ORC_EUNSUPPORTED;
   if (n_values % bv) return ORC_EINVAL;
   if (qtype == ORC_Q4_1) orc_q41_dequant(blocks, n_values / 32, out);
-  else orc_q2k_dequant(blocks, n_values / 256, out);
+  else if (qtype == ORC_Q2_K) orc_q2k_dequant(blocks, n_values / 256, out);
+  else orc_q4k_dequant(blocks, n_values / 256, out);
   return ORC_OK;
 }
 
