@@ -17,8 +17,8 @@ LIB_PATH = os.path.join(_HERE, "libds4moe.so")
 
 DS4MOE_OK, DS4MOE_EINVAL, DS4MOE_EBLOCKER, DS4MOE_EUNSUPPORTED = 0, 1, 2, 3
 DS4MOE_ECUDA, DS4MOE_ETIMEOUT, DS4MOE_EDEVICE, DS4MOE_ESPACE = 4, 5, 6, 7
-DS4MOE_Q4_1, DS4MOE_Q2_K, DS4MOE_IQ2_XXS = 1, 2, 3
-QTYPES = {"q4_1": DS4MOE_Q4_1, "q2_k": DS4MOE_Q2_K, "iq2_xxs": DS4MOE_IQ2_XXS}
+DS4MOE_Q4_1, DS4MOE_Q2_K, DS4MOE_IQ2_XXS, DS4MOE_Q4_K = 1, 2, 3, 4
+QTYPES = {"q4_1": DS4MOE_Q4_1, "q2_k": DS4MOE_Q2_K, "iq2_xxs": DS4MOE_IQ2_XXS, "q4_k": DS4MOE_Q4_K}
 
 # Every symbol include/ds4moe.h declares.
 EXPORTS = (

@@ -28,7 +28,7 @@ namespace {
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-inline bool qtype_ok(int q) { return q == DS4MOE_Q4_1 || q == DS4MOE_Q2_K; }
+inline bool qtype_ok(int q) { return q == DS4MOE_Q4_1 || q == DS4MOE_Q2_K || q == DS4MOE_Q4_K; }
 
 ds4moe_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return DS4MOE_OK;
@@ -71,6 +71,29 @@ __global__ void k_dequant_q2k(const uint8_t *__restrict__ blk, int64_t nb, float
       const int v = 128 * h + l + 32 * s;
       const uint32_t scb = p[v >> 4];
       out[b * 256 + v] = fmaf(d * (float)(scb & 15u), (float)((q >> (2 * s)) & 3u), -(dmin * (float)(scb >> 4)));
+    }
+  }
+}
+
+// Q4_K (standard k-quant reading of the 144-byte block): one thread per
+// (block, qs byte); qs byte 32c + l carries value 64c + l (low nibble, sub-
+// block 2c) and 64c + 32 + l (high nibble, sub-block 2c + 1).  d*sc and
+// dmin*mn are exact, so fmaf(d*sc, q, -dmin*mn) is the single rounding.
+__global__ void k_dequant_q4k(const uint8_t *__restrict__ blk, int64_t nb, float *__restrict__ out) {
+  const int64_t n = nb * 128;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t b = i >> 7;
+    const int byte = (int)(i & 127), c = byte >> 5, l = byte & 31;
+    const uint8_t *p = blk + b * kQ4KBytes;
+    const float d = f16_bits_to_f32(p[0] | (p[1] << 8));
+    const float dmin = f16_bits_to_f32(p[2] | (p[3] << 8));
+    const uint32_t q = p[16 + byte];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t sc, mn;
+      q4k_scale_min(p + 4, 2 * c + hh, sc, mn);
+      out[b * 256 + 64 * c + 32 * hh + l] =
+          fmaf(d * (float)sc, (float)((q >> (4 * hh)) & 15u), -(dmin * (float)mn));
     }
   }
 }
@@ -1034,15 +1057,17 @@ ds4moe_status ds4moe_dequant(int32_t qtype, const void *blocks, int64_t n_values
   if (!blocks || !out || !aligned16(blocks) || !aligned16(out)) return DS4MOE_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t nb = n_values / block_vals(qtype);
-  const int64_t work = qtype == DS4MOE_Q4_1 ? nb * 16 : nb * 64;
+  const int64_t work = qtype == DS4MOE_Q4_1 ? nb * 16 : qtype == DS4MOE_Q2_K ? nb * 64 : nb * 128;
   const int threads = 256;
   const int64_t want = (work + threads - 1) / threads;
   const int grid = (int)(want < (int64_t)num_sms() * 32 ? want : (int64_t)num_sms() * 32);
   ProfScope prof("dequant", s);
   if (qtype == DS4MOE_Q4_1)
     k_dequant_q41<<<grid, threads, 0, s>>>(static_cast<const uint8_t *>(blocks), nb, out);
-  else
+  else if (qtype == DS4MOE_Q2_K)
     k_dequant_q2k<<<grid, threads, 0, s>>>(static_cast<const uint8_t *>(blocks), nb, out);
+  else
+    k_dequant_q4k<<<grid, threads, 0, s>>>(static_cast<const uint8_t *>(blocks), nb, out);
   return cuda_status(cudaGetLastError());
 }
 

@@ -756,10 +756,37 @@ __device__ __forceinline__ void row_dot_q2k(const uint8_t *__restrict__ row, int
   }
 }
 
+// Q4_K row: lane items are (block, qs byte); byte 32c + l holds values
+// 64c + l (low nibble) and 64c + 32 + l (high nibble).
+template <typename In>
+__device__ __forceinline__ void row_dot_q4k(const uint8_t *__restrict__ row, int cols, int nt, In in,
+                                            float (&acc)[kTok]) {
+  const int lane = threadIdx.x & 31;
+  const int nitems = cols / 256 * 128;
+  for (int it = lane; it < nitems; it += 32) {
+    const int b = it >> 7, by = it & 127, c = by >> 5, l = by & 31;
+    const uint8_t *p = row + (int64_t)b * kQ4KBytes;
+    const float d = f16_bits_to_f32(p[0] | (p[1] << 8));
+    const float dmin = f16_bits_to_f32(p[2] | (p[3] << 8));
+    const uint32_t q = p[16 + by];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t sc, mn;
+      q4k_scale_min(p + 4, 2 * c + hh, sc, mn);
+      const int v = 64 * c + 32 * hh + l;
+      const float wv = fmaf(d * (float)sc, (float)((q >> (4 * hh)) & 15u), -(dmin * (float)mn));
+#pragma unroll
+      for (int t = 0; t < kTok; ++t)
+        if (t < nt) acc[t] = fmaf(wv, in(t, 256 * b + v), acc[t]);
+    }
+  }
+}
+
 template <typename In>
 __device__ __forceinline__ void row_dot(int q, const uint8_t *row, int cols, int nt, In in, float (&acc)[kTok]) {
   if (q == DS4MOE_Q4_1) row_dot_q41(row, cols, nt, in, acc);
-  else row_dot_q2k(row, cols, nt, in, acc);
+  else if (q == DS4MOE_Q2_K) row_dot_q2k(row, cols, nt, in, acc);
+  else row_dot_q4k(row, cols, nt, in, acc);
 }
 
 // gate/up + SwiGLU, SIMT: one warp per (token group, hidden row).
@@ -945,6 +972,9 @@ cudaError_t launch_down_mma(const FfnArgs &a, cudaStream_t s) {
 // The tensor-core kernels need rows that split into 16-byte-multiple bulk
 // copies and stages that fit in shared memory; other shapes use SIMT.
 bool decode_mma_ok(const ds4moe_layer &L) {
+  // tensor-core decode kernels: Q4_1 / Q2_K gate and up, Q2_K down
+  const auto mma_fmt = [](int q) { return q == DS4MOE_Q4_1 || q == DS4MOE_Q2_K; };
+  if (!mma_fmt(L.q_gate) || !mma_fmt(L.q_up)) return false;
   if (L.d_model % 16) return false;
   const int kp = pick_kp(L.d_model, L.q_gate, L.q_up);
   if (kp == 0) return false;

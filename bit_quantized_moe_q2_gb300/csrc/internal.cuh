@@ -15,12 +15,24 @@ namespace ds4 {
 // ------------------------------------------------------------ formats
 constexpr int kQ41Vals = 32, kQ41Bytes = 20;
 constexpr int kQ2KVals = 256, kQ2KBytes = 84;
+constexpr int kQ4KVals = 256, kQ4KBytes = 144;
 
 __host__ __device__ inline int block_vals(int q) {
-  return q == DS4MOE_Q4_1 ? kQ41Vals : q == DS4MOE_Q2_K ? kQ2KVals : 0;
+  return q == DS4MOE_Q4_1 ? kQ41Vals : q == DS4MOE_Q2_K ? kQ2KVals : q == DS4MOE_Q4_K ? kQ4KVals : 0;
 }
 __host__ __device__ inline int block_bytes(int q) {
-  return q == DS4MOE_Q4_1 ? kQ41Bytes : q == DS4MOE_Q2_K ? kQ2KBytes : 0;
+  return q == DS4MOE_Q4_1 ? kQ41Bytes : q == DS4MOE_Q2_K ? kQ2KBytes : q == DS4MOE_Q4_K ? kQ4KBytes : 0;
+}
+
+// Q4_K sub-block j's 6-bit scale and min from the 12 packed bytes.
+__device__ __forceinline__ void q4k_scale_min(const uint8_t *s12, int j, uint32_t &sc, uint32_t &mn) {
+  if (j < 4) {
+    sc = s12[j] & 63u;
+    mn = s12[j + 4] & 63u;
+  } else {
+    sc = (s12[j + 4] & 15u) | ((uint32_t)(s12[j - 4] >> 6) << 4);
+    mn = (uint32_t)(s12[j + 4] >> 4) | ((uint32_t)(s12[j] >> 6) << 4);
+  }
 }
 __host__ __device__ inline int64_t row_bytes(int q, int cols) {
   return (int64_t)(cols / block_vals(q)) * block_bytes(q);

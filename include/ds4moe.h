@@ -69,8 +69,17 @@ typedef enum {
                         16 values), qs[64] @16, fp16 d @80, fp16 dmin @82;
                         value i: code (qs[32*(i/128) + i%32] >> 2*((i%128)/32)) & 3,
                         y = d*sc*q - dmin*mn  ([DS4-2] layout table and packing) */
-  DS4MOE_IQ2_XXS = 3 /* named by [DS4-2]; its grid codebook is not given there:
+  DS4MOE_IQ2_XXS = 3, /* named by [DS4-2]; its grid codebook is not given there:
                         every entry point returns DS4MOE_EUNSUPPORTED */
+  DS4MOE_Q4_K = 4    /* 256 values in 144 bytes ([DS4-2] type table; the layout
+                        is the standard k-quant reading): fp16 d @0, fp16 dmin
+                        @2, scales[12] @4, qs[128] @16.  Sub-block j = values
+                        32j..32j+31: j < 4: sc = s[j] & 63, mn = s[j+4] & 63;
+                        j >= 4: sc = (s[j+4] & 15) | (s[j-4] >> 6) << 4,
+                        mn = (s[j+4] >> 4) | (s[j] >> 6) << 4.  Value 64c+l
+                        (l < 32): low nibble of qs[32c+l]; 64c+32+l: its high
+                        nibble.  y = d*sc*q - dmin*mn.  Dequant and the FFN
+                        entry points (SIMT kernels) take it. */
 } ds4moe_qtype;
 
 /* One routed-MoE layer's expert weights (device pointers, 16-byte aligned). */

@@ -198,12 +198,15 @@ def dequant(qtype: int, blocks, n_values: int) -> np.ndarray:
 
 def pack_fields(f) -> np.ndarray:
     """Block bytes of a ``synth.Fields`` matrix (Q4_1 via the lossless
-    re-encode with the fields' explicit bits/group; Q2_K via the packer)."""
+    re-encode with the fields' explicit bits/group; Q2_K / Q4_K via the
+    packers)."""
     if f.qtype == "q4_1":
         st, out = q41_reencode(f.bits, f.group, f.codes, f.scale, f.minv)
         if st:
             raise OracleError(st, "q41_reencode")
         return out
+    if f.qtype == "q4_k":
+        return q4k_pack(f.codes, f.sc, f.mn, f.scale, f.minv)
     return q2k_pack(f.codes, f.sc, f.mn, f.scale, f.minv)
 
 

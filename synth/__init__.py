@@ -116,7 +116,7 @@ def f16_scale_pow2(h: np.ndarray, mult: float) -> np.ndarray:
 # Workload recipes
 # --------------------------------------------------------------------------
 
-Q4_1, Q2_K = "q4_1", "q2_k"
+Q4_1, Q2_K, Q4_K = "q4_1", "q2_k", "q4_k"
 
 
 @dataclass(frozen=True)
@@ -140,6 +140,7 @@ class MatrixRecipe:
 Q41_4BIT = MatrixRecipe(Q4_1, 4, 32, 0.01, -8.0)   # codes U[0,15], m = -8 d
 Q41_3BIT = MatrixRecipe(Q4_1, 3, 32, 0.01, -4.0)   # codes U[0,7], min = -4 scale
 Q2K = MatrixRecipe(Q2_K, 2, 256, 0.002)             # codes U[0,3], sc/mn U[0,15]
+Q4K = MatrixRecipe(Q4_K, 4, 256, 0.0002)            # codes U[0,15], sc/mn U[0,63] per 32 values
 
 
 @dataclass(frozen=True)
@@ -172,6 +173,8 @@ WORKLOADS = {
     3: Workload("flash-layer-prefill-t4096-q41-q2k", 4096, 2048, 256, 6, 4096, 3, Q41_4BIT, Q41_4BIT, Q2K,
                 bias_sigma=1.0, path="prefill"),
     4: Workload("flash-stack43-decode-q2k", 4096, 2048, 256, 6, 1, 4, Q2K, Q2K, Q2K, n_layers=43),
+    # the mixed recipe's Q4_K routed experts (its last six layers)
+    5: Workload("flash-layer-decode-t1-q4k", 4096, 2048, 256, 6, 1, 5, Q4K, Q4K, Q4K),
 }
 
 
@@ -198,8 +201,8 @@ class Fields:
     group: int
     scale: np.ndarray                 # uint16 fp16: Q4_1 per group; Q2_K d per 256
     minv: np.ndarray                  # uint16 fp16: Q4_1 min per group; Q2_K dmin per 256
-    sc: np.ndarray | None = None      # uint8 [n/16] (Q2_K)
-    mn: np.ndarray | None = None      # uint8 [n/16] (Q2_K)
+    sc: np.ndarray | None = None      # uint8 [n/16] (Q2_K) or [n/32] 6-bit (Q4_K)
+    mn: np.ndarray | None = None      # uint8 [n/16] (Q2_K) or [n/32] 6-bit (Q4_K)
 
 
 def matrix_fields(w: Workload, layer: int, tensor: int, expert: int,
@@ -217,6 +220,12 @@ def matrix_fields(w: Workload, layer: int, tensor: int, expert: int,
         d = abs_normal_f16(key(s, layer, tensor, expert, F_D), n // 256, r.sigma, start=v0 // 256)
         dm = abs_normal_f16(key(s, layer, tensor, expert, F_DMIN), n // 256, r.sigma, start=v0 // 256)
         return Fields(Q2_K, nrows, cols, c, 2, 256, d, dm, sc, mn)
+    if r.qtype == Q4_K:
+        sc = codes(key(s, layer, tensor, expert, F_SC), n // 32, 6, start=v0 // 32)
+        mn = codes(key(s, layer, tensor, expert, F_MN), n // 32, 6, start=v0 // 32)
+        d = abs_normal_f16(key(s, layer, tensor, expert, F_D), n // 256, r.sigma, start=v0 // 256)
+        dm = abs_normal_f16(key(s, layer, tensor, expert, F_DMIN), n // 256, r.sigma, start=v0 // 256)
+        return Fields(Q4_K, nrows, cols, c, 4, 256, d, dm, sc, mn)
     g = r.group
     sc16 = abs_normal_f16(key(s, layer, tensor, expert, F_D), n // g, r.sigma, start=v0 // g)
     mn16 = f16_scale_pow2(sc16, r.min_mult)
