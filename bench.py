@@ -71,6 +71,9 @@ def parse_args(argv=None):
                     help="skip the per-kernel, end-to-end and CPU passes (for profiler captures)")
     ap.add_argument("--n-expert", type=int, default=0,
                     help="override the workload's expert count (smaller cases for profiler captures)")
+    ap.add_argument("--quantize", choices=("q2_k", "q4_1"), default=None,
+                    help="time the device float-input quantizer instead (fp32 expert matrices -> blocks, "
+                         "with per-column importance)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's tokens per step (smaller cases for profiler captures)")
     return ap.parse_args(argv)
@@ -159,13 +162,22 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- workload
+# block (values, bytes) per format: Q4_1 20 B / 32, Q2_K 84 B / 256, Q4_K 144 B / 256
+BLOCK = {synth.Q4_1: (32, 20), synth.Q2_K: (256, 84), synth.Q4_K: (256, 144)}
+
+
+def mat_bytes(qtype: str, rows: int, cols: int) -> int:
+    bv, bb = BLOCK[qtype]
+    return rows * cols // bv * bb
+
+
 def host_layer_blocks(w: synth.Workload, layer: int, experts, packer):
     """Experts-major block bytes of the listed experts (others zero) via `packer`."""
     out = {}
     for t in (synth.T_GATE, synth.T_UP, synth.T_DOWN):
         rows, cols = synth.matrix_shape(w, t)
         q = synth.recipe(w, t)
-        per = rows * cols // (256 if q.qtype == synth.Q2_K else 32) * (84 if q.qtype == synth.Q2_K else 20)
+        per = mat_bytes(q.qtype, rows, cols)
         buf = np.zeros(w.n_expert * per, np.uint8)
         for e in experts:
             buf[e * per:(e + 1) * per] = packer(synth.matrix_fields(w, layer, t, e))
@@ -177,6 +189,8 @@ def product_packer(M):
     def pack(f):
         if f.qtype == synth.Q4_1:
             return M.ds4moe_quantize_ref(M.DS4MOE_Q4_1, f.bits, f.group, f.codes, f.scale, f.minv)
+        if f.qtype == synth.Q4_K:
+            return M.ds4moe_quantize_ref(M.DS4MOE_Q4_K, 4, 256, f.codes, f.scale, f.minv, f.sc, f.mn)
         return M.ds4moe_quantize_ref(M.DS4MOE_Q2_K, 2, 256, f.codes, f.scale, f.minv, f.sc, f.mn)
     return pack
 
@@ -184,7 +198,7 @@ def product_packer(M):
 def device_layer(w: synth.Workload, M, torch):
     """All experts of layer 0 packed by the library's host packer, uploaded."""
     from bit_quantized_moe_q2_gb300.device import DeviceLayer
-    qid = {synth.Q4_1: M.DS4MOE_Q4_1, synth.Q2_K: M.DS4MOE_Q2_K}
+    qid = {synth.Q4_1: M.DS4MOE_Q4_1, synth.Q2_K: M.DS4MOE_Q2_K, synth.Q4_K: M.DS4MOE_Q4_K}
     dev = DeviceLayer.empty(w.d_model, w.d_ff, w.n_expert, qid[w.gate.qtype], qid[w.up.qtype], qid[w.down.qtype])
     pack = product_packer(M)
     names = {synth.T_GATE: "gate", synth.T_UP: "up", synth.T_DOWN: "down"}
@@ -206,7 +220,7 @@ def expert_bytes(w: synth.Workload) -> int:
     for t in (synth.T_GATE, synth.T_UP, synth.T_DOWN):
         rows, cols = synth.matrix_shape(w, t)
         q = synth.recipe(w, t)
-        tot += rows * cols // (256 if q.qtype == synth.Q2_K else 32) * (84 if q.qtype == synth.Q2_K else 20)
+        tot += mat_bytes(q.qtype, rows, cols)
     return tot
 
 
@@ -215,7 +229,7 @@ def gate_up_bytes(w: synth.Workload) -> int:
     for t in (synth.T_GATE, synth.T_UP):
         rows, cols = synth.matrix_shape(w, t)
         q = synth.recipe(w, t)
-        tot += rows * cols // (256 if q.qtype == synth.Q2_K else 32) * (84 if q.qtype == synth.Q2_K else 20)
+        tot += mat_bytes(q.qtype, rows, cols)
     return tot
 
 
@@ -671,7 +685,7 @@ def _pack_expert(job):
 def tensor_bytes(w: synth.Workload, t: int) -> int:
     rows, cols = synth.matrix_shape(w, t)
     q = synth.recipe(w, t)
-    return rows * cols // (256 if q.qtype == synth.Q2_K else 32) * (84 if q.qtype == synth.Q2_K else 20)
+    return mat_bytes(q.qtype, rows, cols)
 
 
 def run_ours_stack(args, w: synth.Workload):
@@ -696,7 +710,7 @@ def run_ours_stack(args, w: synth.Workload):
     barrier(world)
     import bit_quantized_moe_q2_gb300 as M
     from bit_quantized_moe_q2_gb300.device import DeviceLayer, check_status, workspace
-    qid = {synth.Q4_1: M.DS4MOE_Q4_1, synth.Q2_K: M.DS4MOE_Q2_K}
+    qid = {synth.Q4_1: M.DS4MOE_Q4_1, synth.Q2_K: M.DS4MOE_Q2_K, synth.Q4_K: M.DS4MOE_Q4_K}
     t_gen = time.perf_counter()
     devs, Wrs, biases = [], [], []
     names = [sh.name for sh in shms]
@@ -848,6 +862,52 @@ def oracle_free_bf16_to_f32(b: np.ndarray) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32)
 
 
+def run_quantize(args, w: synth.Workload):
+    """Device float-input quantizer: 16 fp32 expert matrices (d_ff x d_model,
+    512 MiB, larger than L2) -> Q2_K / Q4_1 blocks with per-column
+    importance; values/s and the input-read bandwidth against HBM."""
+    import torch
+    torch.cuda.set_device(0)
+    from bit_quantized_moe_q2_gb300 import _build
+    _build.build()
+    import bit_quantized_moe_q2_gb300 as M
+    from bit_quantized_moe_q2_gb300.device import check_status
+    q = {"q2_k": M.DS4MOE_Q2_K, "q4_1": M.DS4MOE_Q4_1}[args.quantize]
+    rows, cols, n_mat = w.d_ff, w.d_model, 16
+    n = rows * cols * n_mat
+    g = torch.Generator(device="cuda").manual_seed(w.seed)
+    x = torch.randn(n, device="cuda", generator=g) * 0.02
+    imp = torch.rand(cols, device="cuda", generator=g) ** 2
+    out = torch.empty(n // M.block_values(q) * M.block_bytes(q), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    steps = max(3, min(args.steps, 50))
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup if args.warmup < 50 else 3)):
+            M.ds4moe_quantize_f32(q, x, imp, out, ws, cols=cols, stream=stream)
+    check_status(ws, stream)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            M.ds4moe_quantize_f32(q, x, imp, out, ws, cols=cols, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    check_status(ws, stream)
+    peak, kind = measured_peaks()
+    gbs = (n * 4 + out.numel()) / (ms / 1000) / 1e9
+    print(json.dumps({"metric": "quantized values/s", "value": n / (ms / 1000), "unit": "values/s", "n_gpus": 1,
+                      "steps": steps, "ms_per_step": ms, "higher_is_better": True, "dtype": "f32",
+                      "data": "synthetic", "config": {"workload": f"quantize-{args.quantize}-16x{rows}x{cols}",
+                                                       "importance": True, "l2": "512 MiB input per step"},
+                      "roofline": {"kernel": "quantize_f32", "bound": "hbm", "achieved": gbs, "peak": peak,
+                                   "unit": "GB/s", "frac": gbs / peak, "traffic": None,
+                                   "algorithmic_bytes_per_launch": n * 4 + out.numel(),
+                                   "peak_source": kind}}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     w = synth.WORKLOADS[args.workload]
@@ -856,7 +916,10 @@ def main(argv=None):
     if args.tokens:
         w = w.replace(T=args.tokens)
     if w.path not in ("decode", "prefill"):
-        raise SystemExit("bench.py times workloads 0-4")
+        raise SystemExit("bench.py times workloads 0-5")
+    if args.quantize:
+        run_quantize(args, w)
+        return
     if args.impl == "reference":
         run_reference(args, w)
     elif w.n_layers > 1:

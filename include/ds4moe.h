@@ -119,6 +119,11 @@ const char *ds4moe_status_string(int32_t status);
  *   dmin per 256 values; sub_sc / sub_mn hold the 4-bit scale and min of each
  *   16-value sub-block (n_values / 16 entries, one per byte).  Codes > 3 or
  *   nibbles > 15 return DS4MOE_EBLOCKER.
+ * out_type == DS4MOE_Q4_K: packs 4-bit codes into the 144-byte layout
+ *   above.  bits must be 4 and group 256; scale_f16 / min_f16 hold d and dmin
+ *   per 256 values; sub_sc / sub_mn the 6-bit scale and min of each 32-value
+ *   sub-block (n_values / 32 entries).  Codes > 15 or fields > 63 return
+ *   DS4MOE_EBLOCKER.
  * out_type == DS4MOE_IQ2_XXS: DS4MOE_EUNSUPPORTED.
  * out_bytes must be at least n_values / block_values * block_bytes
  * (DS4MOE_ESPACE otherwise).  `out_blocks` is host memory.

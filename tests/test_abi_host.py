@@ -62,6 +62,22 @@ def test_quantize_ref_q2_k_equals_oracle_pack(M):
     assert np.array_equal(got, ref)
 
 
+def test_quantize_ref_q4_k_equals_oracle_pack(M):
+    w = synth.WORKLOADS[5]
+    f = synth.matrix_fields(w, 0, synth.T_UP, 9, row0=5, nrows=32)
+    got = M.ds4moe_quantize_ref(M.DS4MOE_Q4_K, 4, 256, f.codes, f.scale, f.minv, f.sc, f.mn)
+    assert np.array_equal(got, oracle.pack_fields(f))
+    rng = np.random.default_rng(44)
+    codes = rng.integers(0, 16, 256 * 7).astype(np.uint8)
+    sc, mn = rng.integers(0, 64, 56).astype(np.uint8), rng.integers(0, 64, 56).astype(np.uint8)
+    d, dm = rng.integers(0, 0x7C00, 7).astype(np.uint16), rng.integers(0, 0x7C00, 7).astype(np.uint16)
+    assert np.array_equal(M.ds4moe_quantize_ref(M.DS4MOE_Q4_K, 4, 256, codes, d, dm, sc, mn),
+                          oracle.q4k_pack(codes, sc, mn, d, dm))
+    with pytest.raises(M.Ds4moeError) as ei:  # a 7-bit scale
+        M.ds4moe_quantize_ref(M.DS4MOE_Q4_K, 4, 256, codes, d, dm, np.full(56, 64, np.uint8), mn)
+    assert ei.value.status == M.DS4MOE_EBLOCKER
+
+
 def test_quantize_ref_workload_fields_equal_oracle(M):
     for wid, tensor in ((0, synth.T_GATE), (2, synth.T_UP), (3, synth.T_GATE)):
         f = synth.matrix_fields(synth.WORKLOADS[wid], 0, tensor, 7, row0=3, nrows=8)
