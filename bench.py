@@ -233,6 +233,14 @@ def gate_up_bytes(w: synth.Workload) -> int:
     return tot
 
 
+# DRAM bytes per launch of the roofline kernel from an ncu capture of the
+# current build (dram__bytes_read.sum + dram__bytes_write.sum); a workload
+# missing here reports null.  The summaries with the commands are in profiles/.
+NCU_TRAFFIC = {
+    "flash-layer-decode-t1-q2k": 33_089_792,  # k_gate_up_t1: 33,089,536 read + 256 written
+}
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -474,7 +482,7 @@ def run_ours(args, w: synth.Workload):
     gu_avg_s = gu_ms / gu_n / 1000.0
     roofline = {"kernel": "gate_up (fused dequant GEMV + SwiGLU)", "bound": "hbm",
                 "achieved": gu_algo / gu_avg_s / 1e9, "peak": peak, "unit": "GB/s",
-                "frac": gu_algo / gu_avg_s / 1e9 / peak, "traffic": None,
+                "frac": gu_algo / gu_avg_s / 1e9 / peak, "traffic": NCU_TRAFFIC.get(w.name),
                 "algorithmic_bytes_per_launch": int(gu_algo), "avg_launch_us": gu_avg_s * 1e6,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else
                                "fallback 6.8 TB/s"}
