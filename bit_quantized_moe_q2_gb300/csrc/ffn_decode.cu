@@ -502,8 +502,8 @@ __global__ void __launch_bounds__(256) k_down_mma(FfnArgs a, uint32_t chd) {
 
 // gate/up + SwiGLU for T = 1: warps 0 .. nb-1 consume block w of d_model for
 // the 16 gate and 16 up rows of a tile, warp nb produces.  Units (group,
-// 16-row tile) are split into contiguous ranges, one per CTA; the warp that
-// finishes a unit last sums the blocks and writes h.
+// 16-row tile) are dealt to the CTAs round-robin; the warp that finishes a
+// unit last sums the blocks and writes h.
 template <bool FIN>
 __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -531,14 +531,17 @@ __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage
   __shared__ Group s_grp[kT1MaxGroups];
   __shared__ int s_ngrp;
   t1_load_groups(a, s_grp, &s_ngrp);
+  // units dealt round-robin: at any moment the CTAs read neighbouring tiles,
+  // so DRAM sees a few long sequential streams instead of one short range
+  // per CTA (the activations are the same for every unit)
   const int U = s_ngrp * ntile;
-  const int u0 = (int)((int64_t)U * blockIdx.x / gridDim.x);
-  const int u1 = (int)((int64_t)U * (blockIdx.x + 1) / gridDim.x);
+  const int u0 = blockIdx.x, ustep = gridDim.x;
+  const int nunits = u0 < U ? (U - u0 + ustep - 1) / ustep : 0;
   auto load_group = [&](int u) { return s_grp[u / ntile]; };
   if (w == nb) {
     // producer
     const uint8_t *gate = static_cast<const uint8_t *>(a.L.gate), *up = static_cast<const uint8_t *>(a.L.up);
-    for (int u = u0, it = 0; u < u1; ++u, ++it) {
+    for (int u = u0, it = 0; u < U; u += ustep, ++it) {
       const int st = it % nstage;
       if (it >= nstage && !ptx::mbar_wait(&sm.empty[st], ((it / nstage) - 1) & 1)) {
         record_status(a.hdr, DS4MOE_ETIMEOUT);
@@ -552,12 +555,12 @@ __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage
       ptx::bulk_g2s(smem + (size_t)st * stage_bytes + (size_t)lane * rs, src, rowb, &sm.full[st]);
       if (FIN && blockIdx.x == 0 && it == nstage - 1) finish_routing_weights(const_cast<float *>(a.w), a.T, a.k);
     }
-    if (FIN && blockIdx.x == 0 && u1 - u0 < nstage) finish_routing_weights(const_cast<float *>(a.w), a.T, a.k);
+    if (FIN && blockIdx.x == 0 && nunits < nstage) finish_routing_weights(const_cast<float *>(a.w), a.T, a.k);
     return;
   }
   bool timed_out = false;
   int it = 0;
-  for (int u = u0; u < u1; ++u, ++it) {
+  for (int u = u0; u < U; u += ustep, ++it) {
     const int st = it % nstage;
     if (!timed_out && !ptx::mbar_wait(&sm.full[st], (it / nstage) & 1)) {
       record_status(a.hdr, DS4MOE_ETIMEOUT);
