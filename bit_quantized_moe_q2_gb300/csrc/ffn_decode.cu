@@ -504,12 +504,13 @@ __global__ void __launch_bounds__(256) k_down_mma(FfnArgs a, uint32_t chd) {
 // the 16 gate and 16 up rows of a tile, warp nb produces.  Units (group,
 // 16-row tile) are dealt to the CTAs round-robin; the warp that finishes a
 // unit last sums the blocks and writes h.
-template <bool FIN>
+template <bool FIN, int FMT>
 __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage) {
   extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int kBB = FMT == DS4MOE_Q4_K ? kQ4KBytes : kQ2KBytes;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
   const int D = a.L.d_model, F = a.L.d_ff, nb = D / 256;
-  const uint32_t rowb = (uint32_t)(kQ2KBytes * nb), rs = t1_row_stride(rowb);
+  const uint32_t rowb = (uint32_t)(kBB * nb), rs = t1_row_stride(rowb);
   const uint32_t stage_bytes = 32u * rs;
   const T1Smem sm = t1_smem(smem, nstage, stage_bytes, nb);
   if (threadIdx.x == 0) {
@@ -524,7 +525,10 @@ __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage
   const T1Lane L = t1_lane(c);
   T1B B;
   // the activations are the call's input: loaded before the dependency wait
-  if (w < nb) t1_load_b<true>(B, a.x + 256 * w, g, c);
+  if (w < nb) {
+    if constexpr (FMT == DS4MOE_Q4_K) t1_load_b_q4k<true>(B, a.x + 256 * w, g, c);
+    else t1_load_b<true>(B, a.x + 256 * w, g, c);
+  }
   ptx::pdl_wait();  // groups come from the routing / bucketing grid
   ptx::pdl_launch_dependents();
   const int ntile = F / 16;
@@ -568,9 +572,10 @@ __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage
     }
     float y[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
     if (!timed_out) {
-      const uint8_t *sb = smem + (size_t)st * stage_bytes + kQ2KBytes * w;
+      const uint8_t *sb = smem + (size_t)st * stage_bytes + kBB * w;
       const uint8_t *const mats[2] = {sb, sb + 16 * (size_t)rs};
-      t1_block<2>(mats, rs, 0, g, B, L, y);
+      if constexpr (FMT == DS4MOE_Q4_K) t1_block_q4k<2>(mats, rs, 0, g, c, B, y);
+      else t1_block<2>(mats, rs, 0, g, B, L, y);
     }
     // partials of this block: gate rows g, g+8 at [g], [g+8], up at [16+g], [24+g]
     float *r = sm.red + ((size_t)st * nb + w) * 32;
@@ -625,11 +630,13 @@ __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage
 // warp finishing a unit last writes y; the weighted combine is a grid of
 // its own (a fused one would count arrivals per tile across CTAs, and its
 // fences cost more than the launch).
+template <int FMT>
 __global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
   extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int kBB = FMT == DS4MOE_Q4_K ? kQ4KBytes : kQ2KBytes;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
   const int D = a.L.d_model, F = a.L.d_ff, nb = F / 256;
-  const uint32_t rowb = (uint32_t)(kQ2KBytes * nb), gap = t1_gap4(rowb);
+  const uint32_t rowb = (uint32_t)(kBB * nb), gap = t1_gap4(rowb);
   const uint32_t stage_bytes = t1_gap_stage_bytes(rowb);
   const T1Smem sm = t1_smem(smem, nstage, stage_bytes, nb);
   if (threadIdx.x == 0) {
@@ -679,7 +686,8 @@ __global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
     const int st = it % nstage;
     const Group grp = load_group(u);
     if (grp.p0 != cur) {
-      t1_load_b<false>(B, a.h + (int64_t)grp.p0 * F + 256 * w, g, c);
+      if constexpr (FMT == DS4MOE_Q4_K) t1_load_b_q4k<false>(B, a.h + (int64_t)grp.p0 * F + 256 * w, g, c);
+      else t1_load_b<false>(B, a.h + (int64_t)grp.p0 * F + 256 * w, g, c);
       cur = grp.p0;
     }
     if (!timed_out && !ptx::mbar_wait(&sm.full[st], (it / nstage) & 1)) {
@@ -688,8 +696,9 @@ __global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
     }
     float y[1][2] = {{0.f, 0.f}};
     if (!timed_out) {
-      const uint8_t *const mats[1] = {smem + (size_t)st * stage_bytes + kQ2KBytes * w};
-      t1_block<1>(mats, rowb, gap, g, B, L, y);
+      const uint8_t *const mats[1] = {smem + (size_t)st * stage_bytes + kBB * w};
+      if constexpr (FMT == DS4MOE_Q4_K) t1_block_q4k<1>(mats, rowb, gap, g, c, B, y);
+      else t1_block<1>(mats, rowb, gap, g, B, L, y);
     }
     float *r = sm.red + ((size_t)st * nb + w) * 32;
 #pragma unroll
@@ -911,12 +920,14 @@ constexpr size_t kT1SmemGateUp = 227 * 1024, kT1SmemDown = 100 * 1024;
 
 cudaError_t launch_gate_up_t1(const FfnArgs &a, cudaStream_t s) {
   const int nb = a.L.d_model / 256;
-  const uint32_t stage = 32 * t1_row_stride((uint32_t)(kQ2KBytes * nb));
+  const bool q4k = a.L.q_gate == DS4MOE_Q4_K;
+  const uint32_t stage = 32 * t1_row_stride((uint32_t)(block_bytes(a.L.q_gate) * nb));
   int nstage = 6;
   while (nstage > 2 && t1_smem_bytes(nstage, stage, nb) > kT1SmemGateUp) --nstage;
   const size_t smem = t1_smem_bytes(nstage, stage, nb);
   if (smem > kT1SmemGateUp) return cudaErrorInvalidValue;
-  auto kern = a.w_logits ? k_gate_up_t1<true> : k_gate_up_t1<false>;
+  auto kern = q4k ? (a.w_logits ? k_gate_up_t1<true, DS4MOE_Q4_K> : k_gate_up_t1<false, DS4MOE_Q4_K>)
+                  : (a.w_logits ? k_gate_up_t1<true, DS4MOE_Q2_K> : k_gate_up_t1<false, DS4MOE_Q2_K>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   ProfScope p("gate_up", s);
@@ -925,12 +936,12 @@ cudaError_t launch_gate_up_t1(const FfnArgs &a, cudaStream_t s) {
 
 cudaError_t launch_down_t1(const FfnArgs &a, cudaStream_t s) {
   const int nb = a.L.d_ff / 256;
-  const uint32_t stage = t1_gap_stage_bytes((uint32_t)(kQ2KBytes * nb));
+  const uint32_t stage = t1_gap_stage_bytes((uint32_t)(block_bytes(a.L.q_down) * nb));
   int nstage = 8;
   while (nstage > 2 && t1_smem_bytes(nstage, stage, nb) > kT1SmemDown) --nstage;
   const size_t smem = t1_smem_bytes(nstage, stage, nb);
   if (smem > kT1SmemDown) return cudaErrorInvalidValue;
-  auto kern = k_down_t1;
+  auto kern = a.L.q_down == DS4MOE_Q4_K ? k_down_t1<DS4MOE_Q4_K> : k_down_t1<DS4MOE_Q2_K>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -940,14 +951,16 @@ cudaError_t launch_down_t1(const FfnArgs &a, cudaStream_t s) {
   return launch_pdl(kern, dim3(num_sms() * (per_sm > 0 ? per_sm : 1)), dim3(32 * (nb + 1)), smem, s, a, nstage);
 }
 
-// Single-token kernels: Q2_K, one consumer warp per 256-value block of K
-// (at most 16 for gate/up, 8 for down), rows split into 16-byte units.
+// Single-token kernels: Q2_K or Q4_K (gate and up alike), one consumer warp
+// per 256-value block of K (at most 16 for gate/up, 8 for down), rows split
+// into 16-byte units.
 bool t1_gate_up_ok(const ds4moe_layer &L) {
-  return L.q_gate == DS4MOE_Q2_K && L.q_up == DS4MOE_Q2_K && L.d_model % 1024 == 0 && L.d_model <= 4096 &&
-         L.d_ff % 16 == 0;
+  return (L.q_gate == DS4MOE_Q2_K || L.q_gate == DS4MOE_Q4_K) && L.q_up == L.q_gate && L.d_model % 1024 == 0 &&
+         L.d_model <= 4096 && L.d_ff % 16 == 0;
 }
 bool t1_down_ok(const ds4moe_layer &L) {
-  return L.q_down == DS4MOE_Q2_K && L.d_ff % 1024 == 0 && L.d_ff <= 2048 && L.d_model % 16 == 0;
+  return (L.q_down == DS4MOE_Q2_K || L.q_down == DS4MOE_Q4_K) && L.d_ff % 1024 == 0 && L.d_ff <= 2048 &&
+         L.d_model % 16 == 0;
 }
 
 cudaError_t launch_down_mma(const FfnArgs &a, cudaStream_t s) {
@@ -989,16 +1002,20 @@ bool decode_mma_ok(const ds4moe_layer &L) {
 
 cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s) {
   const ds4moe_layer &L = a.L;
-  if (decode_mma_ok(L)) {
+  // single token: the sub-block-column kernels where the format allows;
+  // both h producers (single-token and multi-token gate/up) write the fp16
+  // operand both down kernels read, so they combine freely
+  const bool t1g = a.T == 1 && t1_gate_up_ok(L), t1d = a.T == 1 && t1_down_ok(L);
+  if (decode_mma_ok(L) || (t1g && t1d)) {
     const int kp = pick_kp(L.d_model, L.q_gate, L.q_up);
     cudaError_t e;
-    if (a.T == 1 && t1_gate_up_ok(L)) e = launch_gate_up_t1(a, s);
+    if (t1g) e = launch_gate_up_t1(a, s);
     else if (L.q_gate == DS4MOE_Q2_K && L.q_up == DS4MOE_Q2_K) e = launch_gate_up_mma<DS4MOE_Q2_K, DS4MOE_Q2_K>(a, s, kp);
     else if (L.q_gate == DS4MOE_Q4_1 && L.q_up == DS4MOE_Q4_1) e = launch_gate_up_mma<DS4MOE_Q4_1, DS4MOE_Q4_1>(a, s, kp);
     else if (L.q_gate == DS4MOE_Q2_K) e = launch_gate_up_mma<DS4MOE_Q2_K, DS4MOE_Q4_1>(a, s, kp);
     else e = launch_gate_up_mma<DS4MOE_Q4_1, DS4MOE_Q2_K>(a, s, kp);
     if (e != cudaSuccess) return e;
-    return a.T == 1 && t1_down_ok(L) ? launch_down_t1(a, s) : launch_down_mma(a, s);
+    return t1d ? launch_down_t1(a, s) : launch_down_mma(a, s);
   }
   const int grid = num_sms() * 8;
   {

@@ -267,3 +267,144 @@ __device__ __forceinline__ void t1_load_groups(const FfnArgs &a, Group *s_grp, i
 }
 
 }  // namespace ds4
+
+namespace ds4 {
+
+// ------------------------------------------------------- Q4_K single token
+// The same scheme for Q4_K blocks (8 sub-blocks of 32 values, 4-bit codes,
+// 6-bit scales and mins): column n of every MMA is sub-block n, K slots 2n,
+// 2n+1 carry two of its values, and the 16 K steps of a block cover all 32.
+// Lane quad c reads sub-block c (qs bytes 32 (c/2) .. +31) and c + 4 (bytes
+// 32 (c/2 + 2) ..), both in nibble c & 1: masking the nibble leaves the
+// subnormal q * 2^-24 (low) or q * 2^-20 (high), so D column 2c is scaled by
+// 2^24 and column 2c + 1 by 2^20.  K step 2i + beta of a sub-block holds its
+// values 4i + beta and 4i + 2 + beta.  The activation operands use T1B with
+// K step s in x[s / 8][s % 8]; the mins MMA pairs each sub-block's mn (twice)
+// with the hi and lo parts of its sum in column 0.
+
+__device__ __forceinline__ void q4k_sc_mn_pair(const uint32_t (&s3)[3], int j, uint32_t &sc, uint32_t &mn) {
+  // scales[12] as three little-endian words
+  const auto byte = [&](int b) { return (s3[b >> 2] >> (8 * (b & 3))) & 0xFFu; };
+  if (j < 4) {
+    sc = byte(j) & 63u;
+    mn = byte(j + 4) & 63u;
+  } else {
+    sc = (byte(j + 4) & 15u) | ((byte(j - 4) >> 6) << 4);
+    mn = (byte(j + 4) >> 4) | ((byte(j) >> 6) << 4);
+  }
+}
+
+// src: the block's 256 activations, bf16 (BF16 = true) or fp16 bits.
+template <bool BF16>
+__device__ __forceinline__ void t1_load_b_q4k(T1B &B, const uint16_t *__restrict__ src, int g, int c) {
+  const bool own0 = g == c, own1 = g == c + 4;
+  // sub-block g: values 32 g .. 32 g + 31
+  uint16_t f[32];
+  float s = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(src + 32 * g) + q);
+    const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t bits = (wd[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
+      float val;
+      if (BF16) {
+        val = bf16_bits_to_f32(bits);
+        f[8 * q + i] = __half_as_ushort(__float2half_rn(val));
+      } else {
+        val = f16_bits_to_f32(bits);
+        f[8 * q + i] = (uint16_t)bits;
+      }
+      s += val;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int beta = 0; beta < 2; ++beta) {
+      const uint32_t p = pack_h2(f[4 * i + beta], f[4 * i + 2 + beta]);
+      const int st = 2 * i + beta;
+      B.x[st >> 3][st & 7][0] = own0 ? p : 0u;
+      B.x[st >> 3][st & 7][1] = own1 ? p : 0u;
+    }
+  const __half hi = __float2half_rn(s);
+  const uint16_t shi = __half_as_ushort(hi), slo = __half_as_ushort(__float2half_rn(s - __half2float(hi)));
+  const uint32_t hl = pack_h2(shi, slo);
+  // lanes of column 0 (g == 0): (hi, lo) of sub-blocks c and c + 4
+  const uint32_t m0 = __shfl_sync(0xffffffffu, hl, 4 * c);
+  const uint32_t m1 = __shfl_sync(0xffffffffu, hl, 4 * c + 16);
+  B.m[0] = g == 0 ? m0 : 0u;
+  B.m[1] = g == 0 ? m1 : 0u;
+}
+
+// One Q4_K block column of NM 16-row tiles (tile m, row r at mat[m] + r * rs
+// + gap4 * (r / 4)) against one activation block: this lane's share of
+// d * sum(sc * q * x) - dmin * sum(mn * xsum) for rows g and g + 8.
+template <int NM>
+__device__ __forceinline__ void t1_block_q4k(const uint8_t *const (&mat)[NM], uint32_t rs, uint32_t gap4, int g, int c,
+                                             const T1B &B, float (&y)[NM][2]) {
+  const uint32_t mask = (c & 1) ? 0x00F000F0u : 0x000F000Fu;
+  const float k0 = 16777216.f, k1 = 1048576.f;  // 2^24, 2^20
+  const uint32_t offa = 16u + 32u * (uint32_t)(c >> 1), offb = offa + 64u;
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+    uint4 qa[2][2], qb[2][2];  // [row][16-byte half]
+    uint32_t dd[2], s3[2][3];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const uint8_t *row = mat[m] + (size_t)(g + 8 * r) * rs + gap4 * (uint32_t)((g + 8 * r) >> 2);
+      dd[r] = ptx::lds32(row);
+#pragma unroll
+      for (int q = 0; q < 3; ++q) s3[r][q] = ptx::lds32(row + 4 + 4 * q);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        qa[r][q] = *reinterpret_cast<const uint4 *>(row + offa + 16 * q);
+        qb[r][q] = *reinterpret_cast<const uint4 *>(row + offb + 16 * q);
+      }
+    }
+    float C[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const auto word = [](const uint4 (&v)[2], int k) {
+        const uint4 &h = v[k >> 2];
+        return (k & 3) == 0 ? h.x : (k & 3) == 1 ? h.y : (k & 3) == 2 ? h.z : h.w;
+      };
+      const uint32_t wa0 = word(qa[0], i), wa1 = word(qa[1], i), wb0 = word(qb[0], i), wb1 = word(qb[1], i);
+      {
+        const uint32_t A[4] = {wa0 & mask, wa1 & mask, wb0 & mask, wb1 & mask};
+        const int st = 2 * i;
+        ptx::mma_f16(C[0], A, B.x[st >> 3][st & 7][0], B.x[st >> 3][st & 7][1]);
+      }
+      {
+        const uint32_t A[4] = {(wa0 >> 8) & mask, (wa1 >> 8) & mask, (wb0 >> 8) & mask, (wb1 >> 8) & mask};
+        const int st = 2 * i + 1;
+        ptx::mma_f16(C[1], A, B.x[st >> 3][st & 7][0], B.x[st >> 3][st & 7][1]);
+      }
+    }
+    // scales of the lane's columns (sub-blocks 2c, 2c + 1) and mins of the
+    // sub-blocks whose K slots it holds (c, c + 4)
+    uint32_t Am[4];
+    float sacc[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      uint32_t sc0, mn0, sc1, mn1, scx, mnc, mnc4;
+      q4k_sc_mn_pair(s3[r], 2 * c, sc0, mn0);
+      q4k_sc_mn_pair(s3[r], 2 * c + 1, sc1, mn1);
+      q4k_sc_mn_pair(s3[r], c, scx, mnc);
+      q4k_sc_mn_pair(s3[r], c + 4, scx, mnc4);
+      sacc[r] = fmaf((float)sc0 * k0, C[0][2 * r] + C[1][2 * r], (float)sc1 * k1 * (C[0][2 * r + 1] + C[1][2 * r + 1]));
+      // fp16 mn (exact small integers), duplicated in both halves
+      const uint32_t hc = __half_as_ushort(__uint2half_rn(mnc)), hc4 = __half_as_ushort(__uint2half_rn(mnc4));
+      Am[r] = hc | (hc << 16);
+      Am[2 + r] = hc4 | (hc4 << 16);
+    }
+    float M[4] = {0.f, 0.f, 0.f, 0.f};
+    ptx::mma_f16(M, Am, B.m[0], B.m[1]);
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      y[m][r] = fmaf(f16_bits_to_f32(dd[r] & 0xFFFFu), sacc[r], -f16_bits_to_f32(dd[r] >> 16) * M[2 * r]);
+  }
+}
+
+}  // namespace ds4

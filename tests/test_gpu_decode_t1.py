@@ -1,6 +1,6 @@
-"""GPU parity of the single-token decode kernels (T = 1: Q2_K gate/up with
-d_model a multiple of 1024 up to 4096, Q2_K down with d_ff 1024 or 2048),
-against the CPU oracle, through both decode entry points.
+"""GPU parity of the single-token decode kernels (T = 1: Q2_K or Q4_K
+gate/up with d_model a multiple of 1024 up to 4096, Q2_K or Q4_K down with
+d_ff 1024 or 2048), against the CPU oracle, through both decode entry points.
 
 Covers: every (d_model, d_ff) the kernels take, including layers where only
 one of the two single-token kernels applies and the other side runs the
@@ -22,6 +22,7 @@ pytestmark = pytest.mark.gpu
 TOL = 2e-3
 
 Q2 = synth.WORKLOADS[1]
+Q4 = synth.WORKLOADS[5]
 SHAPES = [
     # both single-token kernels
     Q2.replace(d_model=1024, d_ff=1024, n_expert=8, k=6, seed=401),
@@ -34,6 +35,13 @@ SHAPES = [
     Q2.replace(d_model=768, d_ff=1024, n_expert=5, k=2, seed=406),
     # Q4_1 gate/up (multi-token kernel), Q2_K down single-token
     synth.WORKLOADS[0].replace(d_model=1024, d_ff=2048, n_expert=6, k=2, T=1, seed=407),
+    # Q4_K: both single-token kernels
+    Q4.replace(d_model=1024, d_ff=1024, n_expert=8, k=6, seed=411),
+    Q4.replace(d_model=4096, d_ff=2048, n_expert=6, k=2, seed=412, bias_sigma=1.0),
+    Q4.replace(d_model=3072, d_ff=1024, n_expert=4, k=1, seed=413),
+    # Q4_K gate/up with Q2_K down, and Q2_K gate/up with Q4_K down
+    Q4.replace(d_model=2048, d_ff=1024, n_expert=5, k=3, seed=414, down=synth.Q2K),
+    Q2.replace(d_model=1024, d_ff=2048, n_expert=5, k=2, seed=415, down=synth.Q4K),
 ]
 
 
@@ -66,8 +74,9 @@ def test_single_token_matches_oracle(M, wi):
         assert np.array_equal(out3.view(np.uint32), out.view(np.uint32))
 
 
-def test_single_token_kernels_are_the_ones_launched(M):
-    w = SHAPES[0]
+@pytest.mark.parametrize("wi", [0, 7])
+def test_single_token_kernels_are_the_ones_launched(M, wi):
+    w = SHAPES[wi]
     L = build_layer(w)
     dev = to_device(L)
     x = synth.activations(w, T=1)
@@ -78,6 +87,7 @@ def test_single_token_kernels_are_the_ones_launched(M):
     finally:
         M.ds4moe_profile_enable(False)
     assert {"gate_up", "down"} <= names
+    assert not {"gate_up_simt", "down_simt"} & names
 
 
 def test_single_token_out_of_range_expert(M):
