@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(512) k_gate_up_mma(FfnArgs a, int kp, uint32_t
   ptx::pdl_wait();
   ptx::pdl_launch_dependents();
   if (FIN && blockIdx.x == 0 && w == 0) finish_routing_weights(const_cast<float *>(a.w), a.T, a.k);
+  clear_combine_counters(a, threadIdx.x, blockDim.x);
   const int ntile = F / 16;
   const int U = __ldcg(&a.hdr->n_groups) * ntile;
   const int64_t rb = is_up ? row_bytes(QU, D) : row_bytes(QG, D);
@@ -531,6 +532,7 @@ __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage
   }
   ptx::pdl_wait();  // groups come from the routing / bucketing grid
   ptx::pdl_launch_dependents();
+  if (w == nb) clear_combine_counters(a, lane, 32);  // the producer warp (the consumers hold x)
   const int ntile = F / 16;
   __shared__ Group s_grp[kT1MaxGroups];
   __shared__ int s_ngrp;
@@ -595,20 +597,26 @@ __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage
       const Group grp = load_group(u);
       const int row0 = (u % ntile) * 16;
       float hv = 0.f;
+      // a group holds more than one slot only when the token names its
+      // expert more than once: every slot gets the same h
       if (lane < 16) {
         // h rounded to bf16 (the definition), stored as the fp16 operand of
         // the down kernel (exact for |h| in [2^-14, 65504])
         hv = bf16_bits_to_f32(f32_to_bf16_bits(silu(sv) * us));
         if (fabsf(hv) > 65504.f) record_status(a.hdr, DS4MOE_EDEVICE);
-        a.h[(int64_t)grp.p0 * F + row0 + lane] = __half_as_ushort(__float2half_rn(hv));
+        uint16_t *hp = a.h + (int64_t)grp.p0 * F + row0 + lane;
+        const uint16_t hb = __half_as_ushort(__float2half_rn(hv));
+#pragma unroll 1
+        for (int j = 0; j < grp.nt; ++j, hp += F) *hp = hb;
       }
 #pragma unroll
       for (int off = 8; off; off >>= 1) hv += __shfl_xor_sync(0xffffffffu, hv, off);
-      if (lane == 0) {
+      if (lane < grp.nt) {
         const int n16 = row0 / 16;
         const __half hi = __float2half_rn(hv);
         const __half lo = __float2half_rn(hv - __half2float(hi));
-        uint16_t *rec = reinterpret_cast<uint16_t *>(a.hs16 + ((int64_t)grp.p0 * (F / 256 + 1) + n16 / 16) * 64);
+        uint16_t *rec =
+            reinterpret_cast<uint16_t *>(a.hs16 + ((int64_t)(grp.p0 + lane) * (F / 256 + 1) + n16 / 16) * 64);
         rec[n16 & 15] = __half_as_ushort(hi);
         rec[16 + (n16 & 15)] = __half_as_ushort(lo);
       }
@@ -712,7 +720,9 @@ __global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
         const float *rr = sm.red + (size_t)st * nb * 32 + lane;
         float sv = 0.f;
         for (int p = 0; p < nb; ++p) sv += rr[32 * p];
-        a.y[(int64_t)grp.p0 * D + row0 + lane] = sv;
+        float *yp = a.y + (int64_t)grp.p0 * D + row0 + lane;
+#pragma unroll 1
+        for (int j = 0; j < grp.nt; ++j, yp += D) *yp = sv;  // one slot per naming of the expert
       }
     }
     __syncwarp();

@@ -173,6 +173,17 @@ struct FfnArgs {
   int32_t *nchunks;       // [2]: chunk counts of chunks_gu / chunks_dn
 };
 
+// The combine's arrival counters start every call at zero: the gate/up grid
+// clears them (the down grid reads them only after that grid completes).
+// The workspace regions move with the call's sizes, so what the previous
+// call left there cannot be relied on.
+// `tid` of `nthr` threads per CTA take part.
+__device__ __forceinline__ void clear_combine_counters(const FfnArgs &a, int tid, int nthr) {
+  if (!a.cnt) return;
+  const int64_t n = (int64_t)a.T * (a.L.d_model / 16);
+  for (int64_t i = blockIdx.x * (int64_t)nthr + tid; i < n; i += (int64_t)gridDim.x * nthr) a.cnt[i] = 0;
+}
+
 cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_ffn_prefill(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s);

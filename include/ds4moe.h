@@ -181,9 +181,10 @@ size_t ds4moe_workspace_bytes(const ds4moe_layer *L, int32_t T, int32_t k,
                               int32_t prefill);
 
 /*
- * ds4moe_workspace_init -- DEVICE.  Zeroes the workspace (status word and
- * the counters the kernels leave at zero after every call).  Call once after
- * allocating it, and again after any call that reported an error.
+ * ds4moe_workspace_init -- DEVICE.  Zeroes the workspace (its status word;
+ * every other region, the combine's arrival counters included, is written
+ * by each call before it is read, so one workspace may serve calls of any
+ * sizes it is large enough for).  Call once after allocating it.
  */
 ds4moe_status ds4moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
