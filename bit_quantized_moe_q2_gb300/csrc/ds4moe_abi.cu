@@ -950,7 +950,8 @@ BucketArgs bucket_args(const ds4moe_layer &L, void *ws, const WsLayout &lay, con
 // with `bucketed` the router kernel has already done the whole bucketing step.
 ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, const int32_t *idx,
                       const float *w, int32_t T, int32_t k, float *out, void *ws, size_t ws_bytes,
-                      void *stream, const float *logits = nullptr, bool bucketed = false) {
+                      void *stream, const float *logits = nullptr, bool bucketed = false,
+                      bool route_t1 = false) {
   ds4moe_status st = check_layer(L);
   if (st != DS4MOE_OK) return st;
   if (T < 0 || k < 1 || k > 32 || k > L->n_expert) return DS4MOE_EINVAL;
@@ -992,7 +993,13 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
   const bool sums = !tc && decode_mma_ok(*L);
   a.cnt = sums ? ws_ptr<int32_t>(ws, lay.cnt) : nullptr;
   const int E = L->n_expert, P = T * k;
-  a.w_logits = logits != nullptr && P <= 32;  // the small bucketing path leaves raw selected logits in w
+  if (route_t1) {
+    // single token: the FFN grids rank the experts from the logits
+    a.lg = logits;
+    a.idx_out = const_cast<int32_t *>(idx);
+  } else {
+    a.w_logits = logits != nullptr && P <= 32;  // the small bucketing path leaves raw selected logits in w
+  }
   const size_t smem = sizeof(int32_t) * (32 * (size_t)E + E + 1);
   static bool attr_set = false;
   if (!attr_set) {
@@ -1238,6 +1245,21 @@ ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const 
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float *lg = ws_ptr<float>(ws, lay.logits);
+  if (T == 1 && t1_chain_ok(*L)) {
+    // one token on the single-token kernels: the router grid only writes the
+    // logits, and every CTA of the FFN grids ranks the experts itself (no
+    // grid waits on one CTA's ranking)
+    ProfScope prof("route", s);
+    const int ni = (D + 1023) / 1024;
+    auto kern = ni <= 1   ? k_route_small<1, kRouteLogits>
+                : ni <= 2 ? k_route_small<2, kRouteLogits>
+                : ni <= 4 ? k_route_small<4, kRouteLogits>
+                          : k_route_small<8, kRouteLogits>;
+    const cudaError_t e = launch_pdl(kern, dim3(E), dim3(256), 0, s, x, Wr, bias, (int)T, (int)D, (int)E, (int)k, lg,
+                                     idx, w, static_cast<WsHeader *>(ws), BucketArgs{});
+    if (e != cudaSuccess) return cuda_status(e);
+    return run_ffn(false, L, x, idx, w, T, k, out, ws, ws_bytes, stream, lg, true, true);
+  }
   // up to 32 pairs: the router's last CTA also does the bucketing
   const bool fused = T * k <= 32;
   {

@@ -511,8 +511,9 @@ __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage
   constexpr int kBB = FMT == DS4MOE_Q4_K ? kQ4KBytes : kQ2KBytes;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
   const int D = a.L.d_model, F = a.L.d_ff, nb = D / 256;
-  const uint32_t rowb = (uint32_t)(kBB * nb), rs = t1_row_stride(rowb);
-  const uint32_t stage_bytes = 32u * rs;
+  const T1Tile tl = t1_tile((uint32_t)(kBB * nb));
+  const uint32_t tile_bytes = t1_tile_bytes(tl), stage_bytes = 2u * tile_bytes;
+  const uint32_t ncp = t1_copies(tl);
   const T1Smem sm = t1_smem(smem, nstage, stage_bytes, nb);
   if (threadIdx.x == 0) {
     for (int st = 0; st < nstage; ++st) {
@@ -530,13 +531,19 @@ __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage
     if constexpr (FMT == DS4MOE_Q4_K) t1_load_b_q4k<true>(B, a.x + 256 * w, g, c);
     else t1_load_b<true>(B, a.x + 256 * w, g, c);
   }
-  ptx::pdl_wait();  // groups come from the routing / bucketing grid
+  ptx::pdl_wait();  // groups (or the logits) come from the routing grid
   ptx::pdl_launch_dependents();
-  if (w == nb) clear_combine_counters(a, lane, 32);  // the producer warp (the consumers hold x)
   const int ntile = F / 16;
   __shared__ Group s_grp[kT1MaxGroups];
   __shared__ int s_ngrp;
-  t1_load_groups(a, s_grp, &s_ngrp);
+  if (a.lg) {
+    // the producer warp ranks the experts (the consumers hold x)
+    if (w == nb) t1_route_warp(a, s_grp, &s_ngrp, blockIdx.x == 0);
+    __syncthreads();
+  } else {
+    t1_load_groups(a, s_grp, &s_ngrp);
+  }
+  if (w == nb) clear_combine_counters(a, lane, 32);
   // units dealt round-robin: at any moment the CTAs read neighbouring tiles,
   // so DRAM sees a few long sequential streams instead of one short range
   // per CTA (the activations are the same for every unit)
@@ -555,10 +562,14 @@ __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage
       }
       const Group grp = load_group(u);
       const int row0 = (u % ntile) * 16;
-      if (lane == 0) ptx::mbar_arrive_expect_tx(&sm.full[st], 32u * rowb);
+      if (lane == 0) ptx::mbar_arrive_expect_tx(&sm.full[st], 32u * tl.rowb);
       __syncwarp();
-      const uint8_t *src = (lane < 16 ? gate : up) + ((int64_t)grp.e * F + row0 + (lane & 15)) * rowb;
-      ptx::bulk_g2s(smem + (size_t)st * stage_bytes + (size_t)lane * rs, src, rowb, &sm.full[st]);
+      // gate tile, then up tile: ncp copies each
+      if ((uint32_t)lane < 2u * ncp) {
+        const uint32_t mat = (uint32_t)lane / ncp, i = (uint32_t)lane % ncp;
+        const uint8_t *src = (mat == 0 ? gate : up) + ((int64_t)grp.e * F + row0) * tl.rowb;
+        t1_tile_copy(smem + (size_t)st * stage_bytes + mat * tile_bytes, src, tl, i, &sm.full[st]);
+      }
       if (FIN && blockIdx.x == 0 && it == nstage - 1) finish_routing_weights(const_cast<float *>(a.w), a.T, a.k);
     }
     if (FIN && blockIdx.x == 0 && nunits < nstage) finish_routing_weights(const_cast<float *>(a.w), a.T, a.k);
@@ -575,9 +586,9 @@ __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage
     float y[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
     if (!timed_out) {
       const uint8_t *sb = smem + (size_t)st * stage_bytes + kBB * w;
-      const uint8_t *const mats[2] = {sb, sb + 16 * (size_t)rs};
-      if constexpr (FMT == DS4MOE_Q4_K) t1_block_q4k<2>(mats, rs, 0, g, c, B, y);
-      else t1_block<2>(mats, rs, 0, g, B, L, y);
+      const uint8_t *const mats[2] = {sb, sb + tile_bytes};
+      if constexpr (FMT == DS4MOE_Q4_K) t1_block_q4k<2>(mats, tl, g, c, B, y);
+      else t1_block<2>(mats, tl, g, B, L, y);
     }
     // partials of this block: gate rows g, g+8 at [g], [g+8], up at [16+g], [24+g]
     float *r = sm.red + ((size_t)st * nb + w) * 32;
@@ -644,8 +655,8 @@ __global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
   constexpr int kBB = FMT == DS4MOE_Q4_K ? kQ4KBytes : kQ2KBytes;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
   const int D = a.L.d_model, F = a.L.d_ff, nb = F / 256;
-  const uint32_t rowb = (uint32_t)(kBB * nb), gap = t1_gap4(rowb);
-  const uint32_t stage_bytes = t1_gap_stage_bytes(rowb);
+  const T1Tile tl = t1_tile((uint32_t)(kBB * nb));
+  const uint32_t stage_bytes = t1_tile_bytes(tl);
   const T1Smem sm = t1_smem(smem, nstage, stage_bytes, nb);
   if (threadIdx.x == 0) {
     for (int st = 0; st < nstage; ++st) {
@@ -657,10 +668,16 @@ __global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
   }
   __syncthreads();
   const int ntile = D / 16;
-  // the groups were complete before the gate/up grid launched this one
+  // the groups (or the logits) were complete before the gate/up grid
+  // launched this one
   __shared__ Group s_grp[kT1MaxGroups];
   __shared__ int s_ngrp;
-  t1_load_groups(a, s_grp, &s_ngrp);
+  if (a.lg) {
+    if (w == 0) t1_route_warp(a, s_grp, &s_ngrp, false);
+    __syncthreads();
+  } else {
+    t1_load_groups(a, s_grp, &s_ngrp);
+  }
   const int U = s_ngrp * ntile;
   const int u0 = (int)((int64_t)U * blockIdx.x / gridDim.x);
   const int u1 = (int)((int64_t)U * (blockIdx.x + 1) / gridDim.x);
@@ -675,12 +692,11 @@ __global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
       }
       const Group grp = load_group(u);
       const int row0 = (u % ntile) * 16;
-      if (lane == 0) ptx::mbar_arrive_expect_tx(&sm.full[st], 16u * rowb);
+      if (lane == 0) ptx::mbar_arrive_expect_tx(&sm.full[st], 16u * tl.rowb);
       __syncwarp();
-      // four copies of 4 rows (row copies this short are issue-bound)
-      if (lane < 4)
-        ptx::bulk_g2s(smem + (size_t)st * stage_bytes + (size_t)lane * (4u * rowb + gap),
-                      down + ((int64_t)grp.e * D + row0 + 4 * lane) * rowb, 4u * rowb, &sm.full[st]);
+      if ((uint32_t)lane < t1_copies(tl))
+        t1_tile_copy(smem + (size_t)st * stage_bytes, down + ((int64_t)grp.e * D + row0) * tl.rowb, tl, (uint32_t)lane,
+                     &sm.full[st]);
     }
     return;
   }
@@ -705,8 +721,8 @@ __global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
     float y[1][2] = {{0.f, 0.f}};
     if (!timed_out) {
       const uint8_t *const mats[1] = {smem + (size_t)st * stage_bytes + kBB * w};
-      if constexpr (FMT == DS4MOE_Q4_K) t1_block_q4k<1>(mats, rowb, gap, g, c, B, y);
-      else t1_block<1>(mats, rowb, gap, g, B, L, y);
+      if constexpr (FMT == DS4MOE_Q4_K) t1_block_q4k<1>(mats, tl, g, c, B, y);
+      else t1_block<1>(mats, tl, g, B, L, y);
     }
     float *r = sm.red + ((size_t)st * nb + w) * 32;
 #pragma unroll
@@ -873,15 +889,30 @@ __global__ void k_combine(FfnArgs a) {
     const int64_t t = (i * 4) / D;
     const int c = (int)((i * 4) % D);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-      const int pos = __ldcg(a.inv + t * k + j);
-      if (pos < 0) continue;
-      const float wt = a.w[t * k + j];
-      const float4 yv = __ldcg(reinterpret_cast<const float4 *>(a.y + (int64_t)pos * D + c));
-      acc.x = fmaf(wt, yv.x, acc.x);
-      acc.y = fmaf(wt, yv.y, acc.y);
-      acc.z = fmaf(wt, yv.z, acc.z);
-      acc.w = fmaf(wt, yv.w, acc.w);
+    // eight slots at a time: every (position, weight) load, then every y
+    // load, issued before the first use (one round trip each, not k)
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      int pos[8];
+      float wt[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int j = j0 + jj;
+        pos[jj] = j < k ? __ldcg(a.inv + t * k + j) : -1;
+        wt[jj] = j < k ? __ldcg(a.w + t * k + j) : 0.f;
+      }
+      float4 yv[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj)
+        yv[jj] = pos[jj] >= 0 ? __ldcg(reinterpret_cast<const float4 *>(a.y + (int64_t)pos[jj] * D + c))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        if (pos[jj] < 0) continue;
+        acc.x = fmaf(wt[jj], yv[jj].x, acc.x);
+        acc.y = fmaf(wt[jj], yv[jj].y, acc.y);
+        acc.z = fmaf(wt[jj], yv[jj].z, acc.z);
+        acc.w = fmaf(wt[jj], yv[jj].w, acc.w);
+      }
     }
     *reinterpret_cast<float4 *>(a.out + t * D + c) = acc;
   }
@@ -931,7 +962,7 @@ constexpr size_t kT1SmemGateUp = 227 * 1024, kT1SmemDown = 100 * 1024;
 cudaError_t launch_gate_up_t1(const FfnArgs &a, cudaStream_t s) {
   const int nb = a.L.d_model / 256;
   const bool q4k = a.L.q_gate == DS4MOE_Q4_K;
-  const uint32_t stage = 32 * t1_row_stride((uint32_t)(block_bytes(a.L.q_gate) * nb));
+  const uint32_t stage = 2 * t1_tile_bytes(t1_tile((uint32_t)(block_bytes(a.L.q_gate) * nb)));
   int nstage = 6;
   while (nstage > 2 && t1_smem_bytes(nstage, stage, nb) > kT1SmemGateUp) --nstage;
   const size_t smem = t1_smem_bytes(nstage, stage, nb);
@@ -946,7 +977,7 @@ cudaError_t launch_gate_up_t1(const FfnArgs &a, cudaStream_t s) {
 
 cudaError_t launch_down_t1(const FfnArgs &a, cudaStream_t s) {
   const int nb = a.L.d_ff / 256;
-  const uint32_t stage = t1_gap_stage_bytes((uint32_t)(block_bytes(a.L.q_down) * nb));
+  const uint32_t stage = t1_tile_bytes(t1_tile((uint32_t)(block_bytes(a.L.q_down) * nb)));
   int nstage = 8;
   while (nstage > 2 && t1_smem_bytes(nstage, stage, nb) > kT1SmemDown) --nstage;
   const size_t smem = t1_smem_bytes(nstage, stage, nb);
@@ -994,6 +1025,8 @@ cudaError_t launch_down_mma(const FfnArgs &a, cudaStream_t s) {
 }
 
 }  // namespace
+
+bool t1_chain_ok(const ds4moe_layer &L) { return t1_gate_up_ok(L) && t1_down_ok(L) && L.n_expert <= 256; }
 
 // The tensor-core kernels need rows that split into 16-byte-multiple bulk
 // copies and stages that fit in shared memory; other shapes use SIMT.

@@ -167,6 +167,11 @@ struct FfnArgs {
   const int32_t *nvalid;  // [T] experts in range per token
   int32_t *cnt;           // [T][D/16] arrival counters of the fused combine (nullptr: separate combine)
   int w_logits;           // w holds the k selected logits per token: the gate/up grid turns them into weights
+  // single-token chain only (nullptr otherwise): the FFN grids rank the
+  // experts themselves from the router's logits [E]; CTA 0 of the gate/up
+  // grid writes idx_out / w and the bucketing outputs
+  const float *lg;
+  int32_t *idx_out;
   // tensor-core prefill only (nullptr otherwise)
   uint16_t *xp;           // [P][D] x of each sorted pair, fp16
   Chunk *chunks_gu, *chunks_dn;
@@ -188,6 +193,9 @@ cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_ffn_prefill(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s);
 bool decode_mma_ok(const ds4moe_layer &L);
+// Both single-token FFN kernels apply (the single-token chain of the fused
+// decode entry ranks the experts inside them).
+bool t1_chain_ok(const ds4moe_layer &L);
 bool prefill_tc_ok(const ds4moe_layer &L);
 
 int num_sms();

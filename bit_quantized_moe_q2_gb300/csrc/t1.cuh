@@ -4,6 +4,7 @@
 
 #include "internal.cuh"
 #include "ptx.cuh"
+#include "route.cuh"
 
 namespace ds4 {
 
@@ -116,22 +117,52 @@ __device__ __forceinline__ void t1_load_b(T1B &B, const uint16_t *__restrict__ s
   B.m[1] = mv[1];
 }
 
+// Shared-memory layout of a staged 16-row tile: row r starts at
+// r * rowb + gap * (r >> gsh); the tile arrives as 16 >> gsh bulk copies of
+// (rowb << gsh) bytes, each followed by a gap-byte hole.  The gap makes the 8
+// rows g = 0 .. 7 that a warp's lane quads read together start in 8 distinct
+// 16-byte bank groups (with R = rowb / 16):
+//   R odd:          no gap, the whole tile in one copy (R g mod 8 distinct);
+//   R = 4 (mod 8):  16 bytes every 2 rows (4 g + g / 2 mod 8 distinct);
+//   R = 2, 6 (mod 8): 16 bytes every 4 rows (2 g + g / 4, 6 g + g / 4);
+//   R = 0 (mod 8):  16 bytes after every row (stride R + 1, odd).
+// Fewer, larger copies matter: a bulk copy of a 1.3 KB row lands noticeably
+// later than one of 2.7 KB carrying the same bytes.
+struct T1Tile {
+  uint32_t rowb, gap, gsh;
+};
+__host__ __device__ constexpr T1Tile t1_tile(uint32_t rowb) {
+  return ((rowb / 16) & 1u)       ? T1Tile{rowb, 0u, 4u}
+         : ((rowb / 16) % 8 == 4) ? T1Tile{rowb, 16u, 1u}
+         : ((rowb / 16) % 8 == 0) ? T1Tile{rowb, 16u, 0u}
+                                  : T1Tile{rowb, 16u, 2u};
+}
+__host__ __device__ constexpr uint32_t t1_tile_bytes(T1Tile t) { return 16u * t.rowb + (16u >> t.gsh) * t.gap; }
+__host__ __device__ constexpr uint32_t t1_row_off(T1Tile t, uint32_t r) { return r * t.rowb + t.gap * (r >> t.gsh); }
+__host__ __device__ constexpr uint32_t t1_copies(T1Tile t) { return 16u >> t.gsh; }
+__host__ __device__ constexpr uint32_t t1_copy_bytes(T1Tile t) { return t.rowb << t.gsh; }
+
+// Issue copy i (< t1_copies) of the 16 rows starting at src into the tile at dst.
+__device__ __forceinline__ void t1_tile_copy(uint8_t *dst, const uint8_t *src, T1Tile t, uint32_t i, uint64_t *bar) {
+  ptx::bulk_g2s(dst + i * (t1_copy_bytes(t) + t.gap), src + (size_t)i * t1_copy_bytes(t), t1_copy_bytes(t), bar);
+}
+
 // One Q2_K block column of NM tiles of 16 staged rows each (tile m, row r at
-// mat[m] + r * rs + gap4 * (r / 4)), against one activation block: this
-// lane's share of
+// mat[m] + t1_row_off(tl, r)), against one activation block: this lane's
+// share of
 // d * sum(sc * q * x) - dmin * sum(mn * xsum) for rows g and g + 8 of every
 // matrix.  Even and odd K steps accumulate separately, so 2 NM MMA chains
 // are in flight.
 template <int NM>
-__device__ __forceinline__ void t1_block(const uint8_t *const (&mat)[NM], uint32_t rs, uint32_t gap4, int g,
-                                         const T1B &B, const T1Lane &L, float (&y)[NM][2]) {
+__device__ __forceinline__ void t1_block(const uint8_t *const (&mat)[NM], T1Tile tl, int g, const T1B &B,
+                                         const T1Lane &L, float (&y)[NM][2]) {
   const uint8_t *row[NM][2];
   uint32_t sp[NM][2][2], dd[NM][2];
 #pragma unroll
   for (int m = 0; m < NM; ++m) {
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      row[m][r] = mat[m] + (size_t)(g + 8 * r) * rs + gap4 * (uint32_t)((g + 8 * r) >> 2);
+      row[m][r] = mat[m] + t1_row_off(tl, (uint32_t)(g + 8 * r));
       // scale bytes of sub-blocks (2c, 2c+1) of half 0 and (8+2c, 9+2c) of half 1
       sp[m][r][0] = __byte_perm(ptx::lds32(row[m][r] + L.soff), 0u, L.ssel);
       sp[m][r][1] = __byte_perm(ptx::lds32(row[m][r] + 8 + L.soff), 0u, L.ssel);
@@ -218,19 +249,6 @@ __device__ __forceinline__ bool t1_last_arriver(int *cnt, int nwarps) {
   return __shfl_sync(0xffffffffu, last, 0) != 0;
 }
 
-// Shared-memory row stride of a staged tile: row bytes rounded so that 8
-// consecutive rows fall into 8 distinct 4-bank groups (an odd number of
-// 16-byte units).
-__host__ __device__ constexpr uint32_t t1_row_stride(uint32_t rowb) { return ((rowb / 16) & 1u) ? rowb : rowb + 16; }
-
-// A 16-row tile staged as four copies of 4 rows, each followed by a gap:
-// with an even number of 16-byte units per row, rows r and r + 4 would
-// share banks; a 16-byte gap every 4 rows moves them four banks apart, which
-// the lanes' word rotation turns into conflict-free loads.  Rows with an odd
-// number of units need no gap.
-__host__ __device__ constexpr uint32_t t1_gap4(uint32_t rowb) { return ((rowb / 16) & 1u) ? 0u : 16u; }
-__host__ __device__ constexpr uint32_t t1_gap_stage_bytes(uint32_t rowb) { return 16u * rowb + 4u * t1_gap4(rowb); }
-
 // Shared-memory layout of the single-token kernels: nstage stages, then
 // the full / empty barriers, the per-stage partials and the per-stage
 // arrival counters.
@@ -254,6 +272,47 @@ __host__ __device__ constexpr size_t t1_smem_bytes(int nstage, uint32_t stage_by
 // With one token there are at most k <= 32 groups: every CTA keeps them in
 // shared memory, so no unit waits on a global load for its expert.
 constexpr int kT1MaxGroups = 32;
+
+// Routing of the single token from the router's E <= 256 logits, by one
+// warp of every CTA that needs it (each computes the same result from the
+// same logits, so no grid waits on another one's ranking): the k experts in
+// rank order (descending logit, ties to the lower id), then one group per
+// selected expert in ascending expert order -- the selected experts are
+// distinct, so every group holds one pair and pair i sits at position
+// inv[i] of the expert-sorted order.  With `publish` (one CTA of the chain)
+// the warp also writes idx and the softmax weights over the selected (the
+// call's outputs) and the bucketing outputs the later grids read.
+__device__ __forceinline__ void t1_route_warp(const FfnArgs &a, Group *s_grp, int *s_ngrp, bool publish) {
+  const int lane = threadIdx.x & 31, E = a.L.n_expert, k = a.k;
+  float v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = e < E ? __ldcg(a.lg + e) : 0.f;
+  }
+  float my_v;
+  int my_e;
+  topk_select_warp(v, E, k, my_v, my_e);
+  int pos = 0;  // experts selected with a smaller id
+  for (int j = 0; j < k; ++j) pos += __shfl_sync(0xffffffffu, my_e, j) < my_e;
+  if (lane < k) s_grp[pos] = Group{my_e, pos, 1, 0};
+  if (lane == 0) *s_ngrp = k;
+  if (publish) {
+    const float wt = softmax_selected_warp(my_v, k);
+    if (lane < k) {
+      a.idx_out[lane] = my_e;
+      const_cast<float *>(a.w)[lane] = wt;
+      const_cast<int32_t *>(a.inv)[lane] = pos;
+      const_cast<int32_t *>(a.perm)[pos] = lane;
+      const_cast<Group *>(a.groups)[pos] = Group{my_e, pos, 1, 0};
+    }
+    if (lane == 0) {
+      const_cast<int32_t *>(a.nvalid)[0] = k;
+      a.hdr->n_groups = k;
+      a.hdr->n_active = k;
+    }
+  }
+}
 __device__ __forceinline__ void t1_load_groups(const FfnArgs &a, Group *s_grp, int *s_ngrp) {
   if (threadIdx.x < 32) {
     const int n = __ldcg(&a.hdr->n_groups);
@@ -338,11 +397,11 @@ __device__ __forceinline__ void t1_load_b_q4k(T1B &B, const uint16_t *__restrict
   B.m[1] = g == 0 ? m1 : 0u;
 }
 
-// One Q4_K block column of NM 16-row tiles (tile m, row r at mat[m] + r * rs
-// + gap4 * (r / 4)) against one activation block: this lane's share of
+// One Q4_K block column of NM 16-row tiles (tile m, row r at mat[m] +
+// t1_row_off(tl, r)) against one activation block: this lane's share of
 // d * sum(sc * q * x) - dmin * sum(mn * xsum) for rows g and g + 8.
 template <int NM>
-__device__ __forceinline__ void t1_block_q4k(const uint8_t *const (&mat)[NM], uint32_t rs, uint32_t gap4, int g, int c,
+__device__ __forceinline__ void t1_block_q4k(const uint8_t *const (&mat)[NM], T1Tile tl, int g, int c,
                                              const T1B &B, float (&y)[NM][2]) {
   const uint32_t mask = (c & 1) ? 0x00F000F0u : 0x000F000Fu;
   const float k0 = 16777216.f, k1 = 1048576.f;  // 2^24, 2^20
@@ -353,7 +412,7 @@ __device__ __forceinline__ void t1_block_q4k(const uint8_t *const (&mat)[NM], ui
     uint32_t dd[2], s3[2][3];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      const uint8_t *row = mat[m] + (size_t)(g + 8 * r) * rs + gap4 * (uint32_t)((g + 8 * r) >> 2);
+      const uint8_t *row = mat[m] + t1_row_off(tl, (uint32_t)(g + 8 * r));
       dd[r] = ptx::lds32(row);
 #pragma unroll
       for (int q = 0; q < 3; ++q) s3[r][q] = ptx::lds32(row + 4 + 4 * q);

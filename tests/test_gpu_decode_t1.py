@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import synth
-from tests.gpu_util import rel_err
+from tests.gpu_util import rel_err, ulp_diff_f32
 from tests.layers import build_layer, to_device
 from tests.test_gpu_ffn import gpu_forward, gpu_moe_decode, oracle_out
 
@@ -65,6 +65,7 @@ def test_single_token_matches_oracle(M, wi):
         out, idx, wt, st = gpu_moe_decode(M, dev, x, L.Wr, L.bias, w.k)
         assert st == M.DS4MOE_OK
         assert np.array_equal(idx, ridx)
+        assert ulp_diff_f32(wt, rw).max() <= 2
         assert rel_err(out, ref) <= TOL
         out2, idx2, wt2, st2 = gpu_forward(M, dev, x, L.Wr, L.bias, w.k)
         assert st2 == M.DS4MOE_OK and np.array_equal(idx2, ridx)
