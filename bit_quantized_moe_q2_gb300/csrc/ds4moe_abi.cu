@@ -549,6 +549,8 @@ struct BucketArgs {
   float *w;
   int32_t *nvalid;
   float *out;
+  int32_t *zero2;  // single-token chain: further counters the router grid zeroes
+  int nzero2;
 };
 
 // Bucketing of a decode batch (P <= 32 pairs) by a CTA of 256 threads
@@ -662,6 +664,10 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict_
   }
   ptx::pdl_wait();
   ptx::pdl_launch_dependents();
+  // single-token chain: the merged FFN grid's per-expert counters start at 0
+  if (MODE == kRouteLogits && bk.counts && tid == 0) bk.counts[blockIdx.x] = 0;
+  if (MODE == kRouteLogits && bk.zero2)
+    for (int i = blockIdx.x * 256 + tid; i < bk.nzero2; i += gridDim.x * 256) bk.zero2[i] = 0;
   if (MODE == kRouteBucket && bk.xs16)
     convert_x(x, T, D, bk.x16, bk.xs16, bk.xs32, hdr, blockIdx.x * 256 + tid, gridDim.x * 256);
   for (int t0 = 0; t0 < T; t0 += 32) {
@@ -997,6 +1003,8 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
     // single token: the FFN grids rank the experts from the logits
     a.lg = logits;
     a.idx_out = const_cast<int32_t *>(idx);
+    a.hready = ws_ptr<int32_t>(ws, lay.counts);
+    a.ccnt = ws_ptr<int32_t>(ws, lay.cnt);
   } else {
     a.w_logits = logits != nullptr && P <= 32;  // the small bucketing path leaves raw selected logits in w
   }
@@ -1255,8 +1263,12 @@ ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const 
                 : ni <= 2 ? k_route_small<2, kRouteLogits>
                 : ni <= 4 ? k_route_small<4, kRouteLogits>
                           : k_route_small<8, kRouteLogits>;
+    BucketArgs zero{};
+    zero.counts = ws_ptr<int32_t>(ws, lay.counts);  // one counter per expert, zeroed by CTA e
+    zero.zero2 = ws_ptr<int32_t>(ws, lay.cnt);       // the merged grid's combine counters
+    zero.nzero2 = (D + 63) / 64;
     const cudaError_t e = launch_pdl(kern, dim3(E), dim3(256), 0, s, x, Wr, bias, (int)T, (int)D, (int)E, (int)k, lg,
-                                     idx, w, static_cast<WsHeader *>(ws), BucketArgs{});
+                                     idx, w, static_cast<WsHeader *>(ws), zero);
     if (e != cudaSuccess) return cuda_status(e);
     return run_ffn(false, L, x, idx, w, T, k, out, ws, ws_bytes, stream, lg, true, true);
   }

@@ -750,6 +750,319 @@ __global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
   }
 }
 
+// The single-token expert FFN as one persistent grid (Q2_K gate, up and
+// down, d_model = 2 d_ff): one CTA per SM with nbg = d_model / 256 consumer
+// warps and one producer.  Every CTA runs its gate/up units first (16 gate +
+// 16 up rows of one selected expert, dealt round-robin, exactly as the
+// gate/up kernel), then its down items (64 rows of one expert's down matrix,
+// dealt in reverse round-robin so that the CTAs holding an extra gate/up
+// unit hold fewer down items).  The producer streams both kinds through one
+// ring of stages, so the down weights land while gate/up still computes and
+// no grid boundary separates the two.  A down item of expert slot j waits
+// (bounded) until all d_ff / 16 gate/up units of slot j have published their
+// h.  Cross-CTA synchronisation stays off the consumer warps: the warp that
+// finishes a gate/up unit only sets the unit's bit in a shared-memory mask,
+// and a sync warp per CTA publishes the completed units (one GPU-scope fence
+// for every batch, then relaxed adds on hready[]), then waits on hready[] for
+// the experts of the CTA's down items and hands them to the consumers
+// through a second shared-memory mask.  A GPU-scope fence in the finishing
+// consumer warp instead costs it about as much as the unit's arithmetic, and
+// every consumer warp polling global counters slows the publishing down.
+// The weighted combine is fused the same way: the warp that finishes a down
+// item only sets its bit in a third mask; the sync warp counts the item on
+// its 64 output rows (ccnt, fence-release / fence-acquire), and if it was
+// the last of the k items over those rows, sums w_i y_i in rank order, as
+// the combine kernel does.  The sync warp also forms the routing weights
+// (and in CTA 0 writes the call's routing outputs), off the producer's path.
+// Consumer warp w
+// takes K block w % nbd of the down rows and tiles 2 (w / nbd), +1 of the
+// item, so both kinds of work run the same two-tile block kernel.  Arithmetic
+// and summation order are those of the two separate kernels, so y is
+// bit-identical to theirs.
+__global__ void __launch_bounds__(18 * 32, 1) k_ffn_t1(FfnArgs a, int nstage) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
+  const int D = a.L.d_model, F = a.L.d_ff, nbg = D / 256, nbd = F / 256;
+  const T1Tile tg = t1_tile((uint32_t)(kQ2KBytes * nbg)), td = t1_tile((uint32_t)(kQ2KBytes * nbd));
+  const uint32_t tile_g = t1_tile_bytes(tg), tile_d = t1_tile_bytes(td);
+  const uint32_t stage_bytes = 2u * tile_g > 4u * tile_d ? 2u * tile_g : 4u * tile_d;
+  const T1Smem sm = t1_smem(smem, nstage, stage_bytes, nbg);
+  __shared__ uint32_t s_done, s_hok, s_ddone;  // gate/up units finished; experts with h ready; down items finished
+  __shared__ float s_lv[kT1MaxGroups], s_w[kT1MaxGroups];  // per slot: selected logit, routing weight
+  __shared__ int s_inv[kT1MaxGroups];                      // per slot: position in expert order
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < nstage; ++st) {
+      ptx::mbar_init(&sm.full[st], 1);
+      ptx::mbar_init(&sm.empty[st], nbg);
+      sm.cnt[st] = 0;
+    }
+    s_done = 0u;
+    s_hok = 0u;
+    s_ddone = 0u;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  const T1Lane L = t1_lane(c);
+  T1B B;
+  if (w < nbg) t1_load_b<true>(B, a.x + 256 * w, g, c);  // the call's input: before the dependency wait
+  ptx::pdl_wait();  // the logits come from the router grid
+  ptx::pdl_launch_dependents();
+  __shared__ Group s_grp[kT1MaxGroups];
+  __shared__ int s_ngrp;
+  if (w == nbg) t1_route_warp(a, s_grp, &s_ngrp, false, s_lv, s_inv);
+  __syncthreads();
+  const int ntg = F / 16, ntd = D / 64;  // gate/up units and down items per expert
+  const int Ug = s_ngrp * ntg, Ud = s_ngrp * ntd, G = gridDim.x;
+  const int ng = (int)blockIdx.x < Ug ? (Ug - (int)blockIdx.x + G - 1) / G : 0;
+  const int rb = G - 1 - (int)blockIdx.x;
+  const int nd = rb < Ud ? (Ud - rb + G - 1) / G : 0;
+  const int n = ng + nd;
+  if (w == nbg + 1) {
+    // sync warp: the routing weights (CTA 0 also writes the routing outputs)
+    t1_weights_warp(a, s_grp, s_lv, s_inv, s_w, blockIdx.x == 0);
+    // then, interleaved: publish this CTA's gate/up units as they finish, and
+    // hand each expert of its down items to the consumers once its h is out
+    const uint32_t all = ng >= 32 ? 0xffffffffu : (1u << ng) - 1u;
+    const uint32_t dall = nd >= 32 ? 0xffffffffu : (1u << nd) - 1u;
+    uint32_t pub = 0, dpub = 0, polls = 0;
+    int t = 0, prev = -1;
+    while (pub != all || t < nd || dpub != dall) {
+      bool progress = false;
+      uint32_t m = 0;
+      if (lane == 0) m = *reinterpret_cast<volatile uint32_t *>(&s_done) & ~pub;
+      m = __shfl_sync(0xffffffffu, m, 0);  // one view of the mask for the whole warp
+      if (m) {
+        if (lane == 0) {
+          __threadfence_block();  // the units' h writes, seen through s_done
+          ptx::fence_acq_rel_gpu();
+          for (uint32_t r = m; r; r &= r - 1u)
+            ptx::red_relaxed_add(a.hready + ((int)blockIdx.x + G * (__ffs(r) - 1)) / ntg, 1);
+        }
+        pub |= m;
+        progress = true;
+      }
+      while (t < nd && (rb + G * t) / ntd == prev) ++t;  // same expert as the previous item
+      if (t < nd) {
+        const int j = (rb + G * t) / ntd;
+        int ready = 0;
+        if (lane == 0) ready = ptx::ld_acquire(a.hready + j) >= ntg;
+        if (__shfl_sync(0xffffffffu, ready, 0)) {
+          if (lane == 0) {
+            __threadfence_block();
+            atomicOr(&s_hok, 1u << j);
+          }
+          prev = j;
+          ++t;
+          progress = true;
+        }
+      }
+      // finished down items: count each on its rows; the last one combines
+      uint32_t dm = 0;
+      if (lane == 0) dm = *reinterpret_cast<volatile uint32_t *>(&s_ddone) & ~dpub;
+      dm = __shfl_sync(0xffffffffu, dm, 0);
+      if (dm) {
+        if (lane == 0) {
+          __threadfence_block();  // the items' y writes, seen through s_ddone
+          ptx::fence_acq_rel_gpu();
+        }
+        for (uint32_t r = dm; r; r &= r - 1u) {
+          const int v = rb + G * (__ffs(r) - 1), row0 = (v % ntd) * 64;
+          int last = 0;
+          if (lane == 0) {
+            last = atomicAdd(a.ccnt + row0 / 64, 1) == s_ngrp - 1;
+            if (last) ptx::fence_acq_rel_gpu();  // acquires the other items' y
+          }
+          last = __shfl_sync(0xffffffffu, last, 0);
+          __syncwarp();
+          if (last) {
+            // out rows row0 + lane and row0 + 32 + lane: sum over the k slots in rank order
+            float o0 = 0.f, o1 = 0.f;
+            for (int i0 = 0; i0 < a.k; i0 += 8) {
+              float y0[8], y1[8];
+#pragma unroll
+              for (int ii = 0; ii < 8; ++ii) {
+                const int i = i0 + ii;
+                const float *ys = a.y + (int64_t)(i < a.k ? s_inv[i] : 0) * D + row0 + lane;
+                y0[ii] = i < a.k ? __ldcg(ys) : 0.f;
+                y1[ii] = i < a.k ? __ldcg(ys + 32) : 0.f;
+              }
+#pragma unroll
+              for (int ii = 0; ii < 8; ++ii)
+                if (i0 + ii < a.k) {
+                  o0 = fmaf(s_w[i0 + ii], y0[ii], o0);
+                  o1 = fmaf(s_w[i0 + ii], y1[ii], o1);
+                }
+            }
+            a.out[row0 + lane] = o0;
+            a.out[row0 + 32 + lane] = o1;
+          }
+        }
+        dpub |= dm;
+        progress = true;
+      }
+      if (!progress) {
+        if (++polls > (1u << 24)) {
+          record_status(a.hdr, DS4MOE_ETIMEOUT);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    return;
+  }
+  if (w == nbg) {
+    // producer: one item per stage, gate/up units then down items
+    const uint8_t *gate = static_cast<const uint8_t *>(a.L.gate), *up = static_cast<const uint8_t *>(a.L.up);
+    const uint8_t *down = static_cast<const uint8_t *>(a.L.down);
+    const uint32_t cg = t1_copies(tg), cd = t1_copies(td);
+    int st = 0;
+    uint32_t ph = 0;
+    for (int it = 0; it < n; ++it) {
+      if (it >= nstage && !ptx::mbar_wait(&sm.empty[st], ph ^ 1u)) {
+        record_status(a.hdr, DS4MOE_ETIMEOUT);
+        break;
+      }
+      uint8_t *dst = smem + (size_t)st * stage_bytes;
+      if (it < ng) {
+        const int u = (int)blockIdx.x + G * it;
+        const Group grp = s_grp[u / ntg];
+        const int row0 = (u % ntg) * 16;
+        if (lane == 0) ptx::mbar_arrive_expect_tx(&sm.full[st], 32u * tg.rowb);
+        __syncwarp();
+        if ((uint32_t)lane < 2u * cg) {
+          const uint32_t mat = (uint32_t)lane / cg, i = (uint32_t)lane % cg;
+          t1_tile_copy(dst + mat * tile_g, (mat == 0 ? gate : up) + ((int64_t)grp.e * F + row0) * tg.rowb, tg, i,
+                       &sm.full[st]);
+        }
+      } else {
+        const int v = rb + G * (it - ng);
+        const Group grp = s_grp[v / ntd];
+        const int row0 = (v % ntd) * 64;
+        if (lane == 0) ptx::mbar_arrive_expect_tx(&sm.full[st], 64u * td.rowb);
+        __syncwarp();
+        if ((uint32_t)lane < 4u * cd) {
+          const uint32_t tile = (uint32_t)lane / cd, i = (uint32_t)lane % cd;
+          t1_tile_copy(dst + tile * tile_d, down + ((int64_t)grp.e * D + row0 + 16 * (int)tile) * td.rowb, td, i,
+                       &sm.full[st]);
+        }
+      }
+      if (++st == nstage) {
+        st = 0;
+        ph ^= 1u;
+      }
+    }
+    return;
+  }
+  bool timed_out = false;
+  int st = 0, it = 0, cur = -1;
+  uint32_t ph = 0;
+  for (; it < n; ++it) {
+    const bool gu = it < ng;
+    int j, row0;
+    if (gu) {
+      const int u = (int)blockIdx.x + G * it;
+      j = u / ntg;
+      row0 = (u % ntg) * 16;
+    } else {
+      const int v = rb + G * (it - ng);
+      j = v / ntd;
+      row0 = (v % ntd) * 64;
+      if (j != cur) {
+        // h of slot j: wait until the sync warp has seen all of it published
+        uint32_t polls = 0;
+        while (!((*reinterpret_cast<volatile uint32_t *>(&s_hok) >> j) & 1u)) {
+          if (++polls > (1u << 24)) {
+            record_status(a.hdr, DS4MOE_ETIMEOUT);
+            break;
+          }
+          __nanosleep(32);
+        }
+        __threadfence_block();  // this lane's h loads after the sync warp's acquire
+        t1_load_b<false>(B, a.h + (int64_t)s_grp[j].p0 * F + 256 * (w % nbd), g, c);
+        cur = j;
+      }
+    }
+    if (!timed_out && !ptx::mbar_wait(&sm.full[st], ph)) {
+      record_status(a.hdr, DS4MOE_ETIMEOUT);
+      timed_out = true;
+    }
+    float y[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    if (!timed_out) {
+      const uint8_t *sb = smem + (size_t)st * stage_bytes;
+      if (gu) {
+        const uint8_t *const mats[2] = {sb + kQ2KBytes * w, sb + tile_g + kQ2KBytes * w};
+        t1_block<2>(mats, tg, g, B, L, y);
+      } else {
+        const uint8_t *t0 = sb + 2u * (uint32_t)(w / nbd) * tile_d + kQ2KBytes * (w % nbd);
+        const uint8_t *const mats[2] = {t0, t0 + tile_d};
+        t1_block<2>(mats, td, g, B, L, y);
+      }
+    }
+    // partials: [16 m + 8 q + g] (gate/up: m = gate / up; down: m = tile)
+    float *r = sm.red + ((size_t)st * nbg + w) * 32;
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const float v = quad_sum(y[m][q]);
+        if (c == 0) r[16 * m + 8 * q + g] = v;
+      }
+    if (t1_last_arriver(&sm.cnt[st], nbg)) {
+      const Group grp = s_grp[j];
+      const float *rr = sm.red + (size_t)st * nbg * 32 + lane;
+      if (gu) {
+        float sv = 0.f;
+        for (int p = 0; p < nbg; ++p) sv += rr[32 * p];
+        const float us = __shfl_down_sync(0xffffffffu, sv, 16);
+        if (lane < 16) {
+          const float hv = bf16_bits_to_f32(f32_to_bf16_bits(silu(sv) * us));
+          if (fabsf(hv) > 65504.f) record_status(a.hdr, DS4MOE_EDEVICE);
+          uint16_t *hp = a.h + (int64_t)grp.p0 * F + row0 + lane;
+          const uint16_t hb = __half_as_ushort(__float2half_rn(hv));
+#pragma unroll 1
+          for (int jj = 0; jj < grp.nt; ++jj, hp += F) *hp = hb;
+        }
+        // hand the unit to the sync warp
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          atomicOr(&s_done, 1u << it);
+        }
+      } else {
+        // rows row0 + lane (K blocks of warps 0 .. nbd-1) and row0 + 32 + lane
+        float s0 = 0.f, s1 = 0.f;
+        for (int p = 0; p < nbd; ++p) {
+          s0 += rr[32 * p];
+          s1 += rr[32 * (nbd + p)];
+        }
+        float *yp = a.y + (int64_t)grp.p0 * D + row0 + lane;
+#pragma unroll 1
+        for (int jj = 0; jj < grp.nt; ++jj, yp += D) {
+          yp[0] = s0;
+          yp[32] = s1;
+        }
+        // hand the item to the sync warp (it counts it for the combine)
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          atomicOr(&s_ddone, 1u << (it - ng));
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&sm.empty[st]);
+    if (++st == nstage) {
+      st = 0;
+      ph ^= 1u;
+    }
+  }
+  // no copy may still be landing in shared memory when the CTA exits
+  if (timed_out && lane == 0) {
+    for (int jj = it - nstage > 0 ? it - nstage : 0; jj < it; ++jj)
+      ptx::mbar_wait(&sm.full[jj % nstage], (jj / nstage) & 1, 1u << 20);
+  }
+}
+
 // ============================================================ SIMT path
 template <typename In>
 __device__ __forceinline__ void row_dot_q41(const uint8_t *__restrict__ row, int cols, int nt, In in,
@@ -975,6 +1288,36 @@ cudaError_t launch_gate_up_t1(const FfnArgs &a, cudaStream_t s) {
   return launch_pdl(kern, dim3(num_sms()), dim3(32 * (nb + 1)), smem, s, a, nstage);
 }
 
+// The merged single-token grid: Q2_K gate, up and down with d_model = 2 d_ff
+// (<= 4096), d_ff a multiple of 1024, within the single-token chain (the
+// grid ranks the experts itself and the router grid zeroes hready).
+bool t1_merged_ok(const ds4moe_layer &L, int k) {
+  // every CTA tracks its gate/up units and its down items in 32-bit masks
+  return L.q_gate == DS4MOE_Q2_K && L.q_up == DS4MOE_Q2_K && L.q_down == DS4MOE_Q2_K && L.d_model == 2 * L.d_ff &&
+         L.d_ff % 1024 == 0 && L.d_model <= 4096 && L.n_expert <= 256 &&
+         ((int64_t)k * (L.d_ff / 16) + num_sms() - 1) / num_sms() <= 32 &&
+         ((int64_t)k * (L.d_model / 64) + num_sms() - 1) / num_sms() <= 32;
+}
+
+bool t1_merged_path(const FfnArgs &a) {
+  return a.T == 1 && a.lg && a.hready && a.ccnt && t1_merged_ok(a.L, a.k);
+}
+
+cudaError_t launch_ffn_t1(const FfnArgs &a, cudaStream_t s) {
+  const int nbg = a.L.d_model / 256, nbd = a.L.d_ff / 256;
+  const uint32_t tile_g = t1_tile_bytes(t1_tile((uint32_t)(kQ2KBytes * nbg)));
+  const uint32_t tile_d = t1_tile_bytes(t1_tile((uint32_t)(kQ2KBytes * nbd)));
+  const uint32_t stage = 2 * tile_g > 4 * tile_d ? 2 * tile_g : 4 * tile_d;
+  int nstage = 8;
+  while (nstage > 2 && t1_smem_bytes(nstage, stage, nbg) > kT1SmemGateUp) --nstage;
+  const size_t smem = t1_smem_bytes(nstage, stage, nbg);
+  if (smem > kT1SmemGateUp) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(k_ffn_t1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  ProfScope p("ffn_t1", s);
+  return launch_pdl(k_ffn_t1, dim3(num_sms()), dim3(32 * (nbg + 2)), smem, s, a, nstage);
+}
+
 cudaError_t launch_down_t1(const FfnArgs &a, cudaStream_t s) {
   const int nb = a.L.d_ff / 256;
   const uint32_t stage = t1_tile_bytes(t1_tile((uint32_t)(block_bytes(a.L.q_down) * nb)));
@@ -1048,6 +1391,7 @@ cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s) {
   // single token: the sub-block-column kernels where the format allows;
   // both h producers (single-token and multi-token gate/up) write the fp16
   // operand both down kernels read, so they combine freely
+  if (t1_merged_path(a)) return launch_ffn_t1(a, s);
   const bool t1g = a.T == 1 && t1_gate_up_ok(L), t1d = a.T == 1 && t1_down_ok(L);
   if (decode_mma_ok(L) || (t1g && t1d)) {
     const int kp = pick_kp(L.d_model, L.q_gate, L.q_up);
@@ -1075,6 +1419,7 @@ cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s) {
+  if (t1_merged_path(a)) return cudaSuccess;                        // fused into the merged grid
   if (a.cnt && !(a.T == 1 && t1_down_ok(a.L))) return cudaSuccess;  // fused into the down kernel
   const int64_t n4 = (int64_t)a.T * a.L.d_model / 4;
   const int grid = (int)((n4 + 255) / 256 < num_sms() * 16 ? (n4 + 255) / 256 : num_sms() * 16);

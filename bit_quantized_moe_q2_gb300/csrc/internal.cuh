@@ -172,6 +172,10 @@ struct FfnArgs {
   // grid writes idx_out / w and the bucketing outputs
   const float *lg;
   int32_t *idx_out;
+  // merged single-token FFN grid only: per selected expert, the gate/up
+  // units that have published their h (zeroed by the router grid)
+  int32_t *hready;
+  int32_t *ccnt;  // and per 64 output rows, the down items finished (zeroed by the router grid)
   // tensor-core prefill only (nullptr otherwise)
   uint16_t *xp;           // [P][D] x of each sorted pair, fp16
   Chunk *chunks_gu, *chunks_dn;

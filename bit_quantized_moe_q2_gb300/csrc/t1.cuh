@@ -282,7 +282,8 @@ constexpr int kT1MaxGroups = 32;
 // inv[i] of the expert-sorted order.  With `publish` (one CTA of the chain)
 // the warp also writes idx and the softmax weights over the selected (the
 // call's outputs) and the bucketing outputs the later grids read.
-__device__ __forceinline__ void t1_route_warp(const FfnArgs &a, Group *s_grp, int *s_ngrp, bool publish) {
+__device__ __forceinline__ void t1_route_warp(const FfnArgs &a, Group *s_grp, int *s_ngrp, bool publish,
+                                              float *s_lv = nullptr, int *s_inv = nullptr) {
   const int lane = threadIdx.x & 31, E = a.L.n_expert, k = a.k;
   float v[8];
 #pragma unroll
@@ -297,6 +298,10 @@ __device__ __forceinline__ void t1_route_warp(const FfnArgs &a, Group *s_grp, in
   for (int j = 0; j < k; ++j) pos += __shfl_sync(0xffffffffu, my_e, j) < my_e;
   if (lane < k) s_grp[pos] = Group{my_e, pos, 1, 0};
   if (lane == 0) *s_ngrp = k;
+  if (s_lv && lane < k) {
+    s_lv[lane] = my_v;  // slot i's logit and sorted position, for a later warp
+    s_inv[lane] = pos;
+  }
   if (publish) {
     const float wt = softmax_selected_warp(my_v, k);
     if (lane < k) {
@@ -313,6 +318,32 @@ __device__ __forceinline__ void t1_route_warp(const FfnArgs &a, Group *s_grp, in
     }
   }
 }
+// The routing weights (softmax over the k selected logits, by one warp) into
+// s_w, and with `publish` the call's routing outputs, from what
+// t1_route_warp left in shared memory.
+__device__ __forceinline__ void t1_weights_warp(const FfnArgs &a, const Group *s_grp, const float *s_lv,
+                                                const int *s_inv, float *s_w, bool publish) {
+  const int lane = threadIdx.x & 31, k = a.k;
+  const float wt = softmax_selected_warp(lane < k ? s_lv[lane] : 0.f, k);
+  if (lane < k) s_w[lane] = wt;
+  if (publish) {
+    if (lane < k) {
+      const int pos = s_inv[lane];
+      a.idx_out[lane] = s_grp[pos].e;
+      const_cast<float *>(a.w)[lane] = wt;
+      const_cast<int32_t *>(a.inv)[lane] = pos;
+      const_cast<int32_t *>(a.perm)[pos] = lane;
+      const_cast<Group *>(a.groups)[pos] = s_grp[pos];
+    }
+    if (lane == 0) {
+      const_cast<int32_t *>(a.nvalid)[0] = k;
+      a.hdr->n_groups = k;
+      a.hdr->n_active = k;
+    }
+  }
+  __syncwarp();
+}
+
 __device__ __forceinline__ void t1_load_groups(const FfnArgs &a, Group *s_grp, int *s_ngrp) {
   if (threadIdx.x < 32) {
     const int n = __ldcg(&a.hdr->n_groups);

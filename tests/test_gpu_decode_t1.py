@@ -29,6 +29,10 @@ SHAPES = [
     Q2.replace(d_model=2048, d_ff=2048, n_expert=16, k=2, seed=402, bias_sigma=1.0),
     Q2.replace(d_model=4096, d_ff=1024, n_expert=4, k=1, seed=403),
     Q2.replace(d_model=3072, d_ff=2048, n_expert=6, k=3, seed=404),
+    # all Q2_K with d_model = 2 d_ff: the merged gate/up + down grid
+    Q2.replace(d_model=4096, d_ff=2048, n_expert=12, k=6, seed=408),
+    Q2.replace(d_model=2048, d_ff=1024, n_expert=7, k=3, seed=409, bias_sigma=1.0),
+    Q2.replace(d_model=2048, d_ff=1024, n_expert=3, k=1, seed=410),
     # gate/up single-token, down multi-token (d_ff not a multiple of 1024)
     Q2.replace(d_model=1024, d_ff=768, n_expert=5, k=2, seed=405),
     # gate/up multi-token (d_model not a multiple of 1024), down single-token
@@ -70,12 +74,19 @@ def test_single_token_matches_oracle(M, wi):
         out2, idx2, wt2, st2 = gpu_forward(M, dev, x, L.Wr, L.bias, w.k)
         assert st2 == M.DS4MOE_OK and np.array_equal(idx2, ridx)
         assert rel_err(out2, ref) <= TOL
+        # the fused entry (merged grid where the layer allows it) and the
+        # separate kernels do the same arithmetic in the same order
+        if np.array_equal(wt.view(np.uint32), wt2.view(np.uint32)):
+            assert np.array_equal(out.view(np.uint32), out2.view(np.uint32))
         # same inputs, same bits
         out3, _, _, _ = gpu_moe_decode(M, dev, x, L.Wr, L.bias, w.k)
         assert np.array_equal(out3.view(np.uint32), out.view(np.uint32))
 
 
-@pytest.mark.parametrize("wi", [0, 7])
+MERGED = [4, 5, 6]
+
+
+@pytest.mark.parametrize("wi", [0, 4, 5, 10])
 def test_single_token_kernels_are_the_ones_launched(M, wi):
     w = SHAPES[wi]
     L = build_layer(w)
@@ -87,7 +98,11 @@ def test_single_token_kernels_are_the_ones_launched(M, wi):
         names = set(M.ds4moe_profile_read())
     finally:
         M.ds4moe_profile_enable(False)
-    assert {"gate_up", "down"} <= names
+    # the all-Q2_K layers with d_model = 2 d_ff run the merged grid
+    if wi in MERGED:
+        assert "ffn_t1" in names and not {"gate_up", "down"} & names
+    else:
+        assert {"gate_up", "down"} <= names
     assert not {"gate_up_simt", "down_simt"} & names
 
 
