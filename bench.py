@@ -234,11 +234,25 @@ def gate_up_bytes(w: synth.Workload) -> int:
 
 
 # DRAM bytes per launch of the roofline kernel from an ncu capture of the
-# current build (dram__bytes_read.sum + dram__bytes_write.sum); a workload
-# missing here reports null.  The summaries with the commands are in profiles/.
-NCU_TRAFFIC = {
-    "flash-layer-decode-t1-q2k": 33_089_792,  # k_gate_up_t1: 33,089,536 read + 256 written
+# current build (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (workload,
+# kernel); a pair missing here reports null.  The summaries with the commands are in profiles/.
+NCU_TRAFFIC: dict = {
 }
+
+
+def dominant_kernel(prof: dict, w: synth.Workload, uniq_avg: float):
+    """The decode step's dominant kernel in the library's per-kernel timings:
+    the merged single-token FFN grid where it ran (expert weights + x + out
+    per launch), else the gate/up kernel (gate/up weights + x + h).
+    Returns (name, description, algorithmic bytes per launch, total ms, launches)."""
+    T, k, D = w.T, w.k, w.d_model
+    if "ffn_t1" in prof:
+        ms, n = prof["ffn_t1"]
+        return ("ffn_t1", "expert FFN (merged gate/up + SwiGLU + down + combine, dequant fused)",
+                uniq_avg * expert_bytes(w) + T * D * 2 + T * D * 4, ms, n)
+    ms, n = prof.get("gate_up", prof.get("gate_up_simt", (float("nan"), 1)))
+    return ("gate_up", "gate_up (fused dequant GEMV + SwiGLU)",
+            uniq_avg * gate_up_bytes(w) + T * D * 2 + T * k * w.d_ff * 2, ms, n)
 
 
 def measured_peaks():
@@ -477,12 +491,11 @@ def run_ours(args, w: synth.Workload):
     prof = M.ds4moe_profile_read()
     M.ds4moe_profile_enable(False)
     launches_per_step = sum(n for _, n in prof.values()) / kp
-    gu_ms, gu_n = prof.get("gate_up", prof.get("gate_up_simt", (float("nan"), 1)))
-    gu_algo = sum(uniq[i % N_SLOTS] * gate_up_bytes(w) + T * D * 2 + T * k * w.d_ff * 2 for i in range(kp)) / kp
+    kname, kdesc, gu_algo, gu_ms, gu_n = dominant_kernel(prof, w, sum(uniq[i % N_SLOTS] for i in range(kp)) / kp)
     gu_avg_s = gu_ms / gu_n / 1000.0
-    roofline = {"kernel": "gate_up (fused dequant GEMV + SwiGLU)", "bound": "hbm",
+    roofline = {"kernel": kdesc, "bound": "hbm",
                 "achieved": gu_algo / gu_avg_s / 1e9, "peak": peak, "unit": "GB/s",
-                "frac": gu_algo / gu_avg_s / 1e9 / peak, "traffic": NCU_TRAFFIC.get(w.name),
+                "frac": gu_algo / gu_avg_s / 1e9 / peak, "traffic": NCU_TRAFFIC.get((w.name, kname)),
                 "algorithmic_bytes_per_launch": int(gu_algo), "avg_launch_us": gu_avg_s * 1e6,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else
                                "fallback 6.8 TB/s"}
@@ -813,10 +826,9 @@ def run_ours_stack(args, w: synth.Workload):
     M.ds4moe_profile_enable(False)
     launches_per_step = sum(n for _, n in prof.values()) / kp
     kernels = {n: {"avg_us": 1000 * t / c, "launches_per_step": c / kp} for n, (t, c) in prof.items()}
-    gu_ms, gu_n = prof.get("gate_up", prof.get("gate_up_simt", (float("nan"), 1)))
-    gu_algo = (sum(uniq) / L) * gate_up_bytes(w) + T * D * 2 + T * k * w.d_ff * 2
+    kname, kdesc, gu_algo, gu_ms, gu_n = dominant_kernel(prof, w, sum(uniq) / L)
     gu_s = gu_ms / gu_n / 1000.0
-    roofline = {"kernel": "gate_up (fused dequant GEMV + SwiGLU), per layer", "bound": "hbm",
+    roofline = {"kernel": kdesc + ", per layer", "bound": "hbm",
                 "achieved": gu_algo / gu_s / 1e9, "peak": peak, "unit": "GB/s", "frac": gu_algo / gu_s / 1e9 / peak,
                 "traffic": None, "algorithmic_bytes_per_launch": int(gu_algo), "avg_launch_us": gu_s * 1e6,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else
