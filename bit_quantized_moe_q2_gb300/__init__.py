@@ -27,7 +27,7 @@ EXPORTS = (
     "ds4moe_ffn_decode", "ds4moe_ffn_prefill", "ds4moe_stream_status",
     "ds4moe_profile_enable", "ds4moe_profile_count", "ds4moe_profile_entry",
     "ds4moe_ffn_decode_noalloc", "ds4moe_moe_decode", "ds4moe_residual_norm", "ds4moe_stack_decode",
-    "ds4moe_quantize_f32", "ds4moe_route_topk_select_bias",
+    "ds4moe_quantize_f32", "ds4moe_route_topk_select_bias", "ds4moe_debug_sync_wait",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -79,6 +79,7 @@ def lib():
         L.ds4moe_stack_decode.argtypes = [ctypes.POINTER(Layer), ctypes.POINTER(p), ctypes.POINTER(p), i32, i32,
                                           i32, ctypes.c_float, p, p, p, p, p, p, sz, p]
         L.ds4moe_profile_enable.argtypes = [i32]
+        L.ds4moe_debug_sync_wait.argtypes = [i32, i32]
         L.ds4moe_profile_count.argtypes = []
         L.ds4moe_profile_entry.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
                                            ctypes.POINTER(ctypes.c_int64)]
@@ -242,6 +243,13 @@ def ds4moe_ffn_decode_noalloc(layer: Layer, x, idx, w, out, status_out=None, str
     T, k = idx.shape
     _check(lib().ds4moe_ffn_decode_noalloc(ctypes.byref(layer), _ptr(x), _ptr(idx), _ptr(w), T, k, _ptr(out),
                                            _ptr(status_out), _stream(stream)), "ds4moe_ffn_decode_noalloc")
+
+
+def ds4moe_debug_sync_wait(budget_polls: int = 1 << 24, extra_target: int = 0):
+    """Fault-injection hook for failure-detection tests: the poll budget and
+    target offset of the merged single-token grid's cross-CTA h-ready wait
+    (defaults restore normal operation)."""
+    _check(lib().ds4moe_debug_sync_wait(int(budget_polls), int(extra_target)), "ds4moe_debug_sync_wait")
 
 
 def ds4moe_profile_enable(on: bool):

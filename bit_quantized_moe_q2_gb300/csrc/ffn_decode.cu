@@ -750,6 +750,11 @@ __global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
   }
 }
 
+// Poll budget and target offset of the merged grid's h-ready wait (a
+// fault-injection hook for tests: ds4moe_debug_sync_wait).
+__device__ int32_t g_sync_budget = 1 << 24;
+__device__ int32_t g_sync_extra = 0;
+
 // The single-token expert FFN as one persistent grid (Q2_K gate, up and
 // down, d_model = 2 d_ff): one CTA per SM with nbg = d_model / 256 consumer
 // warps and one producer.  Every CTA runs its gate/up units first (16 gate +
@@ -824,7 +829,9 @@ __global__ void __launch_bounds__(18 * 32, 1) k_ffn_t1(FfnArgs a, int nstage) {
     // hand each expert of its down items to the consumers once its h is out
     const uint32_t all = ng >= 32 ? 0xffffffffu : (1u << ng) - 1u;
     const uint32_t dall = nd >= 32 ? 0xffffffffu : (1u << nd) - 1u;
-    uint32_t pub = 0, dpub = 0, polls = 0;
+    uint32_t pub = 0, dpub = 0, polls = 0, hpolls = 0;
+    const uint32_t hbudget = (uint32_t)g_sync_budget;
+    const int32_t htarget = ntg + g_sync_extra;
     int t = 0, prev = -1;
     while (pub != all || t < nd || dpub != dall) {
       bool progress = false;
@@ -845,11 +852,20 @@ __global__ void __launch_bounds__(18 * 32, 1) k_ffn_t1(FfnArgs a, int nstage) {
       if (t < nd) {
         const int j = (rb + G * t) / ntd;
         int ready = 0;
-        if (lane == 0) ready = ptx::ld_acquire(a.hready + j) >= ntg;
+        if (lane == 0) {
+          ready = ptx::ld_acquire(a.hready + j) >= htarget;
+          if (!ready && ++hpolls > hbudget) {
+            // the wait ran out: record it, and hand the expert over anyway
+            // so that the grid still finishes
+            record_status(a.hdr, DS4MOE_ETIMEOUT);
+            ready = 1;
+          }
+        }
         if (__shfl_sync(0xffffffffu, ready, 0)) {
           if (lane == 0) {
             __threadfence_block();
             atomicOr(&s_hok, 1u << j);
+            hpolls = 0;
           }
           prev = j;
           ++t;
@@ -1428,3 +1444,10 @@ cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s) {
 }
 
 }  // namespace ds4
+
+extern "C" ds4moe_status ds4moe_debug_sync_wait(int32_t budget_polls, int32_t extra_target) {
+  if (budget_polls < 1 || extra_target < 0) return DS4MOE_EINVAL;
+  cudaError_t e = cudaMemcpyToSymbol(ds4::g_sync_budget, &budget_polls, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(ds4::g_sync_extra, &extra_target, sizeof(int32_t));
+  return e == cudaSuccess ? DS4MOE_OK : DS4MOE_ECUDA;
+}

@@ -356,6 +356,31 @@ ds4moe_status ds4moe_ffn_decode_noalloc(const ds4moe_layer *L, const uint16_t *x
                                         void *stream);
 
 /*
+ * ds4moe_debug_sync_wait -- HOST, synchronous; a fault-injection hook for
+ * tests of failure detection (no counterpart in the pages).  It applies to
+ * the single-token fused decode on all-Q2_K layers with d_model = 2 d_ff:
+ * ds4moe_moe_decode at T = 1, and each layer of ds4moe_stack_decode.  That
+ * path runs the expert FFN as one grid whose CTAs wait on each other.  Every
+ * CTA waits until all gate/up units of an expert have published h before
+ * its down work on that expert.
+ *
+ * The hook sets, for later calls on the current device, two things about
+ * that wait:
+ *   budget_polls  polls before the wait gives up (default 1 << 24, about a
+ *                 second);
+ *   extra_target  added to the count the wait needs (default 0).
+ * With extra_target > 0 the wait cannot succeed.  It gives up after
+ * budget_polls polls, records DS4MOE_ETIMEOUT in the workspace status word,
+ * and the grid finishes normally, so the CUDA context stays usable.
+ * Restore the defaults with (1 << 24, 0).
+ *
+ * Host errors: EINVAL if budget_polls < 1 or extra_target < 0; ECUDA if the
+ * device copy fails.  Call it only while none of this library's kernels is
+ * running.
+ */
+ds4moe_status ds4moe_debug_sync_wait(int32_t budget_polls, int32_t extra_target);
+
+/*
  * Per-kernel timing (tracing aid).  ds4moe_profile_enable(1) clears the
  * totals and, until ds4moe_profile_enable(0), brackets every kernel the
  * library launches with a pair of CUDA events recorded on the launch stream

@@ -163,3 +163,6 @@ def test_device_entry_points_reject_bad_arguments_before_launch(M):
     assert L.ds4moe_route_topk(fake, fake, None, 0, 4096, 256, 6, fake, fake, None, fake, ws_need, None) == \
         M.DS4MOE_OK
     assert M.ds4moe_workspace_bytes(M.Layer(0, 0, 0, 0, 0, 0, None, None, None), 4, 6) == 0
+    # fault-injection hook: a budget below one poll or a negative offset
+    assert L.ds4moe_debug_sync_wait(0, 0) == M.DS4MOE_EINVAL
+    assert L.ds4moe_debug_sync_wait(100, -1) == M.DS4MOE_EINVAL
