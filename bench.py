@@ -237,8 +237,8 @@ def gate_up_bytes(w: synth.Workload) -> int:
 # current build (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (workload,
 # kernel); a pair missing here reports null.  The summaries with the commands are in profiles/.
 NCU_TRAFFIC: dict = {
-    # k_ffn_t1 (merged single-token FFN grid), mean of two launches: 49,625 KB read + 33 KB written
-    ("flash-layer-decode-t1-q2k", "ffn_t1"): 49_657_472,
+    # k_ffn_t1 (merged single-token FFN grid), mean of three launches: 49.63 MB read + 46 KB written
+    ("flash-layer-decode-t1-q2k", "ffn_t1"): 49_675_008,
 }
 
 
