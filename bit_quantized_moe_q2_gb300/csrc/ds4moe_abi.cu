@@ -668,11 +668,16 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict_
   if (MODE == kRouteLogits && bk.counts && tid == 0) bk.counts[blockIdx.x] = 0;
   if (MODE == kRouteLogits && bk.zero2)
     for (int i = blockIdx.x * 256 + tid; i < bk.nzero2; i += gridDim.x * 256) bk.zero2[i] = 0;
-  if (MODE == kRouteBucket && bk.xs16)
+  // the fp16 copy of x and its block sums for the multi-token FFN kernels,
+  // spread over all CTAs of the router (not the single bucketing CTA)
+  if (MODE != kRouteTopk && bk.xs16)
     convert_x(x, T, D, bk.x16, bk.xs16, bk.xs32, hdr, blockIdx.x * 256 + tid, gridDim.x * 256);
   for (int t0 = 0; t0 < T; t0 += 32) {
     const int nt = min(32, T - t0);
-    for (int tt = 0; tt < nt; ++tt) route_dot2_partial<NI>(x + (int64_t)(t0 + tt) * D, wv, D, tid, ps[wid][tt], pc[wid][tt]);
+    int tt = 0;
+    for (; tt + 4 <= nt; tt += 4)
+      route_dot2_partial_n<NI, 4>(x + (int64_t)(t0 + tt) * D, D, wv, D, tid, &ps[wid][tt], &pc[wid][tt]);
+    for (; tt < nt; ++tt) route_dot2_partial<NI>(x + (int64_t)(t0 + tt) * D, wv, D, tid, ps[wid][tt], pc[wid][tt]);
     __syncthreads();
     if (wid == 0 && lane < nt) logits[(int64_t)(t0 + lane) * E + e] = route_dot2_merge(ps, pc, lane, bias ? bias + e : nullptr);
     __syncthreads();
@@ -957,7 +962,7 @@ BucketArgs bucket_args(const ds4moe_layer &L, void *ws, const WsLayout &lay, con
 ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, const int32_t *idx,
                       const float *w, int32_t T, int32_t k, float *out, void *ws, size_t ws_bytes,
                       void *stream, const float *logits = nullptr, bool bucketed = false,
-                      bool route_t1 = false) {
+                      bool route_t1 = false, bool x_converted = false) {
   ds4moe_status st = check_layer(L);
   if (st != DS4MOE_OK) return st;
   if (T < 0 || k < 1 || k > 32 || k > L->n_expert) return DS4MOE_EINVAL;
@@ -1031,7 +1036,8 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
                    ws_ptr<int32_t>(ws, lay.counts), ws_ptr<int32_t>(ws, lay.offs), ws_ptr<int32_t>(ws, lay.active),
                    ws_ptr<int32_t>(ws, lay.perm), ws_ptr<int32_t>(ws, lay.inv), ws_ptr<int32_t>(ws, lay.lrank),
                    ws_ptr<Group>(ws, lay.groups), x, (int)T, (int)L->d_model, ws_ptr<uint16_t>(ws, lay.x16),
-                   sums ? ws_ptr<uint8_t>(ws, lay.xs16) : nullptr, sums ? ws_ptr<float>(ws, lay.xs32) : nullptr,
+                   sums && !x_converted ? ws_ptr<uint8_t>(ws, lay.xs16) : nullptr,
+                   sums && !x_converted ? ws_ptr<float>(ws, lay.xs32) : nullptr,
                    logits, (int)k, const_cast<float *>(w), ws_ptr<int32_t>(ws, lay.nvalid), out);
   }
   if (e != cudaSuccess) return cuda_status(e);
@@ -1290,12 +1296,19 @@ ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const 
                   : ni <= 2 ? k_route_small<2, kRouteLogits>
                   : ni <= 4 ? k_route_small<4, kRouteLogits>
                             : k_route_small<8, kRouteLogits>;
+      BucketArgs cv{};  // the router grid also converts x for the multi-token kernels
+      if (decode_mma_ok(*L)) {
+        cv.x16 = ws_ptr<uint16_t>(ws, lay.x16);
+        cv.xs16 = ws_ptr<uint8_t>(ws, lay.xs16);
+        cv.xs32 = ws_ptr<float>(ws, lay.xs32);
+      }
       e = launch_pdl(kern, dim3(E), dim3(256), 0, s, x, Wr, bias, (int)T, (int)D, (int)E, (int)k, lg, idx, w,
-                     static_cast<WsHeader *>(ws), BucketArgs{});
+                     static_cast<WsHeader *>(ws), cv);
     }
     if (e != cudaSuccess) return cuda_status(e);
   }
-  return run_ffn(false, L, x, idx, w, T, k, out, ws, ws_bytes, stream, lg, fused);
+  return run_ffn(false, L, x, idx, w, T, k, out, ws, ws_bytes, stream, lg, fused, false,
+                 !fused && decode_mma_ok(*L));
 }
 
 ds4moe_status ds4moe_residual_norm(float *x_res, const float *out, uint16_t *x_next, int32_t T, int32_t d_model,

@@ -67,6 +67,74 @@ __device__ __forceinline__ void route_dot2_partial(const uint16_t *__restrict__ 
   }
 }
 
+// The same partial for NT consecutive tokens (row stride D) at once: every
+// token's arithmetic is exactly route_dot2_partial's, in the same order, but
+// the NT independent load / reduction chains overlap (a CTA ranks a batch of
+// tokens an NT-th of the latency apart).
+template <int NI, int NT>
+__device__ __forceinline__ void route_dot2_partial_n(const uint16_t *__restrict__ xr, int64_t stride,
+                                                     const float4 (&wv)[NI], int D, int tid, float *ps,
+                                                     float *pc) {
+  const int lane = threadIdx.x & 31;
+  float s4[NT][4], c4[NT][4];
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) s4[t][q] = c4[t][q] = 0.f;
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int j = 4 * (tid + 256 * i);
+    if (j < D) {
+      uint2 xv[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) xv[t] = __ldcg(reinterpret_cast<const uint2 *>(xr + t * stride + j));
+      const float ws4[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const float xs[4] = {bf16_bits_to_f32(xv[t].x & 0xFFFFu), bf16_bits_to_f32(xv[t].x >> 16),
+                             bf16_bits_to_f32(xv[t].y & 0xFFFFu), bf16_bits_to_f32(xv[t].y >> 16)};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float p, pe, se;
+          two_prod(xs[q], ws4[q], p, pe);
+          two_sum(s4[t][q], p, s4[t][q], se);
+          c4[t][q] = __fadd_rn(c4[t][q], __fadd_rn(pe, se));
+        }
+      }
+    }
+  }
+  float s[NT], c[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    s[t] = s4[t][0];
+    c[t] = __fadd_rn(c4[t][0], __fadd_rn(c4[t][1], __fadd_rn(c4[t][2], c4[t][3])));
+#pragma unroll
+    for (int q = 1; q < 4; ++q) {
+      float se;
+      two_sum(s[t], s4[t][q], s[t], se);
+      c[t] = __fadd_rn(c[t], se);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float so = __shfl_xor_sync(0xffffffffu, s[t], off);
+      const float co = __shfl_xor_sync(0xffffffffu, c[t], off);
+      float se;
+      two_sum(s[t], so, s[t], se);
+      c[t] = __fadd_rn(c[t], __fadd_rn(co, se));
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      ps[t] = s[t];
+      pc[t] = c[t];
+    }
+  }
+}
+
 // Merge of the eight warp partials of column `col` (+ bias), rounded once.
 __device__ __forceinline__ float route_dot2_merge(const float (*ps)[32], const float (*pc)[32], int col,
                                                   const float *bias_e) {
