@@ -284,8 +284,18 @@ __global__ void __launch_bounds__(512) k_gate_up_mma(FfnArgs a, int kp, uint32_t
     const int4 v = __ldcg(reinterpret_cast<const int4 *>(a.groups + u / ntile));
     return Group{v.x, v.y, v.z, v.w};
   };
-  auto issue = [&](int u, int st) {
-    const Group grp = load_group(u);
+  // Every warp of the CTA works on the same unit, so the units' groups and
+  // token ids live in a small shared ring: the group of unit it + 3 is
+  // fetched during iteration it and its token ids during it + 1, so neither
+  // dependent global load sits on a unit's critical path.
+  __shared__ Group s_gq[4];
+  __shared__ int s_tq[4][kGroup];  // token of pair p0 + j of the slot's group
+  const int G = gridDim.x;
+  auto tokens_of = [&](int slot, int j) {  // token id of pair j of the slot's group (-1 past its end)
+    const Group gr = s_gq[slot];
+    return j < gr.nt ? __ldcg(a.perm + gr.p0 + j) / a.k : -1;
+  };
+  auto issue = [&](int u, int st, const Group &grp) {
     const int row0 = (u % ntile) * 16;
     if (lane == 0) ptx::mbar_arrive_expect_tx(&mybar[st], stage_bytes);
     __syncwarp();
@@ -295,13 +305,28 @@ __global__ void __launch_bounds__(512) k_gate_up_mma(FfnArgs a, int kp, uint32_t
 
   uint32_t phase = 0u;  // bit st: parity of stage st
   int u = blockIdx.x;
-  if (u < U) issue(u, 0);
-  if (u + (int)gridDim.x < U) issue(u + gridDim.x, 1);
+  // ring invariant at the top of iteration it: groups of units it .. it + 2
+  // and token ids of units it, it + 1 are in slots (it + i) & 3
+  if (threadIdx.x < 3 && u + G * (int)threadIdx.x < U) s_gq[threadIdx.x] = load_group(u + G * (int)threadIdx.x);
+  __syncthreads();
+  if (threadIdx.x < 2 * kGroup && u + G * (int)(threadIdx.x / kGroup) < U)
+    s_tq[threadIdx.x / kGroup][threadIdx.x % kGroup] = tokens_of(threadIdx.x / kGroup, threadIdx.x % kGroup);
+  __syncthreads();
+  if (u < U) issue(u, 0, s_gq[0]);
+  if (u + G < U) issue(u + G, 1, s_gq[1]);
   bool timed_out = false;
-  for (int it = 0; u < U; u += gridDim.x, ++it) {
-    const int st = it & 1;
-    const Group grp = load_group(u);
+  for (int it = 0; u < U; u += G, ++it) {
+    const int st = it & 1, sl = it & 3;
+    const Group grp = s_gq[sl];
     const int row0 = (u % ntile) * 16;
+    // prefetch (stored after this unit's arithmetic): thread 0 the group of
+    // unit it + 3, threads 32 .. 32 + kGroup - 1 the token ids of unit it + 2
+    Group gpre{};
+    int tpre = -1;
+    const bool pre_g = threadIdx.x == 0 && u + 3 * G < U;
+    const bool pre_t = threadIdx.x >= 32 && threadIdx.x < 32 + kGroup && u + 2 * G < U;
+    if (pre_g) gpre = load_group(u + 3 * G);
+    if (pre_t) tpre = tokens_of((it + 2) & 3, (int)threadIdx.x - 32);
     if (!timed_out && !ptx::mbar_wait(&mybar[st], (phase >> st) & 1u)) {
       record_status(a.hdr, DS4MOE_ETIMEOUT);
       timed_out = true;
@@ -312,12 +337,12 @@ __global__ void __launch_bounds__(512) k_gate_up_mma(FfnArgs a, int kp, uint32_t
     const uint8_t *sums = nullptr;
     const float *xs_a = nullptr, *xs_b = nullptr;
     if (g < grp.nt) {
-      const int t = __ldcg(a.perm + grp.p0 + g) / a.k;
+      const int t = s_tq[sl][g];
       xb = a.x16 + (int64_t)t * D + k0;
       sums = a.xs16 + ((int64_t)t * (D / 256 + 1) + k0 / 256) * 64;
     }
-    if (2 * c < grp.nt) xs_a = a.xs32 + (int64_t)(__ldcg(a.perm + grp.p0 + 2 * c) / a.k) * (D / 32) + k0 / 32;
-    if (2 * c + 1 < grp.nt) xs_b = a.xs32 + (int64_t)(__ldcg(a.perm + grp.p0 + 2 * c + 1) / a.k) * (D / 32) + k0 / 32;
+    if (2 * c < grp.nt) xs_a = a.xs32 + (int64_t)s_tq[sl][2 * c] * (D / 32) + k0 / 32;
+    if (2 * c + 1 < grp.nt) xs_b = a.xs32 + (int64_t)s_tq[sl][2 * c + 1] * (D / 32) + k0 / 32;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (!timed_out) {
       const uint8_t *buf = wbuf + (size_t)st * stage_bytes;
@@ -325,10 +350,13 @@ __global__ void __launch_bounds__(512) k_gate_up_mma(FfnArgs a, int kp, uint32_t
       else tile_rows<QG>(buf, ch, kvals / 256, xb, sums, xs_a, xs_b, kl, g, c, acc);
     }
     __syncwarp();
-    if (u + 2 * (int)gridDim.x < U && !timed_out) issue(u + 2 * gridDim.x, st);
+    if (u + 2 * G < U && !timed_out) issue(u + 2 * G, st, s_gq[(it + 2) & 3]);
     float *r = red + ((size_t)w * 32 + lane) * 4;
 #pragma unroll
     for (int i = 0; i < 4; ++i) r[i] = acc[i];
+    // slot (it + 3) & 3 held unit it - 1, which no warp reads any more
+    if (pre_g) s_gq[(it + 3) & 3] = gpre;
+    if (pre_t) s_tq[(it + 2) & 3][threadIdx.x - 32] = tpre;
     __syncthreads();
     if (w == 0) {
       float gs[4] = {0.f, 0.f, 0.f, 0.f}, us[4] = {0.f, 0.f, 0.f, 0.f};
