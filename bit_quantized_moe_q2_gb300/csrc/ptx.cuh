@@ -106,24 +106,6 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
 }
-// Same with the A operand in TMEM (M rows on lanes, K packed two fp16 per
-// 32-bit column), B from shared memory.
-__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-// Warp-wide store of 16 TMEM columns: thread i writes lane (taddr.lane + i),
-// columns taddr.col .. +15.  tmem_wait_st() waits for this thread's stores.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-               : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Arrive on `bar` once every previously issued tcgen05.mma of this thread
 // has completed.
@@ -159,15 +141,12 @@ __device__ __forceinline__ void tmem_ld32x2_wait(uint32_t ta, uint32_t tb, uint3
 // has completed and its writes are visible (a no-op without the launch
 // attribute); allow the next grid to be scheduled.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-// GPU-scope acquire-release fence, relaxed add, release add and acquire load
-// of a counter in global memory (a fence followed by relaxed adds releases
-// everything ordered before the fence).
+// GPU-scope acquire-release fence, relaxed add and acquire load of a counter
+// in global memory (a fence followed by relaxed adds releases everything
+// ordered before the fence).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ void red_relaxed_add(int32_t *p, int32_t v) {
   asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void red_release_add(int32_t *p, int32_t v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ int32_t ld_acquire(const int32_t *p) {
   int32_t v;
@@ -180,21 +159,8 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
 // Plain C++ loads so the compiler can schedule them; the mbarrier wait's
 // memory clobber keeps shared-memory reads after the copy completes.
 __device__ __forceinline__ uint32_t lds32(const void *p) { return *static_cast<const uint32_t *>(p); }
-__device__ __forceinline__ uint2 ldg_nc_v2(const void *p) { return __ldg(static_cast<const uint2 *>(p)); }
-// L2-only loads for data written by the preceding grid of a dependent launch.
-__device__ __forceinline__ uint2 ldcg_v2(const void *p) { return __ldcg(static_cast<const uint2 *>(p)); }
-__device__ __forceinline__ uint4 ldcg_v4(const void *p) { return __ldcg(static_cast<const uint4 *>(p)); }
 
 // ------------------------------------------------------------------ math
-// D += A * B, m16n8k16, bf16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 // D += A * B, m16n8k16, fp16 inputs, fp32 accumulate.
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
@@ -217,13 +183,6 @@ __device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-// Packed bf16x2 fused multiply-add, one rounding per lane.
-__device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
 
