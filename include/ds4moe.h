@@ -258,10 +258,14 @@ ds4moe_status ds4moe_ffn_prefill(const ds4moe_layer *L, const uint16_t *x,
  * ds4moe_moe_decode -- DEVICE.  One decode step of a routed-MoE layer in
  * one call: ds4moe_route_topk followed by ds4moe_ffn_decode, with the same
  * results (idx / w are written as outputs), but scheduled as one chain of
- * kernels: the router's ranking runs inside the bucketing kernel and the
- * weighted combine inside the down projection.  Same arguments and
- * constraints as those two calls; `ws` must hold
- * ds4moe_workspace_bytes(L, T, k, 0) bytes.
+ * kernels.  Up to 32 (token, expert) pairs, the router's last CTA ranks and
+ * buckets; beyond that the router grid also converts x for the FFN kernels
+ * and the bucketing kernel ranks.  The weighted combine runs inside the
+ * down projection.  At T = 1, the router grid writes only the logits and
+ * the FFN grids rank the experts themselves.  On all-Q2_K layers with
+ * d_model = 2 d_ff, one grid then runs gate/up, SwiGLU, down and the
+ * combine.  Same arguments and constraints as those two calls; `ws` must
+ * hold ds4moe_workspace_bytes(L, T, k, 0) bytes.
  */
 ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const float *Wr,
                                 const float *bias, int32_t T, int32_t k, float *out,
