@@ -59,6 +59,9 @@ def _L():
         lib.orc_q2k_pack.argtypes = [p, p, p, p, p, i64, p]
         lib.orc_q2k_unpack.argtypes = [p, i64, p, p, p, p, p]
         lib.orc_q2k_dequant.argtypes = [p, i64, p]
+        lib.orc_q2k_to_r16.argtypes = [p, i64, i64, p]
+        lib.orc_q2k_from_r16.argtypes = [p, i64, i64, p]
+        lib.orc_r16_dequant.argtypes = [p, i64, i64, p]
         lib.orc_dequant.argtypes = [i32, p, i64, p]
         lib.orc_router_logits.argtypes = [p, p, p, i32, i32, i32, p]
         lib.orc_topk_softmax.argtypes = [p, i32, i32, i32, p, p]
@@ -185,6 +188,36 @@ def q2k_unpack(blocks):
     _L().orc_q2k_unpack(blocks.ctypes.data, nb, codes.ctypes.data, sc.ctypes.data, mn.ctypes.data,
                         d.ctypes.data, dmin.ctypes.data)
     return codes, sc, mn, d, dmin
+
+
+def q2k_to_r16(blocks, rows: int, cols: int) -> np.ndarray:
+    """Plain Q2_K matrix bytes (rows x cols values) -> the 16-row tile order."""
+    src = _c(blocks, np.uint8)
+    out = np.zeros(src.size, dtype=np.uint8)
+    st = _L().orc_q2k_to_r16(_ptr(src), rows, cols, _ptr(out))
+    if st != OK:
+        raise ValueError(f"q2k_to_r16: status {st}")
+    return out
+
+
+def q2k_from_r16(blocks, rows: int, cols: int) -> np.ndarray:
+    """The inverse of q2k_to_r16."""
+    src = _c(blocks, np.uint8)
+    out = np.zeros(src.size, dtype=np.uint8)
+    st = _L().orc_q2k_from_r16(_ptr(src), rows, cols, _ptr(out))
+    if st != OK:
+        raise ValueError(f"q2k_from_r16: status {st}")
+    return out
+
+
+def r16_dequant(blocks, rows: int, cols: int) -> np.ndarray:
+    """fp32 values [rows, cols] of a tile-order matrix, read in place."""
+    src = _c(blocks, np.uint8)
+    out = np.zeros((rows, cols), dtype=np.float32)
+    st = _L().orc_r16_dequant(_ptr(src), rows, cols, _ptr(out))
+    if st != OK:
+        raise ValueError(f"r16_dequant: status {st}")
+    return out
 
 
 def dequant(qtype: int, blocks, n_values: int) -> np.ndarray:

@@ -23,8 +23,7 @@
  *           (bits and group are explicit), "텐서 이름과 KV 메타데이터" (ne[0]
  *           is the input dimension; row-major [out, in] equals block order).
  *
- * Readings where the pages are silent or truncated (each also listed in
- * the design doc): the 4th term of the Q2_K packing expression is the 6-bit shift
+ * Readings where the pages are silent or truncated: the 4th term of the Q2_K packing expression is the 6-bit shift
  * of value l+96; the low nibble of a Q2_K scale byte is the scale and the
  * high nibble the min; the min is subtracted; router scoring is a plain
  * dot product (+ optional bias) with a softmax over the k selected experts;
@@ -251,6 +250,98 @@ static float q2k_value(const uint8_t *blk, int i) {
 void orc_q2k_dequant(const uint8_t *blocks, int64_t nb, float *out) {
   for (int64_t b = 0; b < nb; ++b)
     for (int i = 0; i < 256; ++i) out[256 * b + i] = q2k_value(blocks + 84 * b, i);
+}
+
+/* ------------------------------------------- Q2_K in the 16-row tile order
+ * A storage order of this library's own (the pages give none): the bytes of
+ * the Q2_K blocks above, permuted within every 16-row x 256-column
+ * tile-block of a matrix (rows % 16 == 0, cols % 256 == 0).  The tile-block
+ * of rows 16t .. 16t+15 and block column b keeps the 1344 bytes the plain
+ * layout gives those 16 blocks: byte offset (16t) * row_bytes + b * 1344.
+ * For row r (r8 = r mod 8, upper = r >= 8) and value i of the block
+ * (sub-block s = i / 16, v = i mod 16, half h = s / 8, m = s mod 8):
+ *   the code sits in the 32-bit little-endian word at
+ *     512 h + 16 (4 r8 + m mod 4) + 4 (2 (m >= 4) + upper),
+ *   at bit 16 (v mod 2) + 2 (v / 2);
+ *   the scale byte of (r, s) is byte (s >= 8) + 2 (s mod 2) of the word at
+ *     1024 + 8 (4 r8 + (s mod 8) / 2) + 4 upper;
+ *   row r's d and dmin (block bytes 80 .. 83) are bytes 1280 + 4 r .. +3. */
+
+static int64_t r16_code_word(int r, int i) {
+  const int s = i / 16, h = s / 8, m = s % 8;
+  return 512 * h + 16 * (4 * (r % 8) + m % 4) + 4 * (2 * (m >= 4) + (r >= 8));
+}
+static int r16_code_bit(int i) { return 16 * ((i % 16) % 2) + 2 * ((i % 16) / 2); }
+static int64_t r16_scale_byte(int r, int s) {
+  return 1024 + 8 * (4 * (r % 8) + (s % 8) / 2) + 4 * (r >= 8) + (s >= 8) + 2 * (s % 2);
+}
+
+static int r16_shape_ok(int64_t rows, int64_t cols) {
+  return rows >= 0 && cols >= 0 && rows % 16 == 0 && cols % 256 == 0;
+}
+
+/* Plain Q2_K blocks -> tile order, one value (and one scale byte) at a time. */
+int orc_q2k_to_r16(const uint8_t *src, int64_t rows, int64_t cols, uint8_t *dst) {
+  if (!r16_shape_ok(rows, cols)) return ORC_EINVAL;
+  const int64_t nb = cols / 256, rowb = nb * 84;
+  memset(dst, 0, (size_t)(rows * rowb));
+  for (int64_t t = 0; t < rows / 16; ++t)
+    for (int64_t b = 0; b < nb; ++b) {
+      uint8_t *tile = dst + 16 * t * rowb + 1344 * b;
+      for (int r = 0; r < 16; ++r) {
+        const uint8_t *blk = src + (16 * t + r) * rowb + 84 * b;
+        for (int i = 0; i < 256; ++i) {
+          const int q = (blk[16 + q2k_qs_index(i)] >> q2k_qs_shift(i)) & 3;
+          const int64_t wo = r16_code_word(r, i);
+          const int bit = r16_code_bit(i);
+          tile[wo + bit / 8] |= (uint8_t)(q << (bit % 8));
+        }
+        for (int n = 0; n < 16; ++n) tile[r16_scale_byte(r, n)] = blk[n];
+        for (int j = 0; j < 4; ++j) tile[1280 + 4 * r + j] = blk[80 + j];
+      }
+    }
+  return ORC_OK;
+}
+
+/* The inverse: tile order -> plain Q2_K blocks. */
+int orc_q2k_from_r16(const uint8_t *src, int64_t rows, int64_t cols, uint8_t *dst) {
+  if (!r16_shape_ok(rows, cols)) return ORC_EINVAL;
+  const int64_t nb = cols / 256, rowb = nb * 84;
+  memset(dst, 0, (size_t)(rows * rowb));
+  for (int64_t t = 0; t < rows / 16; ++t)
+    for (int64_t b = 0; b < nb; ++b) {
+      const uint8_t *tile = src + 16 * t * rowb + 1344 * b;
+      for (int r = 0; r < 16; ++r) {
+        uint8_t *blk = dst + (16 * t + r) * rowb + 84 * b;
+        for (int i = 0; i < 256; ++i) {
+          const int64_t wo = r16_code_word(r, i);
+          const int bit = r16_code_bit(i);
+          const int q = (tile[wo + bit / 8] >> (bit % 8)) & 3;
+          blk[16 + q2k_qs_index(i)] |= (uint8_t)(q << q2k_qs_shift(i));
+        }
+        for (int n = 0; n < 16; ++n) blk[n] = tile[r16_scale_byte(r, n)];
+        for (int j = 0; j < 4; ++j) blk[80 + j] = tile[1280 + 4 * r + j];
+      }
+    }
+  return ORC_OK;
+}
+
+/* Value (row, column) of a tile-order matrix read in place: the same value
+ * the plain block gives, d * sc * q - dmin * mn rounded once to fp32. */
+int orc_r16_dequant(const uint8_t *src, int64_t rows, int64_t cols, float *out) {
+  if (!r16_shape_ok(rows, cols)) return ORC_EINVAL;
+  const int64_t nb = cols / 256, rowb = nb * 84;
+  for (int64_t row = 0; row < rows; ++row)
+    for (int64_t col = 0; col < cols; ++col) {
+      const int r = (int)(row % 16), i = (int)(col % 256);
+      const uint8_t *tile = src + (row - r) * rowb + 1344 * (col / 256);
+      const int bit = r16_code_bit(i);
+      const int q = (tile[r16_code_word(r, i) + bit / 8] >> (bit % 8)) & 3;
+      const int sb = tile[r16_scale_byte(r, i / 16)];
+      const double d = orc_f16(get16(tile + 1280 + 4 * r)), dmin = orc_f16(get16(tile + 1282 + 4 * r));
+      out[row * cols + col] = (float)(d * (double)(sb & 15) * (double)q - dmin * (double)(sb >> 4));
+    }
+  return ORC_OK;
 }
 
 /* ------------------------------------------------------------------ Q4_K
@@ -730,8 +821,8 @@ double orc_weighted_sq_error(int qtype, const float *x, const float *importance,
   return s;
 }
 
-/* Routing variant with the bias used for selection only (SURVEY next-row
- * reading, DeepSeek-style): experts are ranked by the biased logit
+/* Routing variant with the bias used for selection only (the DeepSeek-style
+ * reading of a selection bias): experts are ranked by the biased logit
  * lb = fp32(x . Wr_e + bias_e) (ties to the lower id, NaN lowest), and the
  * weights are the softmax of the selected experts' unbiased logits
  * lu = fp32(x . Wr_e), shifted by their maximum, summed in rank order in
