@@ -17,8 +17,9 @@ LIB_PATH = os.path.join(_HERE, "libds4moe.so")
 
 DS4MOE_OK, DS4MOE_EINVAL, DS4MOE_EBLOCKER, DS4MOE_EUNSUPPORTED = 0, 1, 2, 3
 DS4MOE_ECUDA, DS4MOE_ETIMEOUT, DS4MOE_EDEVICE, DS4MOE_ESPACE = 4, 5, 6, 7
-DS4MOE_Q4_1, DS4MOE_Q2_K, DS4MOE_IQ2_XXS, DS4MOE_Q4_K = 1, 2, 3, 4
-QTYPES = {"q4_1": DS4MOE_Q4_1, "q2_k": DS4MOE_Q2_K, "iq2_xxs": DS4MOE_IQ2_XXS, "q4_k": DS4MOE_Q4_K}
+DS4MOE_Q4_1, DS4MOE_Q2_K, DS4MOE_IQ2_XXS, DS4MOE_Q4_K, DS4MOE_Q2_K_R16 = 1, 2, 3, 4, 5
+QTYPES = {"q4_1": DS4MOE_Q4_1, "q2_k": DS4MOE_Q2_K, "iq2_xxs": DS4MOE_IQ2_XXS, "q4_k": DS4MOE_Q4_K,
+          "q2_k_r16": DS4MOE_Q2_K_R16}
 
 # Every symbol include/ds4moe.h declares.
 EXPORTS = (
@@ -28,6 +29,7 @@ EXPORTS = (
     "ds4moe_profile_enable", "ds4moe_profile_count", "ds4moe_profile_entry",
     "ds4moe_ffn_decode_noalloc", "ds4moe_moe_decode", "ds4moe_residual_norm", "ds4moe_stack_decode",
     "ds4moe_quantize_f32", "ds4moe_route_topk_select_bias", "ds4moe_debug_sync_wait",
+    "ds4moe_repack", "ds4moe_profile_span",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -64,6 +66,8 @@ def lib():
         L.ds4moe_status_string.restype = ctypes.c_char_p
         L.ds4moe_quantize_ref.argtypes = [i32, i32, i32, p, p, p, p, p, i64, p, sz]
         L.ds4moe_dequant.argtypes = [i32, p, i64, p, p]
+        L.ds4moe_repack.argtypes = [i32, i32, p, i64, i64, p, p]
+        L.ds4moe_profile_span.argtypes = [i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
         L.ds4moe_quantize_f32.argtypes = [i32, p, p, i64, i64, p, ctypes.c_size_t, p, ctypes.c_size_t, p]
         L.ds4moe_workspace_bytes.argtypes = [ctypes.POINTER(Layer), i32, i32, i32]
         L.ds4moe_workspace_bytes.restype = sz
@@ -149,6 +153,21 @@ def ds4moe_quantize_ref(out_type, bits, group, codes, scale_f16, min_f16, sub_sc
 
 def ds4moe_dequant(qtype, blocks, n_values, out, stream=None):
     _check(lib().ds4moe_dequant(qtype, _ptr(blocks), n_values, _ptr(out), _stream(stream)), "ds4moe_dequant")
+
+
+def ds4moe_repack(src_type, dst_type, src, rows, cols, dst, stream=None):
+    """Rewrite a Q2_K matrix (rows x cols values, device uint8 tensors) between
+    the plain block layout and the 16-row tile order, either way."""
+    _check(lib().ds4moe_repack(src_type, dst_type, _ptr(src), int(rows), int(cols), _ptr(dst), _stream(stream)),
+           "ds4moe_repack")
+
+
+def ds4moe_profile_span(on: int = -1):
+    """(total_ns, launches) of the device-side span record so far; on = 1 / 0
+    then clears it and switches recording on / off (-1: read only)."""
+    ns, n = ctypes.c_double(), ctypes.c_int64()
+    _check(lib().ds4moe_profile_span(int(on), ctypes.byref(ns), ctypes.byref(n)), "ds4moe_profile_span")
+    return ns.value, n.value
 
 
 def ds4moe_quantize_f32(qtype, x, importance, out, ws, cols=None, stream=None):

@@ -931,11 +931,18 @@ __global__ void __launch_bounds__(kNormThreads) k_residual_norm(float *__restric
 }
 
 // ------------------------------------------------------------- validation
+// All three matrices in the 16-row tile order (the single-token kernel's
+// weights; no other path reads that order).
+inline bool layer_r16(const ds4moe_layer &L) {
+  return L.q_gate == DS4MOE_Q2_K_R16 && L.q_up == DS4MOE_Q2_K_R16 && L.q_down == DS4MOE_Q2_K_R16;
+}
+
 ds4moe_status check_layer(const ds4moe_layer *L) {
   if (!L) return DS4MOE_EINVAL;
   if (L->q_gate == DS4MOE_IQ2_XXS || L->q_up == DS4MOE_IQ2_XXS || L->q_down == DS4MOE_IQ2_XXS)
     return DS4MOE_EUNSUPPORTED;
-  if (!qtype_ok(L->q_gate) || !qtype_ok(L->q_up) || !qtype_ok(L->q_down)) return DS4MOE_EUNSUPPORTED;
+  if (!layer_r16(*L) && (!qtype_ok(L->q_gate) || !qtype_ok(L->q_up) || !qtype_ok(L->q_down)))
+    return DS4MOE_EUNSUPPORTED;
   if (L->d_model <= 0 || L->d_ff <= 0 || L->n_expert < 1 || L->n_expert > 1024) return DS4MOE_EINVAL;
   if (L->d_model % block_vals(L->q_gate) || L->d_model % block_vals(L->q_up) ||
       L->d_ff % block_vals(L->q_down) || L->d_ff % 16 || L->d_model % 16)
@@ -971,6 +978,7 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
   if (!x || !idx || !w || !out || !ws) return DS4MOE_EINVAL;
   if (!aligned16(x) || !aligned16(idx) || !aligned16(w) || !aligned16(out) || !aligned16(ws))
     return DS4MOE_EINVAL;
+  if (layer_r16(*L) && (prefill || T != 1 || !t1r_ok(*L, k))) return DS4MOE_EUNSUPPORTED;
   const WsLayout lay = ws_layout(*L, T, k, prefill);
   if (ws_bytes < lay.total) return DS4MOE_ESPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -994,6 +1002,24 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
   a.xs32 = ws_ptr<float>(ws, lay.xs32);
   a.hs16 = ws_ptr<uint8_t>(ws, lay.hs16);
   a.nvalid = ws_ptr<int32_t>(ws, lay.nvalid);
+  if (layer_r16(*L)) {
+    // one token over the tile-order weights: one grid does gate/up, SwiGLU,
+    // down and the combine; it ranks the experts from the router's logits
+    // or reads the caller's idx / w.  Its per-slot h-ready counters and
+    // per-64-row combine counters start at zero (the fused router zeroes
+    // them; here they are cleared first).
+    a.lg = route_t1 ? logits : nullptr;
+    a.idx_out = const_cast<int32_t *>(idx);
+    a.hready = ws_ptr<int32_t>(ws, lay.counts);
+    a.ccnt = ws_ptr<int32_t>(ws, lay.cnt);
+    cudaError_t e = cudaSuccess;
+    if (!route_t1) {
+      e = cudaMemsetAsync(a.hready, 0, sizeof(int32_t) * (size_t)k, s);
+      if (e == cudaSuccess) e = cudaMemsetAsync(a.ccnt, 0, sizeof(int32_t) * (size_t)(L->d_model / 64), s);
+    }
+    if (e == cudaSuccess) e = launch_ffn_t1r(a, s);
+    return cuda_status(e);
+  }
   const bool tc = prefill && prefill_tc_ok(*L);
   if (tc) {
     a.xp = ws_ptr<uint16_t>(ws, lay.xp);
@@ -1090,6 +1116,25 @@ ds4moe_status ds4moe_dequant(int32_t qtype, const void *blocks, int64_t n_values
   else
     k_dequant_q4k<<<grid, threads, 0, s>>>(static_cast<const uint8_t *>(blocks), nb, out);
   return cuda_status(cudaGetLastError());
+}
+
+ds4moe_status ds4moe_repack(int32_t src_type, int32_t dst_type, const void *src, int64_t rows, int64_t cols,
+                            void *dst, void *stream) {
+  const bool to = src_type == DS4MOE_Q2_K && dst_type == DS4MOE_Q2_K_R16;
+  const bool from = src_type == DS4MOE_Q2_K_R16 && dst_type == DS4MOE_Q2_K;
+  if (!to && !from) return DS4MOE_EUNSUPPORTED;
+  if (rows < 0 || cols < 0 || rows % 16 || cols % 256) return DS4MOE_EINVAL;
+  if (rows == 0 || cols == 0) return DS4MOE_OK;
+  if (!src || !dst || !aligned16(src) || !aligned16(dst)) return DS4MOE_EINVAL;
+  const int64_t bytes = rows * (cols / 256) * kQ2KBytes;
+  const char *a = static_cast<const char *>(src), *b = static_cast<const char *>(dst);
+  if (a < b + bytes && b < a + bytes) return DS4MOE_EINVAL;  // overlapping
+  return cuda_status(launch_repack(to, src, dst, rows, cols, static_cast<cudaStream_t>(stream)));
+}
+
+ds4moe_status ds4moe_profile_span(int32_t on, double *total_ns, int64_t *launches) {
+  if (on < -1 || on > 1) return DS4MOE_EINVAL;
+  return cuda_status(t1r_span_control(on, total_ns, launches));
 }
 
 size_t ds4moe_workspace_bytes(const ds4moe_layer *L, int32_t T, int32_t k, int32_t prefill) {
@@ -1251,7 +1296,9 @@ ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const 
     return DS4MOE_EINVAL;
   const WsLayout lay = ws_layout(*L, T, k, 0);
   if (ws_bytes < lay.total) return DS4MOE_ESPACE;
-  if (T > 256 || E > 256 || D > 8192 || D % 8) {
+  const bool r16 = layer_r16(*L);
+  if (r16 && (T != 1 || !t1r_ok(*L, k))) return DS4MOE_EUNSUPPORTED;
+  if (!r16 && (T > 256 || E > 256 || D > 8192 || D % 8)) {
     // the two-call path gives the same results for shapes the fused router does not cover
     st = ds4moe_route_topk(x, Wr, bias, T, D, E, k, idx, w, nullptr, ws, ws_bytes, stream);
     if (st != DS4MOE_OK) return st;
@@ -1259,7 +1306,7 @@ ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const 
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float *lg = ws_ptr<float>(ws, lay.logits);
-  if (T == 1 && t1_chain_ok(*L)) {
+  if (T == 1 && (r16 || t1_chain_ok(*L))) {
     // one token on the single-token kernels: the router grid only writes the
     // logits, and every CTA of the FFN grids ranks the experts itself (no
     // grid waits on one CTA's ranking)
@@ -1332,6 +1379,7 @@ ds4moe_status ds4moe_stack_decode(const ds4moe_layer *layers, const float *const
     const ds4moe_status st = check_layer(&layers[l]);
     if (st != DS4MOE_OK) return st;
     if (layers[l].d_model != layers[0].d_model || !Wr[l] || k > layers[l].n_expert) return DS4MOE_EINVAL;
+    if (layer_r16(layers[l]) && (T != 1 || !t1r_ok(layers[l], k))) return DS4MOE_EUNSUPPORTED;
     if (ws_bytes < ws_layout(layers[l], T, k, 0).total) return DS4MOE_ESPACE;
   }
   if (T == 0) return DS4MOE_OK;

@@ -1477,5 +1477,6 @@ extern "C" ds4moe_status ds4moe_debug_sync_wait(int32_t budget_polls, int32_t ex
   if (budget_polls < 1 || extra_target < 0) return DS4MOE_EINVAL;
   cudaError_t e = cudaMemcpyToSymbol(ds4::g_sync_budget, &budget_polls, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemcpyToSymbol(ds4::g_sync_extra, &extra_target, sizeof(int32_t));
+  if (e == cudaSuccess) e = ds4::t1r_set_sync_hook(budget_polls, extra_target);
   return e == cudaSuccess ? DS4MOE_OK : DS4MOE_ECUDA;
 }

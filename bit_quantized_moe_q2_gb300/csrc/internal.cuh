@@ -17,11 +17,16 @@ constexpr int kQ41Vals = 32, kQ41Bytes = 20;
 constexpr int kQ2KVals = 256, kQ2KBytes = 84;
 constexpr int kQ4KVals = 256, kQ4KBytes = 144;
 
+// The 16-row tile order of Q2_K keeps its 84 bytes per 256 values.
 __host__ __device__ inline int block_vals(int q) {
-  return q == DS4MOE_Q4_1 ? kQ41Vals : q == DS4MOE_Q2_K ? kQ2KVals : q == DS4MOE_Q4_K ? kQ4KVals : 0;
+  return q == DS4MOE_Q4_1 ? kQ41Vals
+         : (q == DS4MOE_Q2_K || q == DS4MOE_Q2_K_R16) ? kQ2KVals
+         : q == DS4MOE_Q4_K ? kQ4KVals : 0;
 }
 __host__ __device__ inline int block_bytes(int q) {
-  return q == DS4MOE_Q4_1 ? kQ41Bytes : q == DS4MOE_Q2_K ? kQ2KBytes : q == DS4MOE_Q4_K ? kQ4KBytes : 0;
+  return q == DS4MOE_Q4_1 ? kQ41Bytes
+         : (q == DS4MOE_Q2_K || q == DS4MOE_Q2_K_R16) ? kQ2KBytes
+         : q == DS4MOE_Q4_K ? kQ4KBytes : 0;
 }
 
 // Q4_K sub-block j's 6-bit scale and min from the 12 packed bytes.
@@ -194,6 +199,14 @@ __device__ __forceinline__ void clear_combine_counters(const FfnArgs &a, int tid
 }
 
 cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s);
+// Single-token FFN over DS4MOE_Q2_K_R16 weights (ffn_t1r.cu): the layer
+// shapes it takes, its launch, the repacking kernels, the fault-injection
+// hook of its h-ready wait and its device-side span record.
+bool t1r_ok(const ds4moe_layer &L, int k);
+cudaError_t launch_ffn_t1r(const FfnArgs &a, cudaStream_t s);
+cudaError_t launch_repack(bool to_r16, const void *src, void *dst, int64_t rows, int64_t cols, cudaStream_t s);
+cudaError_t t1r_set_sync_hook(int32_t budget, int32_t extra);
+cudaError_t t1r_span_control(int on, double *total_ns, int64_t *launches);
 cudaError_t launch_ffn_prefill(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s);
 bool decode_mma_ok(const ds4moe_layer &L);

@@ -51,6 +51,22 @@ class DeviceLayer:
         return make_layer(self.d_model, self.d_ff, self.n_expert, self.q_gate, self.q_up, self.q_down,
                           self.gate, self.up, self.down)
 
+    def repacked_r16(self) -> "DeviceLayer":
+        """A copy of an all-Q2_K layer with every matrix in the 16-row tile
+        order (ds4moe_repack), for the single-token decode kernel."""
+        import torch
+        from . import DS4MOE_Q2_K, DS4MOE_Q2_K_R16, ds4moe_repack
+        assert self.q_gate == self.q_up == self.q_down == DS4MOE_Q2_K, "repacking takes Q2_K matrices"
+        out = {}
+        for name, rows, cols in (("gate", self.d_ff, self.d_model), ("up", self.d_ff, self.d_model),
+                                 ("down", self.d_model, self.d_ff)):
+            src = getattr(self, name)
+            dst = torch.empty_like(src)
+            ds4moe_repack(DS4MOE_Q2_K, DS4MOE_Q2_K_R16, src, self.n_expert * rows, cols, dst)
+            out[name] = dst
+        return DeviceLayer(self.d_model, self.d_ff, self.n_expert, DS4MOE_Q2_K_R16, DS4MOE_Q2_K_R16,
+                           DS4MOE_Q2_K_R16, out["gate"], out["up"], out["down"])
+
     def weight_bytes_per_expert(self) -> int:
         return (matrix_bytes(self.q_gate, self.d_ff, self.d_model) + matrix_bytes(self.q_up, self.d_ff, self.d_model)
                 + matrix_bytes(self.q_down, self.d_model, self.d_ff))

@@ -71,7 +71,7 @@ typedef enum {
                         y = d*sc*q - dmin*mn  ([DS4-2] layout table and packing) */
   DS4MOE_IQ2_XXS = 3, /* named by [DS4-2]; its grid codebook is not given there:
                         every entry point returns DS4MOE_EUNSUPPORTED */
-  DS4MOE_Q4_K = 4    /* 256 values in 144 bytes ([DS4-2] type table; the layout
+  DS4MOE_Q4_K = 4,   /* 256 values in 144 bytes ([DS4-2] type table; the layout
                         is the standard k-quant reading): fp16 d @0, fp16 dmin
                         @2, scales[12] @4, qs[128] @16.  Sub-block j = values
                         32j..32j+31: j < 4: sc = s[j] & 63, mn = s[j+4] & 63;
@@ -80,6 +80,25 @@ typedef enum {
                         (l < 32): low nibble of qs[32c+l]; 64c+32+l: its high
                         nibble.  y = d*sc*q - dmin*mn.  Dequant and the FFN
                         entry points (SIMT kernels) take it. */
+  DS4MOE_Q2_K_R16 = 5 /* the Q2_K blocks above in a 16-row tile order, made by
+                        ds4moe_repack: the same 84 bytes per 256 values and the
+                        same values, each 16-row x 256-column tile-block of a
+                        matrix keeping the 16 x 84 bytes the plain layout gives
+                        it, permuted inside (lane L = 4g + c, rows g, g+8):
+                        [0,1024) codes, half h of lane L at 512h + 16L as four
+                        words (row g, sub-block 8h+c), (g+8, 8h+c), (g, 8h+c+4),
+                        (g+8, 8h+c+4), value v of a sub-block at bit
+                        16(v&1) + 2(v>>1); [1024,1280) scale bytes, lane L at
+                        1024 + 8L: per row g, g+8 the word s[2c] | s[2c+8]<<8 |
+                        s[2c+1]<<16 | s[2c+9]<<24; [1280,1344) row r's d, dmin
+                        at 1280 + 4r.  Matrices need rows % 16 == 0.  Taken by
+                        the single-token decode (ds4moe_moe_decode,
+                        ds4moe_ffn_decode and ds4moe_ffn_decode_noalloc at T = 1,
+                        ds4moe_stack_decode at T = 1) when gate, up and down are
+                        all in this order and d_model = 2 d_ff, d_model a
+                        multiple of 512 up to 4096; everything else returns
+                        DS4MOE_EUNSUPPORTED (ds4moe_dequant included: repack to
+                        DS4MOE_Q2_K first). */
 } ds4moe_qtype;
 
 /* One routed-MoE layer's expert weights (device pointers, 16-byte aligned). */
@@ -160,6 +179,23 @@ ds4moe_status ds4moe_quantize_ref(int32_t out_type, int32_t bits, int32_t group,
 ds4moe_status ds4moe_quantize_f32(int32_t qtype, const float *x, const float *importance, int64_t n_values,
                                   int64_t cols, void *out, size_t out_bytes, void *ws, size_t ws_bytes,
                                   void *stream);
+
+/*
+ * ds4moe_repack -- DEVICE, asynchronous on `stream`.  Rewrites a Q2_K matrix
+ * between the plain block layout (DS4MOE_Q2_K) and the 16-row tile order
+ * (DS4MOE_Q2_K_R16) above, in either direction: (src_type, dst_type) =
+ * (DS4MOE_Q2_K, DS4MOE_Q2_K_R16) or the reverse.  A bijection on the bytes:
+ * every value, scale and d / dmin is kept, so repacking back gives the input
+ * bit for bit.  [DS4-2]'s layout table and qs packing define the values; the
+ * tile order is this library's (it lets a tensor-core lane read its 64 codes
+ * with one 16-byte load), not the pages'.
+ * src, dst: device, 16-byte aligned, rows * cols / 256 * 84 bytes each, not
+ * overlapping.  rows % 16 == 0 and cols % 256 == 0; an experts-major [E][R][C]
+ * tensor is rows = E * R.  Host errors: EINVAL (sizes, NULL or misaligned
+ * pointers, src == dst), EUNSUPPORTED (any other pair of formats).
+ */
+ds4moe_status ds4moe_repack(int32_t src_type, int32_t dst_type, const void *src, int64_t rows,
+                            int64_t cols, void *dst, void *stream);
 
 /*
  * ds4moe_dequant -- DEVICE.  Decodes n_values values of `blocks` (device,
@@ -348,7 +384,10 @@ ds4moe_status ds4moe_stream_status(void *ws, void *stream);
  * host threads without ordering) race on the array: order them on one
  * stream.  The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) and caches it; make that first call before any
- * stream capture.
+ * stream capture.  The cached address belongs to the device's primary
+ * context: after cudaDeviceReset (or anything else that destroys that
+ * context) it is stale, so do not call this entry point again on that
+ * device in the same process.
  *
  * status_out: optional device int32; receives this call's device status
  * (0 or DS4MOE_EDEVICE for an expert id out of range), asynchronously.
@@ -398,6 +437,19 @@ ds4moe_status ds4moe_profile_enable(int32_t on);
 int32_t ds4moe_profile_count(void);
 ds4moe_status ds4moe_profile_entry(int32_t i, const char **name, double *total_ms,
                                    int64_t *launches);
+
+/*
+ * Device-side kernel spans (tracing aid).  ds4moe_profile_span(on, ...)
+ * reads the totals recorded so far into total_ns / launches (either may be
+ * NULL); with on = 1 or 0 it then clears them and switches recording on or
+ * off for later launches on the current device (on = -1: read only).  While
+ * on, the single-token FFN grid over DS4MOE_Q2_K_R16 weights records, per
+ * launch, %globaltimer from the first CTA past its grid-dependency wait to
+ * the last CTA's exit -- a kernel's duration inside a replayed CUDA graph,
+ * where events cannot bracket it.  Call it only while none of this
+ * library's kernels is running.
+ */
+ds4moe_status ds4moe_profile_span(int32_t on, double *total_ns, int64_t *launches);
 
 #ifdef __cplusplus
 }
