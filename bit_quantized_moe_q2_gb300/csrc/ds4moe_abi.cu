@@ -551,6 +551,8 @@ struct BucketArgs {
   float *out;
   int32_t *zero2;  // single-token chain: further counters the router grid zeroes
   int nzero2;
+  int32_t *zero3;  // and the tagged hidden words of the tile-order grid
+  int nzero3;
 };
 
 // Bucketing of a decode batch (P <= 32 pairs) by a CTA of 256 threads
@@ -668,6 +670,8 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict_
   if (MODE == kRouteLogits && bk.counts && tid == 0) bk.counts[blockIdx.x] = 0;
   if (MODE == kRouteLogits && bk.zero2)
     for (int i = blockIdx.x * 256 + tid; i < bk.nzero2; i += gridDim.x * 256) bk.zero2[i] = 0;
+  if (MODE == kRouteLogits && bk.zero3)
+    for (int i = blockIdx.x * 256 + tid; i < bk.nzero3; i += gridDim.x * 256) bk.zero3[i] = 0;
   // the fp16 copy of x and its block sums for the multi-token FFN kernels,
   // spread over all CTAs of the router (not the single bucketing CTA)
   if (MODE != kRouteTopk && bk.xs16)
@@ -1010,11 +1014,10 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
     // them; here they are cleared first).
     a.lg = route_t1 ? logits : nullptr;
     a.idx_out = const_cast<int32_t *>(idx);
-    a.hready = ws_ptr<int32_t>(ws, lay.counts);
     a.ccnt = ws_ptr<int32_t>(ws, lay.cnt);
     cudaError_t e = cudaSuccess;
     if (!route_t1) {
-      e = cudaMemsetAsync(a.hready, 0, sizeof(int32_t) * (size_t)k, s);
+      e = cudaMemsetAsync(a.h, 0, sizeof(int32_t) * (size_t)k * (size_t)L->d_ff, s);
       if (e == cudaSuccess) e = cudaMemsetAsync(a.ccnt, 0, sizeof(int32_t) * (size_t)(L->d_model / 64), s);
     }
     if (e == cudaSuccess) e = launch_ffn_t1r(a, s);
@@ -1320,6 +1323,10 @@ ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const 
     zero.counts = ws_ptr<int32_t>(ws, lay.counts);  // one counter per expert, zeroed by CTA e
     zero.zero2 = ws_ptr<int32_t>(ws, lay.cnt);       // the merged grid's combine counters
     zero.nzero2 = (D + 63) / 64;
+    if (r16) {  // the tile-order grid's hidden words: every call starts them untagged
+      zero.zero3 = ws_ptr<int32_t>(ws, lay.h);
+      zero.nzero3 = k * L->d_ff;
+    }
     const cudaError_t e = launch_pdl(kern, dim3(E), dim3(256), 0, s, x, Wr, bias, (int)T, (int)D, (int)E, (int)k, lg,
                                      idx, w, static_cast<WsHeader *>(ws), zero);
     if (e != cudaSuccess) return cuda_status(e);

@@ -102,7 +102,10 @@ inline WsLayout ws_layout(const ds4moe_layer &L, int T, int k, int prefill) {
   w.xs16 = o;    o += align256((size_t)T * (size_t)(L.d_model / 256 + 1) * 64);
   w.xs32 = o;    o += align256(sizeof(float) * (size_t)T * (size_t)(L.d_model / 32 + 1));
   w.hs16 = o;    o += align256(P * (size_t)(L.d_ff / 256 + 1) * 64);
-  w.h = o;       o += align256(sizeof(uint16_t) * P * (size_t)L.d_ff);
+  // h: bf16 per element; the tile-order single-token grid stores each as a
+  // tagged 32-bit word
+  const bool r16 = L.q_gate == DS4MOE_Q2_K_R16;
+  w.h = o;       o += align256((r16 ? sizeof(uint32_t) : sizeof(uint16_t)) * P * (size_t)L.d_ff);
   w.y = o;       o += align256(sizeof(float) * P * (size_t)L.d_model);
   w.nvalid = o;  o += align256(sizeof(int32_t) * (size_t)T);
   w.cnt = o;     o += align256(sizeof(int32_t) * (size_t)T * (size_t)(L.d_model / 16));

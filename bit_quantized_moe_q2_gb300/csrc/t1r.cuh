@@ -73,17 +73,19 @@ __device__ __forceinline__ uint32_t r16_pack_h2(float lo, float hi) {
   return (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
 }
 
-// src: the block's 256 activations as bf16 bit patterns (device memory;
-// read through L2).  Lane (g, c) owns sub-block g of each half when g == c
-// (b0) or g == c + 4 (b1); every lane reads sub-block 8h + g so that the
-// block maximum is a plain warp reduction.
+// src: the block's 256 activations as bf16 bit patterns, in device memory
+// (read through L2) or, with SMEM, in shared memory.  Lane (g, c) owns
+// sub-block g of each half when g == c (b0) or g == c + 4 (b1); every lane
+// reads sub-block 8h + g so that the block maximum is a plain warp reduction.
+template <bool SMEM = false>
 __device__ __forceinline__ void r16_load_b(R16B &B, const uint16_t *__restrict__ src, int g, int c) {
   float v[2][16];
   float mx = 0.f;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const uint4 q0 = __ldcg(reinterpret_cast<const uint4 *>(src + 16 * (8 * h + g)));
-    const uint4 q1 = __ldcg(reinterpret_cast<const uint4 *>(src + 16 * (8 * h + g)) + 1);
+    const uint4 *p = reinterpret_cast<const uint4 *>(src + 16 * (8 * h + g));
+    const uint4 q0 = SMEM ? p[0] : __ldcg(p);
+    const uint4 q1 = SMEM ? p[1] : __ldcg(p + 1);
     const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
     for (int i = 0; i < 16; ++i) {

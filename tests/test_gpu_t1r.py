@@ -242,3 +242,23 @@ def test_r16_full_flash_layer(M):
         ridx, rw, _ = oracle.route(x, L.Wr, L.bias, w.k)
         assert np.array_equal(idx, ridx)
         assert rel_err(out, oracle_out(L, x, ridx, rw)) <= TOL
+
+
+@pytest.mark.parametrize("case", ["all_tie", "tie_nan"])
+def test_r16_routing_ties_and_nan(M, case):
+    """Every CTA ranks the logits itself: exact ties go to the lower expert
+    id, a NaN logit ranks below every number."""
+    w = SHAPES[1]
+    L = build_layer(w)
+    dev = _r16(L)
+    x = synth.activations(w, T=1)
+    Wr = np.repeat(L.Wr[:1], w.n_expert, axis=0).copy()  # every logit equal
+    if case == "tie_nan":
+        Wr[4] = L.Wr[4] * 3.0   # one distinct expert
+        Wr[0, 0] = np.nan       # expert 0: NaN logit
+    ridx, rw, _ = oracle.route(x, Wr, None, w.k)
+    out, idx, wt, st = gpu_moe_decode(M, dev, x, Wr, None, w.k)
+    assert st == M.DS4MOE_OK
+    assert np.array_equal(idx, ridx)
+    assert ulp_diff_f32(wt, rw).max() <= 2
+    assert rel_err(out, oracle_out(L, x, ridx, rw)) <= TOL
