@@ -4,27 +4,35 @@ combine) on one GB300, through the libds4moe C ABI.
 
 Workload (default): one DeepSeek-V4-Flash-shaped routed-MoE layer at decode
 batch 1 -- d_model 4096, d_ff 2048, 256 experts, top-6 with a softmax over
-the selected, gate/up/down all Q2_K, synthetic seeded weights and tokens.
-A step is one pass of the whole path over one token.  Weights are
-replicated into 8 device copies and tokens come from 16 pre-staged slots;
-step i uses copy i % 8 and slot i % 16, so consecutive steps never re-read
-bytes still resident in L2 (8 copies x 2.1 GB >> 129 MB of L2).
+the selected, gate/up/down all Q2_K, synthetic seeded weights and tokens --
+with the Q2_K weights repacked once at load into the 16-row tile order
+(DS4MOE_Q2_K_R16: the same bytes permuted, see include/ds4moe.h).  A step is
+one pass of the whole path over one token.  Weights are replicated into 8
+device copies and tokens come from 16 pre-staged slots; step i uses copy
+i % 8 and slot i % 16, so consecutive steps never re-read bytes still
+resident in L2 (8 copies x 2.1 GB >> 129 MB of L2).
 
 Printed JSON line: tokens/s (value), weight-stream GB/s and its fraction of
-the measured HBM peak, the dominant kernel's roofline (gate/up GEMV, timed
-with CUDA events on its launch stream), the CPU oracle as a baseline, the
-end-to-end number through the C ABI with host buffers, and SM clocks sampled
-during the timed region.
+the measured HBM peak, the dominant kernel's roofline (its average device
+span per launch, %globaltimer at grid entry and exit, over CUDA-graph
+replays of the timed steps), per-kernel spans, the CPU oracle as a
+baseline, the end-to-end number through the C ABI with host buffers, SM
+clocks sampled during the timed region (with a one-second soak of the same
+replays where the region is too short to sample), and sub-records, each
+with its own roofline: the same layer on plain Q2_K blocks, the 4096-token
+prefill chunk (TFLOP/s against the sustained bf16 peak) and the 43-layer
+stack at T = 1 (tile order).
 
-`--workload 3` times the prefill chunk instead: 4096 tokens per step (router
+`--workload 3` times the prefill chunk alone: 4096 tokens per step (router
 with bias, top-6 of 256, Q4_1 gate/up, Q2_K down) through ds4moe_route_topk +
 ds4moe_ffn_prefill, reported as tokens/s and TFLOP/s with the tensor-core
 roofline of the gate/up grouped GEMM.
 
-`--workload 4` times the 43-layer decode stack (every layer with its own
-router and 256 Q2_K experts, 91 GB resident; residual in fp32, each layer fed
-bf16 of the RMS-normalised residual) through ds4moe_stack_decode, one CUDA graph per step; the
-weights are generated on all host cores into shared memory, layer by layer.
+`--workload 4` times the 43-layer decode stack alone (every layer with its
+own router and 256 Q2_K experts, 91 GB resident; residual in fp32, each
+layer fed bf16 of the RMS-normalised residual) through ds4moe_stack_decode,
+one CUDA graph per step; the weights are generated on all host cores into
+shared memory, layer by layer (`--r16` repacks them to the tile order).
 
 `--impl reference` times the CPU oracle itself (the program the CUDA path is
 checked against) on the same metric, each step a bounded sample.
@@ -50,6 +58,8 @@ import synth  # noqa: E402
 N_COPIES = 8
 N_SLOTS = 16
 METRIC = "routed-MoE tokens/s"
+R16_LAYOUT = "q2_k in the 16-row tile order (DS4MOE_Q2_K_R16, repacked once at load by ds4moe_repack)"
+PLAIN_LAYOUT = "q2_k plain block layout"
 CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -76,6 +86,12 @@ def parse_args(argv=None):
                          "with per-column importance)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's tokens per step (smaller cases for profiler captures)")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="default workload: skip the sub-records (plain Q2_K layer, prefill chunk, 43-layer stack)")
+    ap.add_argument("--r16", action="store_true",
+                    help="single-layer or stack decode at T = 1: repack Q2_K weights into the 16-row tile order")
+    ap.add_argument("--plain", action="store_true",
+                    help="workload 1 alone on plain Q2_K blocks (no sub-records)")
     return ap.parse_args(argv)
 
 
@@ -111,35 +127,31 @@ def barrier(world: int):
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons."""
+    """nvidia-smi sampling of SM clocks and throttle reasons (every 20 ms, read
+    by a background thread); region() reports the samples inside the latest
+    window between mark(True) and mark(False), and nothing else."""
 
     def __init__(self, gpu_index: int, period_ms: int = 20):
         self.cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
                     "-i", str(gpu_index), "-lms", str(period_ms)]
         self.proc = None
+        self.rows = []
         self.t0 = self.t1 = None
+        self.thread = None
 
     def start(self):
+        import threading
         try:
             self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
         time.sleep(0.3)
 
-    def mark(self, begin: bool):
-        if begin:
-            self.t0 = datetime.now()
-        else:
-            self.t1 = datetime.now()
-
-    def stop(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        time.sleep(0.1)
-        self.proc.terminate()
-        out, _ = self.proc.communicate(timeout=10)
-        rows = []
-        for line in out.splitlines():
+    def _read(self):
+        for line in self.proc.stdout:
             f = [c.strip() for c in line.split(",")]
             if len(f) < 10:
                 continue
@@ -147,18 +159,41 @@ class ClockSampler:
                 ts = datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
             except ValueError:
                 continue
-            rows.append((ts, f))
-        inside = [f for ts, f in rows if self.t0 and self.t1 and self.t0 <= ts <= self.t1]
-        use = inside if inside else [f for _, f in rows]
-        sm = [float(f[2]) for f in use if f[2].replace(".", "").isdigit()]
-        smax = [float(f[3]) for f in use if f[3].replace(".", "").isdigit()]
+            self.rows.append((ts, f))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0, self.t1 = datetime.now(), None
+        else:
+            self.t1 = datetime.now()
+
+    def region(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples_in_region": 0}
+        time.sleep(0.1)  # the samples of the window's last period
+        inside = [f for ts, f in list(self.rows) if self.t0 and self.t1 and self.t0 <= ts <= self.t1]
+        region_ms = (self.t1 - self.t0).total_seconds() * 1000.0 if self.t0 and self.t1 else None
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in region"],
+                    "samples_in_region": 0, "region_ms": region_ms}
+        sm = [float(f[2]) for f in inside if f[2].replace(".", "").isdigit()]
+        smax = [float(f[3]) for f in inside if f[3].replace(".", "").isdigit()]
         reasons = set()
-        for f in use:
+        for f in inside:
             for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), f[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(use), "samples_in_region": len(inside)}
+                "reasons": sorted(reasons), "samples_in_region": len(inside), "region_ms": region_ms}
+
+    def close(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=10)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
 
 
 # --------------------------------------------------------------- workload
@@ -234,27 +269,13 @@ def gate_up_bytes(w: synth.Workload) -> int:
 
 
 # DRAM bytes per launch of the roofline kernel from an ncu capture of the
-# current build (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (workload,
-# kernel); a pair missing here reports null.  The summaries with the commands are in profiles/.
+# current build (dram__bytes_read.sum + dram__bytes_write.sum), keyed by
+# (workload, weight layout, kernel); a key missing here reports null.  The summaries with the commands are in profiles/.
 NCU_TRAFFIC: dict = {
-    # k_ffn_t1 (merged single-token FFN grid), mean of three launches: 49.63 MB read + 46 KB written
-    ("flash-layer-decode-t1-q2k", "ffn_t1"): 49_675_008,
+    # k_ffn_t1r, mean of three launches (49.63 MB read + 22 KB written), captured on the
+    # 32-expert case of the same shape: a launch processes the same 6 experts' matrices
+    ("flash-layer-decode-t1-q2k", R16_LAYOUT, "ffn_t1r"): 49_657_088,
 }
-
-
-def dominant_kernel(prof: dict, w: synth.Workload, uniq_avg: float):
-    """The decode step's dominant kernel in the library's per-kernel timings:
-    the merged single-token FFN grid where it ran (expert weights + x + out
-    per launch), else the gate/up kernel (gate/up weights + x + h).
-    Returns (name, description, algorithmic bytes per launch, total ms, launches)."""
-    T, k, D = w.T, w.k, w.d_model
-    if "ffn_t1" in prof:
-        ms, n = prof["ffn_t1"]
-        return ("ffn_t1", "expert FFN (merged gate/up + SwiGLU + down + combine, dequant fused)",
-                uniq_avg * expert_bytes(w) + T * D * 2 + T * D * 4, ms, n)
-    ms, n = prof.get("gate_up", prof.get("gate_up_simt", (float("nan"), 1)))
-    return ("gate_up", "gate_up (fused dequant GEMV + SwiGLU)",
-            uniq_avg * gate_up_bytes(w) + T * D * 2 + T * k * w.d_ff * 2, ms, n)
 
 
 def measured_peaks():
@@ -388,8 +409,7 @@ def workload_config(w: synth.Workload, n_copies: int = N_COPIES) -> dict:
 
 
 # --------------------------------------------------------------- our arm
-def run_ours(args, w: synth.Workload):
-    import torch
+def init_dist(torch):
     rank, world, local = dist_env()
     if world > 1:
         import torch.distributed as dist
@@ -397,17 +417,127 @@ def run_ours(args, w: synth.Workload):
         dist.init_process_group("nccl")
     else:
         torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def load_library(rank, world):
     from bit_quantized_moe_q2_gb300 import _build
     if rank == 0 or world == 1:
         _build.build()
     barrier(world)
     import bit_quantized_moe_q2_gb300 as M
-    from bit_quantized_moe_q2_gb300.device import check_status, workspace
+    return M
 
-    dev = device_layer(w, M, torch)
-    n_copies = max(1, args.copies)
-    copies = [dev] + [type(dev)(dev.d_model, dev.d_ff, dev.n_expert, dev.q_gate, dev.q_up, dev.q_down,
-                                dev.gate.clone(), dev.up.clone(), dev.down.clone()) for _ in range(n_copies - 1)]
+
+def gpu_index(local: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis.replace(",", "").isdigit():
+        return int(vis.split(",")[local])
+    return local
+
+
+def timed_replays(torch, stream, replay, steps, world, sampler):
+    """Exactly `steps` calls of replay(i) between a barrier + synchronize on
+    each side, timed with CUDA events on `stream`; max over ranks (ms)."""
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.mark(True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            replay(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    barrier(world)
+    return reduce_max(ev0.elapsed_time(ev1), world)
+
+
+def clock_soak(torch, stream, replay, sampler, step_ms: float, seconds: float = 1.0) -> dict:
+    """The same replays for about `seconds` right after a timed region too
+    short for the sampler (nothing of it is timed): the clocks under this load."""
+    n = int(max(1, min(200_000, seconds * 1000.0 / max(step_ms, 1e-4))))
+    torch.cuda.synchronize()
+    sampler.mark(True)
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            replay(i)
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    return {"steps": n}
+
+
+def measure_clocks(torch, stream, replay, gpu: int, steps: int, world: int):
+    """Times the region (returns ms) and samples SM clocks during it; where the
+    region is shorter than the sampling period, a one-second soak of the same
+    replays follows and is reported beside it."""
+    sampler = ClockSampler(gpu)
+    sampler.start()
+    ms = timed_replays(torch, stream, replay, steps, world, sampler)
+    clocks = sampler.region()
+    if clocks["samples_in_region"] == 0:
+        soak = clock_soak(torch, stream, replay, sampler, ms / max(steps, 1))
+        soak.update(sampler.region())
+        clocks["soak"] = soak
+    sampler.close()
+    return ms, clocks
+
+
+def span_pass(M, torch, stream, replay, n: int) -> dict:
+    """Per-kernel device spans (ds4moe_profile_span, %globaltimer at grid
+    entry and exit) over n replays: {kernel: {avg_us, launches_per_step}}."""
+    torch.cuda.synchronize()
+    M.ds4moe_profile_span(1)
+    try:
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                replay(i)
+        stream.synchronize()
+        sp = M.ds4moe_profile_span(0)
+    finally:
+        M.ds4moe_profile_span(0)
+    return {k: {"avg_us": ns / c / 1000.0, "launches_per_step": c / n} for k, (ns, c) in sp.items()}
+
+
+def launch_count(M, torch, stream, eager_step, n: int) -> dict:
+    """Kernels launched per step, by name, from the library's launch record
+    over n eager steps (the counts only: eager event times include host gaps)."""
+    torch.cuda.synchronize()
+    M.ds4moe_profile_enable(True)
+    try:
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                eager_step(i)
+        stream.synchronize()
+        prof = M.ds4moe_profile_read()
+    finally:
+        M.ds4moe_profile_enable(False)
+    return {k: c / n for k, (_, c) in prof.items()}
+
+
+def hbm_roofline(kdesc: str, algo_bytes: float, avg_us: float, traffic) -> dict:
+    peak, kind = measured_peaks()
+    gbs = algo_bytes / (avg_us * 1e-6) / 1e9
+    return {"kernel": kdesc, "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+            "traffic": traffic, "algorithmic_bytes_per_launch": int(algo_bytes), "avg_launch_us": avg_us,
+            "timing": "device span per launch (%globaltimer, first CTA past its dependency wait to last warp "
+                      "exit) over CUDA-graph replays of the timed steps",
+            "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if kind == "measured" else "fallback 6.8 TB/s"}
+
+
+def replicate(dev, n: int):
+    return [dev] + [type(dev)(dev.d_model, dev.d_ff, dev.n_expert, dev.q_gate, dev.q_up, dev.q_down,
+                              dev.gate.clone(), dev.up.clone(), dev.down.clone()) for _ in range(n - 1)]
+
+
+def decode_layer_record(args, M, torch, w: synth.Workload, copies, layout: str, rank: int, world: int, local: int,
+                        with_e2e: bool) -> dict:
+    """One layer's decode steps (route + FFN) through ds4moe_moe_decode, one CUDA
+    graph per step position; copy i % len(copies), token slot i % N_SLOTS."""
+    from bit_quantized_moe_q2_gb300.device import check_status, workspace
+    dev = copies[0]
+    n_copies = len(copies)
     Wr, bias = synth.router(w)
     Wr_d = torch.from_numpy(Wr).cuda()
     b_d = None if bias is None else torch.from_numpy(bias).cuda()
@@ -422,147 +552,91 @@ def run_ours(args, w: synth.Workload):
 
     def step(i, s=None):
         j = i % N_SLOTS
-        c = copies[i % n_copies]
-        M.ds4moe_moe_decode(c.abi, xs[j], Wr_d, b_d, k, out[j], idx[j], wt[j], ws, s)
+        M.ds4moe_moe_decode(copies[i % n_copies].abi, xs[j], Wr_d, b_d, k, out[j], idx[j], wt[j], ws, s)
 
     with torch.cuda.stream(stream):
         for i in range(2 * N_SLOTS):
-            step(i)
+            step(i, stream)
     check_status(ws, stream)
-    # per-slot unique experts (algorithmic bytes)
     uniq = [len(set(idx[j].cpu().numpy().ravel().tolist())) for j in range(N_SLOTS)]
-
-    # one CUDA graph per step position (slot j uses copy j % N_COPIES)
     graphs = []
     for j in range(N_SLOTS):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            step(j)
+            step(j, stream)
         graphs.append(g)
 
+    def replay(i):
+        graphs[i % N_SLOTS].replay()
+
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            graphs[i % N_SLOTS].replay()
+        for i in range(max(args.warmup, 3)):
+            replay(i)
     stream.synchronize()
     check_status(ws, stream)
-
-    # ---- timed region: exactly K steps
-    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
-        if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local
-    sampler = ClockSampler(gpu_index)
-    sampler.start()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    sampler.mark(True)
-    ev0.record(stream)
-    with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            graphs[i % N_SLOTS].replay()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    sampler.mark(False)
-    barrier(world)
-    clocks = sampler.stop()
-    ms = reduce_max(ev0.elapsed_time(ev1), world)
+    ms, clocks = measure_clocks(torch, stream, replay, gpu_index(local), args.steps, world)
     check_status(ws, stream)
-
     tokens = world * args.steps * T
-    value = tokens / (ms / 1000.0)
-    ms_per_step = ms / args.steps
     eb = expert_bytes(w)
     algo_step = [u * eb + Wr.nbytes + (0 if bias is None else bias.nbytes) + T * D * 2 + T * D * 4 for u in uniq]
     algo_bytes = sum(algo_step[i % N_SLOTS] for i in range(args.steps))
-    stream_gbs = algo_bytes / (ms / 1000.0) / 1e9 / 1.0 * 1.0
-    peak, peak_kind = measured_peaks()
-
+    peak, _ = measured_peaks()
+    stream_gbs = algo_bytes / (ms / 1000.0) / 1e9
+    rec = {"metric": METRIC, "value": tokens / (ms / 1000.0), "unit": "tokens/s", "steps": args.steps,
+           "ms_per_step": ms / args.steps, "weight_stream_gbs": stream_gbs, "hbm_frac": stream_gbs / peak,
+           "clocks": clocks}
+    cfg = workload_config(w, n_copies)
+    cfg["layout"] = layout
+    rec["config"] = cfg
     if args.timed_only:
-        if rank == 0:
-            print(json.dumps({"metric": METRIC, "value": world * args.steps * T / (ms / 1000.0), "unit": "tokens/s",
-                              "ms_per_step": ms / args.steps, "steps": args.steps, "note": "timed-only run"}),
-                  flush=True)
-        return
-    # ---- per-kernel roofline: same steps, eager ABI calls with the library's
-    # event profiling on (CUDA events on the launch stream around each kernel)
-    kp = min(args.steps, 2000)
-    M.ds4moe_profile_enable(True)
-    with torch.cuda.stream(stream):
-        for i in range(kp):
-            step(i, stream)
-    stream.synchronize()
-    prof = M.ds4moe_profile_read()
-    M.ds4moe_profile_enable(False)
-    launches_per_step = sum(n for _, n in prof.values()) / kp
-    kname, kdesc, gu_algo, gu_ms, gu_n = dominant_kernel(prof, w, sum(uniq[i % N_SLOTS] for i in range(kp)) / kp)
-    gu_avg_s = gu_ms / gu_n / 1000.0
-    roofline = {"kernel": kdesc, "bound": "hbm",
-                "achieved": gu_algo / gu_avg_s / 1e9, "peak": peak, "unit": "GB/s",
-                "frac": gu_algo / gu_avg_s / 1e9 / peak, "traffic": NCU_TRAFFIC.get((w.name, kname)),
-                "algorithmic_bytes_per_launch": int(gu_algo), "avg_launch_us": gu_avg_s * 1e6,
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else
-                               "fallback 6.8 TB/s"}
-    kernels = {n: {"avg_us": 1000 * t / c, "launches_per_step": c / kp} for n, (t, c) in prof.items()}
-
-    # ---- end to end through the C ABI with host buffers
-    ke = min(args.steps, 2000)
-    xh = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs_host]
-    oh = torch.empty((T, D), dtype=torch.float32).pin_memory()
-    x_in = torch.empty((T, D), dtype=torch.int16, device="cuda")
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    with torch.cuda.stream(stream):
-        for i in range(ke):
-            x_in.copy_(xh[i % N_SLOTS], non_blocking=True)
-            c = copies[i % n_copies]
-            M.ds4moe_moe_decode(c.abi, x_in, Wr_d, b_d, k, out[0], idx[0], wt[0], ws, stream)
-            oh.copy_(out[0], non_blocking=True)
-            stream.synchronize()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max(e0.elapsed_time(e1), world)
-    e2e = {"value": world * ke * T / (e2e_ms / 1000.0), "unit": "tokens/s", "steps": ke,
-           "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 4,
-           "path": "pinned H2D x, ds4moe_moe_decode (eager C-ABI call), D2H out, stream sync per step"}
-
-    if rank != 0:
-        return
-    cpu = None
-    if not args.no_cpu_baseline:
-        n = args.cpu_tokens or 2 * cores_available()
-        cpu = cpu_baseline(w, n, batch0=50_000)
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32 accumulate over exact 2-bit codes and bf16 activations",
-            "data": "synthetic", "config": workload_config(w, n_copies),
-            "weight_stream_gbs": stream_gbs, "hbm_frac": stream_gbs / peak,
-            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": int(round(launches_per_step * args.steps)), "clocks": clocks}
-    print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+        return rec
+    kp = min(max(args.steps, 200), 2000)
+    kernels = span_pass(M, torch, stream, replay, kp)
+    uniq_avg = sum(uniq[i % N_SLOTS] for i in range(kp)) / kp
+    ffn = next((n for n in ("ffn_t1r", "ffn_t1") if n in kernels), None)
+    if ffn:
+        algo = uniq_avg * eb + T * D * 2 + T * D * 4
+        desc = ("expert FFN over the 16-row tile order (gate/up + SwiGLU + down + combine, routing fused, "
+                "dequant fused)" if ffn == "ffn_t1r" else
+                "expert FFN (merged gate/up + SwiGLU + down + combine, dequant fused)")
+        rec["roofline"] = hbm_roofline(desc, algo, kernels[ffn]["avg_us"], NCU_TRAFFIC.get((w.name, layout, ffn)))
+    elif "gate_up_mma" in kernels:
+        algo = uniq_avg * gate_up_bytes(w) + T * D * 2 + T * k * w.d_ff * 2
+        rec["roofline"] = hbm_roofline("gate_up (fused dequant GEMV + SwiGLU)", algo,
+                                       kernels["gate_up_mma"]["avg_us"],
+                                       NCU_TRAFFIC.get((w.name, layout, "gate_up_mma")))
+    rec["kernels"] = kernels
+    counts = launch_count(M, torch, stream, lambda i: step(i, stream), 50)
+    rec["launches_per_step"] = counts
+    rec["gpu_launches"] = int(round(sum(counts.values()) * args.steps))
+    if with_e2e:
+        ke = min(args.steps, 2000)
+        xh = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs_host]
+        oh = torch.empty((T, D), dtype=torch.float32).pin_memory()
+        x_in = torch.empty((T, D), dtype=torch.int16, device="cuda")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for i in range(ke):
+                x_in.copy_(xh[i % N_SLOTS], non_blocking=True)
+                M.ds4moe_moe_decode(copies[i % n_copies].abi, x_in, Wr_d, b_d, k, out[0], idx[0], wt[0], ws, stream)
+                oh.copy_(out[0], non_blocking=True)
+                stream.synchronize()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(e0.elapsed_time(e1), world)
+        check_status(ws, stream)
+        rec["e2e"] = {"value": world * ke * T / (e2e_ms / 1000.0), "unit": "tokens/s", "steps": ke,
+                      "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 4,
+                      "path": "pinned H2D x, ds4moe_moe_decode (eager C-ABI call), D2H out, stream sync per step"}
+    return rec
 
 
-# ------------------------------------------------------- prefill chunk arm
-def run_ours_prefill(args, w: synth.Workload):
+def prefill_record(args, M, torch, w: synth.Workload, rank: int, world: int, local: int, with_e2e: bool) -> dict:
     """Prefill: route (with bias) + tensor-core expert FFN over T tokens per
     step.  Inputs (3.4 GB of weights) far exceed L2, so no flush is needed."""
-    import torch
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
-    from bit_quantized_moe_q2_gb300 import _build
-    if rank == 0 or world == 1:
-        _build.build()
-    barrier(world)
-    import bit_quantized_moe_q2_gb300 as M
     from bit_quantized_moe_q2_gb300.device import check_status, workspace
-
     dev = device_layer(w, M, torch)
     Wr, bias = synth.router(w)
     Wr_d = torch.from_numpy(Wr).cuda()
@@ -588,96 +662,58 @@ def run_ours_prefill(args, w: synth.Workload):
     stream.synchronize()
     check_status(ws, stream)
     counts = np.bincount(idx.cpu().numpy().ravel(), minlength=w.n_expert)
-
-    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
-        if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local
-    sampler = ClockSampler(gpu_index)
-    sampler.start()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    sampler.mark(True)
-    ev0.record(stream)
-    with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            step(i)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    sampler.mark(False)
-    barrier(world)
-    clocks = sampler.stop()
-    ms = reduce_max(ev0.elapsed_time(ev1), world)
+    steps = max(3, min(args.steps, 200))
+    ms, clocks = measure_clocks(torch, stream, step, gpu_index(local), steps, world)
     check_status(ws, stream)
     flops_step, flops_gu = prefill_flops(w)
-    value = world * args.steps * T / (ms / 1000.0)
-    tflops = world * args.steps * flops_step / (ms / 1000.0) / 1e12
-    if args.timed_only:
-        if rank == 0:
-            print(json.dumps({"metric": METRIC, "value": value, "unit": "tokens/s", "tflops": tflops,
-                              "ms_per_step": ms / args.steps, "steps": args.steps, "note": "timed-only run"}),
-                  flush=True)
-        return
-
-    # per-kernel times (CUDA events around each launch on its stream)
-    kp = min(args.steps, 10)
-    M.ds4moe_profile_enable(True)
-    with torch.cuda.stream(stream):
-        for i in range(kp):
-            step(i)
-    stream.synchronize()
-    prof = M.ds4moe_profile_read()
-    M.ds4moe_profile_enable(False)
-    launches_per_step = sum(n for _, n in prof.values()) / kp
-    kernels = {n: {"avg_us": 1000 * t / c, "launches_per_step": c / kp} for n, (t, c) in prof.items()}
-    gu_ms, gu_n = prof.get("gate_up_tc", (float("nan"), 1))
-    gu_s = gu_ms / gu_n / 1000.0
-    peak, peak_kind = measured_tensor_peak(sustained=True)
-    roofline = {"kernel": "gate_up_tc (tcgen05 grouped GEMM, fused Q4_1 dequant + SwiGLU)", "bound": "tensor",
-                "achieved": flops_gu / gu_s / 1e12, "peak": peak, "unit": "TFLOP/s",
-                "frac": flops_gu / gu_s / 1e12 / peak, "traffic": None,
-                "algorithmic_flops_per_launch": flops_gu, "avg_launch_us": gu_s * 1e6,
-                "peak_source": f"{peak_kind} bf16_tflops_sustained (kind::f16 runs at the bf16 rate)"}
-
-    # end to end with host buffers: pinned x in, out back, per step
-    ke = min(args.steps, 5)
-    xh = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs_host]
-    oh = torch.empty((T, D), dtype=torch.float32).pin_memory()
-    x_in = torch.empty((T, D), dtype=torch.int16, device="cuda")
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    with torch.cuda.stream(stream):
-        for i in range(ke):
-            x_in.copy_(xh[i % n_slots], non_blocking=True)
-            step(i, x_in)
-            oh.copy_(out, non_blocking=True)
-            stream.synchronize()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max(e0.elapsed_time(e1), world)
-    e2e = {"value": world * ke * T / (e2e_ms / 1000.0), "unit": "tokens/s", "steps": ke,
-           "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 4,
-           "path": "pinned H2D x, ds4moe_route_topk + ds4moe_ffn_prefill (C-ABI calls), D2H out, sync per step"}
-    if rank != 0:
-        return
-    cpu = None
-    if not args.no_cpu_baseline:
-        n = args.cpu_tokens or 2 * cores_available()
-        cpu = cpu_baseline(w, n, batch0=50_000)
+    rec = {"metric": METRIC, "value": world * steps * T / (ms / 1000.0), "unit": "tokens/s", "steps": steps,
+           "ms_per_step": ms / steps, "tflops": world * steps * flops_step / (ms / 1000.0) / 1e12,
+           "clocks": clocks}
     cfg = workload_config(w, 1)
     cfg["l2"] = "inputs larger than L2: every step streams 3.4 GB of expert weights"
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f16 tensor-core operands (exact gate/up split), f32 accumulate",
-            "data": "synthetic", "config": cfg, "tflops": tflops,
-            "tensor_frac": tflops / peak, "roofline": roofline, "kernels": kernels,
-            "expert_load": {"max": int(counts.max()), "min": int(counts.min()), "empty": int((counts == 0).sum())},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(round(launches_per_step * args.steps)),
-            "clocks": clocks}
-    print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    rec["config"] = cfg
+    if args.timed_only:
+        return rec
+    kernels = span_pass(M, torch, stream, step, min(steps, 10))
+    peak, peak_kind = measured_tensor_peak(sustained=True)
+    rec["tensor_frac"] = rec["tflops"] / peak
+    if "gate_up_tc" in kernels:
+        us = kernels["gate_up_tc"]["avg_us"]
+        rec["roofline"] = {"kernel": "gate_up_tc (tcgen05 grouped GEMM, fused Q4_1 dequant + SwiGLU)",
+                           "bound": "tensor", "achieved": flops_gu / (us * 1e-6) / 1e12, "peak": peak,
+                           "unit": "TFLOP/s", "frac": flops_gu / (us * 1e-6) / 1e12 / peak, "traffic": None,
+                           "algorithmic_flops_per_launch": flops_gu, "avg_launch_us": us,
+                           "timing": "device span per launch (%globaltimer, grid entry to last warp exit)",
+                           "peak_source": f"{peak_kind} bf16_tflops_sustained (kind::f16 runs at the bf16 rate)"}
+    rec["kernels"] = kernels
+    cnt = launch_count(M, torch, stream, step, 2)
+    rec["launches_per_step"] = cnt
+    rec["gpu_launches"] = int(round(sum(cnt.values()) * steps))
+    rec["expert_load"] = {"max": int(counts.max()), "min": int(counts.min()), "empty": int((counts == 0).sum())}
+    if with_e2e:
+        ke = min(steps, 5)
+        xh = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs_host]
+        oh = torch.empty((T, D), dtype=torch.float32).pin_memory()
+        x_in = torch.empty((T, D), dtype=torch.int16, device="cuda")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for i in range(ke):
+                x_in.copy_(xh[i % n_slots], non_blocking=True)
+                step(i, x_in)
+                oh.copy_(out, non_blocking=True)
+                stream.synchronize()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(e0.elapsed_time(e1), world)
+        rec["e2e"] = {"value": world * ke * T / (e2e_ms / 1000.0), "unit": "tokens/s", "steps": ke,
+                      "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 4,
+                      "path": "pinned H2D x, ds4moe_route_topk + ds4moe_ffn_prefill (C-ABI calls), D2H out, "
+                              "sync per step"}
+    del dev
+    torch.cuda.empty_cache()
+    return rec
 
 
 # ------------------------------------------------------- decode stack arm
@@ -711,30 +747,23 @@ def tensor_bytes(w: synth.Workload, t: int) -> int:
     return mat_bytes(q.qtype, rows, cols)
 
 
-def run_ours_stack(args, w: synth.Workload):
+def start_stack_pool(w: synth.Workload):
+    """Shared-memory tensors and the generator pool (spawned: it starts
+    before, or independently of, any GPU call of this process)."""
     import multiprocessing as mp
     from multiprocessing import shared_memory
-    rank, world, local = dist_env()
-    from bit_quantized_moe_q2_gb300 import _build
-    if rank == 0 or world == 1:
-        _build.build()
-    # the generator pool starts (spawn) before the first GPU call
     per = {t: tensor_bytes(w, t) for t in (synth.T_GATE, synth.T_UP, synth.T_DOWN)}
     shms = [shared_memory.SharedMemory(create=True, size=w.n_expert * per[t])
             for t in (synth.T_GATE, synth.T_UP, synth.T_DOWN)]
     pool = mp.get_context("spawn").Pool(max(1, cores_available()), initializer=_pool_init)
-    import torch
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
-    barrier(world)
-    import bit_quantized_moe_q2_gb300 as M
-    from bit_quantized_moe_q2_gb300.device import DeviceLayer, check_status, workspace
+    return pool, shms, per
+
+
+def stack_layers(w: synth.Workload, M, torch, pool, shms, per, r16: bool):
+    """All layers generated on the host cores, uploaded (and, with r16,
+    repacked on the device into the 16-row tile order)."""
+    from bit_quantized_moe_q2_gb300.device import DeviceLayer
     qid = {synth.Q4_1: M.DS4MOE_Q4_1, synth.Q2_K: M.DS4MOE_Q2_K, synth.Q4_K: M.DS4MOE_Q4_K}
-    t_gen = time.perf_counter()
     devs, Wrs, biases = [], [], []
     names = [sh.name for sh in shms]
     try:
@@ -744,6 +773,9 @@ def run_ours_stack(args, w: synth.Workload):
                                     qid[w.down.qtype])
             for sh, dst in zip(shms, (dev.gate, dev.up, dev.down)):
                 dst.copy_(torch.frombuffer(sh.buf, dtype=torch.uint8, count=dst.numel()))
+            if r16:
+                dev = dev.repacked_r16()
+                torch.cuda.synchronize()
             Wr, b = synth.router(w, layer)
             devs.append(dev)
             Wrs.append(torch.from_numpy(Wr).cuda())
@@ -754,7 +786,12 @@ def run_ours_stack(args, w: synth.Workload):
         for sh in shms:
             sh.close()
             sh.unlink()
-    t_gen = time.perf_counter() - t_gen
+    return devs, Wrs, biases
+
+
+def stack_record(args, M, torch, w: synth.Workload, devs, Wrs, biases, layout: str, rank: int, world: int,
+                 local: int, with_e2e: bool) -> dict:
+    from bit_quantized_moe_q2_gb300.device import check_status, workspace
     T, k, D, L = w.T, w.k, w.d_model, w.n_layers
     bias_arg = None if biases[0] is None else biases
     x0 = [torch.from_numpy(oracle_free_bf16_to_f32(synth.activations(w, T=T, batch=rank_batch_offset(rank) + s)))
@@ -769,7 +806,7 @@ def run_ours_stack(args, w: synth.Workload):
     stream = torch.cuda.Stream()
 
     def step(j, s=None):
-        x_res.copy_(x0[j], non_blocking=True)
+        x_res.copy_(x0[j % N_SLOTS], non_blocking=True)
         M.ds4moe_stack_decode(abis, Wrs, bias_arg, k, x_res, xb, out, idx, wt, ws, stream=s)
 
     with torch.cuda.stream(stream):
@@ -783,105 +820,206 @@ def run_ours_stack(args, w: synth.Workload):
         with torch.cuda.graph(g, stream=stream):
             step(j, stream)
         graphs.append(g)
+
+    def replay(i):
+        graphs[i % N_SLOTS].replay()
+
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            graphs[i % N_SLOTS].replay()
+        for i in range(max(args.warmup, 3)):
+            replay(i)
     stream.synchronize()
     check_status(ws, stream)
-
-    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
-        if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local
-    sampler = ClockSampler(gpu_index)
-    sampler.start()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    sampler.mark(True)
-    ev0.record(stream)
-    with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            graphs[i % N_SLOTS].replay()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    sampler.mark(False)
-    barrier(world)
-    clocks = sampler.stop()
-    ms = reduce_max(ev0.elapsed_time(ev1), world)
+    ms, clocks = measure_clocks(torch, stream, replay, gpu_index(local), args.steps, world)
     check_status(ws, stream)
-    value = world * args.steps * T / (ms / 1000.0)
     eb = expert_bytes(w)
     algo_step = sum(u * eb for u in uniq) + L * (w.n_expert * D * 4) + T * D * 4 * 2
+    peak, _ = measured_peaks()
     stream_gbs = algo_step / (ms / args.steps / 1000.0) / 1e9
-    peak, peak_kind = measured_peaks()
-    if args.timed_only:
-        if rank == 0:
-            print(json.dumps({"metric": METRIC, "value": value, "unit": "tokens/s", "ms_per_step": ms / args.steps,
-                              "steps": args.steps, "note": "timed-only run"}), flush=True)
-        return
-    kp = min(args.steps, 50)
-    M.ds4moe_profile_enable(True)
-    with torch.cuda.stream(stream):
-        for i in range(kp):
-            step(i % N_SLOTS, stream)
-    stream.synchronize()
-    prof = M.ds4moe_profile_read()
-    M.ds4moe_profile_enable(False)
-    launches_per_step = sum(n for _, n in prof.values()) / kp
-    kernels = {n: {"avg_us": 1000 * t / c, "launches_per_step": c / kp} for n, (t, c) in prof.items()}
-    kname, kdesc, gu_algo, gu_ms, gu_n = dominant_kernel(prof, w, sum(uniq) / L)
-    gu_s = gu_ms / gu_n / 1000.0
-    roofline = {"kernel": kdesc + ", per layer", "bound": "hbm",
-                "achieved": gu_algo / gu_s / 1e9, "peak": peak, "unit": "GB/s", "frac": gu_algo / gu_s / 1e9 / peak,
-                "traffic": None, "algorithmic_bytes_per_launch": int(gu_algo), "avg_launch_us": gu_s * 1e6,
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else
-                               "fallback 6.8 TB/s"}
-    # end to end: pinned x in, x_res out, per step
-    ke = min(args.steps, 50)
-    xh = [x.cpu().pin_memory() for x in x0]
-    oh = torch.empty((T, D), dtype=torch.float32).pin_memory()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    with torch.cuda.stream(stream):
-        for i in range(ke):
-            x_res.copy_(xh[i % N_SLOTS], non_blocking=True)
-            M.ds4moe_stack_decode(abis, Wrs, bias_arg, k, x_res, xb, out, idx, wt, ws, stream=stream)
-            oh.copy_(x_res, non_blocking=True)
-            stream.synchronize()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max(e0.elapsed_time(e1), world)
-    e2e = {"value": world * ke * T / (e2e_ms / 1000.0), "unit": "tokens/s", "steps": ke,
-           "h2d_bytes_per_step": T * D * 4, "d2h_bytes_per_step": T * D * 4,
-           "path": "pinned H2D x_res, ds4moe_stack_decode (eager C-ABI call, 43 layers), D2H x_res, sync per step"}
-    if rank != 0:
-        return
-    cpu = None
-    if not args.no_cpu_baseline:
-        n = args.cpu_tokens or max(2, cores_available() // 2)
-        cpu = cpu_baseline(w, n, batch0=50_000)
-        cpu["value"] /= L
-        cpu["sample"] = (f"{n} tokens through layer 0 (route + selected expert FFNs + combine, fp64 C oracle, "
-                         f"OpenMP over tokens), tokens/s divided by the {L} layers")
     cfg = workload_config(w, 1)
     cfg["n_layers"] = L
+    cfg["layout"] = layout
     cfg["l2"] = f"inputs larger than L2: every step streams {L} layers of expert weights"
-    cfg["weights_generated_s"] = round(t_gen, 1)
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32 accumulate over exact 2-bit codes and bf16 activations",
-            "data": "synthetic", "config": cfg, "weight_stream_gbs": stream_gbs, "hbm_frac": stream_gbs / peak,
-            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": int(round(launches_per_step * args.steps)), "clocks": clocks}
-    print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    rec = {"metric": METRIC, "value": world * args.steps * T / (ms / 1000.0), "unit": "tokens/s",
+           "steps": args.steps, "ms_per_step": ms / args.steps, "weight_stream_gbs": stream_gbs,
+           "hbm_frac": stream_gbs / peak, "config": cfg, "clocks": clocks}
+    if args.timed_only:
+        return rec
+    kp = min(max(args.steps, 20), 50)
+    kernels = span_pass(M, torch, stream, replay, kp)
+    ffn = next((n for n in ("ffn_t1r", "ffn_t1", "gate_up_mma") if n in kernels), None)
+    if ffn:
+        if ffn == "gate_up_mma":
+            algo = sum(uniq) / L * gate_up_bytes(w) + T * D * 2 + T * k * w.d_ff * 2
+            desc = "gate_up (fused dequant GEMV + SwiGLU), per layer"
+        else:
+            algo = sum(uniq) / L * eb + T * D * 2 + T * D * 4
+            desc = ("expert FFN over the 16-row tile order, per layer" if ffn == "ffn_t1r" else
+                    "expert FFN (merged gate/up + SwiGLU + down + combine), per layer")
+        rec["roofline"] = hbm_roofline(desc, algo, kernels[ffn]["avg_us"], None)
+    rec["kernels"] = kernels
+    cnt = launch_count(M, torch, stream, lambda i: step(i, stream), 2)
+    rec["launches_per_step"] = cnt
+    rec["gpu_launches"] = int(round(sum(cnt.values()) * args.steps))
+    if with_e2e:
+        ke = min(args.steps, 50)
+        xh = [x.cpu().pin_memory() for x in x0]
+        oh = torch.empty((T, D), dtype=torch.float32).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for i in range(ke):
+                x_res.copy_(xh[i % N_SLOTS], non_blocking=True)
+                M.ds4moe_stack_decode(abis, Wrs, bias_arg, k, x_res, xb, out, idx, wt, ws, stream=stream)
+                oh.copy_(x_res, non_blocking=True)
+                stream.synchronize()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(e0.elapsed_time(e1), world)
+        rec["e2e"] = {"value": world * ke * T / (e2e_ms / 1000.0), "unit": "tokens/s", "steps": ke,
+                      "h2d_bytes_per_step": T * D * 4, "d2h_bytes_per_step": T * D * 4,
+                      "path": f"pinned H2D x_res, ds4moe_stack_decode (eager C-ABI call, {L} layers), D2H x_res, "
+                              "sync per step"}
+    return rec
 
 
 def oracle_free_bf16_to_f32(b: np.ndarray) -> np.ndarray:
     """Exact widening of bf16 bit patterns (a bit shift; no method arithmetic)."""
     return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def line_from(rec: dict, args, world: int, dtype: str) -> dict:
+    """The contract's JSON line around a measurement record."""
+    line = {"metric": rec["metric"], "value": rec["value"], "unit": rec["unit"], "n_gpus": world,
+            "steps": rec["steps"], "warmup": args.warmup, "ms_per_step": rec["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+            "data": "synthetic", "config": rec["config"]}
+    for key in ("tflops", "tensor_frac", "weight_stream_gbs", "hbm_frac", "roofline", "kernels",
+                "launches_per_step", "expert_load", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
+        if key in rec:
+            line[key] = rec[key]
+    return line
+
+
+DECODE_DTYPE = "f32 accumulate over exact 2-bit codes and bf16 activations"
+PREFILL_DTYPE = "f16 tensor-core operands (exact gate/up split), f32 accumulate"
+
+
+def sub_summary(rec: dict) -> dict:
+    """A sub-record of the default line: the measurement without its host-side extras."""
+    keep = ("metric", "value", "unit", "steps", "ms_per_step", "tflops", "tensor_frac", "weight_stream_gbs",
+            "hbm_frac", "config", "roofline", "kernels", "gpu_launches", "e2e", "clocks", "expert_load")
+    return {k: rec[k] for k in keep if k in rec}
+
+
+def run_default(args, w: synth.Workload):
+    """The Flash decode layer at T = 1 on tile-order weights (the line), with
+    sub-records: the same layer on plain Q2_K blocks, the 4096-token prefill
+    chunk and the 43-layer stack at T = 1."""
+    import torch
+    rank, world, local = init_dist(torch)
+    M = load_library(rank, world)
+    w4 = synth.WORKLOADS[4]
+    sub = not args.no_sub and world == 1   # sub-records at N = 1 only
+    stack_pool = start_stack_pool(w4) if sub else None  # spawned: no CUDA state inherited
+    plain = device_layer(w, M, torch)
+    n_copies = max(1, args.copies)
+    r16 = replicate(plain.repacked_r16(), n_copies)
+    torch.cuda.synchronize()
+    main = decode_layer_record(args, M, torch, w, r16, R16_LAYOUT, rank, world, local, with_e2e=True)
+    del r16
+    torch.cuda.empty_cache()
+    subs = {}
+    if sub:
+        rec = decode_layer_record(args, M, torch, w, replicate(plain, n_copies), PLAIN_LAYOUT, rank, world, local,
+                                  with_e2e=False)
+        subs["flash_layer_t1_plain_q2k"] = sub_summary(rec)
+    del plain
+    torch.cuda.empty_cache()
+    if sub:
+        subs["flash_prefill_t4096"] = sub_summary(
+            prefill_record(args, M, torch, synth.WORKLOADS[3], rank, world, local, with_e2e=False))
+        if stack_pool is not None:
+            pool, shms, per = stack_pool
+            t_gen = time.perf_counter()
+            devs, Wrs, biases = stack_layers(w4, M, torch, pool, shms, per, r16=True)
+            rec = stack_record(args, M, torch, w4, devs, Wrs, biases, R16_LAYOUT, rank, world, local,
+                               with_e2e=False)
+            rec["config"]["weights_generated_s"] = round(time.perf_counter() - t_gen, 1)
+            subs["flash_stack43_t1"] = sub_summary(rec)
+            del devs
+            torch.cuda.empty_cache()
+    if rank == 0:
+        if not args.no_cpu_baseline and not args.timed_only:
+            main["cpu_baseline"] = cpu_baseline(w, args.cpu_tokens or 2 * cores_available(), batch0=50_000)
+        line = line_from(main, args, world, DECODE_DTYPE)
+        if subs:
+            line["sub"] = subs
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_decode(args, w: synth.Workload):
+    """One decode workload alone (plain block layouts, or the tile order with --r16)."""
+    import torch
+    rank, world, local = init_dist(torch)
+    M = load_library(rank, world)
+    dev = device_layer(w, M, torch)
+    layout = PLAIN_LAYOUT if w.gate.qtype == synth.Q2_K else "plain block layouts"
+    if args.r16:
+        dev = dev.repacked_r16()
+        layout = R16_LAYOUT
+    rec = decode_layer_record(args, M, torch, w, replicate(dev, max(1, args.copies)), layout, rank, world, local,
+                              with_e2e=not args.timed_only)
+    if rank == 0:
+        if not args.no_cpu_baseline and not args.timed_only:
+            rec["cpu_baseline"] = cpu_baseline(w, args.cpu_tokens or 2 * cores_available(), batch0=50_000)
+        print(json.dumps(line_from(rec, args, world, DECODE_DTYPE)), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_prefill(args, w: synth.Workload):
+    import torch
+    rank, world, local = init_dist(torch)
+    M = load_library(rank, world)
+    rec = prefill_record(args, M, torch, w, rank, world, local, with_e2e=not args.timed_only)
+    if rank == 0:
+        if not args.no_cpu_baseline and not args.timed_only:
+            rec["cpu_baseline"] = cpu_baseline(w, args.cpu_tokens or 2 * cores_available(), batch0=50_000)
+        print(json.dumps(line_from(rec, args, world, PREFILL_DTYPE)), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_stack(args, w: synth.Workload):
+    import torch
+    rank, world, local = init_dist(torch)
+    M = load_library(rank, world)
+    pool, shms, per = start_stack_pool(w)  # spawned: no CUDA state inherited
+    t_gen = time.perf_counter()
+    r16 = args.r16 and w.T == 1
+    devs, Wrs, biases = stack_layers(w, M, torch, pool, shms, per, r16=r16)
+    t_gen = time.perf_counter() - t_gen
+    rec = stack_record(args, M, torch, w, devs, Wrs, biases, R16_LAYOUT if r16 else PLAIN_LAYOUT, rank, world,
+                       local, with_e2e=not args.timed_only)
+    rec["config"]["weights_generated_s"] = round(t_gen, 1)
+    if rank == 0:
+        if not args.no_cpu_baseline and not args.timed_only:
+            n = args.cpu_tokens or max(2, cores_available() // 2)
+            cpu = cpu_baseline(w, n, batch0=50_000)
+            cpu["value"] /= w.n_layers
+            cpu["sample"] = (f"{n} tokens through layer 0 (route + selected expert FFNs + combine, fp64 C oracle, "
+                             f"OpenMP over tokens), tokens/s divided by the {w.n_layers} layers")
+            rec["cpu_baseline"] = cpu
+        print(json.dumps(line_from(rec, args, world, DECODE_DTYPE)), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
 
 
 def run_quantize(args, w: synth.Workload):
@@ -942,14 +1080,17 @@ def main(argv=None):
     if args.quantize:
         run_quantize(args, w)
         return
+    default = args.workload == 1 and not args.n_expert and not args.tokens and not args.plain
     if args.impl == "reference":
         run_reference(args, w)
     elif w.n_layers > 1:
-        run_ours_stack(args, w)
+        run_stack(args, w)
     elif w.path == "prefill":
-        run_ours_prefill(args, w)
+        run_prefill(args, w)
+    elif default:
+        run_default(args, w)
     else:
-        run_ours(args, w)
+        run_decode(args, w)
 
 
 if __name__ == "__main__":

@@ -162,12 +162,18 @@ def ds4moe_repack(src_type, dst_type, src, rows, cols, dst, stream=None):
            "ds4moe_repack")
 
 
-def ds4moe_profile_span(on: int = -1):
-    """(total_ns, launches) of the device-side span record so far; on = 1 / 0
-    then clears it and switches recording on / off (-1: read only)."""
-    ns, n = ctypes.c_double(), ctypes.c_int64()
-    _check(lib().ds4moe_profile_span(int(on), ctypes.byref(ns), ctypes.byref(n)), "ds4moe_profile_span")
-    return ns.value, n.value
+# ds4moe_span_kernel order
+SPAN_KERNELS = ("route", "ffn_t1", "ffn_t1r", "gate_up_mma", "down_mma", "gate_up_tc", "down_tc")
+
+
+def ds4moe_profile_span(on: int = -1) -> dict:
+    """{kernel: (total_ns, launches)} of the device-side span record so far
+    (kernels with no recorded launch omitted); on = 1 / 0 then clears it and
+    switches recording on / off (-1: read only)."""
+    n = len(SPAN_KERNELS)
+    ns, cnt = (ctypes.c_double * n)(), (ctypes.c_int64 * n)()
+    _check(lib().ds4moe_profile_span(int(on), ns, cnt), "ds4moe_profile_span")
+    return {k: (ns[i], cnt[i]) for i, k in enumerate(SPAN_KERNELS) if cnt[i]}
 
 
 def ds4moe_quantize_f32(qtype, x, importance, out, ws, cols=None, stream=None):

@@ -10,6 +10,7 @@
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "route.cuh"
+#include "span.cuh"
 
 using namespace ds4;
 
@@ -20,6 +21,10 @@ int num_sms() {
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
   return n;
+}
+
+cudaError_t span_control_abi(int on, double *total_ns, int64_t *launches) {
+  return span_control_unit(on, total_ns, launches);
 }
 
 }  // namespace ds4
@@ -656,6 +661,7 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict_
                                                      BucketArgs bk) {
   __shared__ float ps[8][32], pc[8][32];
   __shared__ uint32_t ticket;
+  const SpanExit span_exit(DS4MOE_SPAN_ROUTE);
   const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   // the router row is constant: fetch it before waiting for x
   float4 wv[NI];
@@ -665,6 +671,7 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict_
     wv[i] = j < D ? __ldg(reinterpret_cast<const float4 *>(Wr + (int64_t)e * D + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   ptx::pdl_wait();
+  span_begin(DS4MOE_SPAN_ROUTE);
   ptx::pdl_launch_dependents();
   // single-token chain: the merged FFN grid's per-expert counters start at 0
   if (MODE == kRouteLogits && bk.counts && tid == 0) bk.counts[blockIdx.x] = 0;
@@ -1137,7 +1144,15 @@ ds4moe_status ds4moe_repack(int32_t src_type, int32_t dst_type, const void *src,
 
 ds4moe_status ds4moe_profile_span(int32_t on, double *total_ns, int64_t *launches) {
   if (on < -1 || on > 1) return DS4MOE_EINVAL;
-  return cuda_status(t1r_span_control(on, total_ns, launches));
+  if (total_ns)
+    for (int i = 0; i < DS4MOE_SPAN_COUNT; ++i) total_ns[i] = 0.0;
+  if (launches)
+    for (int i = 0; i < DS4MOE_SPAN_COUNT; ++i) launches[i] = 0;
+  cudaError_t e = span_control_abi(on, total_ns, launches);
+  if (e == cudaSuccess) e = span_control_decode(on, total_ns, launches);
+  if (e == cudaSuccess) e = span_control_t1r(on, total_ns, launches);
+  if (e == cudaSuccess) e = span_control_prefill(on, total_ns, launches);
+  return cuda_status(e);
 }
 
 size_t ds4moe_workspace_bytes(const ds4moe_layer *L, int32_t T, int32_t k, int32_t prefill) {

@@ -19,6 +19,7 @@
 // copies (row bytes not a multiple of 16).
 #include "internal.cuh"
 #include "ptx.cuh"
+#include "span.cuh"
 #include "t1.cuh"
 
 namespace ds4 {
@@ -252,6 +253,7 @@ __device__ __forceinline__ void tile_rows(const uint8_t *buf, uint32_t ch, int n
 template <int QG, int QU, bool FIN>
 __global__ void __launch_bounds__(512) k_gate_up_mma(FfnArgs a, int kp, uint32_t chg, uint32_t chu) {
   extern __shared__ __align__(128) uint8_t smem[];
+  const SpanExit span_exit(DS4MOE_SPAN_GATE_UP_MMA);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
   const int D = a.L.d_model, F = a.L.d_ff;
   const bool is_up = w >= kp;
@@ -271,6 +273,7 @@ __global__ void __launch_bounds__(512) k_gate_up_mma(FfnArgs a, int kp, uint32_t
   const Q2kLane kl = q2k_lane(c);
   // groups, permutation, fp16 x and its sums come from the bucketing grid
   ptx::pdl_wait();
+  span_begin(DS4MOE_SPAN_GATE_UP_MMA);
   ptx::pdl_launch_dependents();
   if (FIN && blockIdx.x == 0 && w == 0) finish_routing_weights(const_cast<float *>(a.w), a.T, a.k);
   clear_combine_counters(a, threadIdx.x, blockDim.x);
@@ -459,6 +462,7 @@ __device__ __forceinline__ void combine_tile(const FfnArgs &a, const Group &grp,
 template <int NST>
 __global__ void __launch_bounds__(256) k_down_mma(FfnArgs a, uint32_t chd) {
   extern __shared__ __align__(128) uint8_t smem[];
+  const SpanExit span_exit(DS4MOE_SPAN_DOWN_MMA);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
   const int nw = blockDim.x >> 5;
   const int D = a.L.d_model, F = a.L.d_ff;
@@ -494,6 +498,7 @@ __global__ void __launch_bounds__(256) k_down_mma(FfnArgs a, uint32_t chd) {
   for (int st = 0; st < NST; ++st)
     if (u + st * nwarps < U) issue(u + st * nwarps, st);
   ptx::pdl_wait();  // h and its sums come from the gate/up grid
+  span_begin(DS4MOE_SPAN_DOWN_MMA);
   ptx::pdl_launch_dependents();
   bool timed_out = false;
   for (int it = 0; u < U; u += nwarps, ++it) {
@@ -814,6 +819,7 @@ __device__ int32_t g_sync_extra = 0;
 // bit-identical to theirs.
 __global__ void __launch_bounds__(18 * 32, 1) k_ffn_t1(FfnArgs a, int nstage) {
   extern __shared__ __align__(128) uint8_t smem[];
+  const SpanExit span_exit(DS4MOE_SPAN_FFN_T1);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
   const int D = a.L.d_model, F = a.L.d_ff, nbg = D / 256, nbd = F / 256;
   const T1Tile tg = t1_tile((uint32_t)(kQ2KBytes * nbg)), td = t1_tile((uint32_t)(kQ2KBytes * nbd));
@@ -839,6 +845,7 @@ __global__ void __launch_bounds__(18 * 32, 1) k_ffn_t1(FfnArgs a, int nstage) {
   T1B B;
   if (w < nbg) t1_load_b<true>(B, a.x + 256 * w, g, c);  // the call's input: before the dependency wait
   ptx::pdl_wait();  // the logits come from the router grid
+  span_begin(DS4MOE_SPAN_FFN_T1);
   ptx::pdl_launch_dependents();
   __shared__ Group s_grp[kT1MaxGroups];
   __shared__ int s_ngrp;
@@ -1469,6 +1476,10 @@ cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s) {
   const int grid = (int)((n4 + 255) / 256 < num_sms() * 16 ? (n4 + 255) / 256 : num_sms() * 16);
   ProfScope p("combine", s);
   return launch_pdl(k_combine, dim3(grid), dim3(256), 0, s, a);
+}
+
+cudaError_t span_control_decode(int on, double *total_ns, int64_t *launches) {
+  return span_control_unit(on, total_ns, launches);
 }
 
 }  // namespace ds4

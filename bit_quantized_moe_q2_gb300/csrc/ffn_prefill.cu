@@ -41,6 +41,7 @@
 
 #include "internal.cuh"
 #include "ptx.cuh"
+#include "span.cuh"
 
 namespace ds4 {
 namespace {
@@ -238,6 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = TcCfg<NMAT, QA, BN>;
   constexpr int QV = QFmt<QA>::kVals, QB = QFmt<QA>::kBytes;
   extern __shared__ uint8_t smem_raw[];
+  const SpanExit span_exit(NMAT == 2 ? DS4MOE_SPAN_GATE_UP_TC : DS4MOE_SPAN_DOWN_TC);
+  span_begin(NMAT == 2 ? DS4MOE_SPAN_GATE_UP_TC : DS4MOE_SPAN_DOWN_TC);
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = sm + C::kOffA, *sB = sm + C::kOffB, *sQ = sm + C::kOffQ;
   uint64_t *qfull = reinterpret_cast<uint64_t *>(sm + C::kOffBar);
@@ -706,6 +709,10 @@ cudaError_t launch_ffn_prefill(const FfnArgs &a, cudaStream_t s) {
   const int dn_units = (ne + P / kChunkDown) * (D / kTileM);
   if (dq2) return launch_tc<1, DS4MOE_Q2_K, kChunkDown>(md, md, mh, dn, dn_units, s, "down_tc");
   return launch_tc<1, DS4MOE_Q4_1, kChunkDown>(md, md, mh, dn, dn_units, s, "down_tc");
+}
+
+cudaError_t span_control_prefill(int on, double *total_ns, int64_t *launches) {
+  return span_control_unit(on, total_ns, launches);
 }
 
 }  // namespace ds4

@@ -9,6 +9,7 @@
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "route.cuh"
+#include "span.cuh"
 #include "t1r.cuh"
 
 namespace ds4 {
@@ -108,24 +109,6 @@ cudaError_t launch_repack(bool to_r16, const void *src, void *dst, int64_t rows,
     k_repack_from_r16<<<blocks, 256, 0, s>>>(static_cast<const uint8_t *>(src), static_cast<uint8_t *>(dst), ntile, nb,
                                              rowb);
   return cudaGetLastError();
-}
-
-// ====================================================== device-side spans
-// Optional %globaltimer record of one kernel's span per launch: from the
-// first CTA past its grid dependency wait to the last CTA's exit, summed over
-// launches (a profiling aid: events cannot bracket a kernel inside a
-// replayed CUDA graph).
-struct KSpan {
-  unsigned long long begin, end, sum_ns;
-  unsigned int exited, count;
-};
-__device__ KSpan g_t1r_span = {~0ull, 0ull, 0ull, 0u, 0u};
-__device__ int g_t1r_span_on = 0;
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 // ============================================= single-token FFN over R16
@@ -244,6 +227,7 @@ __device__ __forceinline__ T1rItem t1r_unpack(uint32_t p) {
 // be resident together, as in any persistent grid with one CTA per SM.
 __global__ void __launch_bounds__(kT1rMaxWarps * 32, 1) k_ffn_t1r(FfnArgs a, int nstage) {
   extern __shared__ __align__(128) uint8_t smem[];
+  const SpanExit span_exit(DS4MOE_SPAN_FFN_T1R);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
   const int D = a.L.d_model, F = a.L.d_ff, nbg = D / 256, nbd = F / 256;
   const uint32_t sb = 2u * (uint32_t)nbg * kR16TileBlock;  // gate + up tile = four 16-row down tiles
@@ -283,8 +267,7 @@ __global__ void __launch_bounds__(kT1rMaxWarps * 32, 1) k_ffn_t1r(FfnArgs a, int
   R16B B;
   if (w < nbg) r16_load_b(B, a.x + 256 * w, g, c);  // the call's input: ready before the router grid started
   ptx::pdl_wait();
-  const bool span = g_t1r_span_on != 0;
-  if (span && threadIdx.x == 0) atomicMin(&g_t1r_span.begin, globaltimer());
+  span_begin(DS4MOE_SPAN_FFN_T1R);
   ptx::pdl_launch_dependents();
   if (w == wsync) {
     // the experts of the single token: all that the producer needs
@@ -550,18 +533,6 @@ __global__ void __launch_bounds__(kT1rMaxWarps * 32, 1) k_ffn_t1r(FfnArgs a, int
       if (lane == 0) ptx::mbar_arrive(&hfull[q & 1]);
     }
   }
-  __syncthreads();
-  if (span && threadIdx.x == 0) {
-    atomicMax(&g_t1r_span.end, globaltimer());
-    __threadfence();
-    if (atomicAdd(&g_t1r_span.exited, 1u) == gridDim.x - 1) {
-      __threadfence();
-      const unsigned long long b0 = atomicExch(&g_t1r_span.begin, ~0ull), e0 = atomicExch(&g_t1r_span.end, 0ull);
-      atomicAdd(&g_t1r_span.sum_ns, e0 - b0);
-      atomicAdd(&g_t1r_span.count, 1u);
-      atomicExch(&g_t1r_span.exited, 0u);
-    }
-  }
 }
 
 // Shared memory of the grid for nbg consumer warps and nstage stages.
@@ -598,18 +569,8 @@ cudaError_t t1r_set_sync_hook(int32_t budget, int32_t extra) {
   return e;
 }
 
-cudaError_t t1r_span_control(int on, double *total_ns, int64_t *launches) {
-  KSpan sp{};
-  cudaError_t e = cudaMemcpyFromSymbol(&sp, g_t1r_span, sizeof(sp));
-  if (e != cudaSuccess) return e;
-  if (total_ns) *total_ns = (double)sp.sum_ns;
-  if (launches) *launches = sp.count;
-  if (on >= 0) {
-    const KSpan z = {~0ull, 0ull, 0ull, 0u, 0u};
-    e = cudaMemcpyToSymbol(g_t1r_span, &z, sizeof(z));
-    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_t1r_span_on, &on, sizeof(int));
-  }
-  return e;
+cudaError_t span_control_t1r(int on, double *total_ns, int64_t *launches) {
+  return span_control_unit(on, total_ns, launches);
 }
 
 }  // namespace ds4

@@ -209,7 +209,6 @@ bool t1r_ok(const ds4moe_layer &L, int k);
 cudaError_t launch_ffn_t1r(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_repack(bool to_r16, const void *src, void *dst, int64_t rows, int64_t cols, cudaStream_t s);
 cudaError_t t1r_set_sync_hook(int32_t budget, int32_t extra);
-cudaError_t t1r_span_control(int on, double *total_ns, int64_t *launches);
 cudaError_t launch_ffn_prefill(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s);
 bool decode_mma_ok(const ds4moe_layer &L);

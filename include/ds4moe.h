@@ -439,16 +439,30 @@ ds4moe_status ds4moe_profile_entry(int32_t i, const char **name, double *total_m
                                    int64_t *launches);
 
 /*
- * Device-side kernel spans (tracing aid).  ds4moe_profile_span(on, ...)
- * reads the totals recorded so far into total_ns / launches (either may be
- * NULL); with on = 1 or 0 it then clears them and switches recording on or
- * off for later launches on the current device (on = -1: read only).  While
- * on, the single-token FFN grid over DS4MOE_Q2_K_R16 weights records, per
- * launch, %globaltimer from the first CTA past its grid-dependency wait to
- * the last CTA's exit -- a kernel's duration inside a replayed CUDA graph,
- * where events cannot bracket it.  Call it only while none of this
- * library's kernels is running.
+ * Device-side kernel spans (tracing aid).  For each kernel below, while
+ * recording is on, every launch adds %globaltimer from the first CTA past its
+ * grid-dependency wait to the last warp's exit -- a kernel's duration inside
+ * a replayed CUDA graph, where events cannot bracket it -- and counts the
+ * launch.
+ *
+ * ds4moe_profile_span(on, total_ns, launches) writes the totals recorded so
+ * far into total_ns[DS4MOE_SPAN_COUNT] / launches[DS4MOE_SPAN_COUNT] (either
+ * may be NULL; indexed by ds4moe_span_kernel); with on = 1 or 0 it then
+ * clears them and switches recording on or off for later launches on the
+ * current device (on = -1: read only).  Call it only while none of this
+ * library's kernels is running.  EINVAL for another `on`; ECUDA if a device
+ * copy fails.
  */
+typedef enum {
+  DS4MOE_SPAN_ROUTE = 0,        /* decode router grid: logits (+ top-k, bucketing) */
+  DS4MOE_SPAN_FFN_T1 = 1,       /* single-token merged FFN grid, plain blocks */
+  DS4MOE_SPAN_FFN_T1R = 2,      /* single-token FFN grid, DS4MOE_Q2_K_R16 */
+  DS4MOE_SPAN_GATE_UP_MMA = 3,  /* multi-token decode gate/up + SwiGLU */
+  DS4MOE_SPAN_DOWN_MMA = 4,     /* multi-token decode down (+ combine) */
+  DS4MOE_SPAN_GATE_UP_TC = 5,   /* prefill tensor-core gate/up + SwiGLU */
+  DS4MOE_SPAN_DOWN_TC = 6,      /* prefill tensor-core down */
+  DS4MOE_SPAN_COUNT = 7
+} ds4moe_span_kernel;
 ds4moe_status ds4moe_profile_span(int32_t on, double *total_ns, int64_t *launches);
 
 #ifdef __cplusplus
