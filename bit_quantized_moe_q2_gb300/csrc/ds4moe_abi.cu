@@ -3,6 +3,7 @@
 // softmax over the selected experts, token->expert bucketing and the
 // weighted combine.  The expert GEMV/GEMM kernels live in ffn_decode.cu and
 // ffn_prefill.cu.
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -974,6 +975,33 @@ BucketArgs bucket_args(const ds4moe_layer &L, void *ws, const WsLayout &lay, con
                     ws_ptr<int32_t>(ws, lay.nvalid), out};
 }
 
+// Attributes of the routing chain's kernels, set once per device (kernel
+// attributes are per device) under a lock; a failed set is returned to the
+// caller and tried again on the next call.  One shared-memory carveout for
+// every kernel of the chain: consecutive grids then never wait for an SM to
+// reconfigure its L1 / shared split.
+constexpr int kAttrDevices = 64;
+cudaError_t chain_attributes() {
+  static std::mutex mu;
+  static std::atomic<bool> done[kAttrDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kAttrDevices) return cudaErrorInvalidDevice;
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  e = cudaFuncSetAttribute(k_bucket, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_bucket, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  for (auto kern : {k_route_small<1, kRouteLogits>, k_route_small<2, kRouteLogits>, k_route_small<4, kRouteLogits>,
+                    k_route_small<8, kRouteLogits>, k_route_small<1, kRouteTopk>, k_route_small<2, kRouteTopk>,
+                    k_route_small<4, kRouteTopk>, k_route_small<8, kRouteTopk>, k_route_small<1, kRouteBucket>,
+                    k_route_small<2, kRouteBucket>, k_route_small<4, kRouteBucket>, k_route_small<8, kRouteBucket>})
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
+  return e;
+}
+
 // Bucketing, expert FFN and combine.  With `logits` (fused decode path) the
 // bucketing kernel first ranks the experts of every token and writes idx / w;
 // with `bucketed` the router kernel has already done the whole bucketing step.
@@ -1050,20 +1078,8 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
     a.w_logits = logits != nullptr && P <= 32;  // the small bucketing path leaves raw selected logits in w
   }
   const size_t smem = sizeof(int32_t) * (32 * (size_t)E + E + 1);
-  static bool attr_set = false;
-  if (!attr_set) {
-    // one shared-memory carveout for every kernel of the chain: consecutive
-    // grids then never wait for an SM to reconfigure its L1/shared split
-    cudaFuncSetAttribute(k_bucket, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-    cudaFuncSetAttribute(k_bucket, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    for (auto kern : {k_route_small<1, kRouteLogits>, k_route_small<2, kRouteLogits>, k_route_small<4, kRouteLogits>,
-                      k_route_small<8, kRouteLogits>, k_route_small<1, kRouteTopk>, k_route_small<2, kRouteTopk>,
-                      k_route_small<4, kRouteTopk>, k_route_small<8, kRouteTopk>, k_route_small<1, kRouteBucket>,
-                      k_route_small<2, kRouteBucket>, k_route_small<4, kRouteBucket>, k_route_small<8, kRouteBucket>})
-      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    attr_set = true;
-  }
-  cudaError_t e = cudaSuccess;
+  cudaError_t e = chain_attributes();
+  if (e != cudaSuccess) return cuda_status(e);
   if (!bucketed) {
     ProfScope prof("bucket", s);
     // the tensor-core prefill reads the expert offsets: always the full path
@@ -1324,6 +1340,8 @@ ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const 
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float *lg = ws_ptr<float>(ws, lay.logits);
+  const cudaError_t ea = chain_attributes();
+  if (ea != cudaSuccess) return cuda_status(ea);
   if (T == 1 && (r16 || t1_chain_ok(*L))) {
     // one token on the single-token kernels: the router grid only writes the
     // logits, and every CTA of the FFN grids ranks the experts itself (no

@@ -1,14 +1,20 @@
 // Expert FFN for decode batches.
 //
-// Tensor-core path (mma.sync m16n8k16, bf16 operands, fp32 accumulate):
-// the 2-bit / 4-bit codes are turned into exact bf16 A-operands in
-// registers (a magic-number OR places the code in the mantissa of 128.0), so
-// each tensor-core product is exact; per-16-value Q2_K scales are folded into
-// the operand with one packed bf16 FMA (sc * q <= 45 is exact in bf16), the
-// Q2_K mins and the Q4_1 (d, m) are applied per block in an fp32 epilogue.
-// Weight rows are staged into shared memory by bulk asynchronous copies (TMA,
-// non-tensor form) completing on mbarriers, two stages per warp.  Tokens of
-// one expert (up to 8 per group) fill the n = 8 side of the MMA.
+// Tensor-core path (mma.sync m16n8k16, fp16 operands, fp32 accumulate).
+// The codes become exact fp16 A-operands in registers:
+//  - multi-token kernels: a code field ORed under the fp16 exponent of 1024
+//    reads as 1024 + 4^s q, and one packed fp16 FMA with (sc 4^-s,
+//    -1024 sc 4^-s) folds the Q2_K sub-block scale in exactly (sc q <= 45);
+//    B is the fp16 rounding of the tokens' activations (values beyond the
+//    fp16 range are flagged), up to 8 tokens of one expert on the n = 8 side;
+//  - single-token kernels (t1.cuh): a 2-bit field at bit 2e of a 16-bit half
+//    is the fp16 subnormal q 2^(2e - 24), used as is after one mask, and the
+//    activation operand is pre-scaled by a power of two per field position,
+//    so every product is exact.
+// The Q2_K mins and the Q4_1 / Q4_K (d, m) are applied per sub-block or block
+// in an fp32 epilogue, against sub-block sums of the activations carried as
+// hi + lo fp16 pairs.  Weight rows are staged into shared memory by bulk
+// asynchronous copies (TMA, non-tensor form) completing on mbarriers.
 //
 //   gate/up: one CTA per (token group, 16-row tile); each warp owns one K
 //            slice of both matrices, the slices are summed in shared memory,
