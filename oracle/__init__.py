@@ -77,6 +77,7 @@ def _L():
         lib.orc_quantize_f32.argtypes = [i32, p, p, i64, i64, p]
         lib.orc_weighted_sq_error.restype = ctypes.c_double
         lib.orc_weighted_sq_error.argtypes = [i32, p, p, i64, i64, p]
+        lib.orc_shared_ffn.argtypes = [i32, i32, p, p, p, i32, p, p, p]
         _lib = lib
     return _lib
 
@@ -306,6 +307,26 @@ def moe_ffn(D, F, E, qg, gate, qu, up, qd, down, x_bf16, idx, w) -> np.ndarray:
                           x.ctypes.data, idx.ctypes.data, w.ctypes.data, T, k, out.ctypes.data)
     if st:
         raise OracleError(st, "moe_ffn")
+    return out
+
+
+def shared_ffn(w1, w3, w2, x_bf16, base=None) -> np.ndarray:
+    """Shared expert ([DS4-2]: kept unquantised): bf16 w1, w3 [Fs, D] and
+    w2 [D, Fs] (bit patterns), x bf16 [T, D]; returns fp32 [T, D] =
+    base + w2 bf16(silu(w1 x) * (w3 x)), one rounding (base may be None)."""
+    w1, w3, w2 = _c(w1, np.uint16), _c(w3, np.uint16), _c(w2, np.uint16)
+    x = _c(x_bf16, np.uint16)
+    Fs, D = w1.shape
+    if w3.shape != (Fs, D) or w2.shape != (D, Fs) or x.ndim != 2 or x.shape[1] != D:
+        raise ValueError("shared_ffn: shapes")
+    T = x.shape[0]
+    b = None if base is None else _c(base, np.float32)
+    if b is not None and b.shape != (T, D):
+        raise ValueError("shared_ffn: base shape")
+    out = np.empty((T, D), np.float32)
+    st = _L().orc_shared_ffn(D, Fs, _ptr(w1), _ptr(w3), _ptr(w2), T, _ptr(x), _ptr(b), out.ctypes.data)
+    if st:
+        raise OracleError(st, "shared_ffn")
     return out
 
 

@@ -32,7 +32,9 @@
  * expert tensors are experts-major; in the 43-layer stack ([DS4-1]) the
  * residual stream stays fp32 (x += moe(..) with one fp32 rounding) and each
  * layer reads bf16(x / rms(x)), an RMS normalisation with unit weight --
- * without it the stated weight distributions overflow within a few layers.
+ * without it the stated weight distributions overflow within a few layers;
+ * the unquantised shared expert is bf16, the same SwiGLU, added with weight
+ * one.
  *
  * Pins: every function here is checked by tests/test_oracle_*.py against
  * facts the pages fix or mathematics fixes (hand-derived golden blocks,
@@ -583,6 +585,45 @@ int orc_moe_ffn(int D, int F, int E, int qg, const uint8_t *gate, int qu,
     }
     for (int c = 0; c < D; ++c) out[(int64_t)t * D + c] = (float)acc[c];
     free(acc); free(y);
+  }
+  return ORC_OK;
+}
+
+/* ---------------------------------------------------------- shared expert */
+/* [DS4-2] (summary bullets and the README's Model Weights bullets): only the
+ * routed experts are quantised; the shared expert, like the projections and
+ * the routing, keeps its original precision and runs for every token.
+ * Reading: its three matrices are bf16 (w1 = gate and w3 = up [Fs x D],
+ * w2 = down [D x Fs], row-major), the same SwiGLU as a routed expert with
+ * the hidden activation rounded to bf16, and its output is added to the
+ * routed combine with weight one.  Per token t:
+ *   g = w1 x, u = w3 x (double over the exact bf16 products),
+ *   h = bf16(silu(g) * u), y = w2 h (double),
+ *   out[t, :] = fp32(base[t, :] + y), or fp32(y) when base is NULL. */
+int orc_shared_ffn(int D, int Fs, const uint16_t *w1, const uint16_t *w3, const uint16_t *w2, int T,
+                   const uint16_t *x, const float *base, float *out) {
+  if (D <= 0 || Fs < 0 || T < 0) return ORC_EINVAL;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int t = 0; t < T; ++t) {
+    double *h = (double *)malloc(sizeof(double) * (size_t)(Fs > 0 ? Fs : 1));
+    const uint16_t *xt = x + (int64_t)t * D;
+    for (int f = 0; f < Fs; ++f) {
+      double g = 0.0, u = 0.0;
+      for (int j = 0; j < D; ++j) {
+        const double xj = orc_bf16(xt[j]);
+        g += orc_bf16(w1[(int64_t)f * D + j]) * xj;
+        u += orc_bf16(w3[(int64_t)f * D + j]) * xj;
+      }
+      const double silu = g / (1.0 + exp(-g));
+      h[f] = orc_bf16(orc_round_bf16(silu * u));
+    }
+    for (int c = 0; c < D; ++c) {
+      double y = 0.0;
+      for (int f = 0; f < Fs; ++f) y += orc_bf16(w2[(int64_t)c * Fs + f]) * h[f];
+      if (base) y += (double)base[(int64_t)t * D + c];
+      out[(int64_t)t * D + c] = (float)y;
+    }
+    free(h);
   }
   return ORC_OK;
 }
