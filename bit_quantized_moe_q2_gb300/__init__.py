@@ -29,7 +29,7 @@ EXPORTS = (
     "ds4moe_profile_enable", "ds4moe_profile_count", "ds4moe_profile_entry",
     "ds4moe_ffn_decode_noalloc", "ds4moe_moe_decode", "ds4moe_residual_norm", "ds4moe_stack_decode",
     "ds4moe_quantize_f32", "ds4moe_route_topk_select_bias", "ds4moe_debug_sync_wait",
-    "ds4moe_repack", "ds4moe_profile_span",
+    "ds4moe_repack", "ds4moe_profile_span", "ds4moe_shared_workspace_bytes", "ds4moe_shared_ffn",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -68,6 +68,9 @@ def lib():
         L.ds4moe_dequant.argtypes = [i32, p, i64, p, p]
         L.ds4moe_repack.argtypes = [i32, i32, p, i64, i64, p, p]
         L.ds4moe_profile_span.argtypes = [i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
+        L.ds4moe_shared_workspace_bytes.argtypes = [i32, i32, i32]
+        L.ds4moe_shared_workspace_bytes.restype = sz
+        L.ds4moe_shared_ffn.argtypes = [p, p, p, i32, i32, p, i32, p, i32, p, sz, p]
         L.ds4moe_quantize_f32.argtypes = [i32, p, p, i64, i64, p, ctypes.c_size_t, p, ctypes.c_size_t, p]
         L.ds4moe_workspace_bytes.argtypes = [ctypes.POINTER(Layer), i32, i32, i32]
         L.ds4moe_workspace_bytes.restype = sz
@@ -162,8 +165,24 @@ def ds4moe_repack(src_type, dst_type, src, rows, cols, dst, stream=None):
            "ds4moe_repack")
 
 
+def ds4moe_shared_workspace_bytes(d_model: int, d_shared: int, T: int) -> int:
+    return int(lib().ds4moe_shared_workspace_bytes(int(d_model), int(d_shared), int(T)))
+
+
+def ds4moe_shared_ffn(w1, w3, w2, x, out, ws, accumulate=False, stream=None):
+    """Shared expert: out (+)= w2 bf16(silu(w1 x) * (w3 x)).  w1, w3 [Fs, D]
+    and w2 [D, Fs] bf16 bit patterns (16-bit device tensors), x [T, D] bf16
+    bits, out [T, D] float32, ws a uint8 device tensor of at least
+    ds4moe_shared_workspace_bytes(D, Fs, T) bytes."""
+    Fs, D = w1.shape
+    T = x.shape[0]
+    _check(lib().ds4moe_shared_ffn(_ptr(w1), _ptr(w3), _ptr(w2), D, Fs, _ptr(x), T, _ptr(out), int(bool(accumulate)),
+                                   _ptr(ws), ws.numel(), _stream(stream)), "ds4moe_shared_ffn")
+
+
 # ds4moe_span_kernel order
-SPAN_KERNELS = ("route", "ffn_t1", "ffn_t1r", "gate_up_mma", "down_mma", "gate_up_tc", "down_tc")
+SPAN_KERNELS = ("route", "ffn_t1", "ffn_t1r", "gate_up_mma", "down_mma", "gate_up_tc", "down_tc",
+                "shared_gate_up_tc", "shared_down_tc")
 
 
 def ds4moe_profile_span(on: int = -1) -> dict:

@@ -11,7 +11,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libds4moe.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["ds4moe_abi.cu", "ffn_decode.cu", "ffn_t1r.cu", "ffn_prefill.cu", "profile.cu", "quantize_f32.cu", "quantize_ref.cpp"]
+SOURCES = ["ds4moe_abi.cu", "ffn_decode.cu", "ffn_t1r.cu", "ffn_prefill.cu", "shared_ffn.cu", "profile.cu", "quantize_f32.cu", "quantize_ref.cpp"]
 HEADERS = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")) + [
     os.path.join(ROOT, "include", "ds4moe.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

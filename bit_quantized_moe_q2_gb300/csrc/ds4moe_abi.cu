@@ -1168,7 +1168,26 @@ ds4moe_status ds4moe_profile_span(int32_t on, double *total_ns, int64_t *launche
   if (e == cudaSuccess) e = span_control_decode(on, total_ns, launches);
   if (e == cudaSuccess) e = span_control_t1r(on, total_ns, launches);
   if (e == cudaSuccess) e = span_control_prefill(on, total_ns, launches);
+  if (e == cudaSuccess) e = span_control_shared(on, total_ns, launches);
   return cuda_status(e);
+}
+
+size_t ds4moe_shared_workspace_bytes(int32_t d_model, int32_t d_shared, int32_t T) {
+  if (d_model <= 0 || d_shared < 0 || T < 0) return 0;
+  return shared_ws_bytes(d_model, d_shared, T);
+}
+
+ds4moe_status ds4moe_shared_ffn(const uint16_t *w1, const uint16_t *w3, const uint16_t *w2, int32_t d_model,
+                                int32_t d_shared, const uint16_t *x, int32_t T, float *out, int32_t accumulate,
+                                void *ws, size_t ws_bytes, void *stream) {
+  if (d_model <= 0 || d_model % 8 || d_shared < 0 || d_shared % 8 || T < 0 || (accumulate != 0 && accumulate != 1))
+    return DS4MOE_EINVAL;
+  if (T == 0) return DS4MOE_OK;
+  if (!x || !out || !ws || !aligned16(x) || !aligned16(out) || !aligned16(ws)) return DS4MOE_EINVAL;
+  if (d_shared > 0 && (!w1 || !w3 || !w2 || !aligned16(w1) || !aligned16(w3) || !aligned16(w2))) return DS4MOE_EINVAL;
+  if (ws_bytes < shared_ws_bytes(d_model, d_shared, T)) return DS4MOE_ESPACE;
+  return cuda_status(
+      launch_shared_ffn(w1, w3, w2, d_model, d_shared, x, T, out, accumulate, ws, static_cast<cudaStream_t>(stream)));
 }
 
 size_t ds4moe_workspace_bytes(const ds4moe_layer *L, int32_t T, int32_t k, int32_t prefill) {

@@ -207,6 +207,11 @@ cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s);
 // hook of its h-ready wait and its device-side span record.
 bool t1r_ok(const ds4moe_layer &L, int k);
 cudaError_t launch_ffn_t1r(const FfnArgs &a, cudaStream_t s);
+// shared expert (shared_ffn.cu)
+size_t shared_ws_bytes(int D, int Fs, int T);
+bool shared_uses_tc(int D, int Fs, int T);
+cudaError_t launch_shared_ffn(const uint16_t *w1, const uint16_t *w3, const uint16_t *w2, int D, int Fs,
+                              const uint16_t *x, int T, float *out, int accumulate, void *ws, cudaStream_t s);
 cudaError_t launch_repack(bool to_r16, const void *src, void *dst, int64_t rows, int64_t cols, cudaStream_t s);
 cudaError_t t1r_set_sync_hook(int32_t budget, int32_t extra);
 cudaError_t launch_ffn_prefill(const FfnArgs &a, cudaStream_t s);

@@ -85,5 +85,6 @@ cudaError_t span_control_abi(int on, double *total_ns, int64_t *launches);
 cudaError_t span_control_decode(int on, double *total_ns, int64_t *launches);
 cudaError_t span_control_t1r(int on, double *total_ns, int64_t *launches);
 cudaError_t span_control_prefill(int on, double *total_ns, int64_t *launches);
+cudaError_t span_control_shared(int on, double *total_ns, int64_t *launches);
 
 }  // namespace ds4

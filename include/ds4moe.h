@@ -399,6 +399,43 @@ ds4moe_status ds4moe_ffn_decode_noalloc(const ds4moe_layer *L, const uint16_t *x
                                         void *stream);
 
 /*
+ * ds4moe_shared_ffn -- DEVICE, asynchronous on `stream`.  The shared expert
+ * of the model ("【#2】ds4.c 해독하기", summary bullets and the README's Model
+ * Weights bullets: only the routed experts are quantised; the shared expert,
+ * like the projections and the routing, keeps its precision and runs for
+ * every token).  The pages give no width, so d_shared is the caller's.
+ * Reading: bf16 weights, the routed experts' SwiGLU with h rounded to bf16,
+ * output added to the routed combine with weight one.  Per token t:
+ *   h[t] = bf16(silu(w1 x[t]) * (w3 x[t])),
+ *   out[t] = w2 h[t]            (accumulate = 0)
+ *   out[t] = out[t] + w2 h[t]   (accumulate = 1: after ds4moe_moe_decode /
+ *                                ds4moe_ffn_decode has written the combine)
+ * fp32 accumulation over the exact bf16 products.
+ *
+ * w1, w3: [d_shared][d_model] bf16 bit patterns, row-major; w2:
+ * [d_model][d_shared]; x: [T][d_model] bf16; out: [T][d_model] fp32.  All
+ * device pointers 16-byte aligned; d_model and d_shared multiples of 8
+ * (d_shared may be 0: out = 0, or unchanged when accumulating).  Up to 64
+ * tokens run bandwidth-bound GEMVs on the CUDA cores; more tokens, with
+ * d_model a multiple of 256 and d_shared of 128, run tcgen05 GEMMs with TMA
+ * operands (other shapes keep the GEMVs).
+ *
+ * ws: caller-owned workspace of at least ds4moe_shared_workspace_bytes
+ * (status word + h [T][d_shared] bf16), initialised once with
+ * ds4moe_workspace_init before its first use (as for the routed entry
+ * points); ds4moe_stream_status(ws) reports and clears a device-side error
+ * (a bounded wait that gave up: DS4MOE_ETIMEOUT; a non-finite h:
+ * DS4MOE_EDEVICE).  Host errors:
+ * EINVAL (sizes, alignment, null pointers, accumulate not 0 / 1), ESPACE
+ * (workspace too small), ECUDA.  Calls sharing a workspace must not overlap.
+ */
+size_t ds4moe_shared_workspace_bytes(int32_t d_model, int32_t d_shared, int32_t T);
+ds4moe_status ds4moe_shared_ffn(const uint16_t *w1, const uint16_t *w3, const uint16_t *w2,
+                                int32_t d_model, int32_t d_shared, const uint16_t *x, int32_t T,
+                                float *out, int32_t accumulate, void *ws, size_t ws_bytes,
+                                void *stream);
+
+/*
  * ds4moe_debug_sync_wait -- HOST, synchronous; a fault-injection hook for
  * tests of failure detection (no counterpart in the pages).  It applies to
  * the single-token fused decode on all-Q2_K layers with d_model = 2 d_ff:
@@ -461,7 +498,9 @@ typedef enum {
   DS4MOE_SPAN_DOWN_MMA = 4,     /* multi-token decode down (+ combine) */
   DS4MOE_SPAN_GATE_UP_TC = 5,   /* prefill tensor-core gate/up + SwiGLU */
   DS4MOE_SPAN_DOWN_TC = 6,      /* prefill tensor-core down */
-  DS4MOE_SPAN_COUNT = 7
+  DS4MOE_SPAN_SHARED_GATE_UP_TC = 7,  /* shared expert, tensor-core gate/up + SwiGLU */
+  DS4MOE_SPAN_SHARED_DOWN_TC = 8,     /* shared expert, tensor-core down */
+  DS4MOE_SPAN_COUNT = 9
 } ds4moe_span_kernel;
 ds4moe_status ds4moe_profile_span(int32_t on, double *total_ns, int64_t *launches);
 

@@ -166,3 +166,28 @@ def test_device_entry_points_reject_bad_arguments_before_launch(M):
     # fault-injection hook: a budget below one poll or a negative offset
     assert L.ds4moe_debug_sync_wait(0, 0) == M.DS4MOE_EINVAL
     assert L.ds4moe_debug_sync_wait(100, -1) == M.DS4MOE_EINVAL
+
+
+def test_shared_ffn_rejects_bad_arguments_before_launch(M):
+    """ds4moe_shared_ffn validates on the host (fake, aligned pointers: nothing
+    is dereferenced when a check fails)."""
+    L = M.lib()
+    A = 1 << 20  # aligned fake addresses
+    D, Fs, T = 256, 128, 4
+    need = M.ds4moe_shared_workspace_bytes(D, Fs, T)
+    assert need >= 256 + T * Fs * 2
+    assert M.ds4moe_shared_workspace_bytes(0, Fs, T) == 0
+    assert M.ds4moe_shared_workspace_bytes(D, -1, T) == 0
+
+    def call(w1=A, w3=A, w2=A, d=D, fs=Fs, x=A, t=T, out=A, acc=0, ws=A, nws=None):
+        return L.ds4moe_shared_ffn(w1, w3, w2, d, fs, x, t, out, acc, ws, need if nws is None else nws, None)
+
+    assert call(d=260) == M.DS4MOE_EINVAL          # d_model not a multiple of 8
+    assert call(fs=-8) == M.DS4MOE_EINVAL
+    assert call(fs=12) == M.DS4MOE_EINVAL          # d_shared not a multiple of 8
+    assert call(acc=2) == M.DS4MOE_EINVAL
+    assert call(x=A + 4) == M.DS4MOE_EINVAL        # misaligned
+    assert call(out=None) == M.DS4MOE_EINVAL
+    assert call(w2=None) == M.DS4MOE_EINVAL
+    assert call(nws=need - 1) == M.DS4MOE_ESPACE
+    assert call(t=0, x=None, out=None) == M.DS4MOE_OK  # zero tokens: nothing to do
