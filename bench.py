@@ -92,6 +92,9 @@ def parse_args(argv=None):
                     help="single-layer or stack decode at T = 1: repack Q2_K weights into the 16-row tile order")
     ap.add_argument("--plain", action="store_true",
                     help="workload 1 alone on plain Q2_K blocks (no sub-records)")
+    ap.add_argument("--shared", type=int, default=0, metavar="D_SHARED",
+                    help="time the shared expert alone (bf16, d_model of the workload, this width; "
+                         "--tokens sets the tokens per step, default 1)")
     return ap.parse_args(argv)
 
 
@@ -1068,6 +1071,89 @@ def run_quantize(args, w: synth.Workload):
                                    "peak_source": kind}}), flush=True)
 
 
+def run_shared(args, w: synth.Workload):
+    """The shared expert alone (ds4moe_shared_ffn): bf16 w1, w3 [Fs, D] and w2
+    [D, Fs], seeded N(0, 0.02) weights, x ~ N(0, 1) bf16, out accumulated
+    into.  8 weight copies rotate (8 x 50 MB > L2 at the Flash shape).  The
+    pages give no width: --shared sets it.  Up to 64 tokens: weight-stream
+    GB/s against HBM; more: TFLOP/s against the sustained bf16 peak."""
+    import torch
+    rank, world, local = init_dist(torch)
+    M = load_library(rank, world)
+    from bit_quantized_moe_q2_gb300.device import check_status
+    D, Fs, T = w.d_model, args.shared, max(1, args.tokens or 1)
+    g = torch.Generator(device="cuda").manual_seed(w.seed)
+    bits = lambda shape: (torch.randn(shape, device="cuda", generator=g) * 0.02).to(torch.bfloat16).view(torch.int16)
+    n_copies = 8
+    W = [(bits((Fs, D)), bits((Fs, D)), bits((D, Fs))) for _ in range(n_copies)]
+    xs = [(torch.randn((T, D), device="cuda", generator=g)).to(torch.bfloat16).view(torch.int16) for _ in range(2)]
+    out = torch.zeros((T, D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(M.ds4moe_shared_workspace_bytes(D, Fs, T), dtype=torch.uint8, device="cuda")
+    M.ds4moe_workspace_init(ws)
+    stream = torch.cuda.Stream()
+
+    def step(i):
+        w1, w3, w2 = W[i % n_copies]
+        M.ds4moe_shared_ffn(w1, w3, w2, xs[i % 2], out, ws, accumulate=True, stream=stream)
+
+    graphs = []
+    with torch.cuda.stream(stream):
+        for i in range(n_copies):
+            step(i)
+    stream.synchronize()
+    check_status(ws, stream)
+    for j in range(n_copies):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            step(j)
+        graphs.append(gr)
+
+    def replay(i):
+        graphs[i % n_copies].replay()
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            replay(i)
+    stream.synchronize()
+    steps = args.steps if T <= 64 else max(3, min(args.steps, 200))
+    ms, clocks = measure_clocks(torch, stream, replay, gpu_index(local), steps, world)
+    check_status(ws, stream)
+    step_s = ms / steps / 1000.0
+    kernels = span_pass(M, torch, stream, replay, min(steps, 50))
+    wbytes = 3 * D * Fs * 2
+    cfg = {"workload": f"shared-expert-bf16-d{D}-f{Fs}-t{T}", "d_model": D, "d_shared": Fs, "tokens_per_step": T,
+           "weights": "bf16, seeded N(0, 0.02)", "l2": f"{n_copies} weight copies of {wbytes / 1e6:.0f} MB rotate"}
+    line = {"metric": "shared-expert tokens/s", "value": world * T / step_s, "unit": "tokens/s", "n_gpus": world,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 operands, f32 accumulate", "data": "synthetic",
+            "config": cfg, "kernels": kernels, "clocks": clocks}
+    if "shared_gate_up_tc" in kernels:
+        flops = 2.0 * 3 * D * Fs * T
+        us = kernels["shared_gate_up_tc"]["avg_us"] + kernels["shared_down_tc"]["avg_us"]
+        peak, kind = measured_tensor_peak(sustained=True)
+        line["tflops"] = flops / step_s / 1e12
+        line["roofline"] = {"kernel": "shared-expert tcgen05 GEMMs (gate/up + SwiGLU, down + accumulate)",
+                            "bound": "tensor", "achieved": flops / (us * 1e-6) / 1e12, "peak": peak,
+                            "unit": "TFLOP/s", "frac": flops / (us * 1e-6) / 1e12 / peak, "traffic": None,
+                            "algorithmic_flops_per_launch": flops, "avg_launch_us": us,
+                            "timing": "device spans of the two kernels",
+                            "peak_source": f"{kind} bf16_tflops_sustained"}
+    else:
+        algo = wbytes + T * D * 2 + 2 * T * D * 4
+        peak, kind = measured_peaks()
+        gbs = algo / step_s / 1e9
+        line["roofline"] = {"kernel": "shared-expert GEMVs (gate/up + SwiGLU, down + accumulate), whole call",
+                            "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                            "traffic": None, "algorithmic_bytes_per_launch": algo, "avg_launch_us": step_s * 1e6,
+                            "timing": "CUDA events over graph replays of the call (two kernels)",
+                            "peak_source": kind}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
     w = synth.WORKLOADS[args.workload]
@@ -1079,6 +1165,9 @@ def main(argv=None):
         raise SystemExit("bench.py times workloads 0-5")
     if args.quantize:
         run_quantize(args, w)
+        return
+    if args.shared:
+        run_shared(args, w)
         return
     default = args.workload == 1 and not args.n_expert and not args.tokens and not args.plain
     if args.impl == "reference":

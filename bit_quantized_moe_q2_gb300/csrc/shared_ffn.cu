@@ -8,7 +8,7 @@
 // over the exact bf16 products.
 //
 // Two paths:
-//  - up to kSimtTokens tokens: bandwidth-bound GEMVs on the CUDA cores, one
+//  - up to kSimtTokens (8) tokens: bandwidth-bound GEMVs on the CUDA cores, one
 //    warp per hidden unit (gate/up) or output row (down), 16-byte loads
 //    along the row, tokens in groups of eight, a fixed-order warp reduction;
 //  - more tokens: persistent tcgen05 GEMMs.  A = 128 tokens x 64 K of the
@@ -28,8 +28,9 @@
 namespace ds4 {
 namespace {
 
-constexpr int kSimtTokens = 64;  // at most this many tokens take the GEMV path
+constexpr int kSimtTokens = 8;   // at most this many tokens take the GEMV path
 constexpr int kGT = 8;           // tokens per group in the GEMV kernels
+constexpr int kGemvWarps = 4;    // warps (rows) per CTA of the GEMV kernels
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -49,12 +50,12 @@ __device__ __forceinline__ float warp_sum(float v) {
 // ------------------------------------------------------------ GEMV path
 // One warp per hidden unit f: g = w1[f] . x[t], u = w3[f] . x[t] for every
 // token, h[t][f] = bf16(silu(g) * u).
-__global__ void __launch_bounds__(256) k_shared_gu_simt(const uint16_t *__restrict__ w1,
+__global__ void __launch_bounds__(32 * kGemvWarps) k_shared_gu_simt(const uint16_t *__restrict__ w1,
                                                         const uint16_t *__restrict__ w3,
                                                         const uint16_t *__restrict__ x, int D, int Fs, int T,
                                                         uint16_t *__restrict__ h) {
   const int lane = threadIdx.x & 31;
-  const int f = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int f = blockIdx.x * kGemvWarps + (threadIdx.x >> 5);
   if (f >= Fs) return;
   const uint4 *r1 = reinterpret_cast<const uint4 *>(w1 + (int64_t)f * D);
   const uint4 *r3 = reinterpret_cast<const uint4 *>(w3 + (int64_t)f * D);
@@ -64,7 +65,7 @@ __global__ void __launch_bounds__(256) k_shared_gu_simt(const uint16_t *__restri
     float g[kGT], u[kGT];
 #pragma unroll
     for (int t = 0; t < kGT; ++t) g[t] = u[t] = 0.f;
-#pragma unroll 2
+#pragma unroll 4
     for (int c = lane; c < nc; c += 32) {
       float a[8], b[8];
       bf16x8_to_f32(__ldg(r1 + c), a);
@@ -93,11 +94,11 @@ __global__ void __launch_bounds__(256) k_shared_gu_simt(const uint16_t *__restri
 }
 
 // One warp per output row d: y = w2[d] . h[t]; out[t][d] = y or out + y.
-__global__ void __launch_bounds__(256) k_shared_down_simt(const uint16_t *__restrict__ w2,
+__global__ void __launch_bounds__(32 * kGemvWarps) k_shared_down_simt(const uint16_t *__restrict__ w2,
                                                           const uint16_t *__restrict__ h, int D, int Fs, int T,
                                                           float *__restrict__ out, int accumulate) {
   const int lane = threadIdx.x & 31;
-  const int d = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int d = blockIdx.x * kGemvWarps + (threadIdx.x >> 5);
   if (d >= D) return;
   const uint4 *r2 = reinterpret_cast<const uint4 *>(w2 + (int64_t)d * Fs);
   const int nc = Fs / 8;
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(256) k_shared_down_simt(const uint16_t *__rest
     float y[kGT];
 #pragma unroll
     for (int t = 0; t < kGT; ++t) y[t] = 0.f;
-#pragma unroll 2
+#pragma unroll 4
     for (int c = lane; c < nc; c += 32) {
       float a[8];
       bf16x8_to_f32(__ldg(r2 + c), a);
@@ -412,11 +413,11 @@ cudaError_t launch_shared_ffn(const uint16_t *w1, const uint16_t *w3, const uint
   }
   {
     ProfScope p("shared_gate_up_simt", s);
-    k_shared_gu_simt<<<(Fs + 7) / 8, 256, 0, s>>>(w1, w3, x, D, Fs, T, h);
+    k_shared_gu_simt<<<(Fs + kGemvWarps - 1) / kGemvWarps, 32 * kGemvWarps, 0, s>>>(w1, w3, x, D, Fs, T, h);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   ProfScope p("shared_down_simt", s);
-  k_shared_down_simt<<<(D + 7) / 8, 256, 0, s>>>(w2, h, D, Fs, T, out, accumulate);
+  k_shared_down_simt<<<(D + kGemvWarps - 1) / kGemvWarps, 32 * kGemvWarps, 0, s>>>(w2, h, D, Fs, T, out, accumulate);
   return cudaGetLastError();
 }
 

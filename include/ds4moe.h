@@ -415,7 +415,7 @@ ds4moe_status ds4moe_ffn_decode_noalloc(const ds4moe_layer *L, const uint16_t *x
  * w1, w3: [d_shared][d_model] bf16 bit patterns, row-major; w2:
  * [d_model][d_shared]; x: [T][d_model] bf16; out: [T][d_model] fp32.  All
  * device pointers 16-byte aligned; d_model and d_shared multiples of 8
- * (d_shared may be 0: out = 0, or unchanged when accumulating).  Up to 64
+ * (d_shared may be 0: out = 0, or unchanged when accumulating).  Up to 8
  * tokens run bandwidth-bound GEMVs on the CUDA cores; more tokens, with
  * d_model a multiple of 256 and d_shared of 128, run tcgen05 GEMMs with TMA
  * operands (other shapes keep the GEMVs).

@@ -1,5 +1,5 @@
 """GPU parity of the shared expert (ds4moe_shared_ffn) against the oracle:
-the GEMV path (up to 64 tokens) and the tcgen05 path (more tokens), with and
+the GEMV path (up to 8 tokens) and the tcgen05 path (more tokens), with and
 without accumulation, ragged token counts, a shape the tensor-core path does
 not take, width zero, run-to-run bit equality, and the routed layer plus the
 shared expert against the oracle's composition.  Bar as for every FFN test:
@@ -60,10 +60,10 @@ def _gpu(M, w1, w3, w2, x, base=None, spans=False):
     return out.cpu().numpy(), st, ran
 
 
-# (d_model, d_shared, tokens): GEMV path up to 64 tokens
+# (d_model, d_shared, tokens): GEMV path up to 8 tokens, or a shape without tensor-core tiles
 SIMT = [(256, 64, 1), (1024, 512, 5), (4096, 2048, 8), (512, 200, 64), (640, 96, 13)]
-# tensor-core path: d_model % 256 == 0, d_shared % 128 == 0, more than 64 tokens
-TC = [(1024, 512, 65), (2048, 1024, 300), (4096, 2048, 130), (1536, 384, 256)]
+# tensor-core path: d_model % 256 == 0, d_shared % 128 == 0, more than 8 tokens
+TC = [(1024, 512, 9), (1024, 512, 65), (2048, 1024, 300), (4096, 2048, 130), (1536, 384, 256)]
 
 
 @pytest.mark.parametrize("D,Fs,T", SIMT)
