@@ -30,6 +30,7 @@ EXPORTS = (
     "ds4moe_ffn_decode_noalloc", "ds4moe_moe_decode", "ds4moe_residual_norm", "ds4moe_stack_decode",
     "ds4moe_quantize_f32", "ds4moe_route_topk_select_bias", "ds4moe_debug_sync_wait",
     "ds4moe_repack", "ds4moe_profile_span", "ds4moe_shared_workspace_bytes", "ds4moe_shared_ffn",
+    "ds4moe_gather_rows", "ds4moe_combine_pairs",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -71,6 +72,8 @@ def lib():
         L.ds4moe_shared_workspace_bytes.argtypes = [i32, i32, i32]
         L.ds4moe_shared_workspace_bytes.restype = sz
         L.ds4moe_shared_ffn.argtypes = [p, p, p, i32, i32, p, i32, p, i32, p, sz, p]
+        L.ds4moe_gather_rows.argtypes = [p, p, i32, i32, p, p]
+        L.ds4moe_combine_pairs.argtypes = [p, p, p, i32, i32, i32, p, p]
         L.ds4moe_quantize_f32.argtypes = [i32, p, p, i64, i64, p, ctypes.c_size_t, p, ctypes.c_size_t, p]
         L.ds4moe_workspace_bytes.argtypes = [ctypes.POINTER(Layer), i32, i32, i32]
         L.ds4moe_workspace_bytes.restype = sz
@@ -178,6 +181,20 @@ def ds4moe_shared_ffn(w1, w3, w2, x, out, ws, accumulate=False, stream=None):
     T = x.shape[0]
     _check(lib().ds4moe_shared_ffn(_ptr(w1), _ptr(w3), _ptr(w2), D, Fs, _ptr(x), T, _ptr(out), int(bool(accumulate)),
                                    _ptr(ws), ws.numel(), _stream(stream)), "ds4moe_shared_ffn")
+
+
+def ds4moe_gather_rows(x, rows, dst, stream=None):
+    """dst[j] = x[rows[j]]: x, dst bf16-bit device tensors [., D]; rows int32 [n]."""
+    _check(lib().ds4moe_gather_rows(_ptr(x), _ptr(rows), rows.numel(), x.shape[1], _ptr(dst), _stream(stream)),
+           "ds4moe_gather_rows")
+
+
+def ds4moe_combine_pairs(y, pos, w, out, stream=None):
+    """out[t] = sum_i w[t, i] * y[pos[t, i]] in rank order (pos < 0 skipped):
+    y float32 [., D], pos int32 [T, k], w float32 [T, k], out float32 [T, D]."""
+    T, k = pos.shape
+    _check(lib().ds4moe_combine_pairs(_ptr(y), _ptr(pos), _ptr(w), T, k, out.shape[1], _ptr(out), _stream(stream)),
+           "ds4moe_combine_pairs")
 
 
 # ds4moe_span_kernel order

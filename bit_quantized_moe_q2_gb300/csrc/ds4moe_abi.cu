@@ -1099,6 +1099,32 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
   return cuda_status(e);
 }
 
+// ------------------------------------------------ expert-parallel data plane
+// dst[j] = x[rows[j]] (bf16 rows of d_model values, 16-byte chunks); one
+// thread per chunk.
+__global__ void k_gather_rows(const uint4 *__restrict__ x, const int32_t *__restrict__ rows, int n, int nc,
+                              uint4 *__restrict__ dst) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)n * nc) return;
+  const int j = (int)(i / nc), c = (int)(i % nc);
+  dst[i] = __ldg(x + (int64_t)rows[j] * nc + c);
+}
+
+// out[t][c] = sum_{i < k} w[t k + i] * y[pos[t k + i]][c], in rank order i,
+// skipping pairs with pos < 0; one thread per output element.
+__global__ void k_combine_pairs(const float *__restrict__ y, const int32_t *__restrict__ pos,
+                                const float *__restrict__ w, int T, int k, int D, float *__restrict__ out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)T * D) return;
+  const int t = (int)(i / D), c = (int)(i % D);
+  float acc = 0.f;
+  for (int j = 0; j < k; ++j) {
+    const int p = pos[(int64_t)t * k + j];
+    if (p >= 0) acc = fmaf(w[(int64_t)t * k + j], y[(int64_t)p * D + c], acc);
+  }
+  out[i] = acc;
+}
+
 }  // namespace
 
 // =================================================================== C ABI
@@ -1415,6 +1441,32 @@ ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const 
   }
   return run_ffn(false, L, x, idx, w, T, k, out, ws, ws_bytes, stream, lg, fused, false,
                  !fused && decode_mma_ok(*L));
+}
+
+ds4moe_status ds4moe_gather_rows(const uint16_t *x, const int32_t *rows, int32_t n, int32_t d_model,
+                                uint16_t *dst, void *stream) {
+  if (n < 0 || d_model <= 0 || d_model % 8) return DS4MOE_EINVAL;
+  if (n == 0) return DS4MOE_OK;
+  if (!x || !rows || !dst || !aligned16(x) || !aligned16(dst)) return DS4MOE_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int nc = d_model / 8;
+  const int64_t total = (int64_t)n * nc;
+  ProfScope prof("gather_rows", s);
+  k_gather_rows<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(reinterpret_cast<const uint4 *>(x), rows, (int)n, nc,
+                                                                reinterpret_cast<uint4 *>(dst));
+  return cuda_status(cudaGetLastError());
+}
+
+ds4moe_status ds4moe_combine_pairs(const float *y, const int32_t *pos, const float *w, int32_t T, int32_t k,
+                                   int32_t d_model, float *out, void *stream) {
+  if (T < 0 || k < 1 || k > 32 || d_model <= 0) return DS4MOE_EINVAL;
+  if (T == 0) return DS4MOE_OK;
+  if (!pos || !w || !out) return DS4MOE_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t total = (int64_t)T * d_model;
+  ProfScope prof("combine_pairs", s);
+  k_combine_pairs<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(y, pos, w, (int)T, (int)k, (int)d_model, out);
+  return cuda_status(cudaGetLastError());
 }
 
 ds4moe_status ds4moe_residual_norm(float *x_res, const float *out, uint16_t *x_next, int32_t T, int32_t d_model,

@@ -399,6 +399,33 @@ ds4moe_status ds4moe_ffn_decode_noalloc(const ds4moe_layer *L, const uint16_t *x
                                         void *stream);
 
 /*
+ * Expert-parallel data plane (no counterpart in the pages' single-process
+ * engine; the pages split the model across machines by layer slices,
+ * "【#6】ds4.c 분석하기").  With the experts of a layer partitioned across
+ * ranks, a rank sends each (token, selected expert) pair's activations to
+ * the expert's owner, the owner runs the expert FFN on the pairs it
+ * receives (ds4moe_ffn_decode / ds4moe_ffn_prefill with k = 1, weight 1),
+ * and the outputs come back to the token's rank for the combine.  The
+ * exchange itself is the caller's (e.g. NCCL all-to-all).
+ *
+ * ds4moe_gather_rows -- DEVICE, asynchronous: dst[j] = x[rows[j]] for
+ * j < n; x and dst bf16 [.][d_model], d_model a multiple of 8, both 16-byte
+ * aligned; rows int32 [n], each in range (not checked on the device).
+ *
+ * ds4moe_combine_pairs -- DEVICE, asynchronous: out[t][c] =
+ * sum_{i < k} w[t k + i] * y[pos[t k + i]][c] in rank order i (fp32 FMA
+ * chain), skipping pairs with pos < 0 (an expert id out of range); y fp32
+ * [.][d_model] (the returned expert outputs), pos int32 [T k] (row of pair
+ * t k + i in y), w fp32 [T k], out fp32 [T][d_model].
+ *
+ * Host errors: EINVAL (sizes, alignment, null pointers), ECUDA.
+ */
+ds4moe_status ds4moe_gather_rows(const uint16_t *x, const int32_t *rows, int32_t n, int32_t d_model,
+                                 uint16_t *dst, void *stream);
+ds4moe_status ds4moe_combine_pairs(const float *y, const int32_t *pos, const float *w, int32_t T,
+                                   int32_t k, int32_t d_model, float *out, void *stream);
+
+/*
  * ds4moe_shared_ffn -- DEVICE, asynchronous on `stream`.  The shared expert
  * of the model ("【#2】ds4.c 해독하기", summary bullets and the README's Model
  * Weights bullets: only the routed experts are quantised; the shared expert,
