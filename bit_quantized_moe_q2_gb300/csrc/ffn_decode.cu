@@ -423,6 +423,205 @@ __global__ void __launch_bounds__(512) k_gate_up_mma(FfnArgs a, int kp, uint32_t
   }
 }
 
+// ====================================================== gate / up, persistent
+// T > 1 with gate and up in one format (Q2_K or Q4_1), d_model <= 4096: one
+// CTA per SM with nbk = d_model / 256 consumer warps (warp w: 256-value K
+// block w of both the gate and the up tile), a producer warp that streams
+// whole 16-row gate + up tiles (one or a few bulk copies each, the T = 1
+// bank-group layout) into a ring, and a reducer warp.  Each CTA takes a
+// contiguous range of the (token group, 16-row tile) units, so consecutive
+// units mostly share their token group and a consumer loads that group's
+// activation operand into registers only when the group changes.  The
+// reducer sums the K partials in a fixed order (warp 0 .. nbk - 1), applies
+// SwiGLU and writes h and its sub-block sums, the operands of the down
+// kernels, exactly as the one-CTA-per-unit kernel does.
+constexpr int kMtMaxK = 16;  // consumer warps: d_model <= 4096
+constexpr int kMtPart = 2;   // partial-sum slots between the consumers and the reducer
+
+size_t gate_up_mt_smem(uint32_t tile, int nbk, int nstage) {
+  return (size_t)nstage * 2 * tile + (size_t)kMtPart * nbk * 32 * 2 * sizeof(float4) +
+         sizeof(uint64_t) * (2 * (size_t)nstage + 2 * kMtPart);
+}
+
+template <int Q, bool FIN>
+__global__ void __launch_bounds__((kMtMaxK + 2) * 32, 1) k_gate_up_mt(FfnArgs a, int nstage) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const SpanExit span_exit(DS4MOE_SPAN_GATE_UP_MMA);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
+  const int D = a.L.d_model, F = a.L.d_ff, nbk = D / 256;
+  const int64_t rb = row_bytes(Q, D);
+  const T1Tile tl = t1_tile((uint32_t)rb);
+  const uint32_t tile = t1_tile_bytes(tl), stage = 2u * tile;
+  const int wprod = nbk, wred = nbk + 1;
+  // shared memory: stages (gate tile | up tile) | partials | barriers
+  float4 *red = reinterpret_cast<float4 *>(smem + (size_t)nstage * stage);  // [kMtPart][nbk][32][2]
+  uint64_t *full = reinterpret_cast<uint64_t *>(red + (size_t)kMtPart * nbk * 64);
+  uint64_t *empty = full + nstage, *pfull = empty + nstage, *pempty = pfull + kMtPart;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < nstage; ++st) {
+      ptx::mbar_init(&full[st], 1);
+      ptx::mbar_init(&empty[st], nbk);
+    }
+    for (int pt = 0; pt < kMtPart; ++pt) {
+      ptx::mbar_init(&pfull[pt], nbk);
+      ptx::mbar_init(&pempty[pt], 1);
+    }
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  const Q2kLane kl = q2k_lane(c);
+  // groups, permutation, fp16 x and its sums come from the bucketing grid
+  ptx::pdl_wait();
+  span_begin(DS4MOE_SPAN_GATE_UP_MMA);
+  ptx::pdl_launch_dependents();
+  if (FIN && blockIdx.x == 0 && w == wred) finish_routing_weights(const_cast<float *>(a.w), a.T, a.k);
+  clear_combine_counters(a, threadIdx.x, blockDim.x);
+  const int ntile = F / 16;
+  const int U = __ldcg(&a.hdr->n_groups) * ntile, G = gridDim.x;
+  const int u0 = (int)((int64_t)blockIdx.x * U / G), u1 = (int)((int64_t)(blockIdx.x + 1) * U / G);
+  auto load_group = [&](int gi) {
+    const int4 v = __ldcg(reinterpret_cast<const int4 *>(a.groups + gi));
+    return Group{v.x, v.y, v.z, v.w};
+  };
+  bool timed_out = false;
+  if (w == wprod) {
+    const uint8_t *gate = static_cast<const uint8_t *>(a.L.gate), *up = static_cast<const uint8_t *>(a.L.up);
+    const uint32_t nc = t1_copies(tl);
+    int gi = -1, issued = 0;
+    Group grp{};
+    for (int u = u0; u < u1; ++u, ++issued) {
+      const int it = u - u0, st = it % nstage;
+      if (it >= nstage && !ptx::mbar_wait(&empty[st], ((it / nstage) & 1) ^ 1)) {
+        if (lane == 0) record_status(a.hdr, DS4MOE_ETIMEOUT);
+        break;
+      }
+      if (u / ntile != gi) {
+        gi = u / ntile;
+        grp = load_group(gi);
+      }
+      const int64_t row0 = (int64_t)grp.e * F + (u % ntile) * 16;
+      uint8_t *dst = smem + (size_t)st * stage;
+      if (lane == 0) ptx::mbar_arrive_expect_tx(&full[st], 32u * (uint32_t)rb);
+      __syncwarp();
+      if ((uint32_t)lane < 2u * nc) {
+        const uint32_t mat = (uint32_t)lane / nc, i = (uint32_t)lane % nc;
+        t1_tile_copy(dst + mat * tile, (mat == 0 ? gate : up) + row0 * rb, tl, i, &full[st]);
+      }
+      __syncwarp();
+    }
+    // no copy may still be landing in shared memory when the CTA exits
+    if (lane == 0)
+      for (int it = issued - nstage > 0 ? issued - nstage : 0; it < issued; ++it)
+        ptx::mbar_wait(&full[it % nstage], (uint32_t)(it / nstage) & 1u, 1u << 20);
+  } else if (w < nbk) {
+    int gi = -1;
+    SegIn in;
+    const float *xs_a = nullptr, *xs_b = nullptr;
+    const uint32_t og = t1_row_off(tl, (uint32_t)g), og8 = t1_row_off(tl, (uint32_t)g + 8u);
+    const uint32_t kb = (uint32_t)w * (uint32_t)seg_bytes<Q>();
+    for (int u = u0; u < u1; ++u) {
+      const int it = u - u0, st = it % nstage;
+      if (u / ntile != gi) {
+        // a new token group: this lane's token (B column g), the tokens of
+        // its D columns 2c, 2c + 1, and K block w of their activations
+        gi = u / ntile;
+        const Group grp = load_group(gi);
+        const int tg = g < grp.nt ? __ldcg(a.perm + grp.p0 + g) / a.k : -1;
+        const int ta = 2 * c < grp.nt ? __ldcg(a.perm + grp.p0 + 2 * c) / a.k : -1;
+        const int tb = 2 * c + 1 < grp.nt ? __ldcg(a.perm + grp.p0 + 2 * c + 1) / a.k : -1;
+        load_seg<Q>(in, tg >= 0 ? a.x16 + (int64_t)tg * D + 256 * w : nullptr,
+                    tg >= 0 ? a.xs16 + ((int64_t)tg * (D / 256 + 1) + w) * 64 : nullptr, c);
+        xs_a = ta >= 0 ? a.xs32 + (int64_t)ta * (D / 32) + 8 * w : nullptr;
+        xs_b = tb >= 0 ? a.xs32 + (int64_t)tb * (D / 32) + 8 * w : nullptr;
+      }
+      if (!timed_out && !ptx::mbar_wait(&full[st], (uint32_t)(it / nstage) & 1u)) {
+        if (lane == 0) record_status(a.hdr, DS4MOE_ETIMEOUT);
+        timed_out = true;
+      }
+      float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
+      if (!timed_out) {
+        const uint8_t *sp = smem + (size_t)st * stage;
+        seg_rows<Q>(sp + og + kb, sp + og8 + kb, in, kl, xs_a, xs_b, c, ag);
+        seg_rows<Q>(sp + tile + og + kb, sp + tile + og8 + kb, in, kl, xs_a, xs_b, c, au);
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&empty[st]);
+      // partial slot it % kMtPart: free once the reducer has read unit it - kMtPart
+      const int pt = it % kMtPart;
+      if (it >= kMtPart && !ptx::mbar_wait(&pempty[pt], ((uint32_t)(it / kMtPart) & 1u) ^ 1u)) {
+        if (!timed_out && lane == 0) record_status(a.hdr, DS4MOE_ETIMEOUT);
+        timed_out = true;
+      }
+      float4 *rp = red + (((size_t)pt * nbk + w) * 32 + lane) * 2;
+      rp[0] = make_float4(ag[0], ag[1], ag[2], ag[3]);
+      rp[1] = make_float4(au[0], au[1], au[2], au[3]);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&pfull[pt]);
+    }
+  } else if (w == wred) {
+    int gi = -1;
+    Group grp{};
+    for (int u = u0; u < u1; ++u) {
+      const int it = u - u0, pt = it % kMtPart;
+      if (u / ntile != gi) {
+        gi = u / ntile;
+        grp = load_group(gi);
+      }
+      if (!ptx::mbar_wait(&pfull[pt], (uint32_t)(it / kMtPart) & 1u)) {
+        if (!timed_out && lane == 0) record_status(a.hdr, DS4MOE_ETIMEOUT);
+        timed_out = true;
+      }
+      float gs[4] = {0.f, 0.f, 0.f, 0.f}, us[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int p = 0; p < nbk; ++p) {  // K blocks in order: a fixed summation order
+        const float4 *q = red + (((size_t)pt * nbk + p) * 32 + lane) * 2;
+        const float4 qg = q[0], qu = q[1];
+        gs[0] += qg.x; gs[1] += qg.y; gs[2] += qg.z; gs[3] += qg.w;
+        us[0] += qu.x; us[1] += qu.y; us[2] += qu.z; us[3] += qu.w;
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&pempty[pt]);
+      const int row0 = (u % ntile) * 16;
+      // h for rows (g, g + 8) x tokens (2c, 2c + 1)
+      float hsum[2] = {0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = row0 + g + 8 * (i >> 1);
+        const int tok = 2 * c + (i & 1);
+        if (tok < grp.nt) {
+          // h is rounded to bf16 (the definition), then stored as the fp16
+          // operand of the down kernel (exact for |h| in [2^-14, 65504])
+          const float hv = bf16_bits_to_f32(f32_to_bf16_bits(silu(gs[i]) * us[i]));
+          if (fabsf(hv) > 65504.f) record_status(a.hdr, DS4MOE_EDEVICE);
+          a.h[(int64_t)(grp.p0 + tok) * F + row] = __half_as_ushort(__float2half_rn(hv));
+          hsum[i & 1] += hv;
+        }
+      }
+      // sub-block sums of h over the tile's 16 rows (for the down kernel's mins)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        hsum[i] += __shfl_xor_sync(0xffffffffu, hsum[i], 4);
+        hsum[i] += __shfl_xor_sync(0xffffffffu, hsum[i], 8);
+        hsum[i] += __shfl_xor_sync(0xffffffffu, hsum[i], 16);
+      }
+      if (g == 0) {
+        const int n16 = row0 / 16;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int tok = 2 * c + i;
+          if (tok < grp.nt) {
+            const __half hi = __float2half_rn(hsum[i]);
+            const __half lo = __float2half_rn(hsum[i] - __half2float(hi));
+            uint16_t *rec = reinterpret_cast<uint16_t *>(
+                a.hs16 + ((int64_t)(grp.p0 + tok) * (F / 256 + 1) + n16 / 16) * 64);
+            rec[n16 & 15] = __half_as_ushort(hi);
+            rec[16 + (n16 & 15)] = __half_as_ushort(lo);
+          }
+        }
+      }
+    }
+  }
+}
+
 // ================================================================ down
 // Weighted combine fused into the down kernel: each warp counts, per token of
 // its group, one arrival at (token, 16-row tile); the warp that brings the
@@ -1329,6 +1528,30 @@ cudaError_t launch_gate_up_mma(const FfnArgs &a, cudaStream_t s, int kp) {
 
 constexpr size_t kT1SmemGateUp = 227 * 1024, kT1SmemDown = 100 * 1024;
 
+// The persistent multi-token gate/up kernel: gate and up in one format with
+// rows that split into 16-byte bulk copies, d_model <= 4096, two stages fit.
+bool gate_up_mt_ok(const ds4moe_layer &L) {
+  if (L.q_gate != L.q_up || (L.q_gate != DS4MOE_Q2_K && L.q_gate != DS4MOE_Q4_1)) return false;
+  if (L.d_model % 256 || L.d_model > 256 * kMtMaxK) return false;
+  const int64_t rb = row_bytes(L.q_gate, L.d_model);
+  if (rb % 16) return false;
+  return gate_up_mt_smem(t1_tile_bytes(t1_tile((uint32_t)rb)), L.d_model / 256, 2) <= kT1SmemGateUp;
+}
+
+template <int Q>
+cudaError_t launch_gate_up_mt(const FfnArgs &a, cudaStream_t s) {
+  const int nbk = a.L.d_model / 256;
+  const uint32_t tile = t1_tile_bytes(t1_tile((uint32_t)row_bytes(Q, a.L.d_model)));
+  int nstage = 6;
+  while (nstage > 2 && gate_up_mt_smem(tile, nbk, nstage) > kT1SmemGateUp) --nstage;
+  const size_t smem = gate_up_mt_smem(tile, nbk, nstage);
+  auto kern = a.w_logits ? k_gate_up_mt<Q, true> : k_gate_up_mt<Q, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  ProfScope p("gate_up", s);
+  return launch_pdl(kern, dim3(num_sms()), dim3(32 * (nbk + 2)), smem, s, a, nstage);
+}
+
 cudaError_t launch_gate_up_t1(const FfnArgs &a, cudaStream_t s) {
   const int nb = a.L.d_model / 256;
   const bool q4k = a.L.q_gate == DS4MOE_Q4_K;
@@ -1454,6 +1677,8 @@ cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s) {
     const int kp = pick_kp(L.d_model, L.q_gate, L.q_up);
     cudaError_t e;
     if (t1g) e = launch_gate_up_t1(a, s);
+    else if (gate_up_mt_ok(L))
+      e = L.q_gate == DS4MOE_Q2_K ? launch_gate_up_mt<DS4MOE_Q2_K>(a, s) : launch_gate_up_mt<DS4MOE_Q4_1>(a, s);
     else if (L.q_gate == DS4MOE_Q2_K && L.q_up == DS4MOE_Q2_K) e = launch_gate_up_mma<DS4MOE_Q2_K, DS4MOE_Q2_K>(a, s, kp);
     else if (L.q_gate == DS4MOE_Q4_1 && L.q_up == DS4MOE_Q4_1) e = launch_gate_up_mma<DS4MOE_Q4_1, DS4MOE_Q4_1>(a, s, kp);
     else if (L.q_gate == DS4MOE_Q2_K) e = launch_gate_up_mma<DS4MOE_Q2_K, DS4MOE_Q4_1>(a, s, kp);
