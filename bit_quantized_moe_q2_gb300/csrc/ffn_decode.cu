@@ -739,6 +739,159 @@ __global__ void __launch_bounds__(256) k_down_mma(FfnArgs a, uint32_t chd) {
   }
 }
 
+// ================================================================ down, persistent
+// T > 1, Q2_K down, d_ff in {1024, 2048, 4096}: one CTA per SM, 16 consumer
+// warps over units of 16 / nbk 16-row tiles (nbk = d_ff / 256): warp w takes
+// K block w % nbk of tile w / nbk, and keeps that K block of its token
+// group's h (the operand the gate/up kernels wrote) in registers while
+// consecutive units share the group -- each CTA takes a contiguous range of
+// units.  A producer warp streams the unit's tiles (the single-token
+// bank-group layout) into a ring; a reducer warp sums each tile's K partials
+// in order and writes y.  The weighted combine runs as its own grid.
+constexpr int kDmtWarps = 16;
+
+size_t down_mt_smem(uint32_t tile, int tpu, int nstage) {
+  return (size_t)nstage * tpu * tile + (size_t)kMtPart * kDmtWarps * 32 * sizeof(float4) +
+         sizeof(uint64_t) * (2 * (size_t)nstage + 2 * kMtPart);
+}
+
+__global__ void __launch_bounds__((kDmtWarps + 2) * 32, 1) k_down_mt(FfnArgs a, int nstage) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const SpanExit span_exit(DS4MOE_SPAN_DOWN_MMA);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
+  const int D = a.L.d_model, F = a.L.d_ff, nbk = F / 256, tpu = kDmtWarps / nbk;
+  const int64_t rbd = row_bytes(DS4MOE_Q2_K, F);
+  const T1Tile tl = t1_tile((uint32_t)rbd);
+  const uint32_t tile = t1_tile_bytes(tl), stage = (uint32_t)tpu * tile;
+  const int wprod = kDmtWarps, wred = kDmtWarps + 1;
+  float4 *red = reinterpret_cast<float4 *>(smem + (size_t)nstage * stage);  // [kMtPart][16][32]
+  uint64_t *full = reinterpret_cast<uint64_t *>(red + (size_t)kMtPart * kDmtWarps * 32);
+  uint64_t *empty = full + nstage, *pfull = empty + nstage, *pempty = pfull + kMtPart;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < nstage; ++st) {
+      ptx::mbar_init(&full[st], 1);
+      ptx::mbar_init(&empty[st], kDmtWarps);
+    }
+    for (int pt = 0; pt < kMtPart; ++pt) {
+      ptx::mbar_init(&pfull[pt], kDmtWarps);
+      ptx::mbar_init(&pempty[pt], 1);
+    }
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  const Q2kLane kl = q2k_lane(c);
+  const int ntu = D / (16 * tpu);  // units per token group
+  // the token groups were complete before the gate/up grid (whose h this
+  // kernel reads) launched it: the producer starts before the dependency wait
+  const int U = __ldcg(&a.hdr->n_groups) * ntu, G = gridDim.x;
+  const int u0 = (int)((int64_t)blockIdx.x * U / G), u1 = (int)((int64_t)(blockIdx.x + 1) * U / G);
+  auto load_group = [&](int gi) {
+    const int4 v = __ldcg(reinterpret_cast<const int4 *>(a.groups + gi));
+    return Group{v.x, v.y, v.z, v.w};
+  };
+  bool timed_out = false;
+  if (w == wprod) {
+    const uint8_t *down = static_cast<const uint8_t *>(a.L.down);
+    const uint32_t nc = t1_copies(tl);
+    int gi = -1, issued = 0;
+    Group grp{};
+    for (int u = u0; u < u1; ++u, ++issued) {
+      const int it = u - u0, st = it % nstage;
+      if (it >= nstage && !ptx::mbar_wait(&empty[st], ((it / nstage) & 1) ^ 1)) {
+        if (lane == 0) record_status(a.hdr, DS4MOE_ETIMEOUT);
+        break;
+      }
+      if (u / ntu != gi) {
+        gi = u / ntu;
+        grp = load_group(gi);
+      }
+      const int64_t row0 = (int64_t)grp.e * D + (int64_t)(u % ntu) * 16 * tpu;
+      uint8_t *dst = smem + (size_t)st * stage;
+      if (lane == 0) ptx::mbar_arrive_expect_tx(&full[st], (uint32_t)(16 * tpu) * (uint32_t)rbd);
+      __syncwarp();
+      if ((uint32_t)lane < (uint32_t)tpu * nc) {
+        const uint32_t m = (uint32_t)lane / nc, i = (uint32_t)lane % nc;
+        t1_tile_copy(dst + m * tile, down + (row0 + 16 * (int64_t)m) * rbd, tl, i, &full[st]);
+      }
+      __syncwarp();
+    }
+    if (lane == 0)
+      for (int it = issued - nstage > 0 ? issued - nstage : 0; it < issued; ++it)
+        ptx::mbar_wait(&full[it % nstage], (uint32_t)(it / nstage) & 1u, 1u << 20);
+  }
+  ptx::pdl_wait();  // h and its sums come from the gate/up grid
+  span_begin(DS4MOE_SPAN_DOWN_MMA);
+  ptx::pdl_launch_dependents();
+  if (w < kDmtWarps) {
+    const int m = w / nbk, kbw = w % nbk;
+    int gi = -1;
+    SegIn in;
+    const uint32_t og = t1_row_off(tl, (uint32_t)g) + (uint32_t)kbw * kQ2KBytes,
+                   og8 = t1_row_off(tl, (uint32_t)g + 8u) + (uint32_t)kbw * kQ2KBytes;
+    for (int u = u0; u < u1; ++u) {
+      const int it = u - u0, st = it % nstage;
+      if (u / ntu != gi) {
+        gi = u / ntu;
+        const Group grp = load_group(gi);
+        const int p = grp.p0 + g;  // this lane's pair (B column g)
+        load_seg<DS4MOE_Q2_K>(in, g < grp.nt ? a.h + (int64_t)p * F + 256 * kbw : nullptr,
+                              g < grp.nt ? a.hs16 + ((int64_t)p * (F / 256 + 1) + kbw) * 64 : nullptr, c);
+      }
+      if (!timed_out && !ptx::mbar_wait(&full[st], (uint32_t)(it / nstage) & 1u)) {
+        if (lane == 0) record_status(a.hdr, DS4MOE_ETIMEOUT);
+        timed_out = true;
+      }
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (!timed_out) {
+        const uint8_t *sp = smem + (size_t)st * stage + (size_t)m * tile;
+        q2k_block(sp + og, sp + og8, in, kl, c, acc);
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&empty[st]);
+      const int pt = it % kMtPart;
+      if (it >= kMtPart && !ptx::mbar_wait(&pempty[pt], ((uint32_t)(it / kMtPart) & 1u) ^ 1u)) {
+        if (!timed_out && lane == 0) record_status(a.hdr, DS4MOE_ETIMEOUT);
+        timed_out = true;
+      }
+      red[((size_t)pt * kDmtWarps + w) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&pfull[pt]);
+    }
+  } else if (w == wred) {
+    int gi = -1;
+    Group grp{};
+    for (int u = u0; u < u1; ++u) {
+      const int it = u - u0, pt = it % kMtPart;
+      if (u / ntu != gi) {
+        gi = u / ntu;
+        grp = load_group(gi);
+      }
+      if (!ptx::mbar_wait(&pfull[pt], (uint32_t)(it / kMtPart) & 1u)) {
+        if (!timed_out && lane == 0) record_status(a.hdr, DS4MOE_ETIMEOUT);
+        timed_out = true;
+      }
+      const int row0 = (u % ntu) * 16 * tpu;
+      for (int m = 0; m < tpu; ++m) {
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int kb = 0; kb < nbk; ++kb) {  // K blocks in order: a fixed summation order
+          const float4 q = red[((size_t)pt * kDmtWarps + m * nbk + kb) * 32 + lane];
+          v[0] += q.x;
+          v[1] += q.y;
+          v[2] += q.z;
+          v[3] += q.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int tok = 2 * c + (i & 1);
+          if (tok < grp.nt) a.y[(int64_t)(grp.p0 + tok) * D + row0 + 16 * m + g + 8 * (i >> 1)] = v[i];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&pempty[pt]);
+    }
+  }
+}
+
 // gate/up + SwiGLU for T = 1: warps 0 .. nb-1 consume block w of d_model for
 // the 16 gate and 16 up rows of a tile, warp nb produces.  Units (group,
 // 16-row tile) are dealt to the CTAs round-robin; the warp that finishes a
@@ -1627,6 +1780,29 @@ bool t1_down_ok(const ds4moe_layer &L) {
          L.d_model % 16 == 0;
 }
 
+// The persistent multi-token down kernel: Q2_K rows that split into 16-byte
+// bulk copies, d_ff / 256 dividing its 16 consumer warps, whole units of rows.
+bool down_mt_ok(const ds4moe_layer &L) {
+  if (L.q_down != DS4MOE_Q2_K || L.d_ff % 256) return false;
+  const int nbk = L.d_ff / 256;
+  if (nbk > kDmtWarps || kDmtWarps % nbk) return false;
+  const int64_t rbd = row_bytes(DS4MOE_Q2_K, L.d_ff);
+  if (rbd % 16 || L.d_model % (16 * (kDmtWarps / nbk))) return false;
+  return down_mt_smem(t1_tile_bytes(t1_tile((uint32_t)rbd)), kDmtWarps / nbk, 2) <= kT1SmemGateUp;
+}
+
+cudaError_t launch_down_mt(const FfnArgs &a, cudaStream_t s) {
+  const int tpu = kDmtWarps / (a.L.d_ff / 256);
+  const uint32_t tile = t1_tile_bytes(t1_tile((uint32_t)row_bytes(DS4MOE_Q2_K, a.L.d_ff)));
+  int nstage = 8;
+  while (nstage > 2 && down_mt_smem(tile, tpu, nstage) > kT1SmemGateUp) --nstage;
+  const size_t smem = down_mt_smem(tile, tpu, nstage);
+  cudaError_t e = cudaFuncSetAttribute(k_down_mt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  ProfScope p("down", s);
+  return launch_pdl(k_down_mt, dim3(num_sms()), dim3(32 * (kDmtWarps + 2)), smem, s, a, nstage);
+}
+
 cudaError_t launch_down_mma(const FfnArgs &a, cudaStream_t s) {
   const int F = a.L.d_ff;
   const uint32_t chd = (uint32_t)row_bytes(DS4MOE_Q2_K, F);
@@ -1666,6 +1842,15 @@ bool decode_mma_ok(const ds4moe_layer &L) {
   return L.q_down == DS4MOE_Q2_K && L.d_ff % 256 == 0 && rbd % 16 == 0 && 8 * 16 * rbd <= 200 * 1024;
 }
 
+// Whether this call's down step runs k_down_mt (whose weighted combine is the
+// separate combine grid) rather than a kernel with the combine fused.
+bool down_mt_runs(const FfnArgs &a) {
+  const ds4moe_layer &L = a.L;
+  if (t1_merged_path(a)) return false;
+  const bool t1g = a.T == 1 && t1_gate_up_ok(L), t1d = a.T == 1 && t1_down_ok(L);
+  return (decode_mma_ok(L) || (t1g && t1d)) && !t1d && down_mt_ok(L);
+}
+
 cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s) {
   const ds4moe_layer &L = a.L;
   // single token: the sub-block-column kernels where the format allows;
@@ -1684,7 +1869,8 @@ cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s) {
     else if (L.q_gate == DS4MOE_Q2_K) e = launch_gate_up_mma<DS4MOE_Q2_K, DS4MOE_Q4_1>(a, s, kp);
     else e = launch_gate_up_mma<DS4MOE_Q4_1, DS4MOE_Q2_K>(a, s, kp);
     if (e != cudaSuccess) return e;
-    return t1d ? launch_down_t1(a, s) : launch_down_mma(a, s);
+    if (t1d) return launch_down_t1(a, s);
+    return down_mt_runs(a) ? launch_down_mt(a, s) : launch_down_mma(a, s);
   }
   const int grid = num_sms() * 8;
   {
@@ -1702,7 +1888,7 @@ cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s) {
 
 cudaError_t launch_combine(const FfnArgs &a, cudaStream_t s) {
   if (t1_merged_path(a)) return cudaSuccess;                        // fused into the merged grid
-  if (a.cnt && !(a.T == 1 && t1_down_ok(a.L))) return cudaSuccess;  // fused into the down kernel
+  if (a.cnt && !(a.T == 1 && t1_down_ok(a.L)) && !down_mt_runs(a)) return cudaSuccess;  // fused into the down kernel
   const int64_t n4 = (int64_t)a.T * a.L.d_model / 4;
   const int grid = (int)((n4 + 255) / 256 < num_sms() * 16 ? (n4 + 255) / 256 : num_sms() * 16);
   ProfScope p("combine", s);
