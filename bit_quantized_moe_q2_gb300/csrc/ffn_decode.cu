@@ -91,7 +91,7 @@ struct SegIn {
 template <int Q>
 __device__ __forceinline__ void load_seg(SegIn &in, const uint16_t *__restrict__ xb,
                                          const uint8_t *__restrict__ sums, int c) {
-  if constexpr (Q == DS4MOE_Q2_K) {
+  if constexpr (Q == DS4MOE_Q2_K || Q == DS4MOE_Q4_K) {
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       uint4 t = make_uint4(0u, 0u, 0u, 0u);
@@ -167,6 +167,79 @@ __device__ __forceinline__ void q2k_block(const uint8_t *__restrict__ blk_a, con
   acc[3] = fmaf(db, dm[0][3] + dm[1][3], fmaf(-dminb, dn[3], acc[3]));
 }
 
+// One Q4_K 256-value block of 16 staged rows (row g at blk_a, g + 8 at
+// blk_b), the same activation mapping as Q2_K: lane quad c owns values
+// 64c .. 64c + 63, i.e. qs bytes 32c .. 32c + 31, whose low nibbles are
+// sub-block 2c and high nibbles sub-block 2c + 1 (32 values each).  qs word
+// wi (values 4wi .. 4wi + 3 of each half) feeds two MMAs: the low nibbles
+// against bx[wi], the high ones against bx[8 + wi].  A code under the fp16
+// exponent of 1024 reads as 1024 + q (low) or 1024 + 16 q (high); one packed
+// fp16 FMA with (sc, -1024 sc) or (sc / 16, -64 sc) leaves sc * q <= 945,
+// exact.  The mins take one MMA pair against the 16-value sub-block sums:
+// sub-block j's mn sits in the K slots of its two 16-value halves.
+__device__ __forceinline__ void q4k_block(const uint8_t *__restrict__ blk_a, const uint8_t *__restrict__ blk_b,
+                                          const SegIn &in, int c, float (&acc)[4]) {
+  const uint32_t dda = ptx::lds32(blk_a), ddb = ptx::lds32(blk_b);
+  uint32_t sa[3], sb[3];
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    sa[q] = ptx::lds32(blk_a + 4 + 4 * q);
+    sb[q] = ptx::lds32(blk_b + 4 + 4 * q);
+  }
+  uint32_t sca[2], mna[2], scb[2], mnb[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    q4k_sc_mn_pair(sa, 2 * c + h, sca[h], mna[h]);
+    q4k_sc_mn_pair(sb, 2 * c + h, scb[h], mnb[h]);
+  }
+  // scale-fold constants: low nibbles (sub-block 2c) and high (2c + 1), rows a / b
+  const auto h2 = [](float v) {
+    const uint32_t b = __half_as_ushort(__float2half_rn(v));
+    return b | (b << 16);
+  };
+  const uint32_t s1a0 = h2((float)sca[0]), s0a0 = h2(-1024.f * (float)sca[0]);
+  const uint32_t s1b0 = h2((float)scb[0]), s0b0 = h2(-1024.f * (float)scb[0]);
+  const uint32_t s1a1 = h2((float)sca[1] * 0.0625f), s0a1 = h2(-64.f * (float)sca[1]);
+  const uint32_t s1b1 = h2((float)scb[1] * 0.0625f), s0b1 = h2(-64.f * (float)scb[1]);
+  const uint8_t *qsa = blk_a + 16 + 32 * c, *qsb = blk_b + 16 + 32 * c;
+  float dm[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+  for (int wi = 0; wi < 8; ++wi) {
+    const uint32_t qa = ptx::lds32(qsa + 4 * wi), qb = ptx::lds32(qsb + 4 * wi);
+    const uint32_t a01 = __byte_perm(qa, 0, 0x4140), a23 = __byte_perm(qa, 0, 0x4342);
+    const uint32_t b01 = __byte_perm(qb, 0, 0x4140), b23 = __byte_perm(qb, 0, 0x4342);
+    uint32_t A[4];
+    A[0] = ptx::fma_f16x2(ptx::and_or(a01, 0x000F000Fu, kMagicH), s1a0, s0a0);
+    A[1] = ptx::fma_f16x2(ptx::and_or(b01, 0x000F000Fu, kMagicH), s1b0, s0b0);
+    A[2] = ptx::fma_f16x2(ptx::and_or(a23, 0x000F000Fu, kMagicH), s1a0, s0a0);
+    A[3] = ptx::fma_f16x2(ptx::and_or(b23, 0x000F000Fu, kMagicH), s1b0, s0b0);
+    ptx::mma_f16(dm[wi & 1], A, in.bx[wi].x, in.bx[wi].y);
+    A[0] = ptx::fma_f16x2(ptx::and_or(a01, 0x00F000F0u, kMagicH), s1a1, s0a1);
+    A[1] = ptx::fma_f16x2(ptx::and_or(b01, 0x00F000F0u, kMagicH), s1b1, s0b1);
+    A[2] = ptx::fma_f16x2(ptx::and_or(a23, 0x00F000F0u, kMagicH), s1a1, s0a1);
+    A[3] = ptx::fma_f16x2(ptx::and_or(b23, 0x00F000F0u, kMagicH), s1b1, s0b1);
+    ptx::mma_f16(dm[wi & 1], A, in.bx[8 + wi].x, in.bx[8 + wi].y);
+  }
+  // mins: K slots 2c, 2c + 1 (16-value sums 4c, 4c + 1) carry mn of
+  // sub-block 2c, slots 2c + 8, 2c + 9 (sums 4c + 2, 4c + 3) mn of 2c + 1
+  float dn[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    uint32_t Am[4];
+    Am[0] = h2((float)mna[0]);
+    Am[1] = h2((float)mnb[0]);
+    Am[2] = h2((float)mna[1]);
+    Am[3] = h2((float)mnb[1]);
+    ptx::mma_f16(dn, Am, in.shi.x, in.shi.y);
+    ptx::mma_f16(dn, Am, in.slo.x, in.slo.y);
+  }
+  const float da = f16_bits_to_f32(dda & 0xFFFFu), dmina = f16_bits_to_f32(dda >> 16);
+  const float db = f16_bits_to_f32(ddb & 0xFFFFu), dminb = f16_bits_to_f32(ddb >> 16);
+  acc[0] = fmaf(da, dm[0][0] + dm[1][0], fmaf(-dmina, dn[0], acc[0]));
+  acc[1] = fmaf(da, dm[0][1] + dm[1][1], fmaf(-dmina, dn[1], acc[1]));
+  acc[2] = fmaf(db, dm[0][2] + dm[1][2], fmaf(-dminb, dn[2], acc[2]));
+  acc[3] = fmaf(db, dm[0][3] + dm[1][3], fmaf(-dminb, dn[3], acc[3]));
+}
+
 // Eight Q4_1 blocks (one 256-value segment): per block
 // acc += d * (sum q*x) + m * (sum x).  Low nibbles -> 1024 + q, high
 // nibbles -> 1024 + 16 q, both turned into exact q by one packed FMA.
@@ -210,12 +283,13 @@ __device__ __forceinline__ void q41_seg(const uint8_t *__restrict__ seg_a, const
 
 // Bytes of one 256-value segment of a row.
 template <int Q>
-constexpr int seg_bytes() { return Q == DS4MOE_Q2_K ? kQ2KBytes : 8 * kQ41Bytes; }
+constexpr int seg_bytes() { return Q == DS4MOE_Q2_K ? kQ2KBytes : Q == DS4MOE_Q4_K ? kQ4KBytes : 8 * kQ41Bytes; }
 
 template <int Q>
 __device__ __forceinline__ void seg_rows(const uint8_t *ra, const uint8_t *rb, const SegIn &in, const Q2kLane &kl,
                                          const float *xs_a, const float *xs_b, int c, float (&acc)[4]) {
   if constexpr (Q == DS4MOE_Q2_K) q2k_block(ra, rb, in, kl, c, acc);
+  else if constexpr (Q == DS4MOE_Q4_K) q4k_block(ra, rb, in, c, acc);
   else q41_seg(ra, rb, in, xs_a, xs_b, c, acc);
 }
 
@@ -740,7 +814,7 @@ __global__ void __launch_bounds__(256) k_down_mma(FfnArgs a, uint32_t chd) {
 }
 
 // ================================================================ down, persistent
-// T > 1, Q2_K down, d_ff in {1024, 2048, 4096}: one CTA per SM, 16 consumer
+// T > 1, Q2_K or Q4_K down, d_ff in {1024, 2048, 4096}: one CTA per SM, 16 consumer
 // warps over units of 16 / nbk 16-row tiles (nbk = d_ff / 256): warp w takes
 // K block w % nbk of tile w / nbk, and keeps that K block of its token
 // group's h (the operand the gate/up kernels wrote) in registers while
@@ -755,12 +829,13 @@ size_t down_mt_smem(uint32_t tile, int tpu, int nstage) {
          sizeof(uint64_t) * (2 * (size_t)nstage + 2 * kMtPart);
 }
 
+template <int Q>
 __global__ void __launch_bounds__((kDmtWarps + 2) * 32, 1) k_down_mt(FfnArgs a, int nstage) {
   extern __shared__ __align__(128) uint8_t smem[];
   const SpanExit span_exit(DS4MOE_SPAN_DOWN_MMA);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
   const int D = a.L.d_model, F = a.L.d_ff, nbk = F / 256, tpu = kDmtWarps / nbk;
-  const int64_t rbd = row_bytes(DS4MOE_Q2_K, F);
+  const int64_t rbd = row_bytes(Q, F);
   const T1Tile tl = t1_tile((uint32_t)rbd);
   const uint32_t tile = t1_tile_bytes(tl), stage = (uint32_t)tpu * tile;
   const int wprod = kDmtWarps, wred = kDmtWarps + 1;
@@ -826,15 +901,15 @@ __global__ void __launch_bounds__((kDmtWarps + 2) * 32, 1) k_down_mt(FfnArgs a, 
     const int m = w / nbk, kbw = w % nbk;
     int gi = -1;
     SegIn in;
-    const uint32_t og = t1_row_off(tl, (uint32_t)g) + (uint32_t)kbw * kQ2KBytes,
-                   og8 = t1_row_off(tl, (uint32_t)g + 8u) + (uint32_t)kbw * kQ2KBytes;
+    const uint32_t og = t1_row_off(tl, (uint32_t)g) + (uint32_t)(kbw * seg_bytes<Q>()),
+                   og8 = t1_row_off(tl, (uint32_t)g + 8u) + (uint32_t)(kbw * seg_bytes<Q>());
     for (int u = u0; u < u1; ++u) {
       const int it = u - u0, st = it % nstage;
       if (u / ntu != gi) {
         gi = u / ntu;
         const Group grp = load_group(gi);
         const int p = grp.p0 + g;  // this lane's pair (B column g)
-        load_seg<DS4MOE_Q2_K>(in, g < grp.nt ? a.h + (int64_t)p * F + 256 * kbw : nullptr,
+        load_seg<Q>(in, g < grp.nt ? a.h + (int64_t)p * F + 256 * kbw : nullptr,
                               g < grp.nt ? a.hs16 + ((int64_t)p * (F / 256 + 1) + kbw) * 64 : nullptr, c);
       }
       if (!timed_out && !ptx::mbar_wait(&full[st], (uint32_t)(it / nstage) & 1u)) {
@@ -844,7 +919,7 @@ __global__ void __launch_bounds__((kDmtWarps + 2) * 32, 1) k_down_mt(FfnArgs a, 
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       if (!timed_out) {
         const uint8_t *sp = smem + (size_t)st * stage + (size_t)m * tile;
-        q2k_block(sp + og, sp + og8, in, kl, c, acc);
+        seg_rows<Q>(sp + og, sp + og8, in, kl, nullptr, nullptr, c, acc);
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&empty[st]);
@@ -1681,10 +1756,12 @@ cudaError_t launch_gate_up_mma(const FfnArgs &a, cudaStream_t s, int kp) {
 
 constexpr size_t kT1SmemGateUp = 227 * 1024, kT1SmemDown = 100 * 1024;
 
-// The persistent multi-token gate/up kernel: gate and up in one format with
+// The persistent multi-token gate/up kernel: gate and up in one format (Q2_K,
+// Q4_1 or Q4_K) with
 // rows that split into 16-byte bulk copies, d_model <= 4096, two stages fit.
 bool gate_up_mt_ok(const ds4moe_layer &L) {
-  if (L.q_gate != L.q_up || (L.q_gate != DS4MOE_Q2_K && L.q_gate != DS4MOE_Q4_1)) return false;
+  if (L.q_gate != L.q_up || (L.q_gate != DS4MOE_Q2_K && L.q_gate != DS4MOE_Q4_1 && L.q_gate != DS4MOE_Q4_K))
+    return false;
   if (L.d_model % 256 || L.d_model > 256 * kMtMaxK) return false;
   const int64_t rb = row_bytes(L.q_gate, L.d_model);
   if (rb % 16) return false;
@@ -1780,27 +1857,29 @@ bool t1_down_ok(const ds4moe_layer &L) {
          L.d_model % 16 == 0;
 }
 
-// The persistent multi-token down kernel: Q2_K rows that split into 16-byte
-// bulk copies, d_ff / 256 dividing its 16 consumer warps, whole units of rows.
+// The persistent multi-token down kernel: Q2_K or Q4_K rows that split into
+// 16-byte bulk copies, d_ff / 256 dividing its 16 consumer warps, whole
+// units of rows.
 bool down_mt_ok(const ds4moe_layer &L) {
-  if (L.q_down != DS4MOE_Q2_K || L.d_ff % 256) return false;
+  if ((L.q_down != DS4MOE_Q2_K && L.q_down != DS4MOE_Q4_K) || L.d_ff % 256) return false;
   const int nbk = L.d_ff / 256;
   if (nbk > kDmtWarps || kDmtWarps % nbk) return false;
-  const int64_t rbd = row_bytes(DS4MOE_Q2_K, L.d_ff);
+  const int64_t rbd = row_bytes(L.q_down, L.d_ff);
   if (rbd % 16 || L.d_model % (16 * (kDmtWarps / nbk))) return false;
   return down_mt_smem(t1_tile_bytes(t1_tile((uint32_t)rbd)), kDmtWarps / nbk, 2) <= kT1SmemGateUp;
 }
 
 cudaError_t launch_down_mt(const FfnArgs &a, cudaStream_t s) {
   const int tpu = kDmtWarps / (a.L.d_ff / 256);
-  const uint32_t tile = t1_tile_bytes(t1_tile((uint32_t)row_bytes(DS4MOE_Q2_K, a.L.d_ff)));
+  const uint32_t tile = t1_tile_bytes(t1_tile((uint32_t)row_bytes(a.L.q_down, a.L.d_ff)));
   int nstage = 8;
   while (nstage > 2 && down_mt_smem(tile, tpu, nstage) > kT1SmemGateUp) --nstage;
   const size_t smem = down_mt_smem(tile, tpu, nstage);
-  cudaError_t e = cudaFuncSetAttribute(k_down_mt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = a.L.q_down == DS4MOE_Q4_K ? k_down_mt<DS4MOE_Q4_K> : k_down_mt<DS4MOE_Q2_K>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   ProfScope p("down", s);
-  return launch_pdl(k_down_mt, dim3(num_sms()), dim3(32 * (kDmtWarps + 2)), smem, s, a, nstage);
+  return launch_pdl(kern, dim3(num_sms()), dim3(32 * (kDmtWarps + 2)), smem, s, a, nstage);
 }
 
 cudaError_t launch_down_mma(const FfnArgs &a, cudaStream_t s) {
@@ -1830,7 +1909,9 @@ bool t1_chain_ok(const ds4moe_layer &L) { return t1_gate_up_ok(L) && t1_down_ok(
 // The tensor-core kernels need rows that split into 16-byte-multiple bulk
 // copies and stages that fit in shared memory; other shapes use SIMT.
 bool decode_mma_ok(const ds4moe_layer &L) {
-  // tensor-core decode kernels: Q4_1 / Q2_K gate and up, Q2_K down
+  // the persistent kernels (one-format gate/up of Q2_K / Q4_1 / Q4_K, Q2_K or
+  // Q4_K down), or the per-unit ones (Q4_1 / Q2_K gate and up, Q2_K down)
+  if (gate_up_mt_ok(L) && down_mt_ok(L)) return true;
   const auto mma_fmt = [](int q) { return q == DS4MOE_Q4_1 || q == DS4MOE_Q2_K; };
   if (!mma_fmt(L.q_gate) || !mma_fmt(L.q_up)) return false;
   if (L.d_model % 16) return false;
@@ -1863,7 +1944,9 @@ cudaError_t launch_ffn_decode(const FfnArgs &a, cudaStream_t s) {
     cudaError_t e;
     if (t1g) e = launch_gate_up_t1(a, s);
     else if (gate_up_mt_ok(L))
-      e = L.q_gate == DS4MOE_Q2_K ? launch_gate_up_mt<DS4MOE_Q2_K>(a, s) : launch_gate_up_mt<DS4MOE_Q4_1>(a, s);
+      e = L.q_gate == DS4MOE_Q2_K   ? launch_gate_up_mt<DS4MOE_Q2_K>(a, s)
+          : L.q_gate == DS4MOE_Q4_K ? launch_gate_up_mt<DS4MOE_Q4_K>(a, s)
+                                    : launch_gate_up_mt<DS4MOE_Q4_1>(a, s);
     else if (L.q_gate == DS4MOE_Q2_K && L.q_up == DS4MOE_Q2_K) e = launch_gate_up_mma<DS4MOE_Q2_K, DS4MOE_Q2_K>(a, s, kp);
     else if (L.q_gate == DS4MOE_Q4_1 && L.q_up == DS4MOE_Q4_1) e = launch_gate_up_mma<DS4MOE_Q4_1, DS4MOE_Q4_1>(a, s, kp);
     else if (L.q_gate == DS4MOE_Q2_K) e = launch_gate_up_mma<DS4MOE_Q2_K, DS4MOE_Q4_1>(a, s, kp);

@@ -66,6 +66,11 @@ SHAPES = [
     Q4.replace(d_model=512, d_ff=1024, n_expert=12, k=2, T=19, seed=602, bias_sigma=1.0),
     Q4.replace(d_model=768, d_ff=256, n_expert=5, k=3, T=33, seed=603, down=synth.Q2K),
     Q4.replace(d_model=1024, d_ff=768, n_expert=6, k=2, T=7, seed=604, gate=synth.Q41_4BIT, up=synth.Q41_4BIT),
+    # the persistent multi-token kernels: all Q4_K at the Flash shape, and
+    # Q4_K gate/up with Q2_K down (the mixed recipe's neighbour layers)
+    Q4.replace(d_model=4096, d_ff=2048, n_expert=6, k=3, T=21, seed=605),
+    Q4.replace(d_model=2048, d_ff=1024, n_expert=9, k=2, T=40, seed=606, down=synth.Q2K),
+    synth.WORKLOADS[1].replace(d_model=2048, d_ff=1024, n_expert=9, k=2, T=12, seed=607, down=synth.Q4K),
 ]
 
 
@@ -93,3 +98,21 @@ def test_q4k_fused_decode_entry_point(M):
     ridx, rw, _ = oracle.route(x, L.Wr, L.bias, w.k)
     assert np.array_equal(idx, ridx)
     assert rel_err(out, oracle_out(L, x, ridx, rw)) <= TOL
+
+
+@pytest.mark.parametrize("wi", [1, 4, 5, 6])
+def test_q4k_multi_token_layers_take_the_tensor_core_kernels(M, wi):
+    """More than one token on layers with Q4_K gate/up or down (every shape
+    here fits the persistent kernels): no SIMT kernel runs."""
+    w = SHAPES[wi]
+    L = build_layer(w)
+    dev = to_device(L)
+    x = synth.activations(w)
+    M.ds4moe_profile_enable(True)
+    try:
+        gpu_forward(M, dev, x, L.Wr, L.bias, w.k)
+        names = set(M.ds4moe_profile_read())
+    finally:
+        M.ds4moe_profile_enable(False)
+    assert {"gate_up", "down"} <= names
+    assert not ({"gate_up_simt", "down_simt"} & names)
