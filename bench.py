@@ -603,11 +603,12 @@ def decode_layer_record(args, M, torch, w: synth.Workload, copies, layout: str, 
                 "dequant fused)" if ffn == "ffn_t1r" else
                 "expert FFN (merged gate/up + SwiGLU + down + combine, dequant fused)")
         rec["roofline"] = hbm_roofline(desc, algo, kernels[ffn]["avg_us"], NCU_TRAFFIC.get((w.name, layout, ffn)))
-    elif "gate_up_mma" in kernels:
-        algo = uniq_avg * gate_up_bytes(w) + T * D * 2 + T * k * w.d_ff * 2
-        rec["roofline"] = hbm_roofline("gate_up (fused dequant GEMV + SwiGLU)", algo,
-                                       kernels["gate_up_mma"]["avg_us"],
-                                       NCU_TRAFFIC.get((w.name, layout, "gate_up_mma")))
+    else:
+        gu = next((n for n in ("gate_up_mma", "gate_up_t1") if n in kernels), None)
+        if gu:
+            algo = uniq_avg * gate_up_bytes(w) + T * D * 2 + T * k * w.d_ff * 2
+            rec["roofline"] = hbm_roofline("gate_up (fused dequant GEMV + SwiGLU)", algo, kernels[gu]["avg_us"],
+                                           NCU_TRAFFIC.get((w.name, layout, gu)))
     rec["kernels"] = kernels
     counts = launch_count(M, torch, stream, lambda i: step(i, stream), 50)
     rec["launches_per_step"] = counts

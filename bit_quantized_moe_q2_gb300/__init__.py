@@ -199,7 +199,7 @@ def ds4moe_combine_pairs(y, pos, w, out, stream=None):
 
 # ds4moe_span_kernel order
 SPAN_KERNELS = ("route", "ffn_t1", "ffn_t1r", "gate_up_mma", "down_mma", "gate_up_tc", "down_tc",
-                "shared_gate_up_tc", "shared_down_tc")
+                "shared_gate_up_tc", "shared_down_tc", "gate_up_t1", "down_t1")
 
 
 def ds4moe_profile_span(on: int = -1) -> dict:

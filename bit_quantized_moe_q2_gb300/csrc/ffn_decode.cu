@@ -974,6 +974,7 @@ __global__ void __launch_bounds__((kDmtWarps + 2) * 32, 1) k_down_mt(FfnArgs a, 
 template <bool FIN, int FMT>
 __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage) {
   extern __shared__ __align__(128) uint8_t smem[];
+  const SpanExit span_exit(DS4MOE_SPAN_GATE_UP_T1);
   constexpr int kBB = FMT == DS4MOE_Q4_K ? kQ4KBytes : kQ2KBytes;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
   const int D = a.L.d_model, F = a.L.d_ff, nb = D / 256;
@@ -998,6 +999,7 @@ __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage
     else t1_load_b<true>(B, a.x + 256 * w, g, c);
   }
   ptx::pdl_wait();  // groups (or the logits) come from the routing grid
+  span_begin(DS4MOE_SPAN_GATE_UP_T1);
   ptx::pdl_launch_dependents();
   const int ntile = F / 16;
   __shared__ Group s_grp[kT1MaxGroups];
@@ -1118,6 +1120,7 @@ __global__ void __launch_bounds__(17 * 32, 1) k_gate_up_t1(FfnArgs a, int nstage
 template <int FMT>
 __global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
   extern __shared__ __align__(128) uint8_t smem[];
+  const SpanExit span_exit(DS4MOE_SPAN_DOWN_T1);
   constexpr int kBB = FMT == DS4MOE_Q4_K ? kQ4KBytes : kQ2KBytes;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
   const int D = a.L.d_model, F = a.L.d_ff, nb = F / 256;
@@ -1169,6 +1172,7 @@ __global__ void __launch_bounds__(9 * 32, 2) k_down_t1(FfnArgs a, int nstage) {
   const T1Lane L = t1_lane(c);
   T1B B;
   ptx::pdl_wait();  // h comes from the gate/up grid
+  span_begin(DS4MOE_SPAN_DOWN_T1);
   ptx::pdl_launch_dependents();
   bool timed_out = false;
   int it = 0, cur = -1;

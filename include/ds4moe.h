@@ -521,13 +521,15 @@ typedef enum {
   DS4MOE_SPAN_ROUTE = 0,        /* decode router grid: logits (+ top-k, bucketing) */
   DS4MOE_SPAN_FFN_T1 = 1,       /* single-token merged FFN grid, plain blocks */
   DS4MOE_SPAN_FFN_T1R = 2,      /* single-token FFN grid, DS4MOE_Q2_K_R16 */
-  DS4MOE_SPAN_GATE_UP_MMA = 3,  /* multi-token decode gate/up + SwiGLU */
-  DS4MOE_SPAN_DOWN_MMA = 4,     /* multi-token decode down (+ combine) */
+  DS4MOE_SPAN_GATE_UP_MMA = 3,  /* multi-token decode gate/up + SwiGLU (either kernel) */
+  DS4MOE_SPAN_DOWN_MMA = 4,     /* multi-token decode down (either kernel) */
   DS4MOE_SPAN_GATE_UP_TC = 5,   /* prefill tensor-core gate/up + SwiGLU */
   DS4MOE_SPAN_DOWN_TC = 6,      /* prefill tensor-core down */
   DS4MOE_SPAN_SHARED_GATE_UP_TC = 7,  /* shared expert, tensor-core gate/up + SwiGLU */
   DS4MOE_SPAN_SHARED_DOWN_TC = 8,     /* shared expert, tensor-core down */
-  DS4MOE_SPAN_COUNT = 9
+  DS4MOE_SPAN_GATE_UP_T1 = 9,   /* single-token gate/up + SwiGLU (separate path, Q2_K / Q4_K) */
+  DS4MOE_SPAN_DOWN_T1 = 10,     /* single-token down (separate path) */
+  DS4MOE_SPAN_COUNT = 11
 } ds4moe_span_kernel;
 ds4moe_status ds4moe_profile_span(int32_t on, double *total_ns, int64_t *launches);
 

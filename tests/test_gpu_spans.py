@@ -92,3 +92,13 @@ def test_off_records_nothing_and_graph_replays_record(M):
         M.ds4moe_moe_decode(dev.abi, xd, Wr, None, w.k, out, idx, wt, ws, s)
     spans = _spans(M, lambda: (g.replay(), torch.cuda.synchronize()), 4)
     _check(spans, {"route", "ffn_t1"}, 4)
+
+
+def test_single_token_separate_kernels(M):
+    # Q4_K experts at T = 1: the separate single-token gate/up and down kernels
+    w = synth.WORKLOADS[5].replace(d_model=1024, d_ff=1024, n_expert=8, k=2, seed=905)
+    L = build_layer(w)
+    dev = to_device(L)
+    x = synth.activations(w, T=1)
+    spans = _spans(M, lambda: gpu_moe_decode(M, dev, x, L.Wr, L.bias, w.k), 2)
+    _check(spans, {"route", "gate_up_t1", "down_t1"}, 2)
