@@ -32,6 +32,8 @@ SHAPES = [
     Q2.replace(d_model=1024, d_ff=512, n_expert=5, k=1, seed=503),
     Q2.replace(d_model=3072, d_ff=1536, n_expert=9, k=8, seed=504),
     Q2.replace(d_model=512, d_ff=256, n_expert=40, k=32, seed=505),
+    # 256 experts: more than one router CTA per SM
+    Q2.replace(d_model=2048, d_ff=1024, n_expert=256, k=8, seed=506),
 ]
 
 
@@ -116,8 +118,9 @@ def test_r16_large_activations_take_the_scaled_operand(M):
     assert rel_err(out, oracle_out(L, xb, ridx, rw)) <= TOL
 
 
-def test_r16_kernel_is_the_one_launched(M):
-    w = SHAPES[0]
+@pytest.mark.parametrize("wi", [0, 2])
+def test_r16_kernel_is_the_one_launched(M, wi):
+    w = SHAPES[wi]
     L = build_layer(w)
     dev = _r16(L)
     x = synth.activations(w, T=1)
@@ -128,6 +131,7 @@ def test_r16_kernel_is_the_one_launched(M):
     finally:
         M.ds4moe_profile_enable(False)
     assert "ffn_t1r" in names
+    assert "route" in names  # the logits' grid, then the tile-order grid
     assert not {"ffn_t1", "gate_up", "down", "combine", "bucket", "gate_up_simt", "down_simt"} & names
 
 
