@@ -66,24 +66,60 @@ template <>
 struct QFmt<DS4MOE_Q2_K> {
   static constexpr int kVals = 1024, kBytes = 336;
 };
+template <>
+struct QFmt<DS4MOE_Q4_K> {
+  static constexpr int kVals = 256, kBytes = 144;
+};
 
-// Gate/up K-steps come in windows of 16 x 64 values (32 Q4_1 blocks) and
-// one extra step for the block minima of the window.
+// Gate/up K-steps come in groups of kMain main steps of 64 values and one
+// extra step for the minima of the group's blocks (the window); the
+// prefill layer's d_model is a multiple of kWinVals.
 constexpr int kWinSteps = 16, kWinVals = kWinSteps * kStepK;
 
-// NMAT = 2: gate and up (Q4_1, exact hi/lo tiles) share each B tile
-// (SwiGLU epilogue); NMAT = 1: down.
+// Gate/up staging per weight format: kStageSteps K-steps per shared-memory
+// stage, kRowBytes bytes per weight row of a stage, kMain main steps per
+// minima step, and whether the minima carry a lo part (the block minimum
+// is exact in fp16 for Q4_1; for Q2_K / Q4_K dmin * mn is split in two).
+//   Q4_1: 4 blocks (80 B) per stage, 2 K-steps.
+//   Q4_K: half a super-block per stage: the 16-byte header and 64 code
+//         bytes for half 0 (words 0..19 of the block), words 16..35 for
+//         half 1 (the header is kept from half 0); 2 K-steps.
+//   Q2_K: one super-block per stage, copied as the six 16-byte chunks that
+//         cover its 84 bytes (it starts at byte 4 (sb % 4) of the 96-byte
+//         row); 4 K-steps; its 16-value sub-blocks give 32 minima per 8
+//         K-steps, so a minima step follows every 8 main steps.
+template <int Q>
+struct GuFmt;
+template <>
+struct GuFmt<DS4MOE_Q4_1> {
+  static constexpr int kStageSteps = 2, kRowBytes = 80, kMain = 16;
+  static constexpr bool kMinLo = false;
+};
+template <>
+struct GuFmt<DS4MOE_Q4_K> {
+  static constexpr int kStageSteps = 2, kRowBytes = 80, kMain = 16;
+  static constexpr bool kMinLo = true;
+};
+template <>
+struct GuFmt<DS4MOE_Q2_K> {
+  static constexpr int kStageSteps = 4, kRowBytes = 96, kMain = 8;
+  static constexpr bool kMinLo = true;
+};
+static_assert(GuFmt<DS4MOE_Q4_1>::kRowBytes == GuFmt<DS4MOE_Q4_K>::kRowBytes, "one tensor-map box for both");
+
+// NMAT = 2: gate and up (exact hi/lo tiles) share each B tile (SwiGLU
+// epilogue); NMAT = 1: down.
 template <int NMAT, int QA, int BN>
 struct TcCfg {
-  static_assert(NMAT == 1 || QA == DS4MOE_Q4_1, "exact gate/up tiles are built from Q4_1 blocks");
   static constexpr int kSA = NMAT == 2 ? 2 : 4;
   static constexpr int kSB = NMAT == 2 ? 3 : 2;
-  static constexpr int kSQ = QA == DS4MOE_Q2_K ? 2 : (NMAT == 2 ? 2 : 4);
+  static constexpr int kSQ = (NMAT == 2 || QA == DS4MOE_Q2_K) ? 2 : 4;
   static constexpr int kATile = kTileM * kStepK * 2;
-  static constexpr int kTiles = NMAT == 2 ? 4 : 1;  // gate hi, up hi, gate -lo, up -lo
+  static constexpr int kTiles = NMAT == 2 ? 4 : 1;  // gate hi, up hi, gate lo, up lo
   static constexpr int kASlot = kTiles * kATile;
   static constexpr int kBSlot = BN * kStepK * 2;
-  static constexpr int kQMat = kTileM * QFmt<QA>::kBytes;
+  static constexpr int kRowQ = NMAT == 2 ? GuFmt<QA>::kRowBytes : QFmt<QA>::kBytes;
+  static constexpr int kQMat = kTileM * kRowQ;
   static constexpr int kQSlot = NMAT * kQMat;
   static constexpr int kNB = kTmemCols / (NMAT * BN);  // TMEM accumulator buffers
   static constexpr int kOffA = 0;
@@ -218,6 +254,141 @@ __device__ __forceinline__ bool dq_q2k(const uint8_t *blk, int qq, uint8_t *tile
   return big;
 }
 
+// Duplicate the low / high fp16 of a word into both halves.
+__device__ __forceinline__ uint32_t dup_lo(uint32_t v) { return __byte_perm(v, 0, 0x1010); }
+__device__ __forceinline__ uint32_t dup_hi(uint32_t v) { return __byte_perm(v, 0, 0x3232); }
+__device__ __forceinline__ uint32_t f16_dup(float v) {
+  const uint32_t h = __half_as_ushort(__float2half_rn(v));
+  return h | (h << 16);
+}
+
+// Q4_K sub-block j's 6-bit scale and min from the 12 scale bytes held in
+// three words (bytes 0..3, 4..7, 8..11).
+__device__ __forceinline__ void q4k_sm_regs(uint32_t w0, uint32_t w1, uint32_t w2, int j, uint32_t &sc,
+                                            uint32_t &mn) {
+  const uint32_t bj = ((j < 4 ? w0 : w1) >> (8 * (j & 3))) & 0xFFu;           // byte j
+  const uint32_t bj4 = ((j < 4 ? w1 : w2) >> (8 * (j & 3))) & 0xFFu;          // byte j + 4
+  const uint32_t bjm4 = (w0 >> (8 * (j & 3))) & 0xFFu;                         // byte j - 4 (j >= 4)
+  if (j < 4) {
+    sc = bj & 63u;
+    mn = bj4 & 63u;
+  } else {
+    sc = (bj4 & 15u) | ((bjm4 >> 6) << 4);
+    mn = (bj4 >> 4) | ((bj >> 6) << 4);
+  }
+}
+
+// The exact gate/up tiles of 32 values v_i = d sc q_i - dmin mn (Q2_K and
+// Q4_K): the integer sc q_i is exact in fp16 (one FMA removes the code
+// field's base), hi = RN(d (sc q)) and lo = d (sc q) - hi (an FMA residual,
+// exact barring underflow).  The minimum -dmin mn is returned split the
+// same way: mh = RN(-dmin mn), ml = -dmin mn - mh.
+
+// Half hb of quarter qq of a Q2_K super-block (values 64 qq + 32 hb .. +31,
+// sub-blocks 4 qq + 2 hb and + 1): hi / lo chunks 4 hb .. + 3 of row r,
+// and the two sub-blocks' (mh0, mh1) and (ml0, ml1) pairs.
+__device__ __forceinline__ void dq_q2k_exact(const uint8_t *blk, int qq, int hb, uint8_t *thi, uint8_t *tlo, int r,
+                                             uint32_t &mhp, uint32_t &mlp, bool &big) {
+  const int h = qq >> 1, s = 2 * (qq & 1) + hb;
+  const uint32_t scw = ptx::lds32(blk + 4 * qq);
+  const uint32_t ddm = ptx::lds32(blk + 80);
+  const uint32_t d2 = dup_lo(ddm);
+  const float d = f16_bits_to_f32(ddm & 0xFFFFu), dmin = f16_bits_to_f32(ddm >> 16);
+  const float magic = (float)(1 << (10 - 2 * s));
+  uint32_t sc2[2], nms2[2];
+  uint32_t mn2 = 0;
+#pragma unroll
+  for (int sb = 0; sb < 2; ++sb) {
+    const uint32_t byte = (scw >> (8 * (2 * hb + sb))) & 0xFFu;
+    const float sc = (float)(byte & 15u);
+    sc2[sb] = f16_dup(sc);
+    nms2[sb] = f16_dup(-magic * sc);
+    mn2 |= (uint32_t)__half_as_ushort(__float2half_rn((float)(byte >> 4))) << (16 * sb);
+  }
+  const uint32_t ndm2 = f16_dup(-dmin);
+  mhp = ptx::mul_f16x2(mn2, ndm2);
+  mlp = ptx::fma_f16x2(mn2, ndm2, mhp ^ 0x80008000u);
+  const uint32_t mask = (3u << (2 * s)) * 0x00010001u;
+  const uint32_t base = ((uint32_t)(25 - 2 * s) << 10) * 0x00010001u;
+  uint32_t hi[16], lo[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t w = ptx::lds32(blk + 16 + 32 * h + 4 * i);
+    const uint32_t p[2] = {__byte_perm(w, 0, 0x4140), __byte_perm(w, 0, 0x4342)};
+    const int sb = i >> 2;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint32_t scq = ptx::fma_f16x2(ptx::and_or(p[j], mask, base), sc2[sb], nms2[sb]);
+      hi[2 * i + j] = ptx::mul_f16x2(scq, d2);
+      lo[2 * i + j] = ptx::fma_f16x2(scq, d2, hi[2 * i + j] ^ 0x80008000u);
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    sts128(thi + sw128_off(r, 4 * hb + c), hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+    sts128(tlo + sw128_off(r, 4 * hb + c), lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+  }
+  big |= fabsf(d) * 45.f > 65504.f || fabsf(dmin) * 15.f > 65504.f;
+}
+
+// Q4_K sub-block j (32 values, nibble hb of the 32 code bytes at qs32) of
+// a super-block whose header (d, dmin, 12 scale bytes) is `hd`: hi / lo
+// chunks 4 hb .. + 3 of row r; returns mh | ml << 16.
+__device__ __forceinline__ uint32_t dq_q4k_exact(const uint8_t *qs32, const uint4 &hd, int j, int hb, uint8_t *thi,
+                                                 uint8_t *tlo, int r, bool &big) {
+  const uint32_t d2 = dup_lo(hd.x);
+  const float d = f16_bits_to_f32(hd.x & 0xFFFFu), dmin = f16_bits_to_f32(hd.x >> 16);
+  uint32_t sc, mn;
+  q4k_sm_regs(hd.y, hd.z, hd.w, j, sc, mn);
+  const float magic = hb ? 64.f : 1024.f;
+  const uint32_t sc2 = f16_dup((float)sc), nms2 = f16_dup(-magic * (float)sc);
+  const uint32_t mask = hb ? 0x00F000F0u : 0x000F000Fu, base = hb ? 0x54005400u : kMagic1024;
+  uint32_t hi[16], lo[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t w = ptx::lds32(qs32 + 4 * i);
+    const uint32_t p[2] = {__byte_perm(w, 0, 0x4140), __byte_perm(w, 0, 0x4342)};
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const uint32_t scq = ptx::fma_f16x2(ptx::and_or(p[jj], mask, base), sc2, nms2);
+      hi[2 * i + jj] = ptx::mul_f16x2(scq, d2);
+      lo[2 * i + jj] = ptx::fma_f16x2(scq, d2, hi[2 * i + jj] ^ 0x80008000u);
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    sts128(thi + sw128_off(r, 4 * hb + c), hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+    sts128(tlo + sw128_off(r, 4 * hb + c), lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+  }
+  big |= fabsf(d) * 945.f > 65504.f || fabsf(dmin) * 63.f > 65504.f;
+  const uint32_t mn2 = f16_dup((float)mn), ndm2 = f16_dup(-dmin);
+  const uint32_t mh = ptx::mul_f16x2(mn2, ndm2), ml = ptx::fma_f16x2(mn2, ndm2, mh ^ 0x80008000u);
+  return (mh & 0xFFFFu) | (ml << 16);
+}
+
+// Q4_K down: K-step kk of the super-block `blk` (144 bytes), sub-block
+// 2 kk + hb, rounded once to fp16 as RN(RN(d sc) q + RN(-dmin mn)) into
+// chunks 4 hb .. + 3 of row r.  Returns whether a value left the fp16 range.
+__device__ __forceinline__ bool dq_q4k(const uint8_t *blk, int kk, uint8_t *tile, int r, int hb) {
+  const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
+  const float d = f16_bits_to_f32(hd.x & 0xFFFFu), dmin = f16_bits_to_f32(hd.x >> 16);
+  uint32_t sc, mn;
+  q4k_sm_regs(hd.y, hd.z, hd.w, 2 * kk + hb, sc, mn);
+  const float a = d * (float)sc, b = -dmin * (float)mn;
+  const uint32_t a2 = f16_dup(a), b2 = f16_dup(b);
+  const uint32_t mask = hb ? 0x00F000F0u : 0x000F000Fu, base = hb ? 0x54005400u : kMagic1024;
+  uint32_t v[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t w = ptx::lds32(blk + 16 + 32 * kk + 4 * i);
+    v[2 * i] = ptx::fma_f16x2(ptx::sub_f16x2(ptx::and_or(__byte_perm(w, 0, 0x4140), mask, base), base), a2, b2);
+    v[2 * i + 1] = ptx::fma_f16x2(ptx::sub_f16x2(ptx::and_or(__byte_perm(w, 0, 0x4342), mask, base), base), a2, b2);
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) sts128(tile + sw128_off(r, 4 * hb + c), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+  return fabsf(a) * 15.f > 65504.f || fabsf(b) > 65504.f;
+}
+
 struct TcArgs {
   const Chunk *chunks;
   const int32_t *nchunks;
@@ -225,6 +396,10 @@ struct TcArgs {
   int rows;  // weight rows per expert = output features
   void *out; // gate/up: h fp16 [P][rows]; down: y fp32 [P][rows]
   WsHeader *hdr;
+  // Q2_K gate/up only: the gate and up matrices and their row length in
+  // bytes (the stages are bulk copies of whole rows' chunks, not TMA tiles)
+  const uint8_t *wq0, *wq1;
+  int64_t wrow_bytes;
 };
 
 __device__ __forceinline__ void tc_fail(WsHeader *hdr, volatile int *abort_flag) {
@@ -270,11 +445,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   const int MT = a.rows / kTileM;
   const int nunits = *a.nchunks * MT;
+  // gate/up: kMain main steps per minima step (16 for Q4_1 / Q4_K, 8 for Q2_K)
+  constexpr int kMain = NMAT == 2 ? GuFmt<QA>::kMain : 1;
   const int nks = a.K / kStepK;                                      // main K-steps
-  const int nsteps = NMAT == 2 ? nks + nks / kWinSteps : nks;       // + one minima step per window
-  // gate/up step s: main step (s / 17) * 16 + s % 17, or the minima step of
-  // window s / 17 when s % 17 == 16
-  auto is_min_step = [](int s) { return NMAT == 2 && s % (kWinSteps + 1) == kWinSteps; };
+  const int nsteps = NMAT == 2 ? nks + nks / kMain : nks;           // + the minima steps
+  // gate/up step s: main step (s / (kMain + 1)) * kMain + s % (kMain + 1),
+  // or the minima step of group s / (kMain + 1) when s % (kMain + 1) == kMain
+  auto is_min_step = [](int s) { return NMAT == 2 && s % (kMain + 1) == kMain; };
 
   if (warp < kDqWarps) {
     // ---------------------------------------------------------- dequant
@@ -293,49 +470,89 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
       if constexpr (NMAT == 2) {
-        for (int win = 0; win < a.K / kWinVals && ok; ++win) {
-          uint32_t mg[kWinSteps], mu[kWinSteps];
+        using G = GuFmt<QA>;
+        constexpr int kSS = G::kStageSteps;
+        for (int grp = 0; grp < nks / kMain && ok; ++grp) {
+          // per main step: Q4_1 the block minimum m; Q4_K mh | ml << 16 of its
+          // sub-block; Q2_K the (mh0, mh1) and (ml0, ml1) pairs at 2 kk, 2 kk + 1
+          uint32_t mg[16], mu[16];
           const uint8_t *qrow = nullptr;
           int qslot = 0;
+          uint4 hg = make_uint4(0u, 0u, 0u, 0u), hu = hg;  // Q4_K: the super-block headers
 #pragma unroll
-          for (int kk = 0; kk < kWinSteps; ++kk) {
+          for (int kk = 0; kk < kMain; ++kk) {
             if (!ok) break;
-            if ((kk & 1) == 0) {  // a Q4_1 stage (4 blocks) feeds two K-steps
+            if (kk % kSS == 0) {
               qslot = qit % C::kSQ;
               if (!wait_all(&qfull[qslot], (qit / C::kSQ) & 1)) { ok = false; break; }
-              qrow = sQ + qslot * C::kQSlot + r * QB;
+              qrow = sQ + qslot * C::kQSlot + r * G::kRowBytes;
             }
             const int aslot = ait % C::kSA;
             if (!wait_all(&aempty[aslot], ((ait / C::kSA) & 1) ^ 1)) { ok = false; break; }
             uint8_t *tile = sA + aslot * C::kASlot;
-            const int b = 2 * (kk & 1) + hb;
             // B tiles of 256 rows: gate rows 0..127 then up rows 128..255, hi then lo
-            mg[kk] = dq_q41_exact(qrow + 20 * b, tile, tile + 2 * C::kATile, r, hb, big);
-            mu[kk] = dq_q41_exact(qrow + C::kQMat + 20 * b, tile + C::kATile, tile + 3 * C::kATile, r, hb, big);
+            if constexpr (QA == DS4MOE_Q4_1) {
+              const int b = 2 * (kk & 1) + hb;  // a stage (4 blocks) feeds two K-steps
+              mg[kk] = dq_q41_exact(qrow + 20 * b, tile, tile + 2 * C::kATile, r, hb, big);
+              mu[kk] = dq_q41_exact(qrow + C::kQMat + 20 * b, tile + C::kATile, tile + 3 * C::kATile, r, hb, big);
+            } else if constexpr (QA == DS4MOE_Q4_K) {
+              const int j = kk & 1, hf = (kk >> 1) & 1;  // step j of super-block half hf
+              if ((kk & 3) == 0) {
+                hg = *reinterpret_cast<const uint4 *>(qrow);
+                hu = *reinterpret_cast<const uint4 *>(qrow + C::kQMat);
+              }
+              const int sub = 2 * (2 * hf + j) + hb;
+              mg[kk] = dq_q4k_exact(qrow + 16 + 32 * j, hg, sub, hb, tile, tile + 2 * C::kATile, r, big);
+              mu[kk] = dq_q4k_exact(qrow + C::kQMat + 16 + 32 * j, hu, sub, hb, tile + C::kATile,
+                                    tile + 3 * C::kATile, r, big);
+            } else {
+              const int sb = grp * (kMain / kSS) + kk / kSS;  // super-block of the row
+              const int off = 4 * (sb & 3);
+              dq_q2k_exact(qrow + off, kk & 3, hb, tile, tile + 2 * C::kATile, r, mg[2 * kk], mg[2 * kk + 1], big);
+              dq_q2k_exact(qrow + C::kQMat + off, kk & 3, hb, tile + C::kATile, tile + 3 * C::kATile, r, mu[2 * kk],
+                           mu[2 * kk + 1], big);
+            }
             publish(aslot);
             ++ait;
-            if (kk & 1) {
+            if (kk % kSS == kSS - 1) {
               __syncwarp();
               if (lane == 0) ptx::mbar_arrive(&qempty[qslot]);
               ++qit;
             }
           }
           if (!ok) break;
-          // minima step: column 32 hb + 2 kk (+1) of the window's extra K-step
-          // holds m of block 2 kk + hb, against the hi (lo) part of its x sum
+          // minima step: its 64 columns pair with the hi and lo parts of the
+          // x block sums (32 hb + 2 kk (+1): the 32-value block 2 kk + hb of
+          // a Q4_1 / Q4_K window; 32 hb + 4 kk + 2 s (+1): the 16-value
+          // sub-block 4 kk + 2 hb + s of a Q2_K group); the hi tiles take m
+          // (or mh), the lo tiles ml
           const int aslot = ait % C::kSA;
           if (!wait_all(&aempty[aslot], ((ait / C::kSA) & 1) ^ 1)) { ok = false; break; }
           uint8_t *tile = sA + aslot * C::kASlot;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            uint32_t g4[4], u4[4];
+            uint32_t gh[4], uh[4], gl[4], ul[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              g4[i] = mg[4 * c + i] | (mg[4 * c + i] << 16);
-              u4[i] = mu[4 * c + i] | (mu[4 * c + i] << 16);
+              if constexpr (QA == DS4MOE_Q2_K) {
+                const int kk = 2 * c + (i >> 1);
+                gh[i] = (i & 1) ? dup_hi(mg[2 * kk]) : dup_lo(mg[2 * kk]);
+                uh[i] = (i & 1) ? dup_hi(mu[2 * kk]) : dup_lo(mu[2 * kk]);
+                gl[i] = (i & 1) ? dup_hi(mg[2 * kk + 1]) : dup_lo(mg[2 * kk + 1]);
+                ul[i] = (i & 1) ? dup_hi(mu[2 * kk + 1]) : dup_lo(mu[2 * kk + 1]);
+              } else {
+                gh[i] = dup_lo(mg[4 * c + i]);
+                uh[i] = dup_lo(mu[4 * c + i]);
+                gl[i] = dup_hi(mg[4 * c + i]);
+                ul[i] = dup_hi(mu[4 * c + i]);
+              }
             }
-            sts128(tile + sw128_off(r, 4 * hb + c), g4[0], g4[1], g4[2], g4[3]);
-            sts128(tile + C::kATile + sw128_off(r, 4 * hb + c), u4[0], u4[1], u4[2], u4[3]);
+            sts128(tile + sw128_off(r, 4 * hb + c), gh[0], gh[1], gh[2], gh[3]);
+            sts128(tile + C::kATile + sw128_off(r, 4 * hb + c), uh[0], uh[1], uh[2], uh[3]);
+            if constexpr (G::kMinLo) {
+              sts128(tile + 2 * C::kATile + sw128_off(r, 4 * hb + c), gl[0], gl[1], gl[2], gl[3]);
+              sts128(tile + 3 * C::kATile + sw128_off(r, 4 * hb + c), ul[0], ul[1], ul[2], ul[3]);
+            }
           }
           publish(aslot);
           ++ait;
@@ -351,6 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t *tile = sA + aslot * C::kASlot;
             if constexpr (QA == DS4MOE_Q4_1)
               big |= dq_q41(qrow + 20 * (2 * kk + hb), tile, r, hb);
+            else if constexpr (QA == DS4MOE_Q4_K)
+              big |= dq_q4k(qrow, kk, tile, r, hb);
             else
               big |= dq_q2k(qrow + 84 * (kk >> 2), kk & 3, tile, r, hb);
             publish(aslot);
@@ -419,19 +638,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (big) record_status(a.hdr, DS4MOE_EDEVICE);
   } else if (warp == kQWarp) {
-    // ------------------------------------------------ TMA: weight blocks
-    if (lane == 0) {
+    // ------------------------------------------------ weight stages
+    constexpr int kSteps = NMAT == 2 ? GuFmt<QA>::kStageSteps : QV / kStepK;  // K-steps per stage
+    const int nst = a.K / (kSteps * kStepK);                                   // stages per row
+    if constexpr (NMAT == 2 && QA == DS4MOE_Q2_K) {
+      // bulk copies: per row and matrix the six 16-byte chunks that cover
+      // the super-block (its 84 bytes never start 16-byte aligned for all
+      // super-blocks, so no tensor-map box fits them); the whole warp issues
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const Chunk ch = a.chunks[u / MT];
+        const int64_t row0 = (int64_t)ch.e * a.rows + (int64_t)(u % MT) * kTileM;
+        for (int qs = 0; qs < nst; ++qs, ++it) {
+          const int slot = it % C::kSQ;
+          bool got = true;
+          if (lane == 0) got = ptx::mbar_wait_or_abort(&qempty[slot], ((it / C::kSQ) & 1) ^ 1, abort_flag);
+          if (!__shfl_sync(~0u, got, 0)) { ok = false; break; }
+          if (lane == 0) ptx::mbar_arrive_expect_tx(&qfull[slot], C::kQSlot);
+          __syncwarp();
+          const int64_t off = (int64_t)(84 * qs) & ~int64_t(15);
+          for (int j = lane; j < 2 * kTileM; j += 32) {
+            const int m = j / kTileM, rr = j % kTileM;
+            const uint8_t *src = (m ? a.wq1 : a.wq0) + (row0 + rr) * a.wrow_bytes + off;
+            ptx::bulk_g2s(sQ + slot * C::kQSlot + m * C::kQMat + rr * GuFmt<QA>::kRowBytes, src,
+                          GuFmt<QA>::kRowBytes, &qfull[slot]);
+          }
+        }
+      }
+      if (!ok && lane == 0) {
+        tc_fail(a.hdr, abort_flag);
+        for (int j = it - C::kSQ < 0 ? 0 : it - C::kSQ; j < it; ++j)  // let issued copies land
+          ptx::mbar_wait(&qfull[j % C::kSQ], (j / C::kSQ) & 1, 1u << 20);
+      }
+    } else if (lane == 0) {
+      // TMA tiles of 128 rows; x in u32 words: Q4_1 20 per stage; Q4_K
+      // 36 per super-block, half 1 from word 16; down: one stage's bytes
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         const Chunk ch = a.chunks[u / MT];
         const int row0 = ch.e * a.rows + (u % MT) * kTileM;
-        for (int qs = 0; qs < a.K / QV; ++qs, ++it) {
+        for (int qs = 0; qs < nst; ++qs, ++it) {
           const int slot = it % C::kSQ;
           if (!ptx::mbar_wait_or_abort(&qempty[slot], ((it / C::kSQ) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          const int x = NMAT == 2 && QA == DS4MOE_Q4_K ? (qs >> 1) * 36 + (qs & 1) * 16 : qs * (C::kRowQ / 4);
           ptx::mbar_arrive_expect_tx(&qfull[slot], C::kQSlot);
-          ptx::tma_load_2d(sQ + slot * C::kQSlot, &mA0, qs * (QB / 4), row0, &qfull[slot]);
-          if constexpr (NMAT == 2) ptx::tma_load_2d(sQ + slot * C::kQSlot + C::kQMat, &mA1, qs * (QB / 4), row0, &qfull[slot]);
+          ptx::tma_load_2d(sQ + slot * C::kQSlot, &mA0, x, row0, &qfull[slot]);
+          if constexpr (NMAT == 2) ptx::tma_load_2d(sQ + slot * C::kQSlot + C::kQMat, &mA1, x, row0, &qfull[slot]);
         }
       }
       if (!ok) {
@@ -453,8 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = it % C::kSB;
           // column of the step: main K-steps first in each window, then the
           // window's block sums (stored after the D values of each row)
-          const int col = NMAT == 2 ? (is_min_step(s) ? a.K + kStepK * (s / (kWinSteps + 1))
-                                                      : kStepK * ((s / (kWinSteps + 1)) * kWinSteps + s % (kWinSteps + 1)))
+          const int col = NMAT == 2 ? (is_min_step(s) ? a.K + kStepK * (s / (kMain + 1))
+                                                      : kStepK * ((s / (kMain + 1)) * kMain + s % (kMain + 1)))
                                     : kStepK * s;
           if (!ptx::mbar_wait_or_abort(&bempty[slot], ((it / C::kSB) & 1) ^ 1, abort_flag)) { ok = false; break; }
           ptx::mbar_arrive_expect_tx(&bfull[slot], nload * kBRowsPerLoad * kStepK * 2);
@@ -494,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a0 = ptx::smem_u32(sA + aslot * C::kASlot), b0 = ptx::smem_u32(sB + bslot * C::kBSlot);
           if constexpr (NMAT == 2) {
             // tokens (the B ring's tile) as A, the 256 weight rows as B
-            const bool lo_too = !is_min_step(s);
+            const bool lo_too = !is_min_step(s) || GuFmt<QA>::kMinLo;
 #pragma unroll
             for (int kk = 0; kk < kStepK / 16; ++kk) {
               const uint64_t xd = sw128_desc(b0 + 32 * kk);
@@ -531,12 +785,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // x of every sorted pair as fp16 (exact for bf16 values within the fp16
-// range; larger magnitudes are flagged), row stride ld.  With `sums`, each
-// row also carries the hi and lo fp16 parts of its 32-value block sums after
-// the D values, in the order the gate/up minima steps read them: block b at
-// D + 64 (b / 32) + 32 (b % 2) + 2 ((b % 32) / 2) (+1 for lo).
+// range; larger magnitudes are flagged), row stride ld.  After the D values
+// each row carries the hi and lo fp16 parts of its block sums, in the order
+// the gate/up minima steps read them:
+//   sums = 1 (Q4_1 / Q4_K): 32-value block b at
+//            D + 64 (b / 32) + 32 (b % 2) + 2 ((b % 32) / 2) (+1 for lo);
+//   sums = 2 (Q2_K): 16-value sub-block g at
+//            D + 64 (g / 32) + 32 ((g % 4) / 2) + 4 ((g % 32) / 4) + 2 (g % 2) (+1).
 __global__ void k_xperm(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm,
-                        const int32_t *__restrict__ offs, int E, int k, int D, int ld, bool sums,
+                        const int32_t *__restrict__ offs, int E, int k, int D, int ld, int sums,
                         uint16_t *__restrict__ xp, WsHeader *__restrict__ hdr) {
   const int nv = offs[E];
   const int nb = D / 32;
@@ -548,7 +805,7 @@ __global__ void k_xperm(const uint16_t *__restrict__ x, const int32_t *__restric
     const int t = perm[p] / k;
     const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)t * D + 32 * b);
     uint4 *dst = reinterpret_cast<uint4 *>(xp + p * ld + 32 * b);
-    float sum = 0.f;
+    float hsum[2] = {0.f, 0.f};  // values 0..15 and 16..31 of the block
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
       const uint4 q = __ldg(src + v);
@@ -558,18 +815,26 @@ __global__ void k_xperm(const uint16_t *__restrict__ x, const int32_t *__restric
       for (int j = 0; j < 4; ++j) {
         const float lo = bf16_bits_to_f32(wd[j] & 0xFFFFu), hi = bf16_bits_to_f32(wd[j] >> 16);
         big |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
-        sum += lo + hi;
+        hsum[v >> 1] += lo + hi;
         o[j] = (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
       }
       dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    if (sums) {
+    auto put = [&](float sum, int64_t col) {
       const __half sh = __float2half_rn(sum);
       const __half sl = __float2half_rn(sum - __half2float(sh));
       big |= !(fabsf(sum) <= 65504.f);
-      const int64_t col = D + 64 * (b >> 5) + 32 * (b & 1) + 2 * ((b & 31) >> 1);
       *reinterpret_cast<uint32_t *>(xp + p * ld + col) =
           (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(sl) << 16);
+    };
+    if (sums == 1) {
+      put(hsum[0] + hsum[1], D + 64 * (b >> 5) + 32 * (b & 1) + 2 * ((b & 31) >> 1));
+    } else if (sums == 2) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int g = 2 * b + hh;
+        put(hsum[hh], D + 64 * (g >> 5) + 32 * ((g & 3) >> 1) + 4 * ((g & 31) >> 2) + 2 * (g & 1));
+      }
     }
   }
   if (big) record_status(hdr, DS4MOE_EDEVICE);
@@ -658,11 +923,14 @@ cudaError_t launch_tc(const CUtensorMap &mA0, const CUtensorMap &mA1, const CUte
 
 bool prefill_tc_ok(const ds4moe_layer &L) {
   const int D = L.d_model, F = L.d_ff;
-  if (L.q_gate != DS4MOE_Q4_1 || L.q_up != DS4MOE_Q4_1) return false;
+  if (L.q_gate != L.q_up) return false;
+  if (L.q_gate != DS4MOE_Q4_1 && L.q_gate != DS4MOE_Q4_K && L.q_gate != DS4MOE_Q2_K) return false;
   if (L.q_down == DS4MOE_Q2_K) {
     if (F % QFmt<DS4MOE_Q2_K>::kVals) return false;
   } else if (L.q_down == DS4MOE_Q4_1) {
     if (F % QFmt<DS4MOE_Q4_1>::kVals) return false;
+  } else if (L.q_down == DS4MOE_Q4_K) {
+    if (F % QFmt<DS4MOE_Q4_K>::kVals) return false;
   } else {
     return false;
   }
@@ -683,7 +951,8 @@ cudaError_t launch_ffn_prefill(const FfnArgs &a, cudaStream_t s) {
     ProfScope p("xperm", s);
     const int64_t work = (int64_t)P * (D / 32);
     const int grid = (int)((work + 255) / 256 < num_sms() * 8 ? (work + 255) / 256 : num_sms() * 8);
-    k_xperm<<<grid, 256, 0, s>>>(a.x, a.perm, a.offs, E, a.k, D, xp_cols(D), true, a.xp, a.hdr);
+    k_xperm<<<grid, 256, 0, s>>>(a.x, a.perm, a.offs, E, a.k, D, xp_cols(D), L.q_gate == DS4MOE_Q2_K ? 2 : 1,
+                                 a.xp, a.hdr);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {
@@ -692,22 +961,30 @@ cudaError_t launch_ffn_prefill(const FfnArgs &a, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   CUtensorMap mg, mu, md, mx, mh;
-  if (!map_weights(&mg, L.gate, row_bytes(L.q_gate, D), (int64_t)E * F, QFmt<DS4MOE_Q4_1>::kBytes) ||
-      !map_weights(&mu, L.up, row_bytes(L.q_up, D), (int64_t)E * F, QFmt<DS4MOE_Q4_1>::kBytes) ||
-      !map_acts(&mx, a.xp, xp_cols(D), P) || !map_acts(&mh, a.h, F, P))
+  if (!map_acts(&mx, a.xp, xp_cols(D), P) || !map_acts(&mh, a.h, F, P)) return cudaErrorInvalidValue;
+  const int qg = L.q_gate, qd = L.q_down;
+  if (qg == DS4MOE_Q2_K) {
+    mg = mu = mx;  // unused: the Q2_K gate/up stages are bulk copies
+  } else if (!map_weights(&mg, L.gate, row_bytes(qg, D), (int64_t)E * F, GuFmt<DS4MOE_Q4_1>::kRowBytes) ||
+             !map_weights(&mu, L.up, row_bytes(qg, D), (int64_t)E * F, GuFmt<DS4MOE_Q4_1>::kRowBytes)) {
     return cudaErrorInvalidValue;
-  const bool dq2 = L.q_down == DS4MOE_Q2_K;
-  if (!map_weights(&md, L.down, row_bytes(L.q_down, F), (int64_t)E * D,
-                   dq2 ? QFmt<DS4MOE_Q2_K>::kBytes : QFmt<DS4MOE_Q4_1>::kBytes))
-    return cudaErrorInvalidValue;
+  }
+  const int dbytes = qd == DS4MOE_Q2_K ? QFmt<DS4MOE_Q2_K>::kBytes
+                     : qd == DS4MOE_Q4_K ? QFmt<DS4MOE_Q4_K>::kBytes
+                                         : QFmt<DS4MOE_Q4_1>::kBytes;
+  if (!map_weights(&md, L.down, row_bytes(qd, F), (int64_t)E * D, dbytes)) return cudaErrorInvalidValue;
   const int ne = E < P ? E : P;
-  TcArgs gu{a.chunks_gu, a.nchunks, D, F, a.h, a.hdr};
-  e = launch_tc<2, DS4MOE_Q4_1, kChunkGateUp>(mg, mu, mx, gu, (ne + P / kChunkGateUp) * (F / kTileM), s,
-                                              "gate_up_tc");
+  TcArgs gu{a.chunks_gu, a.nchunks, D, F, a.h, a.hdr, static_cast<const uint8_t *>(L.gate),
+            static_cast<const uint8_t *>(L.up), row_bytes(qg, D)};
+  const int gu_units = (ne + P / kChunkGateUp) * (F / kTileM);
+  e = qg == DS4MOE_Q2_K   ? launch_tc<2, DS4MOE_Q2_K, kChunkGateUp>(mg, mu, mx, gu, gu_units, s, "gate_up_tc")
+      : qg == DS4MOE_Q4_K ? launch_tc<2, DS4MOE_Q4_K, kChunkGateUp>(mg, mu, mx, gu, gu_units, s, "gate_up_tc")
+                          : launch_tc<2, DS4MOE_Q4_1, kChunkGateUp>(mg, mu, mx, gu, gu_units, s, "gate_up_tc");
   if (e != cudaSuccess) return e;
-  TcArgs dn{a.chunks_dn, a.nchunks + 1, F, D, a.y, a.hdr};
+  TcArgs dn{a.chunks_dn, a.nchunks + 1, F, D, a.y, a.hdr, nullptr, nullptr, 0};
   const int dn_units = (ne + P / kChunkDown) * (D / kTileM);
-  if (dq2) return launch_tc<1, DS4MOE_Q2_K, kChunkDown>(md, md, mh, dn, dn_units, s, "down_tc");
+  if (qd == DS4MOE_Q2_K) return launch_tc<1, DS4MOE_Q2_K, kChunkDown>(md, md, mh, dn, dn_units, s, "down_tc");
+  if (qd == DS4MOE_Q4_K) return launch_tc<1, DS4MOE_Q4_K, kChunkDown>(md, md, mh, dn, dn_units, s, "down_tc");
   return launch_tc<1, DS4MOE_Q4_1, kChunkDown>(md, md, mh, dn, dn_units, s, "down_tc");
 }
 

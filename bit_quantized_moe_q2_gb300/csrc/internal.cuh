@@ -73,8 +73,9 @@ struct Chunk {
 // Token-chunk widths of the prefill kernels (gate/up and down).
 constexpr int kChunkGateUp = 128, kChunkDown = 256;
 // Row length of the gathered prefill activations: D fp16 values, then the
-// hi/lo fp16 parts of the D/32 block sums.
-inline int64_t xp_cols(int64_t D) { return D + D / 16; }
+// hi/lo fp16 parts of the block sums (D/32 blocks of 32 values for Q4_1 /
+// Q4_K gate/up, D/16 sub-blocks of 16 for Q2_K: room for the larger).
+inline int64_t xp_cols(int64_t D) { return D + D / 8; }
 
 struct WsLayout {
   size_t hdr, logits, rnorm, rlist, counts, offs, active, perm, inv, lrank, groups, x16, xs16, xs32, hs16, h, y, nvalid, cnt,

@@ -2,12 +2,13 @@
 the CPU oracle, through ds4moe_ffn_prefill.
 
 Covers: the kernels really run (profiling names them) for eligible layers
-(Q4_1 gate/up with d_model a multiple of 1024) and not for others; Q2_K and
-Q4_1 down; token chunks that split an expert (more than 128 / 256 pairs on
-one expert); experts with no tokens; a single
-token; ragged chunk tails (n not a multiple of 16 or 32); run-to-run bit
-equality (static schedule, fixed accumulation order).  Bar as for every FFN
-test: max |err| <= 2e-3 * max |ref|.
+(gate and up in one of Q4_1 / Q4_K / Q2_K, d_model a multiple of 1024) and
+not for others; Q2_K, Q4_1 and Q4_K down; the exact gate/up tiles of every
+gate/up format (Q2_K: a minima step per 8 main steps, 16-value sub-block
+sums); token chunks that split an expert (more than 128 / 256 pairs on one
+expert); experts with no tokens; a single token; ragged chunk tails (n not a
+multiple of 16 or 32); run-to-run bit equality (static schedule, fixed
+accumulation order).  Bar as for every FFN test: max |err| <= 2e-3 * max |ref|.
 """
 import numpy as np
 import pytest
@@ -37,6 +38,15 @@ TC_SHAPES = [
     synth.WORKLOADS[3].replace(d_model=1024, d_ff=384, n_expert=5, k=3, T=77, seed=302, down=synth.Q41_4BIT),
     # 3-bit codes re-encoded as Q4_1, router bias
     synth.WORKLOADS[2].replace(d_model=2048, d_ff=1024, n_expert=12, k=4, T=45, seed=303, bias_sigma=1.0),
+    # all Q2_K (the decode workload's formats at prefill): two 512-value
+    # minima groups per 1024 values, four per row here
+    synth.WORKLOADS[1].replace(d_model=2048, d_ff=1024, n_expert=8, k=3, T=140, seed=304),
+    # all Q4_K, d_ff a multiple of 256 but not of 1024
+    synth.WORKLOADS[5].replace(d_model=1024, d_ff=768, n_expert=6, k=2, T=130, seed=305),
+    # Q4_K gate/up, Q2_K down (the mixed recipe's Q4 layers next to 2-bit ones)
+    synth.WORKLOADS[5].replace(d_model=2048, d_ff=1024, n_expert=7, k=2, T=90, seed=306, down=synth.Q2K),
+    # Q2_K gate/up, Q4_1 down, one token per expert at most on some experts
+    synth.WORKLOADS[1].replace(d_model=1024, d_ff=512, n_expert=16, k=2, T=9, seed=307, down=synth.Q41_4BIT),
 ]
 
 
@@ -56,12 +66,31 @@ def test_tensor_core_kernels_run_only_for_eligible_layers(M):
     x = synth.activations(w)
     names = _profiled_names(M, lambda: gpu_forward(M, dev, x, L.Wr, L.bias, w.k, prefill=True))
     assert {"gate_up_tc", "down_tc"} <= names
-    # Q2_K gate/up: the prefill call takes the warp-MMA kernels instead
-    w2 = w.replace(gate=synth.Q2K, up=synth.Q2K)
+    # gate and up in different formats: the prefill call takes the warp-MMA
+    # kernels instead
+    w2 = w.replace(gate=synth.Q2K)
     L2 = build_layer(w2)
     dev2 = to_device(L2)
     names2 = _profiled_names(M, lambda: gpu_forward(M, dev2, x, L2.Wr, L2.bias, w2.k, prefill=True))
     assert not ({"gate_up_tc", "down_tc"} & names2)
+    # d_model not a multiple of 1024: likewise
+    w3 = w.replace(d_model=512, d_ff=1024)
+    L3 = build_layer(w3)
+    dev3 = to_device(L3)
+    x3 = synth.activations(w3)
+    names3 = _profiled_names(M, lambda: gpu_forward(M, dev3, x3, L3.Wr, L3.bias, w3.k, prefill=True))
+    assert not ({"gate_up_tc", "down_tc"} & names3)
+
+
+@pytest.mark.parametrize("wi", [3, 4, 5, 6])
+def test_every_gate_up_format_takes_the_tensor_cores(M, wi):
+    w = TC_SHAPES[wi]
+    L = build_layer(w)
+    dev = to_device(L)
+    x = synth.activations(w)
+    names = _profiled_names(M, lambda: gpu_forward(M, dev, x, L.Wr, L.bias, w.k, prefill=True))
+    assert {"gate_up_tc", "down_tc"} <= names
+    assert not ({"gate_up", "down", "gate_up_simt", "down_simt"} & names)
 
 
 @pytest.mark.parametrize("wi", range(len(TC_SHAPES)))
@@ -80,12 +109,12 @@ def test_prefill_tc_matches_oracle_all_tokens(M, wi):
     assert np.array_equal(out2.view(np.uint32), out.view(np.uint32))
 
 
-@pytest.mark.parametrize("T,k", [(300, 1), (301, 2), (1, 6)])
-def test_prefill_tc_heavy_expert_and_single_token(M, T, k):
+@pytest.mark.parametrize("T,k,wi", [(300, 1, 0), (301, 2, 0), (1, 6, 0), (260, 2, 3), (270, 2, 4)])
+def test_prefill_tc_heavy_expert_and_single_token(M, T, k, wi):
     """Slot 0 of every token goes to expert 3: 300 pairs on one expert span
     three 128-pair gate/up chunks and two 256-pair down chunks; the other
     slots spread over the remaining experts, several of which stay empty."""
-    w = TC_SHAPES[0].replace(T=T, k=k, n_expert=8, seed=310 + k)
+    w = TC_SHAPES[wi].replace(T=T, k=k, n_expert=8, seed=310 + k + wi)
     L = build_layer(w)
     dev = to_device(L)
     x = synth.activations(w)

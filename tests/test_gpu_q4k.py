@@ -1,5 +1,6 @@
 """GPU parity of the Q4_K expert path (dequant and the FFN entry points;
-Q4_K layers run the SIMT kernels) against the oracle: dequant bit for bit
+Q4_K layers run the single-token, persistent multi-token and, at prefill
+with d_model a multiple of 1024, the tcgen05 kernels) against the oracle: dequant bit for bit
 (incl. arbitrary bytes with inf / NaN / subnormal scales), the layer output
 within 2e-3 * max |ref| with routing bit-exact, for all-Q4_K layers and
 Q4_K mixed with Q2_K / Q4_1 matrices."""
