@@ -92,6 +92,9 @@ def parse_args(argv=None):
                     help="single-layer or stack decode at T = 1: repack Q2_K weights into the 16-row tile order")
     ap.add_argument("--plain", action="store_true",
                     help="workload 1 alone on plain Q2_K blocks (no sub-records)")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time the prefill path (tensor-core grouped GEMMs) on this workload's layer and formats "
+                         "(--tokens sets the chunk, default 4096)")
     ap.add_argument("--shared", type=int, default=0, metavar="D_SHARED",
                     help="time the shared expert alone (bf16, d_model of the workload, this width; "
                          "--tokens sets the tokens per step, default 1)")
@@ -639,7 +642,8 @@ def decode_layer_record(args, M, torch, w: synth.Workload, copies, layout: str, 
 
 def prefill_record(args, M, torch, w: synth.Workload, rank: int, world: int, local: int, with_e2e: bool) -> dict:
     """Prefill: route (with bias) + tensor-core expert FFN over T tokens per
-    step.  Inputs (3.4 GB of weights) far exceed L2, so no flush is needed."""
+    step.  Inputs (3.4 GB of weights at the Flash shape) far exceed L2, so no
+    flush is needed."""
     from bit_quantized_moe_q2_gb300.device import check_status, workspace
     dev = device_layer(w, M, torch)
     Wr, bias = synth.router(w)
@@ -674,7 +678,8 @@ def prefill_record(args, M, torch, w: synth.Workload, rank: int, world: int, loc
            "ms_per_step": ms / steps, "tflops": world * steps * flops_step / (ms / 1000.0) / 1e12,
            "clocks": clocks}
     cfg = workload_config(w, 1)
-    cfg["l2"] = "inputs larger than L2: every step streams 3.4 GB of expert weights"
+    cfg["l2"] = (f"inputs larger than L2: every step streams {w.n_expert * expert_bytes(w) / 1e9:.2f} GB "
+                 "of expert weights")
     rec["config"] = cfg
     if args.timed_only:
         return rec
@@ -683,7 +688,8 @@ def prefill_record(args, M, torch, w: synth.Workload, rank: int, world: int, loc
     rec["tensor_frac"] = rec["tflops"] / peak
     if "gate_up_tc" in kernels:
         us = kernels["gate_up_tc"]["avg_us"]
-        rec["roofline"] = {"kernel": "gate_up_tc (tcgen05 grouped GEMM, fused Q4_1 dequant + SwiGLU)",
+        qname = synth.recipe(w, synth.T_GATE).qtype.upper()
+        rec["roofline"] = {"kernel": f"gate_up_tc (tcgen05 grouped GEMM, fused {qname} dequant + SwiGLU)",
                            "bound": "tensor", "achieved": flops_gu / (us * 1e-6) / 1e12, "peak": peak,
                            "unit": "TFLOP/s", "frac": flops_gu / (us * 1e-6) / 1e12 / peak, "traffic": None,
                            "algorithmic_flops_per_launch": flops_gu, "avg_launch_us": us,
@@ -1162,6 +1168,9 @@ def main(argv=None):
         w = w.replace(n_expert=args.n_expert)
     if args.tokens:
         w = w.replace(T=args.tokens)
+    if args.prefill and w.path != "prefill":
+        T = args.tokens or 4096
+        w = w.replace(path="prefill", T=T, name=f"{w.name}@prefill-T{T}")
     if w.path not in ("decode", "prefill"):
         raise SystemExit("bench.py times workloads 0-5")
     if args.quantize:

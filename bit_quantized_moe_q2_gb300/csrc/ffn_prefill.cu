@@ -84,9 +84,11 @@ constexpr int kWinSteps = 16, kWinVals = kWinSteps * kStepK;
 //   Q4_K: half a super-block per stage: the 16-byte header and 64 code
 //         bytes for half 0 (words 0..19 of the block), words 16..35 for
 //         half 1 (the header is kept from half 0); 2 K-steps.
-//   Q2_K: one super-block per stage, copied as the six 16-byte chunks that
-//         cover its 84 bytes (it starts at byte 4 (sb % 4) of the 96-byte
-//         row); 4 K-steps; its 16-value sub-blocks give 32 minima per 8
+//   Q2_K: one super-block per stage, as the 96 bytes from the 16-byte
+//         boundary at or below it (a tensor-map box must be a multiple of
+//         16 bytes wide; the block starts at byte 4 (sb % 4) of the staged
+//         row, and for the row's last block the 96 bytes end at the row's
+//         end); 4 K-steps; its 16-value sub-blocks give 32 minima per 8
 //         K-steps, so a minima step follows every 8 main steps.
 template <int Q>
 struct GuFmt;
@@ -396,10 +398,6 @@ struct TcArgs {
   int rows;  // weight rows per expert = output features
   void *out; // gate/up: h fp16 [P][rows]; down: y fp32 [P][rows]
   WsHeader *hdr;
-  // Q2_K gate/up only: the gate and up matrices and their row length in
-  // bytes (the stages are bulk copies of whole rows' chunks, not TMA tiles)
-  const uint8_t *wq0, *wq1;
-  int64_t wrow_bytes;
 };
 
 __device__ __forceinline__ void tc_fail(WsHeader *hdr, volatile int *abort_flag) {
@@ -641,39 +639,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ weight stages
     constexpr int kSteps = NMAT == 2 ? GuFmt<QA>::kStageSteps : QV / kStepK;  // K-steps per stage
     const int nst = a.K / (kSteps * kStepK);                                   // stages per row
-    if constexpr (NMAT == 2 && QA == DS4MOE_Q2_K) {
-      // bulk copies: per row and matrix the six 16-byte chunks that cover
-      // the super-block (its 84 bytes never start 16-byte aligned for all
-      // super-blocks, so no tensor-map box fits them); the whole warp issues
-      int it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-        const Chunk ch = a.chunks[u / MT];
-        const int64_t row0 = (int64_t)ch.e * a.rows + (int64_t)(u % MT) * kTileM;
-        for (int qs = 0; qs < nst; ++qs, ++it) {
-          const int slot = it % C::kSQ;
-          bool got = true;
-          if (lane == 0) got = ptx::mbar_wait_or_abort(&qempty[slot], ((it / C::kSQ) & 1) ^ 1, abort_flag);
-          if (!__shfl_sync(~0u, got, 0)) { ok = false; break; }
-          if (lane == 0) ptx::mbar_arrive_expect_tx(&qfull[slot], C::kQSlot);
-          __syncwarp();
-          const int64_t off = (int64_t)(84 * qs) & ~int64_t(15);
-          for (int j = lane; j < 2 * kTileM; j += 32) {
-            const int m = j / kTileM, rr = j % kTileM;
-            const uint8_t *src = (m ? a.wq1 : a.wq0) + (row0 + rr) * a.wrow_bytes + off;
-            ptx::bulk_g2s(sQ + slot * C::kQSlot + m * C::kQMat + rr * GuFmt<QA>::kRowBytes, src,
-                          GuFmt<QA>::kRowBytes, &qfull[slot]);
-          }
-        }
-      }
-      if (!ok && lane == 0) {
-        tc_fail(a.hdr, abort_flag);
-        for (int j = it - C::kSQ < 0 ? 0 : it - C::kSQ; j < it; ++j)  // let issued copies land
-          ptx::mbar_wait(&qfull[j % C::kSQ], (j / C::kSQ) & 1, 1u << 20);
-      }
-    } else if (lane == 0) {
+    if (lane == 0) {
       // TMA tiles of 128 rows; x in u32 words: Q4_1 20 per stage; Q4_K
-      // 36 per super-block, half 1 from word 16; down: one stage's bytes
+      // 36 per super-block, half 1 from word 16; Q2_K the 24 words from the
+      // 16-byte boundary at or below super-block qs (21 qs words in); down:
+      // one stage's bytes
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
@@ -682,7 +652,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int qs = 0; qs < nst; ++qs, ++it) {
           const int slot = it % C::kSQ;
           if (!ptx::mbar_wait_or_abort(&qempty[slot], ((it / C::kSQ) & 1) ^ 1, abort_flag)) { ok = false; break; }
-          const int x = NMAT == 2 && QA == DS4MOE_Q4_K ? (qs >> 1) * 36 + (qs & 1) * 16 : qs * (C::kRowQ / 4);
+          const int x = NMAT == 2 && QA == DS4MOE_Q4_K   ? (qs >> 1) * 36 + (qs & 1) * 16
+                        : NMAT == 2 && QA == DS4MOE_Q2_K ? (21 * qs) & ~3
+                                                         : qs * (C::kRowQ / 4);
           ptx::mbar_arrive_expect_tx(&qfull[slot], C::kQSlot);
           ptx::tma_load_2d(sQ + slot * C::kQSlot, &mA0, x, row0, &qfull[slot]);
           if constexpr (NMAT == 2) ptx::tma_load_2d(sQ + slot * C::kQSlot + C::kQMat, &mA1, x, row0, &qfull[slot]);
@@ -963,25 +935,22 @@ cudaError_t launch_ffn_prefill(const FfnArgs &a, cudaStream_t s) {
   CUtensorMap mg, mu, md, mx, mh;
   if (!map_acts(&mx, a.xp, xp_cols(D), P) || !map_acts(&mh, a.h, F, P)) return cudaErrorInvalidValue;
   const int qg = L.q_gate, qd = L.q_down;
-  if (qg == DS4MOE_Q2_K) {
-    mg = mu = mx;  // unused: the Q2_K gate/up stages are bulk copies
-  } else if (!map_weights(&mg, L.gate, row_bytes(qg, D), (int64_t)E * F, GuFmt<DS4MOE_Q4_1>::kRowBytes) ||
-             !map_weights(&mu, L.up, row_bytes(qg, D), (int64_t)E * F, GuFmt<DS4MOE_Q4_1>::kRowBytes)) {
+  const int gbytes = qg == DS4MOE_Q2_K ? GuFmt<DS4MOE_Q2_K>::kRowBytes : GuFmt<DS4MOE_Q4_1>::kRowBytes;
+  if (!map_weights(&mg, L.gate, row_bytes(qg, D), (int64_t)E * F, gbytes) ||
+      !map_weights(&mu, L.up, row_bytes(qg, D), (int64_t)E * F, gbytes))
     return cudaErrorInvalidValue;
-  }
   const int dbytes = qd == DS4MOE_Q2_K ? QFmt<DS4MOE_Q2_K>::kBytes
                      : qd == DS4MOE_Q4_K ? QFmt<DS4MOE_Q4_K>::kBytes
                                          : QFmt<DS4MOE_Q4_1>::kBytes;
   if (!map_weights(&md, L.down, row_bytes(qd, F), (int64_t)E * D, dbytes)) return cudaErrorInvalidValue;
   const int ne = E < P ? E : P;
-  TcArgs gu{a.chunks_gu, a.nchunks, D, F, a.h, a.hdr, static_cast<const uint8_t *>(L.gate),
-            static_cast<const uint8_t *>(L.up), row_bytes(qg, D)};
+  TcArgs gu{a.chunks_gu, a.nchunks, D, F, a.h, a.hdr};
   const int gu_units = (ne + P / kChunkGateUp) * (F / kTileM);
   e = qg == DS4MOE_Q2_K   ? launch_tc<2, DS4MOE_Q2_K, kChunkGateUp>(mg, mu, mx, gu, gu_units, s, "gate_up_tc")
       : qg == DS4MOE_Q4_K ? launch_tc<2, DS4MOE_Q4_K, kChunkGateUp>(mg, mu, mx, gu, gu_units, s, "gate_up_tc")
                           : launch_tc<2, DS4MOE_Q4_1, kChunkGateUp>(mg, mu, mx, gu, gu_units, s, "gate_up_tc");
   if (e != cudaSuccess) return e;
-  TcArgs dn{a.chunks_dn, a.nchunks + 1, F, D, a.y, a.hdr, nullptr, nullptr, 0};
+  TcArgs dn{a.chunks_dn, a.nchunks + 1, F, D, a.y, a.hdr};
   const int dn_units = (ne + P / kChunkDown) * (D / kTileM);
   if (qd == DS4MOE_Q2_K) return launch_tc<1, DS4MOE_Q2_K, kChunkDown>(md, md, mh, dn, dn_units, s, "down_tc");
   if (qd == DS4MOE_Q4_K) return launch_tc<1, DS4MOE_Q4_K, kChunkDown>(md, md, mh, dn, dn_units, s, "down_tc");
