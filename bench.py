@@ -689,12 +689,25 @@ def prefill_record(args, M, torch, w: synth.Workload, rank: int, world: int, loc
     if "gate_up_tc" in kernels:
         us = kernels["gate_up_tc"]["avg_us"]
         qname = synth.recipe(w, synth.T_GATE).qtype.upper()
+        # experts with at most `small` pairs stream through the multi-token
+        # kernels: the grouped GEMM's own flops are those of the other pairs
+        small = M.ds4moe_prefill_small_pairs(dev.abi)
+        tc_pairs = int(counts[counts > small].sum()) if small > 0 else w.T * w.k
+        flops_tc = flops_gu * tc_pairs / (w.T * w.k)
+        rec["prefill_split"] = {"small_pairs": small, "tc_pairs": tc_pairs,
+                                "streamed_pairs": w.T * w.k - tc_pairs,
+                                "streamed_experts": int(((counts > 0) & (counts <= small)).sum()) if small > 0 else 0}
         rec["roofline"] = {"kernel": f"gate_up_tc (tcgen05 grouped GEMM, fused {qname} dequant + SwiGLU)",
-                           "bound": "tensor", "achieved": flops_gu / (us * 1e-6) / 1e12, "peak": peak,
-                           "unit": "TFLOP/s", "frac": flops_gu / (us * 1e-6) / 1e12 / peak, "traffic": None,
-                           "algorithmic_flops_per_launch": flops_gu, "avg_launch_us": us,
+                           "bound": "tensor", "achieved": flops_tc / (us * 1e-6) / 1e12, "peak": peak,
+                           "unit": "TFLOP/s", "frac": flops_tc / (us * 1e-6) / 1e12 / peak, "traffic": None,
+                           "algorithmic_flops_per_launch": flops_tc, "avg_launch_us": us,
                            "timing": "device span per launch (%globaltimer, grid entry to last warp exit)",
                            "peak_source": f"{peak_kind} bf16_tflops_sustained (kind::f16 runs at the bf16 rate)"}
+        if "gate_up_mma" in kernels:  # the streamed experts' gate/up, right after the grouped GEMM
+            us_all = us + kernels["gate_up_mma"]["avg_us"]
+            rec["gate_up_phase"] = {"kernels": "gate_up_tc + gate_up (streamed experts)", "us": us_all,
+                                    "tflops": flops_gu / (us_all * 1e-6) / 1e12,
+                                    "frac": flops_gu / (us_all * 1e-6) / 1e12 / peak}
     rec["kernels"] = kernels
     cnt = launch_count(M, torch, stream, step, 2)
     rec["launches_per_step"] = cnt
@@ -904,8 +917,9 @@ def line_from(rec: dict, args, world: int, dtype: str) -> dict:
             "steps": rec["steps"], "warmup": args.warmup, "ms_per_step": rec["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
             "data": "synthetic", "config": rec["config"]}
-    for key in ("tflops", "tensor_frac", "weight_stream_gbs", "hbm_frac", "roofline", "kernels",
-                "launches_per_step", "expert_load", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
+    for key in ("tflops", "tensor_frac", "weight_stream_gbs", "hbm_frac", "roofline", "gate_up_phase",
+                "prefill_split", "kernels", "launches_per_step", "expert_load", "cpu_baseline", "e2e",
+                "gpu_launches", "clocks"):
         if key in rec:
             line[key] = rec[key]
     return line
@@ -918,7 +932,8 @@ PREFILL_DTYPE = "f16 tensor-core operands (exact gate/up split), f32 accumulate"
 def sub_summary(rec: dict) -> dict:
     """A sub-record of the default line: the measurement without its host-side extras."""
     keep = ("metric", "value", "unit", "steps", "ms_per_step", "tflops", "tensor_frac", "weight_stream_gbs",
-            "hbm_frac", "config", "roofline", "kernels", "gpu_launches", "e2e", "clocks", "expert_load")
+            "hbm_frac", "config", "roofline", "gate_up_phase", "prefill_split", "kernels", "gpu_launches", "e2e",
+            "clocks", "expert_load")
     return {k: rec[k] for k in keep if k in rec}
 
 

@@ -24,6 +24,7 @@ QTYPES = {"q4_1": DS4MOE_Q4_1, "q2_k": DS4MOE_Q2_K, "iq2_xxs": DS4MOE_IQ2_XXS, "
 # Every symbol include/ds4moe.h declares.
 EXPORTS = (
     "ds4moe_block_values", "ds4moe_block_bytes", "ds4moe_status_string", "ds4moe_quantize_ref",
+    "ds4moe_prefill_small_pairs",
     "ds4moe_dequant", "ds4moe_workspace_bytes", "ds4moe_workspace_init", "ds4moe_route_topk",
     "ds4moe_ffn_decode", "ds4moe_ffn_prefill", "ds4moe_stream_status",
     "ds4moe_profile_enable", "ds4moe_profile_count", "ds4moe_profile_entry",
@@ -78,6 +79,7 @@ def lib():
         L.ds4moe_workspace_bytes.argtypes = [ctypes.POINTER(Layer), i32, i32, i32]
         L.ds4moe_workspace_bytes.restype = sz
         L.ds4moe_workspace_init.argtypes = [p, sz, p]
+        L.ds4moe_prefill_small_pairs.argtypes = [ctypes.POINTER(Layer)]
         L.ds4moe_route_topk.argtypes = [p, p, p, i32, i32, i32, i32, p, p, p, p, sz, p]
         L.ds4moe_route_topk_select_bias.argtypes = [p, p, p, i32, i32, i32, i32, p, p, p, p, sz, p]
         L.ds4moe_ffn_decode.argtypes = [ctypes.POINTER(Layer), p, p, p, i32, i32, p, p, sz, p]
@@ -225,6 +227,10 @@ def ds4moe_quantize_f32(qtype, x, importance, out, ws, cols=None, stream=None):
 
 def ds4moe_workspace_bytes(layer: Layer, T: int, k: int, prefill: bool = False) -> int:
     return int(lib().ds4moe_workspace_bytes(ctypes.byref(layer), T, k, int(bool(prefill))))
+
+
+def ds4moe_prefill_small_pairs(layer: Layer) -> int:
+    return int(lib().ds4moe_prefill_small_pairs(ctypes.byref(layer)))
 
 
 def ds4moe_workspace_init(ws, stream=None):

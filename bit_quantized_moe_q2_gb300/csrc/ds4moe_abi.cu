@@ -541,6 +541,12 @@ __device__ __forceinline__ void convert_x(const uint16_t *__restrict__ x, int T,
   }
 }
 
+// convert_x over a whole grid (the prefill's weight-streaming experts).
+__global__ void k_convert_x(const uint16_t *__restrict__ x, int T, int D, uint16_t *__restrict__ x16,
+                            uint8_t *__restrict__ xs16, float *__restrict__ xs32, WsHeader *__restrict__ hdr) {
+  convert_x(x, T, D, x16, xs16, xs32, hdr, (int)(blockIdx.x * blockDim.x + threadIdx.x), (int)(gridDim.x * blockDim.x));
+}
+
 // Outputs of the bucketing step (pairs p = t*k + i grouped by expert).
 struct BucketArgs {
   int32_t *idx;
@@ -1093,6 +1099,19 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
                    logits, (int)k, const_cast<float *>(w), ws_ptr<int32_t>(ws, lay.nvalid), out);
   }
   if (e != cudaSuccess) return cuda_status(e);
+  if (tc && prefill_split_ok(*L)) {
+    // the experts with few pairs stream their weights through the
+    // multi-token kernels, which read x as fp16 with its block sums
+    ProfScope prof("convert_x", s);
+    const int64_t work = (int64_t)T * (L->d_model / 32);
+    const int grid = (int)((work + 255) / 256 < num_sms() * 8 ? (work + 255) / 256 : num_sms() * 8);
+    k_convert_x<<<grid, 256, 0, s>>>(x, T, L->d_model, ws_ptr<uint16_t>(ws, lay.x16), ws_ptr<uint8_t>(ws, lay.xs16),
+                                     ws_ptr<float>(ws, lay.xs32), a.hdr);
+    e = cudaGetLastError();
+  } else if (tc) {
+    a.x16 = nullptr;  // no split: the grouped kernels do not run
+  }
+  if (e != cudaSuccess) return cuda_status(e);
   e = prefill ? launch_ffn_prefill(a, s) : launch_ffn_decode(a, s);
   if (e != cudaSuccess) return cuda_status(e);
   e = launch_combine(a, s);
@@ -1132,6 +1151,11 @@ extern "C" {
 
 int32_t ds4moe_block_values(int32_t qtype) { return block_vals(qtype); }
 int32_t ds4moe_block_bytes(int32_t qtype) { return block_bytes(qtype); }
+
+int32_t ds4moe_prefill_small_pairs(const ds4moe_layer *L) {
+  if (check_layer(L) != DS4MOE_OK) return -1;
+  return prefill_tc_ok(*L) && prefill_split_ok(*L) ? kSmallPairs : 0;
+}
 
 const char *ds4moe_status_string(int32_t s) {
   switch (s) {

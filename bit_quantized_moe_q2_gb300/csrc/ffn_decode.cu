@@ -1910,6 +1910,20 @@ cudaError_t launch_down_mma(const FfnArgs &a, cudaStream_t s) {
 
 bool t1_chain_ok(const ds4moe_layer &L) { return t1_gate_up_ok(L) && t1_down_ok(L) && L.n_expert <= 256; }
 
+// Prefill: the experts with few pairs go to the persistent weight-streaming
+// kernels (token groups in a.groups, their count in the header), the rest to
+// the tensor-core grouped GEMMs; both write h and y by sorted pair.
+bool prefill_split_ok(const ds4moe_layer &L) { return gate_up_mt_ok(L) && down_mt_ok(L); }
+
+cudaError_t launch_gate_up_groups(const FfnArgs &a, cudaStream_t s) {
+  const int q = a.L.q_gate;
+  return q == DS4MOE_Q2_K   ? launch_gate_up_mt<DS4MOE_Q2_K>(a, s)
+         : q == DS4MOE_Q4_K ? launch_gate_up_mt<DS4MOE_Q4_K>(a, s)
+                            : launch_gate_up_mt<DS4MOE_Q4_1>(a, s);
+}
+
+cudaError_t launch_down_groups(const FfnArgs &a, cudaStream_t s) { return launch_down_mt(a, s); }
+
 // The tensor-core kernels need rows that split into 16-byte-multiple bulk
 // copies and stages that fit in shared memory; other shapes use SIMT.
 bool decode_mma_ok(const ds4moe_layer &L) {

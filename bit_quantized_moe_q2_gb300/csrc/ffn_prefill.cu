@@ -812,21 +812,30 @@ __global__ void k_xperm(const uint16_t *__restrict__ x, const int32_t *__restric
   if (big) record_status(hdr, DS4MOE_EDEVICE);
 }
 
-// Token chunks per expert for both kernels (one CTA, E <= 1024 threads).
+// Token chunks per expert for both tensor-core kernels (one CTA, E <= 1024
+// threads).  With `small` > 0, an expert with 1 .. small pairs gets token
+// groups of <= kGroup pairs for the weight-streaming kernels instead, in
+// expert order, their count in hdr->n_groups.
 __global__ void __launch_bounds__(1024) k_chunks(const int32_t *__restrict__ offs, int E, Chunk *__restrict__ cgu,
-                                                 Chunk *__restrict__ cdn, int32_t *__restrict__ nchunks) {
-  __shared__ int s1[1024], s2[1024];
+                                                 Chunk *__restrict__ cdn, int32_t *__restrict__ nchunks, int small,
+                                                 Group *__restrict__ groups, WsHeader *__restrict__ hdr) {
+  __shared__ int s1[1024], s2[1024], s3[1024];
   const int e = threadIdx.x;
   const int n = e < E ? offs[e + 1] - offs[e] : 0;
-  const int a1 = (n + kChunkGateUp - 1) / kChunkGateUp, a2 = (n + kChunkDown - 1) / kChunkDown;
+  const bool grouped = n <= small;
+  const int a1 = grouped ? 0 : (n + kChunkGateUp - 1) / kChunkGateUp;
+  const int a2 = grouped ? 0 : (n + kChunkDown - 1) / kChunkDown;
+  const int a3 = grouped ? (n + kGroup - 1) / kGroup : 0;
   s1[e] = a1;
   s2[e] = a2;
+  s3[e] = a3;
   __syncthreads();
   for (int o = 1; o < 1024; o <<= 1) {
-    const int v1 = e >= o ? s1[e - o] : 0, v2 = e >= o ? s2[e - o] : 0;
+    const int v1 = e >= o ? s1[e - o] : 0, v2 = e >= o ? s2[e - o] : 0, v3 = e >= o ? s3[e - o] : 0;
     __syncthreads();
     s1[e] += v1;
     s2[e] += v2;
+    s3[e] += v3;
     __syncthreads();
   }
   if (e < E) {
@@ -835,10 +844,13 @@ __global__ void __launch_bounds__(1024) k_chunks(const int32_t *__restrict__ off
       cgu[b] = Chunk{e, p0 + j * kChunkGateUp, min(kChunkGateUp, n - j * kChunkGateUp), 0};
     for (int j = 0, b = s2[e] - a2; j < a2; ++j, ++b)
       cdn[b] = Chunk{e, p0 + j * kChunkDown, min(kChunkDown, n - j * kChunkDown), 0};
+    for (int j = 0, b = s3[e] - a3; j < a3; ++j, ++b)
+      groups[b] = Group{e, p0 + j * kGroup, min(kGroup, n - j * kGroup), 0};
   }
   if (e == 1023) {
     nchunks[0] = s1[1023];
     nchunks[1] = s2[1023];
+    if (small > 0) hdr->n_groups = s3[1023];
   }
 }
 
@@ -927,9 +939,13 @@ cudaError_t launch_ffn_prefill(const FfnArgs &a, cudaStream_t s) {
                                  a.xp, a.hdr);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  // experts with few pairs: the weight-streaming kernels (x as fp16 with its
+  // sums for them was converted before this call)
+  const bool split = a.x16 && a.xs16 && a.xs32 && prefill_split_ok(L);
   {
     ProfScope p("chunks", s);
-    k_chunks<<<1, 1024, 0, s>>>(a.offs, E, a.chunks_gu, a.chunks_dn, a.nchunks);
+    k_chunks<<<1, 1024, 0, s>>>(a.offs, E, a.chunks_gu, a.chunks_dn, a.nchunks, split ? kSmallPairs : 0,
+                                const_cast<Group *>(a.groups), a.hdr);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   CUtensorMap mg, mu, md, mx, mh;
@@ -950,11 +966,14 @@ cudaError_t launch_ffn_prefill(const FfnArgs &a, cudaStream_t s) {
       : qg == DS4MOE_Q4_K ? launch_tc<2, DS4MOE_Q4_K, kChunkGateUp>(mg, mu, mx, gu, gu_units, s, "gate_up_tc")
                           : launch_tc<2, DS4MOE_Q4_1, kChunkGateUp>(mg, mu, mx, gu, gu_units, s, "gate_up_tc");
   if (e != cudaSuccess) return e;
+  if (split && (e = launch_gate_up_groups(a, s)) != cudaSuccess) return e;
   TcArgs dn{a.chunks_dn, a.nchunks + 1, F, D, a.y, a.hdr};
   const int dn_units = (ne + P / kChunkDown) * (D / kTileM);
-  if (qd == DS4MOE_Q2_K) return launch_tc<1, DS4MOE_Q2_K, kChunkDown>(md, md, mh, dn, dn_units, s, "down_tc");
-  if (qd == DS4MOE_Q4_K) return launch_tc<1, DS4MOE_Q4_K, kChunkDown>(md, md, mh, dn, dn_units, s, "down_tc");
-  return launch_tc<1, DS4MOE_Q4_1, kChunkDown>(md, md, mh, dn, dn_units, s, "down_tc");
+  e = qd == DS4MOE_Q2_K   ? launch_tc<1, DS4MOE_Q2_K, kChunkDown>(md, md, mh, dn, dn_units, s, "down_tc")
+      : qd == DS4MOE_Q4_K ? launch_tc<1, DS4MOE_Q4_K, kChunkDown>(md, md, mh, dn, dn_units, s, "down_tc")
+                          : launch_tc<1, DS4MOE_Q4_1, kChunkDown>(md, md, mh, dn, dn_units, s, "down_tc");
+  if (e != cudaSuccess) return e;
+  return split ? launch_down_groups(a, s) : cudaSuccess;
 }
 
 cudaError_t span_control_prefill(int on, double *total_ns, int64_t *launches) {

@@ -222,6 +222,13 @@ bool decode_mma_ok(const ds4moe_layer &L);
 // decode entry ranks the experts inside them).
 bool t1_chain_ok(const ds4moe_layer &L);
 bool prefill_tc_ok(const ds4moe_layer &L);
+// Prefill split (ffn_decode.cu): layers whose formats the persistent
+// multi-token kernels take send experts with at most kSmallPairs pairs to
+// them (one token group of <= 8 pairs streams the expert's weights once).
+constexpr int kSmallPairs = 16;
+bool prefill_split_ok(const ds4moe_layer &L);
+cudaError_t launch_gate_up_groups(const FfnArgs &a, cudaStream_t s);
+cudaError_t launch_down_groups(const FfnArgs &a, cudaStream_t s);
 
 int num_sms();
 

@@ -283,12 +283,23 @@ ds4moe_status ds4moe_ffn_decode(const ds4moe_layer *L, const uint16_t *x,
  * ds4moe_ffn_prefill -- DEVICE.  Same contract as ds4moe_ffn_decode for a
  * prefill chunk (large T, e.g. the 4096-token chunk of [DS4-1]'s distributed
  * prefill): tokens are bucketed per expert and each expert runs as a grouped
- * GEMM.
+ * GEMM.  On layers where ds4moe_prefill_small_pairs() is n > 0, an expert
+ * with 1 .. n pairs of the call streams its weights through the multi-token
+ * decode kernels instead (the results agree to the same tolerance).
  */
 ds4moe_status ds4moe_ffn_prefill(const ds4moe_layer *L, const uint16_t *x,
                                  const int32_t *idx, const float *w, int32_t T,
                                  int32_t k, float *out, void *ws, size_t ws_bytes,
                                  void *stream);
+
+/*
+ * ds4moe_prefill_small_pairs -- HOST.  The pair count at or below which
+ * ds4moe_ffn_prefill sends an expert of this layer to the weight-streaming
+ * kernels, 0 if it sends every expert to the grouped GEMMs (or takes the
+ * decode kernels for the whole layer).  Returns -1 for an invalid layer.
+ * Needs the CUDA device (reads its compute capability).
+ */
+int32_t ds4moe_prefill_small_pairs(const ds4moe_layer *L);
 
 /*
  * ds4moe_moe_decode -- DEVICE.  One decode step of a routed-MoE layer in

@@ -90,7 +90,7 @@ def test_every_gate_up_format_takes_the_tensor_cores(M, wi):
     x = synth.activations(w)
     names = _profiled_names(M, lambda: gpu_forward(M, dev, x, L.Wr, L.bias, w.k, prefill=True))
     assert {"gate_up_tc", "down_tc"} <= names
-    assert not ({"gate_up", "down", "gate_up_simt", "down_simt"} & names)
+    assert not ({"gate_up_simt", "down_simt"} & names)
 
 
 @pytest.mark.parametrize("wi", range(len(TC_SHAPES)))
@@ -127,6 +127,29 @@ def test_prefill_tc_heavy_expert_and_single_token(M, T, k, wi):
     wt = rng.random((T, k)).astype(np.float32)
     wt /= wt.sum(axis=1, keepdims=True)
     out, _, _, st = gpu_forward(M, dev, x, L.Wr, None, k, True, idx, wt)
+    assert st == M.DS4MOE_OK
+    assert rel_err(out, oracle_out(L, x, idx, wt)) <= TOL
+
+
+@pytest.mark.parametrize("wi", [0, 3, 5])
+def test_prefill_split_small_experts_stream(M, wi):
+    """Experts with at most ds4moe_prefill_small_pairs() pairs take the
+    weight-streaming kernels, the rest the grouped GEMMs, in one call: 150
+    pairs on expert 3, 17 on expert 5 (just above), 16, 9, 5, 2 and 1 on
+    others (at or below), none on expert 7."""
+    w = TC_SHAPES[wi].replace(T=200, k=1, n_expert=8, seed=330 + wi)
+    L = build_layer(w)
+    dev = to_device(L)
+    n_small = M.ds4moe_prefill_small_pairs(dev.abi)
+    assert n_small == 16
+    x = synth.activations(w)
+    sizes = [(3, 150), (5, 17), (4, 16), (2, 9), (1, 5), (0, 2), (6, 1)]
+    idx = np.concatenate([np.full(n, e, np.int32) for e, n in sizes]).reshape(200, 1)
+    idx = idx[np.random.default_rng(wi).permutation(200)]
+    wt = np.ones((200, 1), np.float32)
+    names = _profiled_names(M, lambda: gpu_forward(M, dev, x, L.Wr, None, 1, True, idx, wt))
+    assert {"gate_up_tc", "down_tc", "gate_up", "down"} <= names
+    out, _, _, st = gpu_forward(M, dev, x, L.Wr, None, 1, True, idx, wt)
     assert st == M.DS4MOE_OK
     assert rel_err(out, oracle_out(L, x, idx, wt)) <= TOL
 
