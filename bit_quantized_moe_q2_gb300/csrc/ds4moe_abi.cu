@@ -320,60 +320,79 @@ __global__ void k_topk_selbias(const float *__restrict__ lb, const float *__rest
 // |x_j w_j| with gamma_n = n u / (1 - n u), u = 2^-24 (Higham, "Accuracy and
 // Stability of Numerical Algorithms", 2nd ed., section 3.1).
 constexpr int kRT = 64, kRK = 32;
+// The staged K slices are stored transposed ([k][row]); row index XOR
+// 8 ((k / 8) % 4) keeps the stores of one warp on distinct banks and the
+// float4 groups read back intact.  The next slice is fetched into
+// registers while the current one is multiplied (two shared buffers, one
+// barrier per slice).  Arithmetic and its order are the plain tiled GEMM's.
+__device__ __forceinline__ int router_sw(int k) { return 8 * ((k >> 3) & 3); }
+
 __global__ void __launch_bounds__(256) k_router_approx(const uint16_t *__restrict__ x, const float *__restrict__ Wr,
                                                        int T, int D, int E, float *__restrict__ lg) {
-  __shared__ __align__(16) float Xs[kRK][kRT + 4];
-  __shared__ __align__(16) float Ws[kRK][kRT + 4];
+  __shared__ __align__(16) float Xs[2][kRK][kRT + 4];
+  __shared__ __align__(16) float Ws[2][kRK][kRT + 4];
   const int t0 = blockIdx.y * kRT, e0 = blockIdx.x * kRT;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   const int lr = tid >> 2, lc = (tid & 3) * 8;  // staging: row lr, k lc .. lc + 7
-  float tot[4][4];
+  const int t_ld = t0 + lr, e_ld = e0 + lr;
+  uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+  float4 wa = make_float4(0.f, 0.f, 0.f, 0.f), wb = wa;
+  auto fetch = [&](int kc) {
+    if (t_ld < T) xv = *reinterpret_cast<const uint4 *>(x + (int64_t)t_ld * D + kc + lc);
+    if (e_ld < E) {
+      wa = *reinterpret_cast<const float4 *>(Wr + (int64_t)e_ld * D + kc + lc);
+      wb = *reinterpret_cast<const float4 *>(Wr + (int64_t)e_ld * D + kc + lc + 4);
+    }
+  };
+  auto stage = [&](int b) {
+    const int col = lr ^ router_sw(lc);  // the same for k = lc .. lc + 7
+    const uint32_t wd[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      Xs[b][lc + 2 * q][col] = bf16_bits_to_f32(wd[q] & 0xFFFFu);
+      Xs[b][lc + 2 * q + 1][col] = bf16_bits_to_f32(wd[q] >> 16);
+    }
+    const float w8[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+    for (int q = 0; q < 8; ++q) Ws[b][lc + q][col] = w8[q];
+  };
+  float tot[4][4], acc[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) tot[i][j] = 0.f;
-  for (int k0 = 0; k0 < D; k0 += 64) {
-    float acc[4][4];
+    for (int j = 0; j < 4; ++j) tot[i][j] = acc[i][j] = 0.f;
+  fetch(0);
+  stage(0);
+  __syncthreads();
+  for (int kc = 0, b = 0; kc < D; kc += kRK, b ^= 1) {
+    const bool more = kc + kRK < D;
+    if (more) fetch(kc + kRK);
+    // each output: 64-term FMA chains over consecutive 64-value chunks of K,
+    // each started from zero and then added to the running total
+    if ((kc & 63) == 0) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-    for (int kc = k0; kc < k0 + 64; kc += kRK) {
-      {
-        const int t = t0 + lr;
-        const uint4 v = t < T ? *reinterpret_cast<const uint4 *>(x + (int64_t)t * D + kc + lc) : make_uint4(0, 0, 0, 0);
-        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          Xs[lc + 2 * q][lr] = bf16_bits_to_f32(wd[q] & 0xFFFFu);
-          Xs[lc + 2 * q + 1][lr] = bf16_bits_to_f32(wd[q] >> 16);
-        }
-        const int e = e0 + lr;
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-        if (e < E) {
-          a = *reinterpret_cast<const float4 *>(Wr + (int64_t)e * D + kc + lc);
-          b = *reinterpret_cast<const float4 *>(Wr + (int64_t)e * D + kc + lc + 4);
-        }
-        Ws[lc + 0][lr] = a.x; Ws[lc + 1][lr] = a.y; Ws[lc + 2][lr] = a.z; Ws[lc + 3][lr] = a.w;
-        Ws[lc + 4][lr] = b.x; Ws[lc + 5][lr] = b.y; Ws[lc + 6][lr] = b.z; Ws[lc + 7][lr] = b.w;
-      }
-      __syncthreads();
-#pragma unroll 8
-      for (int kk = 0; kk < kRK; ++kk) {
-        const float4 xv = *reinterpret_cast<const float4 *>(&Xs[kk][ty * 4]);
-        const float4 wv = *reinterpret_cast<const float4 *>(&Ws[kk][tx * 4]);
-        const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xa[i], wa[j], acc[i][j]);
-      }
-      __syncthreads();
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
     }
+#pragma unroll 8
+    for (int kk = 0; kk < kRK; ++kk) {
+      const float4 xq = *reinterpret_cast<const float4 *>(&Xs[b][kk][(ty * 4) ^ router_sw(kk)]);
+      const float4 wq = *reinterpret_cast<const float4 *>(&Ws[b][kk][(tx * 4) ^ router_sw(kk)]);
+      const float xa[4] = {xq.x, xq.y, xq.z, xq.w}, wv[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) tot[i][j] = __fadd_rn(tot[i][j], acc[i][j]);
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xa[i], wv[j], acc[i][j]);
+    }
+    if ((kc & 63) == 32) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tot[i][j] = __fadd_rn(tot[i][j], acc[i][j]);
+    }
+    if (more) stage(b ^ 1);
+    __syncthreads();
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
