@@ -3,6 +3,7 @@
 // softmax over the selected experts, token->expert bucketing and the
 // weighted combine.  The expert GEMV/GEMM kernels live in ffn_decode.cu and
 // ffn_prefill.cu.
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -584,6 +585,13 @@ struct BucketArgs {
   int nzero2;
   int32_t *zero3;  // and the tagged hidden words of the tile-order grid
   int nzero3;
+  // single token, layer input made here (nullptr otherwise): x = bf16 of
+  // RMS-normalised (nrm_res + nrm_add), as k_residual_norm computes it; CTA 0
+  // stores the sum to nrm_res_next and x to nrm_x
+  const float *nrm_res, *nrm_add;
+  float *nrm_res_next;
+  uint16_t *nrm_x;
+  float nrm_eps;
 };
 
 // Bucketing of a decode batch (P <= 32 pairs) by a CTA of 256 threads
@@ -709,6 +717,54 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t *__restrict_
   // spread over all CTAs of the router (not the single bucketing CTA)
   if (MODE != kRouteTopk && bk.xs16)
     convert_x(x, T, D, bk.x16, bk.xs16, bk.xs32, hdr, blockIdx.x * 256 + tid, gridDim.x * 256);
+  if (MODE == kRouteLogits && bk.nrm_res) {
+    // one token: the residual add and the RMS norm of k_residual_norm, with
+    // its thread mapping and summation order (every CTA the same values)
+    __shared__ float s_part[8];
+    float4 v[NI];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int q = tid + 256 * i;
+      v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (4 * q < D) {
+        float4 a = __ldcg(reinterpret_cast<const float4 *>(bk.nrm_res) + q);
+        const float4 o = __ldcg(reinterpret_cast<const float4 *>(bk.nrm_add) + q);
+        a.x = __fadd_rn(a.x, o.x);
+        a.y = __fadd_rn(a.y, o.y);
+        a.z = __fadd_rn(a.z, o.z);
+        a.w = __fadd_rn(a.w, o.w);
+        v[i] = a;
+        ss = fmaf(a.x, a.x, ss);
+        ss = fmaf(a.y, a.y, ss);
+        ss = fmaf(a.z, a.z, ss);
+        ss = fmaf(a.w, a.w, ss);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (lane == 0) s_part[wid] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < 8; ++ww) tot += s_part[ww];
+    const float r = 1.0f / sqrtf(tot / (float)D + bk.nrm_eps);
+    uint2 xv[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int q = tid + 256 * i;
+      xv[i] = make_uint2((uint32_t)f32_to_bf16_bits(v[i].x * r) | ((uint32_t)f32_to_bf16_bits(v[i].y * r) << 16),
+                         (uint32_t)f32_to_bf16_bits(v[i].z * r) | ((uint32_t)f32_to_bf16_bits(v[i].w * r) << 16));
+      if (blockIdx.x == 0 && 4 * q < D) {
+        reinterpret_cast<float4 *>(bk.nrm_res_next)[q] = v[i];
+        reinterpret_cast<uint2 *>(bk.nrm_x)[q] = xv[i];
+      }
+    }
+    route_dot2_regs<NI>(xv, wv, D, tid, ps[wid][0], pc[wid][0]);
+    __syncthreads();
+    if (wid == 0 && lane == 0) logits[e] = route_dot2_merge(ps, pc, 0, bias ? bias + e : nullptr);
+    return;
+  }
   for (int t0 = 0; t0 < T; t0 += 32) {
     const int nt = min(32, T - t0);
     int tt = 0;
@@ -927,25 +983,28 @@ __global__ void __launch_bounds__(1024) k_bucket(int32_t *__restrict__ idx, int 
 // x_next = bf16_RNE(x_res * r), r = 1 / sqrt(mean(x_res^2) + eps), the sum of
 // squares reduced in a fixed order (thread, warp, CTA).
 constexpr int kNormThreads = 256;
+// With `src`, the residual is read from src and the sum written to x_res.
 __global__ void __launch_bounds__(kNormThreads) k_residual_norm(float *__restrict__ x_res, const float *__restrict__ out,
-                                                               uint16_t *__restrict__ x_next, int D, float eps) {
+                                                               uint16_t *__restrict__ x_next, int D, float eps,
+                                                               const float *__restrict__ src) {
   ptx::pdl_wait();  // out comes from the preceding grid
   ptx::pdl_launch_dependents();
   __shared__ float s_part[kNormThreads / 32];
   const int t = blockIdx.x, tid = threadIdx.x;
   float4 *xr = reinterpret_cast<float4 *>(x_res + (int64_t)t * D);
+  const float4 *xs = src ? reinterpret_cast<const float4 *>(src + (int64_t)t * D) : xr;
   const float4 *orow = out ? reinterpret_cast<const float4 *>(out + (int64_t)t * D) : nullptr;
   float ss = 0.f;
   for (int i = tid; i < D / 4; i += kNormThreads) {
-    float4 v = xr[i];
+    float4 v = xs[i];
     if (orow) {
       const float4 o = __ldcg(orow + i);
       v.x = __fadd_rn(v.x, o.x);
       v.y = __fadd_rn(v.y, o.y);
       v.z = __fadd_rn(v.z, o.z);
       v.w = __fadd_rn(v.w, o.w);
-      xr[i] = v;
     }
+    if (orow || src) xr[i] = v;
     ss = fmaf(v.x, v.x, ss);
     ss = fmaf(v.y, v.y, ss);
     ss = fmaf(v.z, v.z, ss);
@@ -1033,7 +1092,7 @@ cudaError_t chain_attributes() {
 ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, const int32_t *idx,
                       const float *w, int32_t T, int32_t k, float *out, void *ws, size_t ws_bytes,
                       void *stream, const float *logits = nullptr, bool bucketed = false,
-                      bool route_t1 = false, bool x_converted = false) {
+                      bool route_t1 = false, bool x_converted = false, bool x_late = false) {
   ds4moe_status st = check_layer(L);
   if (st != DS4MOE_OK) return st;
   if (T < 0 || k < 1 || k > 32 || k > L->n_expert) return DS4MOE_EINVAL;
@@ -1049,6 +1108,7 @@ ds4moe_status run_ffn(bool prefill, const ds4moe_layer *L, const uint16_t *x, co
   FfnArgs a{};
   a.L = *L;
   a.x = x;
+  a.x_late = x_late;
   a.w = w;
   a.T = T;
   a.k = k;
@@ -1164,6 +1224,16 @@ __global__ void k_combine_pairs(const float *__restrict__ y, const int32_t *__re
 }
 
 }  // namespace
+
+// The layer input of a single-token tile-order layer formed inside its
+// router grid: x = bf16(rmsnorm(res + add)), the sum stored to res_next
+// (a buffer other than res) and x to `x`.
+struct NormFuse {
+  const float *res, *add;
+  float *res_next;
+  uint16_t *x;
+  float eps;
+};
 
 // =================================================================== C ABI
 extern "C" {
@@ -1404,9 +1474,12 @@ ds4moe_status ds4moe_ffn_prefill(const ds4moe_layer *L, const uint16_t *x, const
   return run_ffn(true, L, x, idx, w, T, k, out, ws, ws_bytes, stream);
 }
 
-ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const float *Wr, const float *bias,
-                               int32_t T, int32_t k, float *out, int32_t *idx, float *w, void *ws,
-                               size_t ws_bytes, void *stream) {
+// ds4moe_moe_decode's body; with `nf` (one token on tile-order weights
+// only), the router grid forms the layer input itself from the residual
+// stream (NormFuse) instead of reading x.
+static ds4moe_status moe_decode_impl(const ds4moe_layer *L, const uint16_t *x, const float *Wr, const float *bias,
+                                     int32_t T, int32_t k, float *out, int32_t *idx, float *w, void *ws,
+                                     size_t ws_bytes, void *stream, const NormFuse *nf) {
   ds4moe_status st = check_layer(L);
   if (st != DS4MOE_OK) return st;
   const int E = L->n_expert, D = L->d_model;
@@ -1420,6 +1493,9 @@ ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const 
   if (ws_bytes < lay.total) return DS4MOE_ESPACE;
   const bool r16 = layer_r16(*L);
   if (r16 && (T != 1 || !t1r_ok(*L, k))) return DS4MOE_EUNSUPPORTED;
+  if (nf && (!r16 || D > 4096 || !nf->res || !nf->add || !nf->res_next || nf->x != x || !aligned16(nf->res) ||
+             !aligned16(nf->add) || !aligned16(nf->res_next) || nf->res == nf->res_next))
+    return DS4MOE_EINVAL;
   if (!r16 && (T > 256 || E > 256 || D > 8192 || D % 8)) {
     // the two-call path gives the same results for shapes the fused router does not cover
     st = ds4moe_route_topk(x, Wr, bias, T, D, E, k, idx, w, nullptr, ws, ws_bytes, stream);
@@ -1448,10 +1524,19 @@ ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const 
       zero.zero3 = ws_ptr<int32_t>(ws, lay.h);
       zero.nzero3 = k * L->d_ff;
     }
+    if (nf) {
+      zero.nrm_res = nf->res;
+      zero.nrm_add = nf->add;
+      zero.nrm_res_next = nf->res_next;
+      zero.nrm_x = nf->x;
+      zero.nrm_eps = nf->eps;
+    }
     const cudaError_t e = launch_pdl(kern, dim3(E), dim3(256), 0, s, x, Wr, bias, (int)T, (int)D, (int)E, (int)k, lg,
                                      idx, w, static_cast<WsHeader *>(ws), zero);
     if (e != cudaSuccess) return cuda_status(e);
-    return run_ffn(false, L, x, idx, w, T, k, out, ws, ws_bytes, stream, lg, true, true);
+    // with nf the router grid writes x: the FFN grid reads it after its dependency wait
+    return run_ffn(false, L, x, idx, w, T, k, out, ws, ws_bytes, stream, lg, /*bucketed=*/true, /*route_t1=*/true,
+                   /*x_converted=*/false, /*x_late=*/nf != nullptr);
   }
   // up to 32 pairs: the router's last CTA also does the bucketing
   const bool fused = T * k <= 32;
@@ -1484,6 +1569,12 @@ ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const 
   }
   return run_ffn(false, L, x, idx, w, T, k, out, ws, ws_bytes, stream, lg, fused, false,
                  !fused && decode_mma_ok(*L));
+}
+
+ds4moe_status ds4moe_moe_decode(const ds4moe_layer *L, const uint16_t *x, const float *Wr, const float *bias,
+                               int32_t T, int32_t k, float *out, int32_t *idx, float *w, void *ws,
+                               size_t ws_bytes, void *stream) {
+  return moe_decode_impl(L, x, Wr, bias, T, k, out, idx, w, ws, ws_bytes, stream, nullptr);
 }
 
 ds4moe_status ds4moe_gather_rows(const uint16_t *x, const int32_t *rows, int32_t n, int32_t d_model,
@@ -1521,7 +1612,7 @@ ds4moe_status ds4moe_residual_norm(float *x_res, const float *out, uint16_t *x_n
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ProfScope prof("residual_norm", s);
   return cuda_status(launch_pdl(k_residual_norm, dim3(T), dim3(kNormThreads), 0, s, x_res, out, x_next,
-                                (int)d_model, eps));
+                                (int)d_model, eps, static_cast<const float *>(nullptr)));
 }
 
 ds4moe_status ds4moe_stack_decode(const ds4moe_layer *layers, const float *const *Wr, const float *const *bias,
@@ -1541,10 +1632,35 @@ ds4moe_status ds4moe_stack_decode(const ds4moe_layer *layers, const float *const
   const int D = layers[0].d_model;
   const size_t ldk = ((size_t)T * k + 3) & ~size_t(3);
   ds4moe_status st = ds4moe_residual_norm(x_res, nullptr, x_bf16, T, D, eps, stream);
+  // one token over tile-order layers: each layer after the first forms its
+  // input inside its router grid (residual add + norm of the previous
+  // layer's output), the residual alternating between x_res and a
+  // workspace buffer; the last layer's add + norm runs as its own grid
+  bool fuse = T == 1 && D <= 4096;
+  for (int l = 0; l < n_layers; ++l) fuse = fuse && layer_r16(layers[l]);
+  // the second buffer past every layer's other regions (each layer's
+  // workspace check covers its own offset plus the buffer)
+  size_t res2 = 0;
+  for (int l = 0; l < n_layers; ++l) res2 = std::max(res2, ws_layout(layers[l], T, k, 0).res2);
+  float *res[2] = {x_res, ws_ptr<float>(ws, res2)};
+  int cur = 0;
   for (int l = 0; l < n_layers && st == DS4MOE_OK; ++l) {
-    st = ds4moe_moe_decode(&layers[l], x_bf16, Wr[l], bias ? bias[l] : nullptr, T, k, out, idx + l * ldk,
-                           w + l * ldk, ws, ws_bytes, stream);
-    if (st == DS4MOE_OK) st = ds4moe_residual_norm(x_res, out, x_bf16, T, D, eps, stream);
+    if (fuse && l > 0) {
+      const NormFuse nf{res[cur], out, res[cur ^ 1], x_bf16, eps};
+      st = moe_decode_impl(&layers[l], x_bf16, Wr[l], bias ? bias[l] : nullptr, T, k, out, idx + l * ldk,
+                           w + l * ldk, ws, ws_bytes, stream, &nf);
+      cur ^= 1;
+    } else {
+      st = ds4moe_moe_decode(&layers[l], x_bf16, Wr[l], bias ? bias[l] : nullptr, T, k, out, idx + l * ldk,
+                             w + l * ldk, ws, ws_bytes, stream);
+      if (st == DS4MOE_OK && !fuse) st = ds4moe_residual_norm(x_res, out, x_bf16, T, D, eps, stream);
+    }
+  }
+  if (st == DS4MOE_OK && fuse) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ProfScope prof("residual_norm", s);
+    st = cuda_status(launch_pdl(k_residual_norm, dim3(T), dim3(kNormThreads), 0, s, x_res, static_cast<const float *>(out),
+                                x_bf16, (int)D, eps, cur ? static_cast<const float *>(res[1]) : nullptr));
   }
   return st;
 }

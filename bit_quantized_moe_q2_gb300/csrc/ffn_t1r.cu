@@ -265,10 +265,13 @@ __global__ void __launch_bounds__(kT1rMaxWarps * 32, 1) k_ffn_t1r(FfnArgs a, int
   }
   __syncthreads();
   R16B B;
-  if (w < nbg) r16_load_b(B, a.x + 256 * w, g, c);  // the call's input: ready before the router grid started
+  // the call's input: ready before the router grid started, unless that
+  // grid forms it (x_late)
+  if (!a.x_late && w < nbg) r16_load_b(B, a.x + 256 * w, g, c);
   ptx::pdl_wait();
   span_begin(DS4MOE_SPAN_FFN_T1R);
   ptx::pdl_launch_dependents();
+  if (a.x_late && w < nbg) r16_load_b(B, a.x + 256 * w, g, c);
   if (w == wsync) {
     // the experts of the single token: all that the producer needs
     const int k = a.k, E = a.L.n_expert;

@@ -79,7 +79,7 @@ inline int64_t xp_cols(int64_t D) { return D + D / 8; }
 
 struct WsLayout {
   size_t hdr, logits, rnorm, rlist, counts, offs, active, perm, inv, lrank, groups, x16, xs16, xs32, hs16, h, y, nvalid, cnt,
-      xp, chunks_gu, chunks_dn, nchunks, total;
+      xp, chunks_gu, chunks_dn, nchunks, res2, total;
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -110,6 +110,7 @@ inline WsLayout ws_layout(const ds4moe_layer &L, int T, int k, int prefill) {
   w.y = o;       o += align256(sizeof(float) * P * (size_t)L.d_model);
   w.nvalid = o;  o += align256(sizeof(int32_t) * (size_t)T);
   w.cnt = o;     o += align256(sizeof(int32_t) * (size_t)T * (size_t)(L.d_model / 16));
+  w.res2 = o;    o += align256(sizeof(float) * (size_t)T * (size_t)L.d_model);  // the stack's second residual buffer
   if (prefill) {  // tensor-core prefill: x gathered in pair order, token chunks
     const size_t ne = E < P ? E : P;
     w.xp = o;        o += align256(sizeof(uint16_t) * P * (size_t)xp_cols(L.d_model));
@@ -161,6 +162,7 @@ __device__ __forceinline__ void finish_routing_weights(float *w, int T, int k) {
 struct FfnArgs {
   ds4moe_layer L;
   const uint16_t *x;
+  int x_late;  // x is written by the preceding grid: read it only after the dependency wait
   const float *w;
   int T, k;
   float *out;

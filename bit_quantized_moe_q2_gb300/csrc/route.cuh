@@ -22,18 +22,19 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
 
 // Dot2 partial of x . Wr_e for one 256-thread group (thread tid < 256 of
 // the group holds the router row's float4 slices j = 4 (tid + 256 i) in
-// wv): four compensated chains per thread, merged with TwoSum, then across
-// the warp; lane 0 leaves the warp's (sum, error) in (ps, pc).
+// wv, and the matching four bf16 values of x in xv[i]): four compensated
+// chains per thread, merged with TwoSum, then across the warp; lane 0
+// leaves the warp's (sum, error) in (ps, pc).
 template <int NI>
-__device__ __forceinline__ void route_dot2_partial(const uint16_t *__restrict__ xr, const float4 (&wv)[NI], int D,
-                                                   int tid, float &ps, float &pc) {
+__device__ __forceinline__ void route_dot2_regs(const uint2 (&xin)[NI], const float4 (&wv)[NI], int D, int tid,
+                                                float &ps, float &pc) {
   const int lane = threadIdx.x & 31;
   float s4[4] = {0.f, 0.f, 0.f, 0.f}, c4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
     const int j = 4 * (tid + 256 * i);
     if (j < D) {
-      const uint2 xv = __ldcg(reinterpret_cast<const uint2 *>(xr + j));
+      const uint2 xv = xin[i];
       const float xs[4] = {bf16_bits_to_f32(xv.x & 0xFFFFu), bf16_bits_to_f32(xv.x >> 16),
                            bf16_bits_to_f32(xv.y & 0xFFFFu), bf16_bits_to_f32(xv.y >> 16)};
       const float ws4[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
@@ -65,6 +66,19 @@ __device__ __forceinline__ void route_dot2_partial(const uint16_t *__restrict__ 
     ps = s;
     pc = c;
   }
+}
+
+// The partial above with x read from global memory (row xr).
+template <int NI>
+__device__ __forceinline__ void route_dot2_partial(const uint16_t *__restrict__ xr, const float4 (&wv)[NI], int D,
+                                                   int tid, float &ps, float &pc) {
+  uint2 xv[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int j = 4 * (tid + 256 * i);
+    xv[i] = j < D ? __ldcg(reinterpret_cast<const uint2 *>(xr + j)) : make_uint2(0u, 0u);
+  }
+  route_dot2_regs<NI>(xv, wv, D, tid, ps, pc);
 }
 
 // The same partial for NT consecutive tokens (row stride D) at once: every

@@ -97,6 +97,59 @@ def test_stack_layer_by_layer_matches_oracle(M, stack, T):
                               trace["w"][l].cpu().numpy().view(np.uint32))
 
 
+@pytest.mark.parametrize("n_layers", [1, 2, 5])
+def test_tile_order_stack_forms_inputs_in_the_router(M, stack, n_layers):
+    """One token over tile-order layers: every layer after the first forms
+    its input (residual add + RMS norm of the previous output) inside its
+    router grid, the residual alternating between the caller's buffer and a
+    workspace buffer.  The results must be the bits of the layer-by-layer
+    calls (ds4moe_moe_decode then ds4moe_residual_norm), for an odd and an
+    even number of layers."""
+    import torch
+    from bit_quantized_moe_q2_gb300.device import workspace
+    w, Ls, devs = stack
+    r16 = [d.repacked_r16() for d in devs[:n_layers]]
+    T, D, k = 1, w.d_model, w.k
+    x0 = synth.activations(w, T=T, batch=7)
+    Wr = [torch.from_numpy(L.Wr).cuda() for L in Ls[:n_layers]]
+    ws = workspace(r16[0], T, k)
+    # layer by layer
+    x_res = torch.from_numpy(oracle.bf16_to_f32(x0).copy()).cuda()
+    xb = torch.empty((T, D), dtype=torch.int16, device="cuda")
+    out = torch.empty((T, D), dtype=torch.float32, device="cuda")
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    M.ds4moe_residual_norm(x_res, None, xb)
+    ref_idx, ref_w = [], []
+    for l in range(n_layers):
+        M.ds4moe_moe_decode(r16[l].abi, xb, Wr[l], None, k, out, idx, wt, ws)
+        M.ds4moe_residual_norm(x_res, out, xb)
+        ref_idx.append(idx.clone())
+        ref_w.append(wt.clone())
+    assert M.ds4moe_stream_status(ws) == M.DS4MOE_OK
+    ref_res, ref_xb = x_res.clone(), xb.clone()
+    # one call
+    xs = torch.from_numpy(oracle.bf16_to_f32(x0).copy()).cuda()
+    xb2 = torch.empty_like(xb)
+    ldk = M.stack_ldk(T, k)
+    idx_all = torch.empty((n_layers, ldk), dtype=torch.int32, device="cuda")
+    w_all = torch.empty((n_layers, ldk), dtype=torch.float32, device="cuda")
+    M.ds4moe_profile_enable(True)
+    try:
+        M.ds4moe_stack_decode([d.abi for d in r16], Wr, None, k, xs, xb2, out, idx_all, w_all, ws)
+        names = M.ds4moe_profile_read()
+    finally:
+        M.ds4moe_profile_enable(False)
+    assert M.ds4moe_stream_status(ws) == M.DS4MOE_OK
+    assert np.array_equal(xs.cpu().numpy().view(np.uint32), ref_res.cpu().numpy().view(np.uint32))
+    assert np.array_equal(xb2.cpu().numpy(), ref_xb.cpu().numpy())
+    for l in range(n_layers):
+        assert np.array_equal(idx_all[l, :k].cpu().numpy(), ref_idx[l].cpu().numpy().ravel()), l
+        assert np.array_equal(w_all[l, :k].cpu().numpy().view(np.uint32), ref_w[l].cpu().numpy().ravel().view(np.uint32)), l
+    # one residual grid for the whole stack besides the input's (the layers' are in the routers)
+    assert names["residual_norm"][1] == 2
+
+
 def test_stack_rejects_bad_arguments_before_launching(M, stack):
     import torch
     from bit_quantized_moe_q2_gb300.device import workspace
