@@ -57,6 +57,10 @@ import synth  # noqa: E402
 
 N_COPIES = 8
 N_SLOTS = 16
+# Decode steps captured per CUDA graph (consecutive steps, each with its own
+# input slot and weight copy, as a decode loop runs them); a step count that
+# is not a multiple is completed with one-step graphs, so exactly K steps run.
+STEPS_PER_GRAPH = 8
 METRIC = "routed-MoE tokens/s"
 R16_LAYOUT = "q2_k in the 16-row tile order (DS4MOE_Q2_K_R16, repacked once at load by ds4moe_repack)"
 PLAIN_LAYOUT = "q2_k plain block layout"
@@ -539,8 +543,9 @@ def replicate(dev, n: int):
 
 def decode_layer_record(args, M, torch, w: synth.Workload, copies, layout: str, rank: int, world: int, local: int,
                         with_e2e: bool) -> dict:
-    """One layer's decode steps (route + FFN) through ds4moe_moe_decode, one CUDA
-    graph per step position; copy i % len(copies), token slot i % N_SLOTS."""
+    """One layer's decode steps (route + FFN) through ds4moe_moe_decode, step i
+    on copy i % len(copies) and token slot i % N_SLOTS; CUDA graphs of
+    STEPS_PER_GRAPH consecutive steps (and one-step graphs for a remainder)."""
     from bit_quantized_moe_q2_gb300.device import check_status, workspace
     dev = copies[0]
     n_copies = len(copies)
@@ -565,27 +570,40 @@ def decode_layer_record(args, M, torch, w: synth.Workload, copies, layout: str, 
             step(i, stream)
     check_status(ws, stream)
     uniq = [len(set(idx[j].cpu().numpy().ravel().tolist())) for j in range(N_SLOTS)]
-    graphs = []
+    G = STEPS_PER_GRAPH
+    graphs, single = [], []
     for j in range(N_SLOTS):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            step(j, stream)
+            for q in range(G):
+                step(j * G + q, stream)
         graphs.append(g)
+        g1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1, stream=stream):
+            step(j, stream)
+        single.append(g1)
+    # the timed region: exactly args.steps steps; schedule entry = (graph, its steps)
+    n_full, rem = divmod(args.steps, G)
+    sched = [(graphs[i % N_SLOTS], [(i % N_SLOTS) * G + q for q in range(G)]) for i in range(n_full)]
+    sched += [(single[(n_full * G + q) % N_SLOTS], [n_full * G + q]) for q in range(rem)]
 
     def replay(i):
+        sched[i % len(sched)][0].replay()
+
+    def replay_g(i):
         graphs[i % N_SLOTS].replay()
 
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
-            replay(i)
+            replay_g(i)
     stream.synchronize()
     check_status(ws, stream)
-    ms, clocks = measure_clocks(torch, stream, replay, gpu_index(local), args.steps, world)
+    ms, clocks = measure_clocks(torch, stream, replay, gpu_index(local), len(sched), world)
     check_status(ws, stream)
     tokens = world * args.steps * T
     eb = expert_bytes(w)
     algo_step = [u * eb + Wr.nbytes + (0 if bias is None else bias.nbytes) + T * D * 2 + T * D * 4 for u in uniq]
-    algo_bytes = sum(algo_step[i % N_SLOTS] for i in range(args.steps))
+    algo_bytes = sum(algo_step[st % N_SLOTS] for _, sts in sched for st in sts)
     peak, _ = measured_peaks()
     stream_gbs = algo_bytes / (ms / 1000.0) / 1e9
     rec = {"metric": METRIC, "value": tokens / (ms / 1000.0), "unit": "tokens/s", "steps": args.steps,
@@ -593,12 +611,15 @@ def decode_layer_record(args, M, torch, w: synth.Workload, copies, layout: str, 
            "clocks": clocks}
     cfg = workload_config(w, n_copies)
     cfg["layout"] = layout
+    cfg["steps_per_graph"] = G
     rec["config"] = cfg
     if args.timed_only:
         return rec
-    kp = min(max(args.steps, 200), 2000)
-    kernels = span_pass(M, torch, stream, replay, kp)
-    uniq_avg = sum(uniq[i % N_SLOTS] for i in range(kp)) / kp
+    kp = max(min(max(args.steps, 200), 2000) // G, 1)
+    kernels = span_pass(M, torch, stream, replay_g, kp)
+    for v in kernels.values():
+        v["launches_per_step"] /= G
+    uniq_avg = sum(uniq[((i % N_SLOTS) * G + q) % N_SLOTS] for i in range(kp) for q in range(G)) / (kp * G)
     ffn = next((n for n in ("ffn_t1r", "ffn_t1") if n in kernels), None)
     if ffn:
         algo = uniq_avg * eb + T * D * 2 + T * D * 4
