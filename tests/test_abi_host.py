@@ -163,6 +163,10 @@ def test_device_entry_points_reject_bad_arguments_before_launch(M):
     assert L.ds4moe_route_topk(fake, fake, None, 0, 4096, 256, 6, fake, fake, None, fake, ws_need, None) == \
         M.DS4MOE_OK
     assert M.ds4moe_workspace_bytes(M.Layer(0, 0, 0, 0, 0, 0, None, None, None), 4, 6) == 0
+    # prefill split threshold: an invalid layer is -1 before any device query
+    assert M.ds4moe_prefill_small_pairs(bad) == -1
+    assert M.ds4moe_prefill_small_pairs(ragged) == -1
+    assert M.ds4moe_prefill_small_pairs(lay) in (0, 16)  # 0 without a tensor-core device
     # fault-injection hook: a budget below one poll or a negative offset
     assert L.ds4moe_debug_sync_wait(0, 0) == M.DS4MOE_EINVAL
     assert L.ds4moe_debug_sync_wait(100, -1) == M.DS4MOE_EINVAL
