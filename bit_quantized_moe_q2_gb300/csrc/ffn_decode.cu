@@ -815,17 +815,20 @@ __global__ void __launch_bounds__(256) k_down_mma(FfnArgs a, uint32_t chd) {
 
 // ================================================================ down, persistent
 // T > 1, Q2_K or Q4_K down, d_ff in {1024, 2048, 4096}: one CTA per SM, 16 consumer
-// warps over units of 16 / nbk 16-row tiles (nbk = d_ff / 256): warp w takes
-// K block w % nbk of tile w / nbk, and keeps that K block of its token
-// group's h (the operand the gate/up kernels wrote) in registers while
-// consecutive units share the group -- each CTA takes a contiguous range of
-// units.  A producer warp streams the unit's tiles (the single-token
-// bank-group layout) into a ring; a reducer warp sums each tile's K partials
-// in order and writes y.  The weighted combine runs as its own grid.
+// warps over units of kDmtTpw * 16 / nbk 16-row tiles (nbk = d_ff / 256): warp
+// w takes K block w % nbk of tiles w / nbk + (16 / nbk) j, j < kDmtTpw, and
+// keeps that K block of its token group's h (the operand the gate/up kernels
+// wrote) in registers while consecutive units share the group -- each CTA
+// takes a contiguous range of units.  A producer warp streams the unit's
+// tiles (the single-token bank-group layout) into a ring; a reducer warp sums
+// each tile's K partials in order and writes y.  The weighted combine runs
+// as its own grid.  Two tiles per warp and unit halve the unit's fixed cost
+// (ring and partial hand-offs) per MMA.
 constexpr int kDmtWarps = 16;
+constexpr int kDmtTpw = 2;
 
 size_t down_mt_smem(uint32_t tile, int tpu, int nstage) {
-  return (size_t)nstage * tpu * tile + (size_t)kMtPart * kDmtWarps * 32 * sizeof(float4) +
+  return (size_t)nstage * tpu * kDmtTpw * tile + (size_t)kMtPart * kDmtWarps * kDmtTpw * 32 * sizeof(float4) +
          sizeof(uint64_t) * (2 * (size_t)nstage + 2 * kMtPart);
 }
 
@@ -837,10 +840,11 @@ __global__ void __launch_bounds__((kDmtWarps + 2) * 32, 1) k_down_mt(FfnArgs a, 
   const int D = a.L.d_model, F = a.L.d_ff, nbk = F / 256, tpu = kDmtWarps / nbk;
   const int64_t rbd = row_bytes(Q, F);
   const T1Tile tl = t1_tile((uint32_t)rbd);
-  const uint32_t tile = t1_tile_bytes(tl), stage = (uint32_t)tpu * tile;
+  const int upt = tpu * kDmtTpw;  // tiles per unit
+  const uint32_t tile = t1_tile_bytes(tl), stage = (uint32_t)upt * tile;
   const int wprod = kDmtWarps, wred = kDmtWarps + 1;
-  float4 *red = reinterpret_cast<float4 *>(smem + (size_t)nstage * stage);  // [kMtPart][16][32]
-  uint64_t *full = reinterpret_cast<uint64_t *>(red + (size_t)kMtPart * kDmtWarps * 32);
+  float4 *red = reinterpret_cast<float4 *>(smem + (size_t)nstage * stage);  // [kMtPart][kDmtTpw][16][32]
+  uint64_t *full = reinterpret_cast<uint64_t *>(red + (size_t)kMtPart * kDmtWarps * kDmtTpw * 32);
   uint64_t *empty = full + nstage, *pfull = empty + nstage, *pempty = pfull + kMtPart;
   if (threadIdx.x == 0) {
     for (int st = 0; st < nstage; ++st) {
@@ -855,7 +859,7 @@ __global__ void __launch_bounds__((kDmtWarps + 2) * 32, 1) k_down_mt(FfnArgs a, 
   }
   __syncthreads();
   const Q2kLane kl = q2k_lane(c);
-  const int ntu = D / (16 * tpu);  // units per token group
+  const int ntu = D / (16 * upt);  // units per token group
   // the token groups were complete before the gate/up grid (whose h this
   // kernel reads) launched it: the producer starts before the dependency wait
   const int U = __ldcg(&a.hdr->n_groups) * ntu, G = gridDim.x;
@@ -880,12 +884,12 @@ __global__ void __launch_bounds__((kDmtWarps + 2) * 32, 1) k_down_mt(FfnArgs a, 
         gi = u / ntu;
         grp = load_group(gi);
       }
-      const int64_t row0 = (int64_t)grp.e * D + (int64_t)(u % ntu) * 16 * tpu;
+      const int64_t row0 = (int64_t)grp.e * D + (int64_t)(u % ntu) * 16 * upt;
       uint8_t *dst = smem + (size_t)st * stage;
-      if (lane == 0) ptx::mbar_arrive_expect_tx(&full[st], (uint32_t)(16 * tpu) * (uint32_t)rbd);
+      if (lane == 0) ptx::mbar_arrive_expect_tx(&full[st], (uint32_t)(16 * upt) * (uint32_t)rbd);
       __syncwarp();
-      if ((uint32_t)lane < (uint32_t)tpu * nc) {
-        const uint32_t m = (uint32_t)lane / nc, i = (uint32_t)lane % nc;
+      for (uint32_t ci = (uint32_t)lane; ci < (uint32_t)upt * nc; ci += 32u) {  // upt * nc may exceed 32
+        const uint32_t m = ci / nc, i = ci % nc;
         t1_tile_copy(dst + m * tile, down + (row0 + 16 * (int64_t)m) * rbd, tl, i, &full[st]);
       }
       __syncwarp();
@@ -916,10 +920,14 @@ __global__ void __launch_bounds__((kDmtWarps + 2) * 32, 1) k_down_mt(FfnArgs a, 
         if (lane == 0) record_status(a.hdr, DS4MOE_ETIMEOUT);
         timed_out = true;
       }
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (!timed_out) {
-        const uint8_t *sp = smem + (size_t)st * stage + (size_t)m * tile;
-        seg_rows<Q>(sp + og, sp + og8, in, kl, nullptr, nullptr, c, acc);
+      float acc[kDmtTpw][4];
+#pragma unroll
+      for (int j = 0; j < kDmtTpw; ++j) {
+        acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+        if (!timed_out) {
+          const uint8_t *sp = smem + (size_t)st * stage + (size_t)(m + tpu * j) * tile;
+          seg_rows<Q>(sp + og, sp + og8, in, kl, nullptr, nullptr, c, acc[j]);
+        }
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&empty[st]);
@@ -928,7 +936,10 @@ __global__ void __launch_bounds__((kDmtWarps + 2) * 32, 1) k_down_mt(FfnArgs a, 
         if (!timed_out && lane == 0) record_status(a.hdr, DS4MOE_ETIMEOUT);
         timed_out = true;
       }
-      red[((size_t)pt * kDmtWarps + w) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+#pragma unroll
+      for (int j = 0; j < kDmtTpw; ++j)
+        red[(((size_t)pt * kDmtTpw + j) * kDmtWarps + w) * 32 + lane] =
+            make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&pfull[pt]);
     }
@@ -945,11 +956,12 @@ __global__ void __launch_bounds__((kDmtWarps + 2) * 32, 1) k_down_mt(FfnArgs a, 
         if (!timed_out && lane == 0) record_status(a.hdr, DS4MOE_ETIMEOUT);
         timed_out = true;
       }
-      const int row0 = (u % ntu) * 16 * tpu;
-      for (int m = 0; m < tpu; ++m) {
+      const int row0 = (u % ntu) * 16 * upt;
+      for (int mt = 0; mt < upt; ++mt) {  // tile mt = m + tpu j of the unit
+        const int j = mt / tpu, m = mt % tpu;
         float v[4] = {0.f, 0.f, 0.f, 0.f};
         for (int kb = 0; kb < nbk; ++kb) {  // K blocks in order: a fixed summation order
-          const float4 q = red[((size_t)pt * kDmtWarps + m * nbk + kb) * 32 + lane];
+          const float4 q = red[(((size_t)pt * kDmtTpw + j) * kDmtWarps + m * nbk + kb) * 32 + lane];
           v[0] += q.x;
           v[1] += q.y;
           v[2] += q.z;
@@ -958,7 +970,7 @@ __global__ void __launch_bounds__((kDmtWarps + 2) * 32, 1) k_down_mt(FfnArgs a, 
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int tok = 2 * c + (i & 1);
-          if (tok < grp.nt) a.y[(int64_t)(grp.p0 + tok) * D + row0 + 16 * m + g + 8 * (i >> 1)] = v[i];
+          if (tok < grp.nt) a.y[(int64_t)(grp.p0 + tok) * D + row0 + 16 * mt + g + 8 * (i >> 1)] = v[i];
         }
       }
       __syncwarp();
@@ -1869,7 +1881,7 @@ bool down_mt_ok(const ds4moe_layer &L) {
   const int nbk = L.d_ff / 256;
   if (nbk > kDmtWarps || kDmtWarps % nbk) return false;
   const int64_t rbd = row_bytes(L.q_down, L.d_ff);
-  if (rbd % 16 || L.d_model % (16 * (kDmtWarps / nbk))) return false;
+  if (rbd % 16 || L.d_model % (16 * kDmtTpw * (kDmtWarps / nbk))) return false;
   return down_mt_smem(t1_tile_bytes(t1_tile((uint32_t)rbd)), kDmtWarps / nbk, 2) <= kT1SmemGateUp;
 }
 
