@@ -24,17 +24,24 @@
 // Rings of shared-memory stages hand data between roles on mbarriers; every
 // wait is bounded and gives up (status DS4MOE_ETIMEOUT) instead of hanging.
 //
-// Numerics.  Gate/up (Q4_1) are exact up to fp32 accumulation: d*q is
-// carried as two fp16 tiles, RN(d*q) and the exact FMA residual
-// d*q - RN(d*q), each multiplied against the same x tile; the block minima
-// enter through extra K-steps that multiply m against the hi and lo fp16
-// parts of the 32-value block sums of x (precomputed per pair).  Rounding
-// gate/up weights to fp16 instead would perturb g and u by ~2^-12 relative,
-// enough to flip the bf16 rounding of a few percent of h.  Down weights are
-// rounded once to fp16 (Q2_K: RN(RN(d*sc)*q + RN(-dmin*mn)); Q4_1:
-// RN(d*q + m)) -- h is final by then, and the effect on y is ~2e-4
-// relative.  Activations are exact in fp16 (bf16 values; larger than the
-// fp16 range is flagged); products are exact and accumulate in fp32.
+// Numerics.  Gate/up are exact up to fp32 accumulation for every format:
+// the scaled code (Q4_1: d*q; Q2_K / Q4_K: d*(sc*q), sc*q an exact fp16
+// integer) is carried as two fp16 tiles, RN(.) and its exact FMA residual,
+// each multiplied against the same x tile; the block minima (Q4_1: m;
+// Q2_K / Q4_K: -dmin*mn as a hi/lo pair) enter through extra K-steps against
+// the hi and lo fp16 parts of the x block sums (precomputed per pair:
+// 32-value blocks, 16-value sub-blocks for Q2_K).  Rounding gate/up weights
+// to fp16 instead would perturb g and u by ~2^-12 relative, enough to flip
+// the bf16 rounding of a few percent of h.  Down weights are rounded once
+// to fp16 (Q2_K / Q4_K: RN(RN(d*sc)*q + RN(-dmin*mn)); Q4_1: RN(d*q + m))
+// -- h is final by then, and the effect on y is ~2e-4 relative.
+// Activations are exact in fp16 (bf16 values; larger than the fp16 range is
+// flagged); products are exact and accumulate in fp32.
+//
+// Experts with few pairs of a call (at most kSmallPairs) do not come here:
+// on layers the persistent multi-token kernels take, they stream their
+// weights through those kernels (token groups from k_chunks), which write h
+// and y at the same sorted pair rows.
 #include <cudaTypedefs.h>
 
 #include <mutex>
