@@ -536,6 +536,17 @@ def hbm_roofline(kdesc: str, algo_bytes: float, avg_us: float, traffic) -> dict:
             "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if kind == "measured" else "fallback 6.8 TB/s"}
 
 
+def graph_schedule(steps: int, g: int, n_slots: int):
+    """The timed region's graph replays for exactly `steps` steps: (graph kind,
+    graph index, the step numbers it runs) -- full graphs of g consecutive
+    steps (graph j holds steps j g .. j g + g - 1, j < n_slots), then one-step
+    graphs (graph j holds step j) for the remainder."""
+    n_full, rem = divmod(steps, g)
+    sched = [("full", i % n_slots, [(i % n_slots) * g + q for q in range(g)]) for i in range(n_full)]
+    sched += [("single", (n_full * g + q) % n_slots, [n_full * g + q]) for q in range(rem)]
+    return sched
+
+
 def replicate(dev, n: int):
     return [dev] + [type(dev)(dev.d_model, dev.d_ff, dev.n_expert, dev.q_gate, dev.q_up, dev.q_down,
                               dev.gate.clone(), dev.up.clone(), dev.down.clone()) for _ in range(n - 1)]
@@ -583,9 +594,8 @@ def decode_layer_record(args, M, torch, w: synth.Workload, copies, layout: str, 
             step(j, stream)
         single.append(g1)
     # the timed region: exactly args.steps steps; schedule entry = (graph, its steps)
-    n_full, rem = divmod(args.steps, G)
-    sched = [(graphs[i % N_SLOTS], [(i % N_SLOTS) * G + q for q in range(G)]) for i in range(n_full)]
-    sched += [(single[(n_full * G + q) % N_SLOTS], [n_full * G + q]) for q in range(rem)]
+    sched = [(graphs[j] if kind == "full" else single[j], sts)
+             for kind, j, sts in graph_schedule(args.steps, G, N_SLOTS)]
 
     def replay(i):
         sched[i % len(sched)][0].replay()
