@@ -59,7 +59,8 @@ N_COPIES = 8
 N_SLOTS = 16
 # Decode steps captured per CUDA graph (consecutive steps, each with its own
 # input slot and weight copy, as a decode loop runs them); a step count that
-# is not a multiple is completed with one-step graphs, so exactly K steps run.
+# is not a multiple ends with one graph of the remaining steps, so exactly K
+# steps run.
 STEPS_PER_GRAPH = 8
 METRIC = "routed-MoE tokens/s"
 R16_LAYOUT = "q2_k in the 16-row tile order (DS4MOE_Q2_K_R16, repacked once at load by ds4moe_repack)"
@@ -539,11 +540,12 @@ def hbm_roofline(kdesc: str, algo_bytes: float, avg_us: float, traffic) -> dict:
 def graph_schedule(steps: int, g: int, n_slots: int):
     """The timed region's graph replays for exactly `steps` steps: (graph kind,
     graph index, the step numbers it runs) -- full graphs of g consecutive
-    steps (graph j holds steps j g .. j g + g - 1, j < n_slots), then one-step
-    graphs (graph j holds step j) for the remainder."""
+    steps (graph j holds steps j g .. j g + g - 1, j < n_slots), then, for a
+    remainder r, one graph of the r steps that follow."""
     n_full, rem = divmod(steps, g)
     sched = [("full", i % n_slots, [(i % n_slots) * g + q for q in range(g)]) for i in range(n_full)]
-    sched += [("single", (n_full * g + q) % n_slots, [n_full * g + q]) for q in range(rem)]
+    if rem:
+        sched.append(("rest", 0, [n_full * g + q for q in range(rem)]))
     return sched
 
 
@@ -556,7 +558,7 @@ def decode_layer_record(args, M, torch, w: synth.Workload, copies, layout: str, 
                         with_e2e: bool) -> dict:
     """One layer's decode steps (route + FFN) through ds4moe_moe_decode, step i
     on copy i % len(copies) and token slot i % N_SLOTS; CUDA graphs of
-    STEPS_PER_GRAPH consecutive steps (and one-step graphs for a remainder)."""
+    STEPS_PER_GRAPH consecutive steps (and one graph for a remainder)."""
     from bit_quantized_moe_q2_gb300.device import check_status, workspace
     dev = copies[0]
     n_copies = len(copies)
@@ -582,20 +584,24 @@ def decode_layer_record(args, M, torch, w: synth.Workload, copies, layout: str, 
     check_status(ws, stream)
     uniq = [len(set(idx[j].cpu().numpy().ravel().tolist())) for j in range(N_SLOTS)]
     G = STEPS_PER_GRAPH
-    graphs, single = [], []
+    graphs = []
     for j in range(N_SLOTS):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for q in range(G):
                 step(j * G + q, stream)
         graphs.append(g)
-        g1 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g1, stream=stream):
-            step(j, stream)
-        single.append(g1)
     # the timed region: exactly args.steps steps; schedule entry = (graph, its steps)
-    sched = [(graphs[j] if kind == "full" else single[j], sts)
-             for kind, j, sts in graph_schedule(args.steps, G, N_SLOTS)]
+    sched = []
+    for kind, j, sts in graph_schedule(args.steps, G, N_SLOTS):
+        if kind == "full":
+            sched.append((graphs[j], sts))
+        else:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for st in sts:
+                    step(st, stream)
+            sched.append((g, sts))
 
     def replay(i):
         sched[i % len(sched)][0].replay()
@@ -606,6 +612,8 @@ def decode_layer_record(args, M, torch, w: synth.Workload, copies, layout: str, 
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
             replay_g(i)
+        for g_, _ in sched[len(sched) - 1:]:  # a remainder graph, uploaded before the timed region
+            g_.replay()
     stream.synchronize()
     check_status(ws, stream)
     ms, clocks = measure_clocks(torch, stream, replay, gpu_index(local), len(sched), world)

@@ -1,6 +1,6 @@
 """bench.py's timed region runs exactly K decode steps whatever K is: full
-graphs of STEPS_PER_GRAPH consecutive steps, then one-step graphs for the
-remainder, every step number once and in order within each graph."""
+graphs of STEPS_PER_GRAPH consecutive steps, then one graph of the
+remaining steps, every step number once and in order within each graph."""
 import pytest
 
 import bench
@@ -13,14 +13,10 @@ def test_schedule_runs_exactly_k_steps(steps):
     counted = [st for _, _, sts in sched for st in sts]
     assert len(counted) == steps
     full = [e for e in sched if e[0] == "full"]
-    single = [e for e in sched if e[0] == "single"]
-    assert len(full) == steps // g and len(single) == steps % g
-    assert sched == full + single  # full graphs first
-    for kind, j, sts in sched:
-        assert 0 <= j < n
-        if kind == "full":
-            assert sts == list(range(j * g, j * g + g))  # graph j's own consecutive steps
-        else:
-            assert len(sts) == 1 and sts[0] % n == j  # the one-step graph of that slot
+    rest = [e for e in sched if e[0] == "rest"]
+    assert len(full) == steps // g and len(rest) == (1 if steps % g else 0)
+    assert sched == full + rest  # full graphs first
+    for kind, j, sts in full:
+        assert 0 <= j < n and sts == list(range(j * g, j * g + g))  # graph j's own consecutive steps
     # the remainder's step numbers continue after the full graphs' count
-    assert [s for _, _, sts in single for s in sts] == list(range((steps // g) * g, steps))
+    assert [s for _, _, sts in rest for s in sts] == list(range((steps // g) * g, steps))
