@@ -142,3 +142,24 @@ def test_plan_dispatch_orders_pairs_by_owner():
     assert expert_ranges(8, 2) == [(0, 4), (4, 8)]
     with pytest.raises(ValueError):
         expert_ranges(8, 3)
+
+
+@pytest.mark.parametrize("R", [1, 2, 4, 8])
+def test_emulated_ranks_reproduce_the_single_rank_layer(R):
+    """R ranks emulated in one process (run_local_ranks): every rank's output
+    equals the single-rank oracle layer on its tokens, including ranks whose
+    experts receive no pair (at R = 8 each rank owns one expert)."""
+    import torch
+    import oracle
+    from bit_quantized_moe_q2_gb300 import ep
+    from tests.layers import build_layer
+    L = build_layer(W)
+    xs = [torch.from_numpy(synth.activations(W, batch=200 + r).view(np.int16).copy()) for r in range(R)]
+    backends = [OracleBackend(L, lo, hi) for lo, hi in ep.expert_ranges(W.n_expert, R)]
+    outs = ep.run_local_ranks(xs, backends, W.n_expert)
+    for r, (out, idx, w) in enumerate(outs):
+        x = xs[r].numpy().view(np.uint16)
+        ridx, rw, _ = oracle.route(x, L.Wr, L.bias, W.k)
+        assert np.array_equal(idx.numpy(), ridx)
+        ref = oracle.moe_ffn(W.d_model, W.d_ff, W.n_expert, L.qg, L.gate, L.qu, L.up, L.qd, L.down, x, ridx, rw)
+        assert np.max(np.abs(out.numpy() - ref)) <= 1e-5 * max(np.max(np.abs(ref)), 1e-30)
